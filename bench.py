@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""KVM layer benchmark on GB300: prefill tokens/s at 8k (+ roofline) and decode-step time.
+
+One step = one kvm_prefill over the whole fixed-state 8k workload (B=8, H=12,
+N=8192, head_dim 64, chunk 128, window 512, 256 slots incl. 16 sinks, bf16),
+inputs resident in HBM.  Inputs (q, k, v: 302 MB) are larger than L2, so no
+explicit flush is done between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its
+GPU (the (batch, head) rows are independent: no collective on the data path),
+timing is max over ranks, and value = total tokens of all ranks / that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from compressed_kv_state_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "KVM layer prefill tokens/s @8k (1 GB300)"
+UNIT = "tokens/s"
+W = wl.FIXED_8K
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d["bf16_tflops_sustained"],
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# --------------------------------------------------------------- work model
+
+def attention_work(w):
+    """Algorithmic attention work of one prefill: (query, key) pairs of the state
+    and of the window, FLOPs (state QK over the d - r non-rotary dims only),
+    exponentials, and the FLOPs counted at 4d per pair for every key."""
+    C, Wc, d, r = w.chunk, w.window // w.chunk, w.d, w.rope_dims
+    n_after = _schedule(w)
+    state_pairs = win_pairs = 0
+    for p in range(w.N):
+        c = p // C
+        e = c - Wc - 1
+        state_pairs += n_after[e] if e >= 0 else 0
+        win_pairs += p - max(0, (c - Wc) * C) + 1
+    rows = w.B * w.H
+    state_pairs *= rows
+    win_pairs *= rows
+    flops = state_pairs * (2 * (d - r) + 2 * d) + win_pairs * 4 * d
+    return dict(state_pairs=state_pairs, window_pairs=win_pairs, flops=flops,
+                flops_4d=(state_pairs + win_pairs) * 4 * d, exps=state_pairs + win_pairs)
+
+
+def _schedule(w):
+    import math
+    C = w.chunk
+    nchunks = -(-w.N // C)
+    E = max(0, nchunks - w.window // C - 1)
+    out, n, t = [], 0, 0
+    for e in range(E):
+        sinks = sum(1 for i in range(C) if e * C + i < w.n_sinks)
+        n0 = n + sinks
+        t += C
+        cap = w.max_slots if w.sched == 0 else w.n_sinks + math.ceil(w.coef * t ** w.expo)
+        a = min(max(cap - n0, 0), C - sinks)
+        n = n0 + a
+        out.append(n)
+    return out
+
+
+def fold_work(w):
+    """Similarity FLOPs of the fold chain (each token against every mergeable slot
+    once, plus the remaining tokens against the new slots)."""
+    C, S, d = w.chunk, w.n_sinks, w.d
+    n_prev, fl = 0, 0
+    for e, n_after in enumerate(_schedule(w)):
+        sinks = sum(1 for i in range(C) if e * C + i < S)
+        n0 = n_prev + sinks
+        cand = C - sinks
+        a = n_after - n0
+        fl += 2 * d * (cand * max(0, n0 - S) + (cand - a) * a)
+        n_prev = n_after
+    return fl * w.B * w.H
+
+
+def decode_bytes(dw, r_in_chunk, n):
+    """Algorithmic HBM bytes of one decode step (all rows): window K, V (bf16),
+    the state's read view (key on the d - r non-rotary dims, value), q, out, and
+    the new token written into the ring."""
+    d, r = dw.d, dw.rope_dims
+    per_row = (dw.window + r_in_chunk + 1) * d * 2 * 2 + n * (d - r + d) * 2 + 2 * d * 2 \
+        + 2 * d * 2 + 4
+    return per_row * dw.B * dw.H
+
+
+# ------------------------------------------------------------------ clocks
+
+class Clocks:
+    """nvidia-smi sampler (every 200 ms) running while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        pmax = max(r["power"] for r in rows)
+        load = [r for r in rows if r["power"] >= 0.5 * pmax] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() in ("active", "1", "0x1"):
+                    reasons.add(name)
+        return dict(sm_mhz=statistics.median(r["sm"] for r in load),
+                    sm_max_mhz=max(r["smax"] for r in load), reasons=sorted(reasons),
+                    samples=len(load), power_w_max=pmax)
+
+
+# -------------------------------------------------------------- traffic
+
+def _ncu_traffic(kernel_file):
+    """DRAM bytes per launch from a committed ncu summary, only if it was taken on
+    the current source of the kernel (same sha256); else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(os.path.basename(kernel_file))
+    if not d:
+        return None
+    sha = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
+    return d["dram_bytes_per_launch"] if d.get("source_sha256") == sha else None
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(w, heads_per_thread=1):
+    """Time the fp64 oracle on a bounded sample of the workload: one full-length
+    (batch, head) row per host core, all cores in parallel.  Returns tokens/s in
+    the layer's unit (a layer token needs all H heads)."""
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    nh = min(w.B * w.H, cores * heads_per_thread)
+    sub = w.with_(B=1, H=nh) if nh <= w.H else w
+    q, k, v, g = wl.prefill_inputs(sub.with_(B=1, H=min(nh, sub.H)))
+    q, k, v, g = q[0], k[0], v[0], g[0]
+    ocfg = oracle.OracleConfig(head_dim=w.d, rope_dims=w.rope_dims, chunk=w.chunk,
+                               window=w.window, n_sinks=w.n_sinks, sched=w.sched,
+                               max_slots=w.max_slots, coef=w.coef, expo=w.expo)
+    t0 = time.perf_counter()
+    oracle.prefill(ocfg, q, k, v, g, threads=cores)
+    dt = time.perf_counter() - t0
+    layer_tokens = w.N * q.shape[0] / w.H
+    return dict(value=layer_tokens / dt, unit=UNIT, cores=min(cores, q.shape[0]), kind="oracle",
+                sample=f"{q.shape[0]} of {w.B * w.H} (batch, head) rows x {w.N} tokens of "
+                       f"{w.name}, one row per thread, {dt:.1f} s wall")
+
+
+# ------------------------------------------------------------------ ours
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from compressed_kv_state_gb300 import kvm
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    q, k, v, g = wl.prefill_inputs(W)
+    dq = torch.from_numpy(q).to(dev).bfloat16()
+    dk = torch.from_numpy(k).to(dev).bfloat16()
+    dv = torch.from_numpy(v).to(dev).bfloat16()
+    dg = torch.from_numpy(g).to(dev)
+    cfg = kvm.make_config(batch=W.B, heads=W.H, rope_dims=W.rope_dims, chunk=W.chunk,
+                          window=W.window, n_sinks=W.n_sinks, sched=W.sched,
+                          max_slots=W.max_slots, max_tokens=W.N)
+    layer = kvm.KvmLayer(cfg, device=dev)
+    out = torch.empty_like(dq)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kvm.kvm_prefill(layer.handle, dq, dk, dv, dg, W.N, out, stream)
+
+    for _ in range(args.warmup):
+        step()
+    layer.sync()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    kvm.kvm_layer_set_timing(layer.handle, True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = ev0.elapsed_time(ev1)
+    tm = kvm.kvm_layer_get_timing(layer.handle)
+    kvm.kvm_layer_set_timing(layer.handle, False)
+    layer.sync()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = world * W.B * W.N / (ms_step / 1e3)
+
+    # end to end through the C ABI: pinned host inputs in, output back to host
+    hq = torch.from_numpy(q).bfloat16().pin_memory()
+    hk = torch.from_numpy(k).bfloat16().pin_memory()
+    hv = torch.from_numpy(v).bfloat16().pin_memory()
+    hg = torch.from_numpy(g).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        dg.copy_(hg, non_blocking=True)
+        kvm.kvm_prefill(layer.handle, dq, dk, dv, dg, W.N, out, stream)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    ke2e = max(3, args.steps // 2)
+    for _ in range(ke2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1) / ke2e
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
+    d2h = hout.numel() * hout.element_size()
+
+    decode = None if args.no_decode else run_decode(dev, stream)
+    clk = clocks.stop()
+
+    peaks = _peaks()
+    aw = attention_work(W)
+    ffl = fold_work(W)
+    attn_ms = tm["attn_ms"] / max(1, tm["attn_launches"])
+    fold_ms = tm["fold_ms"] / max(1, tm["fold_launches"])
+    other_ms = tm["other_ms"] / max(1, tm["other_launches"])
+    attn_tf = aw["flops"] / (attn_ms / 1e3) / 1e12
+    fold_tf = ffl / (fold_ms / 1e3) / 1e12
+    kernels = {
+        "attention": dict(ms_per_launch=attn_ms, tflops=attn_tf, flops_per_launch=aw["flops"],
+                          share=tm["attn_ms"] / max(1e-9, tm["attn_ms"] + tm["fold_ms"] + tm["other_ms"])),
+        "fold_chain": dict(ms_per_launch=fold_ms, tflops=fold_tf, flops_per_launch=ffl,
+                           share=tm["fold_ms"] / max(1e-9, tm["attn_ms"] + tm["fold_ms"] + tm["other_ms"])),
+        "ring_fill": dict(ms_per_launch=other_ms),
+    }
+    dom = "attention" if tm["attn_ms"] >= tm["fold_ms"] else "fold_chain"
+    dom_src = os.path.join(ROOT, "compressed_kv_state_gb300", "csrc",
+                           "kvm_attn_simt.cu" if dom == "attention" else "kvm_fold.cu")
+    ach = kernels[dom]["tflops"]
+    roofline = dict(kernel=dom, bound="tensor", achieved=ach, peak=peaks["bf16"], unit="TFLOP/s",
+                    frac=ach / peaks["bf16"], peak_source=f"{peaks['src']} bf16 burst",
+                    traffic=_ncu_traffic(dom_src))
+    launches = tm["attn_launches"] + tm["fold_launches"] + tm["other_launches"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": W.name, "batch": W.B, "heads": W.H, "seq_len": W.N,
+                   "head_dim": W.d, "chunk": W.chunk, "window": W.window,
+                   "slots": W.max_slots, "sinks": W.n_sinks, "rope_dims": W.rope_dims,
+                   "keys": "5% repeated keys", "l2": "inputs larger than L2 (302 MB), no flush",
+                   "parallelism": f"rows (batch x head) independent, {world} replica(s)"},
+        "roofline": roofline,
+        "kernels": kernels,
+        "algorithmic_flops_per_step": {"attention": aw["flops"], "attention_4d_count": aw["flops_4d"],
+                                       "fold_similarity": ffl},
+        "e2e": {"value": W.B * W.N / (ms_e2e / 1e3), "unit": UNIT, "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "decode": decode,
+    }
+    return line
+
+
+def run_decode(dev, stream):
+    """Decode sweep: 128 steps from a chunk boundary with an imported state of
+    n = 256, 512, 1024 slots (B=64, H=16, window 512, bf16)."""
+    import torch
+    from compressed_kv_state_gb300 import kvm
+    peaks = _peaks()
+    res = {}
+    for n, dw in wl.DECODE.items():
+        state, (wk, wv, wg), (q, k, v, g) = wl.decode_inputs(dw)
+        cfg = kvm.make_config(batch=dw.B, heads=dw.H, rope_dims=dw.rope_dims, chunk=dw.chunk,
+                              window=dw.window, n_sinks=dw.n_sinks, sched=kvm.KVM_SCHED_FIXED,
+                              max_slots=n, max_tokens=dw.pos0 + dw.steps)
+        layer = kvm.KvmLayer(cfg, device=dev)
+        L = dw.window + dw.chunk
+        idx = (dw.pos0 - L + np.arange(L)) % L
+        bufs = layer.state_buffers(dev)
+        bufs["sum_k"][:, :, :n] = torch.from_numpy(state["sum_k"]).to(dev)
+        bufs["sum_v"][:, :, :n] = torch.from_numpy(state["sum_v"]).to(dev)
+        bufs["counts"][:, :, :n] = torch.from_numpy(state["counts"]).to(dev)
+        bufs["rho"][:, :, :n] = torch.from_numpy(state["rho"]).to(dev)
+        rk = np.zeros_like(wk); rv = np.zeros_like(wv); rg = np.zeros_like(wg)
+        rk[:, :, idx], rv[:, :, idx], rg[:, :, idx] = wk, wv, wg
+        bufs["ring_k"].copy_(torch.from_numpy(rk).bfloat16())
+        bufs["ring_v"].copy_(torch.from_numpy(rv).bfloat16())
+        bufs["ring_g"].copy_(torch.from_numpy(rg))
+        bufs.update(n_slots=n, n_overflow=state["t"], pos=dw.pos0)
+        dq = torch.from_numpy(q).to(dev).bfloat16()
+        dk = torch.from_numpy(k).to(dev).bfloat16()
+        dv = torch.from_numpy(v).to(dev).bfloat16()
+        dg = torch.from_numpy(g).to(dev)
+        out = torch.empty(dw.B, dw.H, dw.d, dtype=torch.bfloat16, device=dev)
+        times = []
+        for rep in range(2):  # first pass warms up; second is timed
+            layer.import_state(bufs)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(dw.steps + 1)]
+            evs[0].record(stream)
+            for s in range(dw.steps):
+                kvm.kvm_decode_step(layer.handle, dq[s], dk[s], dv[s], dg[s], out, stream)
+                evs[s + 1].record(stream)
+            torch.cuda.synchronize(dev)
+            times = [evs[s].elapsed_time(evs[s + 1]) * 1e3 for s in range(dw.steps)]
+        layer.sync()
+        nb = times[1:]
+        med = statistics.median(nb)
+        mid = 1 + int(np.argsort(nb)[len(nb) // 2])
+        byt = decode_bytes(dw, mid, n)
+        res[f"n{n}"] = dict(boundary_us=times[0], median_us=med, mean_us=float(np.mean(times)),
+                            hbm_frac=byt / (med * 1e-6) / (peaks["hbm"] * 1e9),
+                            bytes_median_step=byt, peak_gbs=peaks["hbm"])
+        layer.close()
+    return res
+
+
+# ------------------------------------------------------------- reference
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores: each step is a bounded sample
+    of the same workload (one full-length row per core)."""
+    for _ in range(args.warmup):
+        cpu_oracle_sample(W)
+    vals, walls = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(W)
+        vals.append(r["value"])
+    wall = time.perf_counter() - t0
+    tokens_per_step = W.N * r["cores"] / W.H
+    value = tokens_per_step * args.steps / wall
+    cb = dict(value=value, unit=UNIT, cores=r["cores"], kind="oracle", sample=r["sample"])
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": W.name, "batch": W.B, "heads": W.H,
+                                            "seq_len": W.N},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu:
+            line["cpu_baseline"] = cpu_oracle_sample(W)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

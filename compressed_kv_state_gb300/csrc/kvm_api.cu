@@ -1,0 +1,560 @@
+// Host side of the C ABI declared in include/kvm.h: argument validation,
+// workspace layout, the data-independent growth schedule, RoPE tables and
+// kernel launches.  Nothing here touches tensor data on the host.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/kvm.h"
+#include "kvm_internal.cuh"
+
+using kvm::D;
+using kvm::Sched;
+
+namespace {
+
+thread_local std::string g_err = "no error";
+
+constexpr size_t ALIGN = 256;
+size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
+
+struct Layout {
+    size_t sum_k, sum_v, counts, rho, simdir, view_k, view_v;
+    size_t ring_k, ring_v, ring_g, snap_k, snap_v, rope, sched, status, total;
+};
+
+int64_t n_events_for(const kvm_config& c, int64_t N) {
+    const int64_t nchunks = (N + c.chunk - 1) / c.chunk;
+    const int64_t e = nchunks - c.window / c.chunk - 1;
+    return e > 0 ? e : 0;
+}
+
+// Capacity after t overflowed tokens ("Key-Value Means", technical summary,
+// Core mechanism 3: fixed-size or power-law growth), in double precision.
+int64_t capacity(const kvm_config& c, int64_t t) {
+    if (c.sched == KVM_SCHED_FIXED) return c.max_slots;
+    if (t <= 0) return c.n_sinks;
+    return (int64_t)c.n_sinks + (int64_t)std::ceil((double)c.coef * std::pow((double)t, (double)c.expo));
+}
+
+// One fold event's slot bookkeeping from the slot count n and overflow count t before it.
+Sched event_sched(const kvm_config& c, int64_t first_pos, int64_t n, int64_t t) {
+    Sched s;
+    int64_t sinks = 0;
+    for (int64_t i = 0; i < c.chunk; ++i) sinks += (first_pos + i < c.n_sinks);
+    const int64_t n0 = n + sinks;
+    const int64_t ncand = c.chunk - sinks;
+    int64_t a = capacity(c, t + c.chunk) - n0;
+    if (a < 0) a = 0;
+    if (a > ncand) a = ncand;
+    s.n_before = (int)n;
+    s.n0 = (int)n0;
+    s.a = (int)a;
+    s.n_after = (int)(n0 + a);
+    return s;
+}
+
+bool validate(const kvm_config* c, std::string& why) {
+    if (!c) { why = "config is NULL"; return false; }
+    if (c->batch < 1 || c->heads < 1) { why = "batch and heads must be >= 1"; return false; }
+    if (c->head_dim != D) { why = "head_dim must be 64 in this build"; return false; }
+    if (c->rope_dims < 0 || c->rope_dims > c->head_dim || (c->rope_dims & 1)) {
+        why = "rope_dims must be even and in [0, head_dim]"; return false;
+    }
+    if (!(c->rope_theta > 0.0f)) { why = "rope_theta must be > 0"; return false; }
+    if (c->chunk < 16 || c->chunk > 256 || c->chunk % 16) {
+        why = "chunk must be a multiple of 16 in [16, 256]"; return false;
+    }
+    if (c->window < 0 || c->window % c->chunk) { why = "window must be a non-negative multiple of chunk"; return false; }
+    if (c->n_sinks < 0 || c->n_sinks > c->chunk) { why = "n_sinks must be in [0, chunk]"; return false; }
+    if (c->max_slots < c->n_sinks + 1 || c->max_slots > 4096) {
+        why = "max_slots must be in [n_sinks + 1, 4096]"; return false;
+    }
+    if (c->sched != KVM_SCHED_FIXED && c->sched != KVM_SCHED_POWER) { why = "unknown schedule"; return false; }
+    if (c->sched == KVM_SCHED_POWER && (!(c->coef > 0.0f) || !(c->expo > 0.0f) || c->expo > 1.0f)) {
+        why = "power schedule needs coef > 0 and 0 < expo <= 1"; return false;
+    }
+    if (!(c->ln_eps > 0.0f)) { why = "ln_eps must be > 0"; return false; }
+    if (c->dtype != KVM_BF16 && c->dtype != KVM_FP32) { why = "unknown dtype"; return false; }
+    if (c->max_tokens < 1 || c->max_tokens > (1 << 22)) { why = "max_tokens must be in [1, 2^22]"; return false; }
+    return true;
+}
+
+Layout layout_of(const kvm_config& c) {
+    Layout L;
+    const size_t BH = (size_t)c.batch * c.heads, M = c.max_slots, d = D;
+    const size_t es = c.dtype == KVM_BF16 ? 2 : 4;
+    const size_t ring = (size_t)c.window + c.chunk;
+    const size_t E = (size_t)n_events_for(c, c.max_tokens);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes); return at; };
+    L.sum_k = take(BH * M * d * 4);
+    L.sum_v = take(BH * M * d * 4);
+    L.counts = take(BH * M * 4);
+    L.rho = take(BH * M * 4);
+    L.simdir = take(BH * M * d * 4);
+    L.view_k = take(BH * M * d * es);
+    L.view_v = take(BH * M * d * es);
+    L.ring_k = take(BH * ring * d * es);
+    L.ring_v = take(BH * ring * d * es);
+    L.ring_g = take(BH * ring * 4);
+    L.snap_k = take(BH * E * M * d * es);
+    L.snap_v = take(BH * E * M * d * es);
+    L.rope = take((size_t)c.max_tokens * (c.rope_dims / 2) * sizeof(float2) + 16);
+    L.sched = take((E + 1) * sizeof(Sched));
+    L.status = take(16);
+    L.total = o;
+    return L;
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        cudaGetDevice(&prev);
+        if (prev != dev) cudaSetDevice(dev);
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (prev >= 0 && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+struct kvm_layer {
+    kvm_config cfg;
+    char* ws;
+    size_t ws_bytes;
+    Layout L;
+    int device;
+    int64_t n_slots, n_overflow, pos;
+    int64_t E_max;
+    std::vector<Sched> sched;  // prefill-from-empty schedule (host copy)
+    cudaStream_t last_stream;
+    std::string err;
+    // optional per-kernel timing (kvm_layer_set_timing)
+    struct Timed { int phase; cudaEvent_t a, b; };
+    bool timing = false;
+    std::vector<Timed> pool;
+    size_t used = 0;
+    double acc_ms[4] = {0, 0, 0, 0};
+    int64_t acc_n[4] = {0, 0, 0, 0};
+    ~kvm_layer() {
+        for (auto& t : pool) {
+            cudaEventDestroy(t.a);
+            cudaEventDestroy(t.b);
+        }
+    }
+
+    template <typename P> P* at(size_t off) const { return reinterpret_cast<P*>(ws + off); }
+    kvm_status fail(kvm_status st, const std::string& why) {
+        err = why;
+        return st;
+    }
+    kvm_status cuda_fail(cudaError_t e, const char* where) {
+        err = std::string(where) + ": " + cudaGetErrorString(e);
+        return KVM_ERR_CUDA;
+    }
+};
+
+enum { PH_FOLD = 0, PH_ATTN = 1, PH_DECODE = 2, PH_OTHER = 3 };
+
+// Launch through f(), bracketed by timing events on s when timing is on.
+template <class F>
+static cudaError_t timed(kvm_layer* ly, int phase, cudaStream_t s, F&& f) {
+    if (!ly->timing) return f();
+    if (ly->used == ly->pool.size()) {
+        kvm_layer::Timed t{phase, nullptr, nullptr};
+        cudaError_t e = cudaEventCreate(&t.a);
+        if (e == cudaSuccess) e = cudaEventCreate(&t.b);
+        if (e != cudaSuccess) return e;
+        ly->pool.push_back(t);
+    }
+    kvm_layer::Timed& t = ly->pool[ly->used++];
+    t.phase = phase;
+    cudaEventRecord(t.a, s);
+    cudaError_t e = f();
+    cudaEventRecord(t.b, s);
+    return e;
+}
+
+extern "C" {
+
+size_t kvm_workspace_bytes(const kvm_config* cfg) {
+    std::string why;
+    if (!validate(cfg, why)) {
+        g_err = why;
+        return 0;
+    }
+    return layout_of(*cfg).total;
+}
+
+kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t bytes, kvm_layer** out) {
+    std::string why;
+    if (!out) { g_err = "out is NULL"; return KVM_ERR_INVALID_ARG; }
+    *out = nullptr;
+    if (!validate(cfg, why)) { g_err = why; return KVM_ERR_INVALID_ARG; }
+    const Layout L = layout_of(*cfg);
+    if (!dev_workspace || bytes < L.total) { g_err = "workspace missing or smaller than kvm_workspace_bytes"; return KVM_ERR_WORKSPACE; }
+    if (reinterpret_cast<uintptr_t>(dev_workspace) % ALIGN) { g_err = "workspace must be 256-byte aligned"; return KVM_ERR_WORKSPACE; }
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, dev_workspace);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
+        cudaGetLastError();
+        g_err = "workspace is not device memory";
+        return KVM_ERR_WORKSPACE;
+    }
+    kvm_layer* ly = new kvm_layer();
+    ly->cfg = *cfg;
+    ly->ws = static_cast<char*>(dev_workspace);
+    ly->ws_bytes = bytes;
+    ly->L = L;
+    ly->device = attr.device;
+    ly->n_slots = ly->n_overflow = ly->pos = 0;
+    ly->E_max = n_events_for(*cfg, cfg->max_tokens);
+    ly->last_stream = nullptr;
+    DeviceGuard g(ly->device);
+    // growth schedule of a prefill from the empty state
+    ly->sched.resize((size_t)ly->E_max + 1);
+    int64_t n = 0, t = 0;
+    for (int64_t ev = 0; ev < ly->E_max; ++ev) {
+        ly->sched[ev] = event_sched(*cfg, ev * cfg->chunk, n, t);
+        n = ly->sched[ev].n_after;
+        t += cfg->chunk;
+    }
+    // RoPE table: angle p * theta^(-2i/r) for pair i, computed in double
+    const int half = cfg->rope_dims / 2;
+    std::vector<float2> rope((size_t)cfg->max_tokens * half + 2);
+    for (int64_t p = 0; p < cfg->max_tokens; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double f = std::pow((double)cfg->rope_theta, -2.0 * i / (double)cfg->rope_dims);
+            const double ang = (double)p * f;
+            rope[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    e = cudaMemcpy(ly->ws + L.rope, rope.data(), (size_t)cfg->max_tokens * half * sizeof(float2),
+                   cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(ly->ws + L.sched, ly->sched.data(), ly->sched.size() * sizeof(Sched),
+                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(ly->ws + L.status, 0, 16);
+    if (e == cudaSuccess) e = cudaMemset(ly->ws + L.counts, 0, L.rho - L.counts);
+    if (e != cudaSuccess) {
+        g_err = std::string("kvm_layer_create: ") + cudaGetErrorString(e);
+        delete ly;
+        return KVM_ERR_CUDA;
+    }
+    *out = ly;
+    return KVM_OK;
+}
+
+kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* v, const float* gate,
+                       int64_t n_tokens, void* out, void* cuda_stream, const kvm_debug* dbg) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    const kvm_config& c = ly->cfg;
+    if (n_tokens < 0 || n_tokens > c.max_tokens)
+        return ly->fail(KVM_ERR_INVALID_ARG, "n_tokens must be in [0, max_tokens]");
+    if (n_tokens > 0 && (!q || !k || !v || !gate || !out))
+        return ly->fail(KVM_ERR_INVALID_ARG, "q, k, v, gate and out must be non-NULL");
+    const int64_t E = n_events_for(c, n_tokens);
+    if (E > 0 && ly->sched[E - 1].n_after > c.max_slots)
+        return ly->fail(KVM_ERR_CAPACITY, "growth schedule exceeds max_slots for this n_tokens");
+    if (dbg && dbg->max_events < 0) return ly->fail(KVM_ERR_INVALID_ARG, "dbg->max_events < 0");
+    DeviceGuard g(ly->device);
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    ly->last_stream = s;
+    const bool bf16 = c.dtype == KVM_BF16;
+    const int BH = c.batch * c.heads;
+    const Layout& L = ly->L;
+    cudaError_t e = cudaSuccess;
+
+    if (E > 0) {
+        kvm::FoldArgs fa{};
+        fa.sum_k = ly->at<float>(L.sum_k);
+        fa.sum_v = ly->at<float>(L.sum_v);
+        fa.counts = ly->at<int>(L.counts);
+        fa.rho = ly->at<float>(L.rho);
+        fa.simdir = ly->at<float>(L.simdir);
+        fa.view_k = ly->ws + L.view_k;
+        fa.view_v = ly->ws + L.view_v;
+        fa.M = c.max_slots;
+        fa.C = c.chunk;
+        fa.S = c.n_sinks;
+        fa.r = c.rope_dims;
+        fa.ln_eps = c.ln_eps;
+        fa.k_src = k;
+        fa.v_src = v;
+        fa.g_src = gate;
+        fa.src_row = n_tokens;
+        fa.src_len = INT64_MAX / 4;
+        fa.e_begin = 0;
+        fa.e_end = (int)E;
+        fa.sched = ly->at<Sched>(L.sched);
+        fa.snap_k = ly->ws + L.snap_k;
+        fa.snap_v = ly->ws + L.snap_v;
+        fa.snap_events = (int)ly->E_max;
+        if (dbg) {
+            fa.dbg_assign = dbg->assign;
+            fa.dbg_kind = dbg->kind;
+            fa.dbg_m = dbg->max_sim;
+            fa.dbg_gap = dbg->gap;
+            fa.dbg_events = (int)(dbg->max_events < E ? dbg->max_events : E);
+        }
+        fa.status = ly->at<int>(L.status);
+        fa.BH = BH;
+        e = timed(ly, PH_FOLD, s, [&] { return kvm::launch_fold(fa, bf16, s); });
+        if (e != cudaSuccess) return ly->cuda_fail(e, "fold chain launch");
+    }
+    if (n_tokens > 0) {
+        kvm::AttnArgs aa{};
+        aa.q = q;
+        aa.k = k;
+        aa.v = v;
+        aa.out = out;
+        aa.N = n_tokens;
+        aa.C = c.chunk;
+        aa.W = c.window;
+        aa.snap_k = ly->ws + L.snap_k;
+        aa.snap_v = ly->ws + L.snap_v;
+        aa.snap_events = (int)ly->E_max;
+        aa.M = c.max_slots;
+        aa.sched = ly->at<Sched>(L.sched);
+        aa.rope = ly->at<float2>(L.rope);
+        aa.r = c.rope_dims;
+        aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+        aa.BH = BH;
+        e = timed(ly, PH_ATTN, s, [&] { return kvm::launch_attn(aa, bf16, s); });
+        if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
+
+        kvm::RingFillArgs ra{};
+        ra.k = k;
+        ra.v = v;
+        ra.g = gate;
+        ra.ring_k = ly->ws + L.ring_k;
+        ra.ring_v = ly->ws + L.ring_v;
+        ra.ring_g = ly->at<float>(L.ring_g);
+        ra.N = n_tokens;
+        ra.first = E * c.chunk;
+        ra.L = c.window + c.chunk;
+        ra.BH = BH;
+        e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_ring_fill(ra, bf16, s); });
+        if (e != cudaSuccess) return ly->cuda_fail(e, "ring fill launch");
+    }
+    ly->n_slots = E > 0 ? ly->sched[E - 1].n_after : 0;
+    ly->n_overflow = E * c.chunk;
+    ly->pos = n_tokens;
+    return KVM_OK;
+}
+
+kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const void* v, const float* gate,
+                           void* out, void* cuda_stream) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    const kvm_config& c = ly->cfg;
+    if (!q || !k || !v || !gate || !out)
+        return ly->fail(KVM_ERR_INVALID_ARG, "q, k, v, gate and out must be non-NULL");
+    const int64_t p = ly->pos;
+    if (p >= c.max_tokens) return ly->fail(KVM_ERR_CAPACITY, "position reached max_tokens");
+    DeviceGuard g(ly->device);
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    ly->last_stream = s;
+    const bool bf16 = c.dtype == KVM_BF16;
+    const int BH = c.batch * c.heads;
+    const Layout& L = ly->L;
+    const int L_ring = c.window + c.chunk;
+    const int64_t ch = p / c.chunk, Wc = c.window / c.chunk;
+    int64_t n = ly->n_slots, t = ly->n_overflow;
+    const bool fold = (p % c.chunk == 0) && ch >= Wc + 1;
+    Sched sc{};
+    if (fold) {
+        const int64_t ev = ch - Wc - 1;
+        sc = event_sched(c, ev * c.chunk, n, t);
+        if (sc.n_after > c.max_slots) return ly->fail(KVM_ERR_CAPACITY, "growth schedule exceeds max_slots");
+        kvm::FoldArgs fa{};
+        fa.sum_k = ly->at<float>(L.sum_k);
+        fa.sum_v = ly->at<float>(L.sum_v);
+        fa.counts = ly->at<int>(L.counts);
+        fa.rho = ly->at<float>(L.rho);
+        fa.simdir = ly->at<float>(L.simdir);
+        fa.view_k = ly->ws + L.view_k;
+        fa.view_v = ly->ws + L.view_v;
+        fa.M = c.max_slots;
+        fa.C = c.chunk;
+        fa.S = c.n_sinks;
+        fa.r = c.rope_dims;
+        fa.ln_eps = c.ln_eps;
+        fa.k_src = ly->ws + L.ring_k;
+        fa.v_src = ly->ws + L.ring_v;
+        fa.g_src = ly->at<float>(L.ring_g);
+        fa.src_row = L_ring;
+        fa.src_len = L_ring;
+        fa.e_begin = (int)ev;
+        fa.e_end = (int)ev + 1;
+        fa.sched = nullptr;
+        fa.sched0 = sc;
+        fa.status = ly->at<int>(L.status);
+        fa.BH = BH;
+        cudaError_t e = timed(ly, PH_FOLD, s, [&] { return kvm::launch_fold(fa, bf16, s); });
+        if (e != cudaSuccess) return ly->cuda_fail(e, "decode fold launch");
+        n = sc.n_after;
+        t += c.chunk;
+    }
+    kvm::DecodeArgs da{};
+    da.q = q;
+    da.k = k;
+    da.v = v;
+    da.g = gate;
+    da.out = out;
+    da.ring_k = ly->ws + L.ring_k;
+    da.ring_v = ly->ws + L.ring_v;
+    da.ring_g = ly->at<float>(L.ring_g);
+    da.view_k = ly->ws + L.view_k;
+    da.view_v = ly->ws + L.view_v;
+    da.M = c.max_slots;
+    da.n_slots = (int)n;
+    da.C = c.chunk;
+    da.W = c.window;
+    da.pos = p;
+    da.rope = ly->at<float2>(L.rope);
+    da.r = c.rope_dims;
+    da.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    da.BH = BH;
+    cudaError_t e = timed(ly, PH_DECODE, s, [&] { return kvm::launch_decode(da, bf16, s); });
+    if (e != cudaSuccess) return ly->cuda_fail(e, "decode launch");
+    ly->n_slots = n;
+    ly->n_overflow = t;
+    ly->pos = p + 1;
+    return KVM_OK;
+}
+
+static kvm_status copy_state(kvm_layer* ly, kvm_state_bufs* ext, bool to_ext, cudaStream_t s) {
+    const kvm_config& c = ly->cfg;
+    const Layout& L = ly->L;
+    const size_t BH = (size_t)c.batch * c.heads, M = c.max_slots;
+    const size_t es = c.dtype == KVM_BF16 ? 2 : 4;
+    const size_t ring = (size_t)c.window + c.chunk;
+    struct Item { void* ext; size_t off; size_t bytes; } items[] = {
+        {ext->sum_k, L.sum_k, BH * M * D * 4}, {ext->sum_v, L.sum_v, BH * M * D * 4},
+        {ext->counts, L.counts, BH * M * 4},   {ext->rho, L.rho, BH * M * 4},
+        {ext->ring_k, L.ring_k, BH * ring * D * es}, {ext->ring_v, L.ring_v, BH * ring * D * es},
+        {ext->ring_g, L.ring_g, BH * ring * 4},
+    };
+    for (auto& it : items) {
+        if (!it.ext) return ly->fail(KVM_ERR_INVALID_ARG, "state buffer pointer is NULL");
+    }
+    for (auto& it : items) {
+        cudaError_t e = to_ext ? cudaMemcpyAsync(it.ext, ly->ws + it.off, it.bytes, cudaMemcpyDeviceToDevice, s)
+                               : cudaMemcpyAsync(ly->ws + it.off, it.ext, it.bytes, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return ly->cuda_fail(e, "state copy");
+    }
+    return KVM_OK;
+}
+
+kvm_status kvm_state_export(const kvm_layer* cly, kvm_state_bufs* dst, void* cuda_stream) {
+    kvm_layer* ly = const_cast<kvm_layer*>(cly);
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    if (!dst) return ly->fail(KVM_ERR_INVALID_ARG, "dst is NULL");
+    DeviceGuard g(ly->device);
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    ly->last_stream = s;
+    kvm_status st = copy_state(ly, dst, true, s);
+    if (st != KVM_OK) return st;
+    dst->n_slots = ly->n_slots;
+    dst->n_overflow = ly->n_overflow;
+    dst->pos = ly->pos;
+    return KVM_OK;
+}
+
+kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda_stream) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    if (!src) return ly->fail(KVM_ERR_INVALID_ARG, "src is NULL");
+    const kvm_config& c = ly->cfg;
+    if (src->n_slots < 0 || src->n_slots > c.max_slots) return ly->fail(KVM_ERR_INVALID_ARG, "n_slots out of range");
+    if (src->pos < 0 || src->pos > c.max_tokens) return ly->fail(KVM_ERR_INVALID_ARG, "pos out of range");
+    if (src->n_overflow < 0 || src->n_overflow > src->pos) return ly->fail(KVM_ERR_INVALID_ARG, "n_overflow out of range");
+    DeviceGuard g(ly->device);
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    ly->last_stream = s;
+    kvm_state_bufs tmp = *src;
+    kvm_status st = copy_state(ly, &tmp, false, s);
+    if (st != KVM_OK) return st;
+    kvm::RenormArgs ra{};
+    const Layout& L = ly->L;
+    ra.sum_k = ly->at<float>(L.sum_k);
+    ra.sum_v = ly->at<float>(L.sum_v);
+    ra.counts = ly->at<int>(L.counts);
+    ra.rho = ly->at<float>(L.rho);
+    ra.simdir = ly->at<float>(L.simdir);
+    ra.view_k = ly->ws + L.view_k;
+    ra.view_v = ly->ws + L.view_v;
+    ra.M = c.max_slots;
+    ra.n = (int)src->n_slots;
+    ra.r = c.rope_dims;
+    ra.ln_eps = c.ln_eps;
+    ra.BH = c.batch * c.heads;
+    cudaError_t e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_renorm(ra, c.dtype == KVM_BF16, s); });
+    if (e != cudaSuccess) return ly->cuda_fail(e, "renormalise launch");
+    ly->n_slots = src->n_slots;
+    ly->n_overflow = src->n_overflow;
+    ly->pos = src->pos;
+    return KVM_OK;
+}
+
+kvm_status kvm_layer_sync(kvm_layer* ly) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    DeviceGuard g(ly->device);
+    cudaError_t e = cudaStreamSynchronize(ly->last_stream);
+    if (e != cudaSuccess) return ly->cuda_fail(e, "stream synchronise");
+    int status = 0;
+    e = cudaMemcpy(&status, ly->ws + ly->L.status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return ly->cuda_fail(e, "status read");
+    if (status) {
+        cudaMemset(ly->ws + ly->L.status, 0, sizeof(int));
+        if (status & kvm::STATUS_TIMEOUT) return ly->fail(KVM_ERR_TIMEOUT, "a bounded device-side wait expired");
+        return ly->fail(KVM_ERR_DEVICE, "a device-side consistency check failed");
+    }
+    return KVM_OK;
+}
+
+kvm_status kvm_layer_set_timing(kvm_layer* ly, int enable) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    ly->timing = enable != 0;
+    ly->used = 0;
+    for (int i = 0; i < 4; ++i) {
+        ly->acc_ms[i] = 0.0;
+        ly->acc_n[i] = 0;
+    }
+    return KVM_OK;
+}
+
+kvm_status kvm_layer_get_timing(kvm_layer* ly, kvm_timing* out) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    if (!out) return ly->fail(KVM_ERR_INVALID_ARG, "out is NULL");
+    DeviceGuard g(ly->device);
+    for (size_t i = 0; i < ly->used; ++i) {
+        auto& t = ly->pool[i];
+        cudaError_t e = cudaEventSynchronize(t.b);
+        float ms = 0.0f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.a, t.b);
+        if (e != cudaSuccess) return ly->cuda_fail(e, "timing events");
+        ly->acc_ms[t.phase] += ms;
+        ly->acc_n[t.phase] += 1;
+    }
+    ly->used = 0;
+    out->fold_ms = ly->acc_ms[PH_FOLD];
+    out->attn_ms = ly->acc_ms[PH_ATTN];
+    out->decode_ms = ly->acc_ms[PH_DECODE];
+    out->other_ms = ly->acc_ms[PH_OTHER];
+    out->fold_launches = ly->acc_n[PH_FOLD];
+    out->attn_launches = ly->acc_n[PH_ATTN];
+    out->decode_launches = ly->acc_n[PH_DECODE];
+    out->other_launches = ly->acc_n[PH_OTHER];
+    return KVM_OK;
+}
+
+const char* kvm_last_error(const kvm_layer* ly) { return ly ? ly->err.c_str() : g_err.c_str(); }
+
+void kvm_layer_destroy(kvm_layer* ly) { delete ly; }
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// Portable KVM attention for the prefill: one query per thread, fp32 math.
+//
+// "Key-Value Means" (gist.science technical summary), Methodology and Core
+// mechanism 4: one softmax over the compressed state (state keys zero on the
+// rotary dims, read by the unrotated query) and the block-sliding window
+// (RoPE on query and keys).  Query p of chunk c sees the state as it stands
+// after chunk c - W/C - 1 was folded and the window tokens (c - W/C)*C .. p.
+//
+// This kernel serves the fp32 dtype and every shape the tensor-core kernel
+// does not cover.  Because the key view is exactly zero on dims [0, r), the
+// rotated query gives the same state scores as the unrotated one, so one
+// rotated query register file serves both parts.
+#include "kvm_internal.cuh"
+
+namespace kvm {
+
+constexpr int KT = 32;  // keys per shared-memory tile
+
+template <typename T>
+__global__ void __launch_bounds__(64) attn_simt_kernel(AttnArgs a, int QB) {
+    __shared__ float ks[KT][D];
+    __shared__ float vs[KT][D];
+    const int bh = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int64_t p0 = (int64_t)blockIdx.x * QB;
+    const int64_t p = p0 + tid;
+    const bool valid = p < a.N;
+    const int64_t c = p0 / a.C;
+    const int64_t Wc = a.W / a.C;
+    const int64_t e = c - Wc - 1;  // last event folded before chunk c
+    const int n = e >= 0 ? a.sched[e].n_after : 0;
+    const int64_t ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
+    const int64_t kend = min(a.N, p0 + QB);
+    const int half = a.r / 2;
+
+    const T* qrow = reinterpret_cast<const T*>(a.q) + ((int64_t)bh * a.N + (valid ? p : p0)) * D;
+    const T* kb = reinterpret_cast<const T*>(a.k) + (int64_t)bh * a.N * D;
+    const T* vb = reinterpret_cast<const T*>(a.v) + (int64_t)bh * a.N * D;
+
+    float qr[D];
+#pragma unroll
+    for (int x = 0; x < D; ++x) qr[x] = to_f<T>(qrow[x]);
+    {
+        const float2* rp = a.rope + (valid ? p : p0) * half;
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) {
+            if (i < half) {
+                const float2 cs = rp[i];
+                const float x0 = qr[i], x1 = qr[i + half];
+                qr[i] = x0 * cs.x - x1 * cs.y;
+                qr[i + half] = x1 * cs.x + x0 * cs.y;
+            }
+        }
+    }
+#pragma unroll
+    for (int x = 0; x < D; ++x) qr[x] *= a.scale_log2;
+
+    float m = -INFINITY, l = 0.0f;
+    float acc[D];
+#pragma unroll
+    for (int x = 0; x < D; ++x) acc[x] = 0.0f;
+
+    auto process = [&](int cnt, int64_t key_pos0, bool causal) {
+        float s[KT];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < KT; ++jj) {
+            float d = 0.0f;
+#pragma unroll
+            for (int x = 0; x < D; ++x) d = fmaf(qr[x], ks[jj][x], d);
+            const bool ok = jj < cnt && (!causal || key_pos0 + jj <= p);
+            s[jj] = ok ? d : -INFINITY;
+            tmax = fmaxf(tmax, s[jj]);
+        }
+        if (tmax == -INFINITY) return;
+        const float mnew = fmaxf(m, tmax);
+        const float corr = exp2f(m - mnew);
+        l *= corr;
+#pragma unroll
+        for (int x = 0; x < D; ++x) acc[x] *= corr;
+#pragma unroll
+        for (int jj = 0; jj < KT; ++jj) {
+            const float pj = exp2f(s[jj] - mnew);
+            l += pj;
+#pragma unroll
+            for (int x = 0; x < D; ++x) acc[x] = fmaf(pj, vs[jj][x], acc[x]);
+        }
+        m = mnew;
+    };
+
+    // state rows (snapshot after event e)
+    if (n > 0) {
+        const T* sk = reinterpret_cast<const T*>(a.snap_k) + ((int64_t)bh * a.snap_events + e) * a.M * D;
+        const T* sv = reinterpret_cast<const T*>(a.snap_v) + ((int64_t)bh * a.snap_events + e) * a.M * D;
+        for (int j0 = 0; j0 < n; j0 += KT) {
+            const int cnt = min(KT, n - j0);
+            __syncthreads();
+            for (int i = tid; i < KT * D; i += blockDim.x) {
+                const int jj = i / D, x = i % D;
+                ks[jj][x] = jj < cnt ? to_f<T>(sk[(int64_t)(j0 + jj) * D + x]) : 0.0f;
+                vs[jj][x] = jj < cnt ? to_f<T>(sv[(int64_t)(j0 + jj) * D + x]) : 0.0f;
+            }
+            __syncthreads();
+            process(cnt, 0, false);
+        }
+    }
+    // window keys with RoPE at their own positions, causal
+    for (int64_t k0 = ws; k0 < kend; k0 += KT) {
+        const int cnt = (int)min((int64_t)KT, kend - k0);
+        __syncthreads();
+        for (int i = tid; i < KT * D; i += blockDim.x) {
+            const int jj = i / D, x = i % D;
+            float kv = 0.0f, vv = 0.0f;
+            if (jj < cnt) {
+                const int64_t kp = k0 + jj;
+                const T* kr = kb + kp * D;
+                kv = to_f<T>(kr[x]);
+                if (x < 2 * half) {
+                    const int i2 = x < half ? x : x - half;
+                    const float2 cs = a.rope[kp * half + i2];
+                    if (x < half)
+                        kv = kv * cs.x - to_f<T>(kr[x + half]) * cs.y;
+                    else
+                        kv = kv * cs.x + to_f<T>(kr[x - half]) * cs.y;
+                }
+                vv = to_f<T>(vb[kp * D + x]);
+            }
+            ks[jj][x] = kv;
+            vs[jj][x] = vv;
+        }
+        __syncthreads();
+        process(cnt, k0, true);
+    }
+
+    if (valid) {
+        T* orow = reinterpret_cast<T*>(a.out) + ((int64_t)bh * a.N + p) * D;
+        const float il = 1.0f / l;
+#pragma unroll
+        for (int x = 0; x < D; ++x) orow[x] = from_f<T>(acc[x] * il);
+    }
+}
+
+template <typename T>
+__global__ void ring_fill_kernel(RingFillArgs a) {
+    const int bh = blockIdx.y;
+    const int64_t cnt = a.N - a.first;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < cnt * D;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tok = a.first + i / D;
+        const int x = (int)(i % D);
+        const int64_t slot = tok % a.L;
+        const int64_t src = ((int64_t)bh * a.N + tok) * D + x;
+        const int64_t dst = ((int64_t)bh * a.L + slot) * D + x;
+        reinterpret_cast<T*>(a.ring_k)[dst] = reinterpret_cast<const T*>(a.k)[src];
+        reinterpret_cast<T*>(a.ring_v)[dst] = reinterpret_cast<const T*>(a.v)[src];
+        if (x == 0) a.ring_g[(int64_t)bh * a.L + slot] = a.g[(int64_t)bh * a.N + tok];
+    }
+}
+
+cudaError_t launch_attn(const AttnArgs& a, bool bf16, cudaStream_t s) {
+    if (a.N == 0) return cudaSuccess;
+    const int QB = (a.C % 64 == 0) ? 64 : (a.C % 32 == 0 ? 32 : 16);
+    dim3 grid((unsigned)((a.N + QB - 1) / QB), (unsigned)a.BH);
+    if (bf16)
+        attn_simt_kernel<__nv_bfloat16><<<grid, QB, 0, s>>>(a, QB);
+    else
+        attn_simt_kernel<float><<<grid, QB, 0, s>>>(a, QB);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ring_fill(const RingFillArgs& a, bool bf16, cudaStream_t s) {
+    const int64_t cnt = (a.N - a.first) * D;
+    if (cnt <= 0) return cudaSuccess;
+    const int64_t nb = (cnt + 255) / 256;
+    dim3 grid((unsigned)(nb < 64 ? nb : 64), (unsigned)a.BH);
+    if (bf16)
+        ring_fill_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
+    else
+        ring_fill_kernel<float><<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvm

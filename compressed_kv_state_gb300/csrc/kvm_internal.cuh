@@ -1,0 +1,157 @@
+// Internal declarations shared by the translation units of libkvm.so.
+// Device code for sm_103a; head_dim is fixed at 64 in this build.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvm {
+
+constexpr int D = 64;  // head_dim supported by every kernel
+
+// Device status word bits (latched, read and cleared by kvm_layer_sync).
+enum : int { STATUS_TIMEOUT = 1, STATUS_DEVICE = 2 };
+
+// Per-event schedule entry, computed on the host in double precision (the
+// schedule depends only on counts of tokens, never on data).
+struct Sched {
+    int n_before;  // slots before the event
+    int n0;        // slots after this event's sink founding
+    int a;         // slots appended by this event
+    int n_after;   // slots after the event
+};
+
+// ---------------------------------------------------------------- scalars
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ------------------------------------------------------------ fold chain
+// State of every (b,h) row lives in the workspace:
+//   sum_k, sum_v [BH, M, D] fp32; counts [BH, M] int32; rho [BH, M] fp32;
+//   simdir [BH, M, D] fp32 = unit(sum_k - mean(sum_k)), the direction the
+//   winner-take-all cosine compares against (cosine against LayerNorm(x) is
+//   cosine against x - mean(x));
+//   view_k / view_v [BH, M, D] in the I/O dtype = the just-in-time read view.
+struct FoldArgs {
+    float* sum_k;
+    float* sum_v;
+    int* counts;
+    float* rho;
+    float* simdir;
+    void* view_k;
+    void* view_v;
+    int M, C, S, r;
+    float ln_eps;
+    // tokens: row bh, token i of event e sits at src + bh*src_row + ((e*C) % src_len + i)
+    const void* k_src;
+    const void* v_src;
+    const float* g_src;
+    int64_t src_row;  // tokens per (b,h) row of the source arrays
+    int64_t src_len;  // modulus of the token offset (ring length, or a huge value)
+    int e_begin, e_end;
+    const Sched* sched;  // device table indexed by event, or nullptr to use sched0
+    Sched sched0;
+    // per-event snapshots of the read view for the prefill's attention
+    void* snap_k;
+    void* snap_v;
+    int snap_events;  // events per (b,h) row in the snapshot arrays
+    // optional debug record [BH, dbg_events, C]
+    int* dbg_assign;
+    int* dbg_kind;
+    float* dbg_m;
+    float* dbg_gap;
+    int dbg_events;
+    int* status;
+    int BH;
+};
+
+// ------------------------------------------------------------- attention
+struct AttnArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    int64_t N;          // tokens per (b,h) row
+    int C, W;
+    const void* snap_k; // [BH, snap_events, M, D]
+    const void* snap_v;
+    int snap_events, M;
+    const Sched* sched; // events' slot counts (n_after)
+    const float2* rope; // [max_tokens, r/2] (cos, sin)
+    int r;
+    float scale_log2;   // log2(e) / sqrt(D)
+    int BH;
+};
+
+struct DecodeArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    void* out;
+    void* ring_k;
+    void* ring_v;
+    float* ring_g;
+    const void* view_k;
+    const void* view_v;
+    int M, n_slots, C, W;
+    int64_t pos;
+    const float2* rope;
+    int r;
+    float scale_log2;
+    int BH;
+};
+
+struct RingFillArgs {
+    const void* k;
+    const void* v;
+    const float* g;
+    void* ring_k;
+    void* ring_v;
+    float* ring_g;
+    int64_t N, first;  // copy tokens [first, N) of each row
+    int L;             // ring length W + C
+    int BH;
+};
+
+struct RenormArgs {
+    const float* sum_k;
+    const float* sum_v;
+    const int* counts;
+    const float* rho;
+    float* simdir;
+    void* view_k;
+    void* view_v;
+    int M, n, r;
+    float ln_eps;
+    int BH;
+};
+
+// Host launchers (return the launch error).
+cudaError_t launch_fold(const FoldArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_attn(const AttnArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_ring_fill(const RingFillArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_renorm(const RenormArgs& a, bool bf16, cudaStream_t s);
+
+}  // namespace kvm

@@ -1,0 +1,267 @@
+"""Thin ctypes binding of libkvm.so (include/kvm.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions keep the C names; tensors are torch CUDA tensors (torch is
+used for device memory and streams only).  There is no fallback: if the
+library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libkvm.so")
+
+KVM_OK, KVM_ERR_INVALID_ARG, KVM_ERR_UNSUPPORTED, KVM_ERR_CAPACITY = 0, 1, 2, 3
+KVM_ERR_WORKSPACE, KVM_ERR_CUDA, KVM_ERR_TIMEOUT, KVM_ERR_DEVICE = 4, 5, 6, 7
+KVM_BF16, KVM_FP32 = 0, 1
+KVM_SCHED_FIXED, KVM_SCHED_POWER = 0, 1
+STATUS_NAMES = {0: "KVM_OK", 1: "KVM_ERR_INVALID_ARG", 2: "KVM_ERR_UNSUPPORTED",
+                3: "KVM_ERR_CAPACITY", 4: "KVM_ERR_WORKSPACE", 5: "KVM_ERR_CUDA",
+                6: "KVM_ERR_TIMEOUT", 7: "KVM_ERR_DEVICE"}
+
+
+class kvm_config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("rope_dims", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("chunk", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("n_sinks", ctypes.c_int32),
+                ("sched", ctypes.c_int32), ("max_slots", ctypes.c_int32),
+                ("coef", ctypes.c_float), ("expo", ctypes.c_float),
+                ("ln_eps", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int32)]
+
+
+class kvm_state_bufs(ctypes.Structure):
+    _fields_ = [("sum_k", ctypes.c_void_p), ("sum_v", ctypes.c_void_p),
+                ("counts", ctypes.c_void_p), ("rho", ctypes.c_void_p),
+                ("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p),
+                ("ring_g", ctypes.c_void_p), ("n_slots", ctypes.c_int64),
+                ("n_overflow", ctypes.c_int64), ("pos", ctypes.c_int64)]
+
+
+class kvm_debug(ctypes.Structure):
+    _fields_ = [("assign", ctypes.c_void_p), ("kind", ctypes.c_void_p),
+                ("max_sim", ctypes.c_void_p), ("gap", ctypes.c_void_p),
+                ("max_events", ctypes.c_int64)]
+
+
+class kvm_timing(ctypes.Structure):
+    _fields_ = [("fold_ms", ctypes.c_double), ("attn_ms", ctypes.c_double),
+                ("decode_ms", ctypes.c_double), ("other_ms", ctypes.c_double),
+                ("fold_launches", ctypes.c_int64), ("attn_launches", ctypes.c_int64),
+                ("decode_launches", ctypes.c_int64), ("other_launches", ctypes.c_int64)]
+
+
+class KvmError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libkvm.so not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    lib.kvm_workspace_bytes.restype = ctypes.c_size_t
+    lib.kvm_workspace_bytes.argtypes = [P]
+    lib.kvm_layer_create.restype = ctypes.c_int
+    lib.kvm_layer_create.argtypes = [P, P, ctypes.c_size_t, ctypes.POINTER(P)]
+    lib.kvm_prefill.restype = ctypes.c_int
+    lib.kvm_prefill.argtypes = [P, P, P, P, P, I64, P, P, P]
+    lib.kvm_decode_step.restype = ctypes.c_int
+    lib.kvm_decode_step.argtypes = [P, P, P, P, P, P, P]
+    lib.kvm_state_export.restype = ctypes.c_int
+    lib.kvm_state_export.argtypes = [P, P, P]
+    lib.kvm_state_import.restype = ctypes.c_int
+    lib.kvm_state_import.argtypes = [P, P, P]
+    lib.kvm_layer_sync.restype = ctypes.c_int
+    lib.kvm_layer_sync.argtypes = [P]
+    lib.kvm_last_error.restype = ctypes.c_char_p
+    lib.kvm_last_error.argtypes = [P]
+    lib.kvm_layer_set_timing.restype = ctypes.c_int
+    lib.kvm_layer_set_timing.argtypes = [P, ctypes.c_int]
+    lib.kvm_layer_get_timing.restype = ctypes.c_int
+    lib.kvm_layer_get_timing.argtypes = [P, P]
+    lib.kvm_layer_destroy.restype = None
+    lib.kvm_layer_destroy.argtypes = [P]
+    return lib
+
+
+lib = _load()
+
+
+def _check(status: int, layer=None):
+    if status != KVM_OK:
+        raise KvmError(status, kvm_last_error(layer))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(getattr(stream, "cuda_stream", stream))
+
+
+# ------------------------------------------------------------- C entry points
+
+def kvm_workspace_bytes(cfg: kvm_config) -> int:
+    n = lib.kvm_workspace_bytes(ctypes.byref(cfg))
+    if n == 0:
+        raise KvmError(KVM_ERR_INVALID_ARG, kvm_last_error(None))
+    return int(n)
+
+
+def kvm_layer_create(cfg: kvm_config, workspace) -> ctypes.c_void_p:
+    out = ctypes.c_void_p()
+    st = lib.kvm_layer_create(ctypes.byref(cfg), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), ctypes.byref(out))
+    _check(st, None)
+    return out
+
+
+def kvm_prefill(layer, q, k, v, gate, n_tokens: int, out, stream=None, dbg: kvm_debug | None = None):
+    st = lib.kvm_prefill(layer, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), int(n_tokens), _ptr(out),
+                         _stream(stream), ctypes.byref(dbg) if dbg is not None else None)
+    _check(st, layer)
+
+
+def kvm_decode_step(layer, q, k, v, gate, out, stream=None):
+    st = lib.kvm_decode_step(layer, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out),
+                             _stream(stream))
+    _check(st, layer)
+
+
+def kvm_state_export(layer, dst: kvm_state_bufs, stream=None):
+    _check(lib.kvm_state_export(layer, ctypes.byref(dst), _stream(stream)), layer)
+
+
+def kvm_state_import(layer, src: kvm_state_bufs, stream=None):
+    _check(lib.kvm_state_import(layer, ctypes.byref(src), _stream(stream)), layer)
+
+
+def kvm_layer_sync(layer):
+    _check(lib.kvm_layer_sync(layer), layer)
+
+
+def kvm_layer_set_timing(layer, enable: bool):
+    _check(lib.kvm_layer_set_timing(layer, 1 if enable else 0), layer)
+
+
+def kvm_layer_get_timing(layer) -> dict:
+    t = kvm_timing()
+    _check(lib.kvm_layer_get_timing(layer, ctypes.byref(t)), layer)
+    return {name: getattr(t, name) for name, _ in kvm_timing._fields_}
+
+
+def kvm_last_error(layer) -> str:
+    return lib.kvm_last_error(layer).decode()
+
+
+def kvm_layer_destroy(layer):
+    lib.kvm_layer_destroy(layer)
+
+
+# --------------------------------------------------------- convenience owner
+
+def make_config(*, batch, heads, head_dim=64, rope_dims=32, rope_theta=10000.0, chunk=128,
+                window=512, n_sinks=16, sched=KVM_SCHED_FIXED, max_slots=256, coef=4.0, expo=0.5,
+                ln_eps=1e-5, dtype=KVM_BF16, max_tokens=8192) -> kvm_config:
+    return kvm_config(batch, heads, head_dim, rope_dims, rope_theta, chunk, window, n_sinks, sched,
+                      max_slots, coef, expo, ln_eps, dtype, max_tokens)
+
+
+class KvmLayer:
+    """Owns one layer handle and its device workspace (a torch uint8 tensor)."""
+
+    def __init__(self, cfg: kvm_config, device="cuda"):
+        import torch
+        self.cfg = cfg
+        self.ws = torch.empty(kvm_workspace_bytes(cfg), dtype=torch.uint8, device=device)
+        self.handle = kvm_layer_create(cfg, self.ws)
+        self.io_dtype = torch.bfloat16 if cfg.dtype == KVM_BF16 else torch.float32
+
+    def _io(self, t, shape, dtype=None):
+        import torch
+        dtype = dtype or self.io_dtype
+        if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape) or not t.is_cuda:
+            raise ValueError(f"expected contiguous CUDA {dtype} tensor of shape {shape}, got "
+                             f"{t.dtype} {tuple(t.shape)}")
+        return t
+
+    def prefill(self, q, k, v, gate, out=None, stream=None, dbg: kvm_debug | None = None):
+        import torch
+        c = self.cfg
+        N = q.shape[2]
+        shp = (c.batch, c.heads, N, c.head_dim)
+        for t in (q, k, v):
+            self._io(t, shp)
+        self._io(gate, shp[:3], torch.float32)
+        if out is None:
+            out = torch.empty(shp, dtype=self.io_dtype, device=q.device)
+        self._io(out, shp)
+        kvm_prefill(self.handle, q, k, v, gate, N, out, stream, dbg)
+        return out
+
+    def decode_step(self, q, k, v, gate, out=None, stream=None):
+        import torch
+        c = self.cfg
+        shp = (c.batch, c.heads, c.head_dim)
+        for t in (q, k, v):
+            self._io(t, shp)
+        self._io(gate, shp[:2], torch.float32)
+        if out is None:
+            out = torch.empty(shp, dtype=self.io_dtype, device=q.device)
+        self._io(out, shp)
+        kvm_decode_step(self.handle, q, k, v, gate, out, stream)
+        return out
+
+    def state_buffers(self, device="cuda"):
+        """Fresh caller-owned tensors shaped for export/import."""
+        import torch
+        c = self.cfg
+        B, H, M, d, L = c.batch, c.heads, c.max_slots, c.head_dim, c.window + c.chunk
+        return dict(sum_k=torch.zeros(B, H, M, d, device=device),
+                    sum_v=torch.zeros(B, H, M, d, device=device),
+                    counts=torch.zeros(B, H, M, dtype=torch.int32, device=device),
+                    rho=torch.zeros(B, H, M, device=device),
+                    ring_k=torch.zeros(B, H, L, d, dtype=self.io_dtype, device=device),
+                    ring_v=torch.zeros(B, H, L, d, dtype=self.io_dtype, device=device),
+                    ring_g=torch.zeros(B, H, L, device=device))
+
+    @staticmethod
+    def _bufs(t, n_slots=0, n_overflow=0, pos=0) -> kvm_state_bufs:
+        return kvm_state_bufs(t["sum_k"].data_ptr(), t["sum_v"].data_ptr(), t["counts"].data_ptr(),
+                              t["rho"].data_ptr(), t["ring_k"].data_ptr(), t["ring_v"].data_ptr(),
+                              t["ring_g"].data_ptr(), n_slots, n_overflow, pos)
+
+    def export_state(self, stream=None):
+        t = self.state_buffers(self.ws.device)
+        b = self._bufs(t)
+        kvm_state_export(self.handle, b, stream)
+        t.update(n_slots=b.n_slots, n_overflow=b.n_overflow, pos=b.pos)
+        return t
+
+    def import_state(self, t, stream=None):
+        b = self._bufs(t, t["n_slots"], t["n_overflow"], t["pos"])
+        kvm_state_import(self.handle, b, stream)
+
+    def sync(self):
+        kvm_layer_sync(self.handle)
+
+    def close(self):
+        if getattr(self, "handle", None) is not None:
+            kvm_layer_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

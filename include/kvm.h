@@ -1,0 +1,205 @@
+/*
+ * kvm.h - C ABI of libkvm.so: the chunked forward of a Key-Value Means (KVM)
+ * attention layer on one NVIDIA GB300 GPU (sm_103a).
+ *
+ * Source of the operation: "Key-Value Means" (gist.science technical
+ * summary, Methodology and Core mechanisms 1-5; chatpaper.ai abstract).
+ * A KVM layer is one softmax attention layer whose keys are
+ *   - a block-sliding window of recent tokens with RoPE on both sides
+ *     (Core mechanism 1 and 4), and
+ *   - a compressed state of slots read "just in time": key = LayerNorm of the
+ *     slot's mean key with the rotary dims zeroed, value = the slot's read
+ *     radius rho_i times the unit direction of its value sum (Core
+ *     mechanisms 2 and 4), read with the unrotated query,
+ * combined in one softmax.  Each chunk of C tokens that leaves the window is
+ * folded into the state (Core mechanism 1): the first S tokens of the
+ * sequence found protected sink slots (Core mechanism 5); the most surprising
+ * tokens (lowest best cosine to the current slots) are appended as new slots
+ * up to the growth schedule's capacity (Core mechanism 3); every other token
+ * goes to the slot whose LayerNorm'd key has the highest cosine with it (ties
+ * to the lowest slot index) and adds its gate-weighted key and value to that
+ * slot's raw sums and 1 to its count (Core mechanism 2; lay part "smart
+ * merge").
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, contiguous, row-major.
+ *     Prefill tensors are [B, H, N, d]; decode tensors are [B, H, d];
+ *     gates are fp32 [B, H, N] / [B, H].  Element type of q, k, v, out and of
+ *     the window ring is the config's dtype (bf16 or fp32).  Keys are passed
+ *     UNROTATED: the library applies RoPE itself (the state needs raw keys).
+ *   - The caller owns every buffer, including the workspace.  The layer owns
+ *     only host-side metadata.
+ *   - Calls enqueue work on the given CUDA stream (NULL = legacy default
+ *     stream) and return without synchronising.  Arguments are validated
+ *     before anything is enqueued; a call that returns an error enqueued
+ *     nothing.  Errors raised on the device are latched in a status word in
+ *     the workspace and reported by kvm_layer_sync.
+ *   - No entry point aborts the process.  kvm_last_error gives a message.
+ *   - A layer may be used from one host thread at a time.
+ */
+#ifndef KVM_H
+#define KVM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVM_OK = 0,
+    KVM_ERR_INVALID_ARG = 1,   /* bad pointer, size, shape or config value */
+    KVM_ERR_UNSUPPORTED = 2,   /* valid config this build does not implement */
+    KVM_ERR_CAPACITY = 3,      /* the growth schedule would exceed max_slots / max_tokens */
+    KVM_ERR_WORKSPACE = 4,     /* workspace too small or misaligned */
+    KVM_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+    KVM_ERR_TIMEOUT = 6,       /* a bounded device-side wait expired */
+    KVM_ERR_DEVICE = 7         /* a device-side check failed */
+} kvm_status;
+
+typedef enum { KVM_BF16 = 0, KVM_FP32 = 1 } kvm_dtype;
+
+/* Growth schedule (Core mechanism 3).  FIXED: capacity = max_slots.
+ * POWER: capacity after t overflowed tokens = n_sinks + ceil(coef * t^expo)
+ * (the "sqrt" state is expo = 0.5, coef = 4).  Capacities count sink slots. */
+typedef enum { KVM_SCHED_FIXED = 0, KVM_SCHED_POWER = 1 } kvm_sched;
+
+typedef struct {
+    int32_t batch;       /* B >= 1 */
+    int32_t heads;       /* H >= 1; one state per (batch, head) */
+    int32_t head_dim;    /* d; this build supports 64 */
+    int32_t rope_dims;   /* r: RoPE on dims [0, r), rotate-half pairs (i, i + r/2); even, 0..d */
+    float rope_theta;    /* RoPE base, e.g. 10000 */
+    int32_t chunk;       /* C: multiple of 16, 16..256 */
+    int32_t window;      /* W: multiple of C, >= 0; a query in chunk c sees chunks c-W/C..c */
+    int32_t n_sinks;     /* S: 0..C protected sink slots (the first S tokens) */
+    int32_t sched;       /* kvm_sched */
+    int32_t max_slots;   /* M: slot rows reserved per (batch, head), S+1..4096 */
+    float coef, expo;    /* POWER schedule parameters (coef > 0, 0 < expo <= 1) */
+    float ln_eps;        /* LayerNorm epsilon for the state keys, e.g. 1e-5 */
+    int32_t dtype;       /* kvm_dtype of q, k, v, out and the window ring */
+    int32_t max_tokens;  /* longest sequence the layer will see (prefill + decode) */
+} kvm_config;
+
+typedef struct kvm_layer kvm_layer;
+
+/* State of every (batch, head), for export/import (checkpoint / resume).
+ * Device buffers owned by the caller:
+ *   sum_k, sum_v : fp32 [B, H, max_slots, d] raw gate-weighted sums
+ *   counts       : int32 [B, H, max_slots]  member tokens per slot
+ *   rho          : fp32 [B, H, max_slots]   read radius per slot
+ *   ring_k, ring_v : dtype [B, H, W + C, d] unrotated window tokens; the token
+ *                  at position p sits in row p mod (W + C)
+ *   ring_g       : fp32 [B, H, W + C]        their merge gates
+ * Host scalars (identical for every (batch, head): the schedule is data
+ * independent): n_slots, n_overflow (tokens folded so far), pos (next
+ * position).  Rows >= n_slots of the slot arrays are unspecified on export
+ * and ignored on import. */
+typedef struct {
+    float* sum_k;
+    float* sum_v;
+    int32_t* counts;
+    float* rho;
+    void* ring_k;
+    void* ring_v;
+    float* ring_g;
+    int64_t n_slots;
+    int64_t n_overflow;
+    int64_t pos;
+} kvm_state_bufs;
+
+/* Optional per-fold-event record of a prefill (device buffers, may be NULL
+ * individually).  Event e folds chunk e (tokens e*C .. e*C+C-1); only events
+ * e < max_events are recorded.  Shapes [B, H, max_events, C]:
+ *   assign  : int32 slot the token went to
+ *   kind    : int32 0 merged, 1 appended as a new slot, 2 founded a sink slot
+ *   max_sim : fp32 surprise score (best cosine to the slots that existed
+ *             before this event's appends; -inf if none; NaN for sinks)
+ *   gap     : fp32 top-2 cosine gap of a merged token's argmax (+inf with a
+ *             single candidate slot; NaN for appended tokens and sinks) */
+typedef struct {
+    int32_t* assign;
+    int32_t* kind;
+    float* max_sim;
+    float* gap;
+    int64_t max_events;
+} kvm_debug;
+
+/* Bytes of device workspace a layer with this config needs (0 if the config
+ * is invalid; kvm_last_error(NULL) then says why).  Alignment: 256 bytes. */
+size_t kvm_workspace_bytes(const kvm_config* cfg);
+
+/* Validate cfg, carve the caller's workspace (device pointer, >= the size
+ * above, 256-byte aligned) and build the RoPE and schedule tables in it
+ * (synchronous copies on the legacy stream).  On success *out receives a new
+ * layer in the empty state at position 0. */
+kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t bytes,
+                            kvm_layer** out);
+
+/* Chunked prefill (Core mechanism 1; abstract: chunk-wise parallel prefill).
+ * Resets the layer to the empty state at position 0, then computes, for
+ * every (b, h) and token p < n_tokens, the KVM attention output of query p
+ * into out, folding chunk c - W/C - 1 into the state before chunk c runs.
+ * q, k, v, out: dtype [B, H, n_tokens, d]; gate: fp32 [B, H, n_tokens].
+ * 0 <= n_tokens <= max_tokens.  On return of the work the layer holds the
+ * state and window ring after n_tokens tokens (ready for kvm_decode_step).
+ * dbg may be NULL.  KVM_ERR_CAPACITY if the schedule exceeds max_slots. */
+kvm_status kvm_prefill(kvm_layer* layer, const void* q, const void* k, const void* v,
+                       const float* gate, int64_t n_tokens, void* out, void* cuda_stream,
+                       const kvm_debug* dbg);
+
+/* One decode step at the layer's position p (then p + 1): if p is the first
+ * token of chunk c >= W/C + 1, chunk c - W/C - 1 is folded from the window
+ * ring first; the new unrotated k, v and gate enter the ring; the query
+ * attends to the state and to tokens (c - W/C)*C .. p.  Equal to row p of a
+ * prefill of p + 1 tokens.  q, k, v, out: dtype [B, H, d]; gate fp32 [B, H]. */
+kvm_status kvm_decode_step(kvm_layer* layer, const void* q, const void* k, const void* v,
+                           const float* gate, void* out, void* cuda_stream);
+
+/* Copy the layer's state and window ring into dst (device-to-device, async
+ * on the stream) and fill dst's host scalars. */
+kvm_status kvm_state_export(const kvm_layer* layer, kvm_state_bufs* dst, void* cuda_stream);
+
+/* Replace the layer's state and window ring by src (device-to-device, async)
+ * and recompute the state's read view.  src->n_slots <= max_slots,
+ * src->pos < max_tokens, counts >= 1 for rows < n_slots. */
+kvm_status kvm_state_import(kvm_layer* layer, const kvm_state_bufs* src, void* cuda_stream);
+
+/* Wait for the layer's last stream, then report (and clear) the device-side
+ * status word: KVM_OK, KVM_ERR_TIMEOUT or KVM_ERR_DEVICE. */
+kvm_status kvm_layer_sync(kvm_layer* layer);
+
+/* Message of the layer's last error (or, with NULL, of the last failed
+ * kvm_workspace_bytes / kvm_layer_create on this thread).  Never NULL. */
+const char* kvm_last_error(const kvm_layer* layer);
+
+/* Device time of the layer's kernels, by phase, accumulated between
+ * kvm_layer_set_timing(layer, 1) and kvm_layer_get_timing.  Measured with CUDA
+ * events recorded on the launch stream immediately before and after each
+ * kernel: a phase's time is its kernels' device duration (the start event
+ * completes only when the stream reaches the kernel, so queueing behind earlier
+ * work is not counted). */
+typedef struct {
+    double fold_ms;      /* fold-chain kernels (prefill chains and decode-boundary folds) */
+    double attn_ms;      /* prefill attention kernels */
+    double decode_ms;    /* decode attention kernels */
+    double other_ms;     /* ring fill, state renormalisation */
+    int64_t fold_launches, attn_launches, decode_launches, other_launches;
+} kvm_timing;
+
+/* Enable (1) or disable (0) per-kernel timing; enabling resets the totals.
+ * Timing adds two event records per kernel launch. */
+kvm_status kvm_layer_set_timing(kvm_layer* layer, int enable);
+
+/* Wait for the recorded events and return the totals since timing was enabled. */
+kvm_status kvm_layer_get_timing(kvm_layer* layer, kvm_timing* out);
+
+/* Free the layer's host metadata.  The workspace stays the caller's. */
+void kvm_layer_destroy(kvm_layer* layer);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVM_H */

@@ -90,7 +90,9 @@ def lib():
         _lib.kvo_state_view.restype = None
         _lib.kvo_state_view.argtypes = [P, I64, P, P, P, P, P, P]
         _lib.kvo_attend_query.restype = None
-        _lib.kvo_attend_query.argtypes = [P, I64, P, P, P, I64, I64, I64, P, P, P]
+        _lib.kvo_attend_query.argtypes = [P, I64, P, P, P, I64, I64, P, P, P]
+        _lib.kvo_rope_rows.restype = None
+        _lib.kvo_rope_rows.argtypes = [P, I64, I64, P, P]
         _lib.kvo_prefill_head.restype = ctypes.c_int
         _lib.kvo_prefill.restype = ctypes.c_int
         _lib.kvo_prefill.argtypes = [P, I64, I64, P, P, P, P, P, P, P, P, P, P, P, I64,
@@ -185,8 +187,10 @@ def attend_query(cfg: OracleConfig, key_view, val_view, q, p: int, wk, wv, w_fir
     wk, wv, q = _f64(wk).reshape(-1, d), _f64(wv).reshape(-1, d), _f64(q)
     out = np.zeros(d)
     c = cfg.c()
+    wk_rot = np.zeros_like(wk)
+    lib().kvo_rope_rows(ctypes.byref(c), wk.shape[0], int(w_first_pos), _p(wk), _p(wk_rot))
     lib().kvo_attend_query(ctypes.byref(c), key_view.shape[0], _p(key_view), _p(val_view),
-                           _p(q), int(p), wk.shape[0], int(w_first_pos), _p(wk), _p(wv), _p(out))
+                           _p(q), int(p), wk.shape[0], _p(wk_rot), _p(wv), _p(out))
     return out
 
 

@@ -310,29 +310,31 @@ void kvo_state_view(const kvo_config* cfg, int64_t n, const double* sum_k, const
 
 /* ------------------------------------------------------------- attention */
 
+/* RoPE of nw rows at positions first_pos, first_pos + 1, ... */
+void kvo_rope_rows(const kvo_config* cfg, int64_t nw, int64_t first_pos, const double* x,
+                   double* out) {
+    int d = cfg->head_dim;
+    for (int64_t i = 0; i < nw; ++i) rope(x + i * d, first_pos + i, cfg, out + i * d);
+}
+
 /*
- * One query at absolute position p over n state rows and nw window tokens
- * at positions w_first_pos .. w_first_pos + nw - 1, in one softmax
- * (KVM summary, Methodology and Core mechanism 4).  The state is scored with
- * the unrotated query, the window with RoPE applied to query and keys; both
- * use scale 1/sqrt(d).  Two-pass softmax.
+ * One query at absolute position p over n state rows and nw window tokens,
+ * in one softmax (KVM summary, Methodology and Core mechanism 4).  The state
+ * is scored with the unrotated query q; the window with the rotated query
+ * against wk_rot, the window keys already rotated at their own positions.
+ * Both parts use scale 1/sqrt(d).  Two-pass softmax.
  */
 void kvo_attend_query(const kvo_config* cfg, int64_t n, const double* key_view,
                       const double* val_view, const double* q, int64_t p,
-                      int64_t nw, int64_t w_first_pos, const double* wk, const double* wv,
-                      double* out) {
+                      int64_t nw, const double* wk_rot, const double* wv, double* out) {
     int d = cfg->head_dim;
     double scale = 1.0 / sqrt((double)d);
     int64_t nk = n + nw;
     double* s = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
     double* qr = (double*)malloc(sizeof(double) * d);
-    double* kr = (double*)malloc(sizeof(double) * d);
     rope(q, p, cfg, qr);
     for (int64_t j = 0; j < n; ++j) s[j] = dot(q, key_view + j * d, d) * scale;
-    for (int64_t i = 0; i < nw; ++i) {
-        rope(wk + i * d, w_first_pos + i, cfg, kr);
-        s[n + i] = dot(qr, kr, d) * scale;
-    }
+    for (int64_t i = 0; i < nw; ++i) s[n + i] = dot(qr, wk_rot + i * d, d) * scale;
     double mx = -INFINITY;
     for (int64_t j = 0; j < nk; ++j) if (s[j] > mx) mx = s[j];
     double den = 0.0;
@@ -343,7 +345,7 @@ void kvo_attend_query(const kvo_config* cfg, int64_t n, const double* key_view,
     for (int64_t i = 0; i < nw; ++i)
         for (int x = 0; x < d; ++x) out[x] += s[n + i] * wv[i * d + x];
     for (int x = 0; x < d; ++x) out[x] /= den;
-    free(s); free(qr); free(kr);
+    free(s); free(qr);
 }
 
 /* --------------------------------------------------------------- prefill */
@@ -374,6 +376,7 @@ int kvo_prefill_head(const kvo_config* cfg, int64_t N, const double* q, const do
     memset(rho, 0, sizeof(double) * (size_t)M);
     double* key_view = (double*)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * d);
     double* val_view = (double*)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * d);
+    double* wk_rot = (double*)malloc(sizeof(double) * (size_t)(cfg->window + C) * d);
     int64_t nchunks = (N + C - 1) / C;
     int rc = KVO_OK;
     for (int64_t c = 0; c < nchunks; ++c) {
@@ -392,11 +395,13 @@ int kvo_prefill_head(const kvo_config* cfg, int64_t N, const double* q, const do
         int64_t ws = (c - Wc) * C;
         if (ws < 0) ws = 0;
         int64_t pe = (c + 1) * C < N ? (c + 1) * C : N;
+        /* every query of the chunk sees the same rotated window keys */
+        kvo_rope_rows(cfg, pe - ws, ws, k + ws * d, wk_rot);
         for (int64_t p = c * C; p < pe; ++p)
             kvo_attend_query(cfg, *n_slots, key_view, val_view, q + p * d, p,
-                             p - ws + 1, ws, k + ws * d, v + ws * d, out + p * d);
+                             p - ws + 1, wk_rot, v + ws * d, out + p * d);
     }
-    free(key_view); free(val_view);
+    free(key_view); free(val_view); free(wk_rot);
     return rc;
 }
 

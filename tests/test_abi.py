@@ -1,0 +1,92 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/kvm.h declares, and validates configurations on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvm():
+    from compressed_kv_state_gb300 import build
+    build.build()
+    from compressed_kv_state_gb300 import kvm as mod
+    return mod
+
+
+def _declared(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(kvm):
+    names = _declared("kvm.h")
+    assert "kvm_prefill" in names and "kvm_decode_step" in names
+    lib = ctypes.CDLL(kvm.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_headers_cover_the_boundary():
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        assert f.endswith(".h")
+    names = _declared("kvm.h")
+    for n in ("kvm_workspace_bytes", "kvm_layer_create", "kvm_prefill", "kvm_decode_step",
+              "kvm_state_export", "kvm_state_import", "kvm_layer_sync", "kvm_last_error",
+              "kvm_layer_destroy"):
+        assert n in names
+
+
+def test_struct_sizes_match_header(kvm):
+    # 15 four-byte fields, no padding
+    assert ctypes.sizeof(kvm.kvm_config) == 60
+    assert ctypes.sizeof(kvm.kvm_state_bufs) == 7 * 8 + 3 * 8
+    assert ctypes.sizeof(kvm.kvm_debug) == 5 * 8
+
+
+@pytest.mark.parametrize("field,value,msg", [
+    ("head_dim", 32, "head_dim"),
+    ("chunk", 24, "chunk"),
+    ("chunk", 512, "chunk"),
+    ("window", 100, "window"),
+    ("n_sinks", 200, "n_sinks"),
+    ("max_slots", 16, "max_slots"),
+    ("rope_dims", 3, "rope_dims"),
+    ("dtype", 9, "dtype"),
+    ("sched", 5, "schedule"),
+    ("batch", 0, "batch"),
+    ("max_tokens", 0, "max_tokens"),
+])
+def test_invalid_configs_rejected(kvm, field, value, msg):
+    cfg = kvm.make_config(batch=1, heads=2)
+    setattr(cfg, field, value)
+    assert kvm.lib.kvm_workspace_bytes(ctypes.byref(cfg)) == 0
+    assert msg in kvm.kvm_last_error(None)
+
+
+def test_power_schedule_needs_positive_coef(kvm):
+    cfg = kvm.make_config(batch=1, heads=1, sched=kvm.KVM_SCHED_POWER, coef=0.0)
+    assert kvm.lib.kvm_workspace_bytes(ctypes.byref(cfg)) == 0
+
+
+def test_workspace_size_grows_with_slots_and_tokens(kvm):
+    a = kvm.kvm_workspace_bytes(kvm.make_config(batch=8, heads=12))
+    b = kvm.kvm_workspace_bytes(kvm.make_config(batch=8, heads=12, max_slots=512))
+    c = kvm.kvm_workspace_bytes(kvm.make_config(batch=8, heads=12, max_tokens=16384))
+    assert 0 < a < b and a < c
+    assert a % 256 == 0
+
+
+def test_null_handles_are_rejected(kvm):
+    assert kvm.lib.kvm_prefill(None, None, None, None, None, 0, None, None, None) == \
+        kvm.KVM_ERR_INVALID_ARG
+    assert kvm.lib.kvm_layer_sync(None) == kvm.KVM_ERR_INVALID_ARG
+    out = ctypes.c_void_p()
+    cfg = kvm.make_config(batch=1, heads=1)
+    assert kvm.lib.kvm_layer_create(ctypes.byref(cfg), None, 0, ctypes.byref(out)) == \
+        kvm.KVM_ERR_WORKSPACE
+    assert out.value is None

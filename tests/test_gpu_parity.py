@@ -1,0 +1,326 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle
+on the same seeded inputs.
+
+Small shapes: every head end to end (assignments exact up to counted near
+ties; outputs and state within tolerance).  Full-size workloads: every head
+on the GPU; sampled heads end to end on the oracle; sampled fold events and
+chunks teacher-forced from the GPU's own exported state, so that one
+near-tie flip cannot cascade into the comparison.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from compressed_kv_state_gb300 import workloads as wl
+from kvm_testlib import (NEAR_TIE, compare_chain, compare_event_teacher_forced, gpu_prefill,
+                         make_layer, oracle_cfg, state_to_oracle, tol_of)
+
+pytestmark = pytest.mark.gpu
+
+
+def _sized(w):
+    """Power-law workloads: max_slots = capacity after the last fold."""
+    if w.sched != 1:
+        return w
+    ocfg = oracle_cfg(w.with_(max_slots=10**6))
+    E = oracle.n_events(ocfg, w.N)
+    return w.with_(max_slots=max(oracle.capacity(ocfg, E * w.chunk), w.n_sinks + 1))
+
+
+SMALL = [
+    wl.TINY_FP32,
+    wl.Workload("fixed_B2H3N1000_C64W128", B=2, H=3, N=1000, chunk=64, window=128, n_sinks=8,
+                max_slots=48, keys="repeat5"),
+    _sized(wl.Workload("sqrt_B1H4N1500_C64W192", B=1, H=4, N=1500, chunk=64, window=192,
+                       n_sinks=16, sched=1, keys="needles10")),
+    wl.Workload("fixed_r64_C16W32", B=1, H=2, N=300, chunk=16, window=32, n_sinks=3, max_slots=20,
+                rope_dims=64, keys="repeat5"),
+    wl.Workload("fixed_r0_S0_C32W64", B=1, H=2, N=700, chunk=32, window=64, n_sinks=0,
+                max_slots=24, rope_dims=0, keys="repeat5"),
+    wl.Workload("fixed_W0_SeqC_C32", B=1, H=2, N=520, chunk=32, window=0, n_sinks=32,
+                max_slots=40),
+    _sized(wl.Workload("sqrt_fp32_C256W256", B=1, H=2, N=2100, chunk=256, window=256,
+                       n_sinks=16, sched=1, dtype="fp32", keys="neardup20")),
+    wl.Workload("fixed_C128_ragged", B=1, H=2, N=1337, chunk=128, window=256, n_sinks=16,
+                max_slots=64, keys="repeat5"),
+]
+
+
+def _end_to_end(w, heads=None, threads=None):
+    q, k, v, g = wl.prefill_inputs(w)
+    layer = make_layer(w)
+    out, dbg, state = gpu_prefill(layer, w, q, k, v, g)
+    ocfg = oracle_cfg(w)
+    hs = heads if heads is not None else [(b, h) for b in range(w.B) for h in range(w.H)]
+    oq = np.stack([q[b, h] for b, h in hs])
+    ok_ = np.stack([k[b, h] for b, h in hs])
+    ov = np.stack([v[b, h] for b, h in hs])
+    og = np.stack([g[b, h] for b, h in hs])
+    oout, ostates, odbg = oracle.prefill(ocfg, oq, ok_, ov, og, threads=threads)
+    tol = tol_of(w)
+    E = oracle.n_events(ocfg, w.N)
+    Wc = w.window // w.chunk
+    report = []
+    for i, (b, h) in enumerate(hs):
+        div, n_ex = (None, 0) if E == 0 else compare_chain(dbg, odbg, i, b, h)
+        rows = w.N if div is None else min(w.N, (div + Wc + 1) * w.chunk)
+        err = np.abs(out[b, h, :rows] - oout[i, :rows]).max() if rows else 0.0
+        assert err <= tol, f"(b={b},h={h}) output max-abs error {err} > {tol} over {rows} rows"
+        if div is None:
+            st = ostates[i]
+            n = st.n
+            assert state["n_slots"] == n and state["n_overflow"] == st.t
+            np.testing.assert_array_equal(state["counts"][b, h, :n], st.count[:n])
+            for key, ref in (("sum_k", st.sum_k), ("sum_v", st.sum_v)):
+                e2 = np.abs(state[key][b, h, :n] - ref[:n]).max() if n else 0.0
+                assert e2 <= tol, f"(b={b},h={h}) {key} max-abs error {e2}"
+            np.testing.assert_allclose(state["rho"][b, h, :n], st.rho[:n], rtol=1e-5)
+        else:
+            report.append((b, h, div, n_ex))
+    return report, (q, k, v, g), layer, out, dbg
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_end_to_end(w):
+    report, *_ = _end_to_end(w)
+    # near-tie divergences are allowed but must be rare at these sizes
+    assert len(report) <= max(1, (w.B * w.H) // 4), report
+
+
+@pytest.mark.parametrize("N", [0, 1, 5, 127, 128, 129])
+def test_short_sequences_without_folds(N):
+    w = wl.Workload("short", B=1, H=2, N=N, chunk=128, window=512, n_sinks=16, max_slots=64)
+    if N == 0:
+        layer = make_layer(w.with_(N=1))
+        _, _, state = gpu_prefill(layer, w, *wl.prefill_inputs(w.with_(N=1)), n_tokens=0)
+        assert state["n_slots"] == 0 and state["pos"] == 0
+        return
+    report, *_ = _end_to_end(w)
+    assert not report
+
+
+# ------------------------------------------------------------ full sizes
+
+FULL = [wl.FIXED_8K, wl.SQRT_8K, wl.LONG_64K]
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_full_size_sampled_heads(w):
+    """Every head runs on the GPU in the benchmark's launch configuration;
+    two sampled heads are checked end to end against the oracle."""
+    heads = [(0, 0), (w.B - 1, w.H - 1)]
+    report, *_ = _end_to_end(w, heads=heads)
+    for b, h, e, n in report:
+        print(f"near-tie divergence (b={b}, h={h}) at event {e} ({n} tokens)")
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_full_size_teacher_forced(w):
+    """Sampled fold events and chunks, each started from the GPU's own state:
+    events exact up to near ties, states and outputs within tolerance."""
+    q, k, v, g = wl.prefill_inputs(w)
+    layer = make_layer(w)
+    out, dbg, _ = gpu_prefill(layer, w, q, k, v, g)
+    ocfg = oracle_cfg(w)
+    C, Wc = w.chunk, w.window // w.chunk
+    E = oracle.n_events(ocfg, w.N)
+    tol = tol_of(w)
+    rng = np.random.default_rng(0)
+    events = sorted({0, 1, E // 2, E - 1})
+    heads = [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(3)]
+    exempt = 0
+    for e in events:
+        # the GPU state before event e is the state a prefill of (e + W/C + 1) chunks leaves
+        _, _, st_before = gpu_prefill(layer, w, q, k, v, g, n_tokens=(e + Wc + 1) * C, debug=False)
+        _, _, st_after = gpu_prefill(layer, w, q, k, v, g,
+                                     n_tokens=min(w.N, (e + Wc + 2) * C), debug=False)
+        for b, h in heads:
+            sl = slice(e * C, (e + 1) * C)
+            ost = state_to_oracle(w, st_before, b, h)
+            r, n_ex = compare_event_teacher_forced(w, ost, e * C, k[b, h, sl], v[b, h, sl],
+                                                   g[b, h, sl], dbg["assign"][b, h, e],
+                                                   dbg["kind"][b, h, e])
+            exempt += n_ex
+            if n_ex == 0:
+                n = ost.n
+                assert st_after["n_slots"] == n
+                np.testing.assert_array_equal(st_after["counts"][b, h, :n], ost.count[:n])
+                assert np.abs(st_after["sum_k"][b, h, :n] - ost.sum_k[:n]).max() <= tol
+                assert np.abs(st_after["sum_v"][b, h, :n] - ost.sum_v[:n]).max() <= tol
+                # GPU surprise scores agree with the oracle's where defined
+                msk = (r["kind"] != oracle.SINK) & np.isfinite(r["max_sim"])
+                if msk.any():
+                    assert np.abs(dbg["max_sim"][b, h, e][msk] - r["max_sim"][msk]).max() < 1e-4
+    # outputs of sampled chunks from the GPU state those chunks read
+    nch = -(-w.N // C)
+    for c in sorted({Wc + 1, nch // 2, nch - 1}):
+        if c < Wc + 1:
+            continue
+        _, _, st = gpu_prefill(layer, w, q, k, v, g, n_tokens=min(w.N, (c + 1) * C), debug=False)
+        for b, h in heads:
+            ost = state_to_oracle(w, st, b, h)
+            kv, vv = oracle.state_view(ocfg, ost)
+            ws = (c - Wc) * C
+            for p in rng.choice(np.arange(c * C, min(w.N, (c + 1) * C)), size=8, replace=False):
+                ref = oracle.attend_query(ocfg, kv, vv, q[b, h, p], int(p), k[b, h, ws:p + 1],
+                                          v[b, h, ws:p + 1], ws)
+                err = np.abs(out[b, h, p] - ref).max()
+                assert err <= tol, f"chunk {c} (b={b},h={h}) p={p}: {err}"
+    print(f"teacher-forced: {len(events)} events x {len(heads)} heads, {exempt} near-tie tokens")
+
+
+def test_tiny_fp32_full():
+    """The tiny fp32 workload in full, both heads, at the fp32 tolerance."""
+    report, *_ = _end_to_end(wl.TINY_FP32)
+    assert not report
+
+
+# ---------------------------------------------------------------- decode
+
+def _decode_from_prefill(w, N0, steps):
+    import torch
+    q, k, v, g = wl.prefill_inputs(w.with_(N=N0 + steps))
+    layer = make_layer(w, max_tokens=N0 + steps)
+    gpu_prefill(layer, w.with_(N=N0 + steps), q, k, v, g, n_tokens=N0, debug=False)
+    outs = []
+    for p in range(N0, N0 + steps):
+        dq = torch.from_numpy(np.ascontiguousarray(q[:, :, p])).cuda()
+        dk = torch.from_numpy(np.ascontiguousarray(k[:, :, p])).cuda()
+        dv = torch.from_numpy(np.ascontiguousarray(v[:, :, p])).cuda()
+        if w.dtype == "bf16":
+            dq, dk, dv = dq.bfloat16(), dk.bfloat16(), dv.bfloat16()
+        dg = torch.from_numpy(np.ascontiguousarray(g[:, :, p])).cuda()
+        outs.append(layer.decode_step(dq, dk, dv, dg).float().cpu().numpy())
+    layer.sync()
+    return np.stack(outs, axis=2), (q, k, v, g), layer
+
+
+@pytest.mark.parametrize("w,N0,steps", [
+    (wl.Workload("dec_fixed", B=2, H=2, N=0, chunk=64, window=128, n_sinks=8, max_slots=40,
+                 keys="repeat5"), 300, 200),
+    (wl.Workload("dec_fp32", B=1, H=2, N=0, chunk=32, window=64, n_sinks=4, max_slots=24,
+                 dtype="fp32"), 100, 140),
+    (wl.Workload("dec_from_start", B=1, H=2, N=0, chunk=16, window=32, n_sinks=16, max_slots=30),
+     0, 120),
+])
+def test_decode_matches_prefill_and_oracle(w, N0, steps):
+    """Decoding token by token equals the last rows of one longer prefill
+    (GPU against GPU and against the oracle)."""
+    dec, (q, k, v, g), _ = _decode_from_prefill(w, N0, steps)
+    wf = w.with_(N=N0 + steps)
+    layer2 = make_layer(wf)
+    full, _, _ = gpu_prefill(layer2, wf, q, k, v, g, debug=False)
+    tol = tol_of(w)
+    assert np.abs(dec - full[:, :, N0:]).max() <= tol
+    ocfg = oracle_cfg(w)
+    oout, _, _ = oracle.prefill(ocfg, q.reshape(-1, *q.shape[2:]), k.reshape(-1, *k.shape[2:]),
+                                v.reshape(-1, *v.shape[2:]), g.reshape(-1, g.shape[2]))
+    oout = oout.reshape(full.shape)
+    assert np.abs(dec - oout[:, :, N0:]).max() <= tol
+
+
+@pytest.mark.parametrize("n", [256, 1024])
+def test_decode_sweep_imported_state(n):
+    """Decode sweep workload: imported synthetic state, full window, 128 steps
+    starting on a chunk boundary (the first step folds 128 tokens); sampled
+    heads against the oracle decoder started from the same state."""
+    import torch
+    from compressed_kv_state_gb300 import kvm
+    w = wl.DECODE[n]
+    state, (wk, wv, wg), (q, k, v, g) = wl.decode_inputs(w)
+    cfg = kvm.make_config(batch=w.B, heads=w.H, rope_dims=w.rope_dims, chunk=w.chunk,
+                          window=w.window, n_sinks=w.n_sinks, sched=kvm.KVM_SCHED_FIXED,
+                          max_slots=n, max_tokens=w.pos0 + w.steps)
+    layer = kvm.KvmLayer(cfg)
+    L = w.window + w.chunk
+    ring_k = np.zeros((w.B, w.H, L, w.d), np.float32)
+    ring_v = np.zeros_like(ring_k)
+    ring_g = np.zeros((w.B, w.H, L), np.float32)
+    pos_first = w.pos0 - L
+    for i in range(L):
+        ring_k[:, :, (pos_first + i) % L] = wk[:, :, i]
+        ring_v[:, :, (pos_first + i) % L] = wv[:, :, i]
+        ring_g[:, :, (pos_first + i) % L] = wg[:, :, i]
+    bufs = layer.state_buffers()
+    bufs["sum_k"][:, :, :n] = torch.from_numpy(state["sum_k"])
+    bufs["sum_v"][:, :, :n] = torch.from_numpy(state["sum_v"])
+    bufs["counts"][:, :, :n] = torch.from_numpy(state["counts"])
+    bufs["rho"][:, :, :n] = torch.from_numpy(state["rho"])
+    bufs["ring_k"].copy_(torch.from_numpy(ring_k).bfloat16())
+    bufs["ring_v"].copy_(torch.from_numpy(ring_v).bfloat16())
+    bufs["ring_g"].copy_(torch.from_numpy(ring_g))
+    bufs.update(n_slots=n, n_overflow=state["t"], pos=w.pos0)
+    layer.import_state(bufs)
+    outs = []
+    for s in range(w.steps):
+        dq, dk, dv = (torch.from_numpy(x[s]).cuda().bfloat16() for x in (q, k, v))
+        dg = torch.from_numpy(g[s]).cuda()
+        outs.append(layer.decode_step(dq, dk, dv, dg).float().cpu().numpy())
+    layer.sync()
+    outs = np.stack(outs)
+    ocfg = oracle.OracleConfig(chunk=w.chunk, window=w.window, n_sinks=w.n_sinks, sched=0,
+                               max_slots=n)
+    for b, h in [(0, 0), (w.B - 1, w.H - 1), (17, 5)]:
+        st = oracle.OracleState(ocfg)
+        st.n, st.t = n, state["t"]
+        st.sum_k[:n], st.sum_v[:n] = state["sum_k"][b, h], state["sum_v"][b, h]
+        st.count[:n], st.rho[:n] = state["counts"][b, h], state["rho"][b, h]
+        dec = oracle.OracleDecoder(ocfg, st, w.pos0, wk[b, h], wv[b, h], wg[b, h])
+        for s in range(w.steps):
+            ref = dec.step(q[s, b, h], k[s, b, h], v[s, b, h], g[s, b, h])
+            err = np.abs(outs[s, b, h] - ref).max()
+            assert err <= 2e-2, f"step {s} (b={b},h={h}): {err}"
+
+
+# --------------------------------------------------- state, determinism, errors
+
+def test_export_import_roundtrip_and_determinism():
+    import torch
+    w = wl.Workload("rt", B=2, H=2, N=900, chunk=64, window=128, n_sinks=8, max_slots=40,
+                    keys="repeat5")
+    q, k, v, g = wl.prefill_inputs(w)
+    layer = make_layer(w, max_tokens=w.N + 80)
+    o1, d1, s1 = gpu_prefill(layer, w, q, k, v, g)
+    o2, d2, s2 = gpu_prefill(layer, w, q, k, v, g)
+    np.testing.assert_array_equal(o1, o2)
+    for key in ("assign", "kind", "max_sim"):
+        np.testing.assert_array_equal(d1[key], d2[key])
+    for key in ("sum_k", "sum_v", "counts", "rho", "ring_k", "ring_v", "ring_g"):
+        np.testing.assert_array_equal(s1[key], s2[key])
+    # a second layer resumed from the exported state decodes identically
+    st = layer.export_state()
+    other = make_layer(w, max_tokens=w.N + 80)
+    other.import_state(st)
+    rng = np.random.default_rng(1)
+    for _ in range(70):
+        x = [torch.from_numpy(rng.standard_normal((2, 2, 64), dtype=np.float32)).cuda().bfloat16()
+             for _ in range(3)]
+        gg = torch.rand(2, 2, device="cuda")
+        a = layer.decode_step(*x, gg)
+        b = other.decode_step(*x, gg)
+        assert torch.equal(a, b)
+    layer.sync()
+    other.sync()
+
+
+def test_errors_are_reported_not_raised_on_device():
+    import torch
+    from compressed_kv_state_gb300 import kvm
+    w = wl.Workload("cap", B=1, H=1, N=4096, chunk=64, window=64, n_sinks=4, sched=1,
+                    max_slots=40)
+    layer = make_layer(w)
+    q, k, v, g = wl.prefill_inputs(w)
+    with pytest.raises(kvm.KvmError) as ei:
+        gpu_prefill(layer, w, q, k, v, g, debug=False)
+    assert ei.value.status == kvm.KVM_ERR_CAPACITY
+    with pytest.raises(kvm.KvmError) as ei:
+        kvm.kvm_prefill(layer.handle, None, None, None, None, 10, None)
+    assert ei.value.status == kvm.KVM_ERR_INVALID_ARG
+    with pytest.raises(kvm.KvmError) as ei:
+        kvm.kvm_prefill(layer.handle, None, None, None, None, 10**7, None)
+    assert ei.value.status == kvm.KVM_ERR_INVALID_ARG
+    small = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvm.KvmError) as ei:
+        kvm.kvm_layer_create(layer.cfg, small)
+    assert ei.value.status == kvm.KVM_ERR_WORKSPACE
+    layer.sync()  # nothing latched on the device
