@@ -241,6 +241,9 @@ kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t b
                        cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = cudaMemset(ly->ws + L.status, 0, 16);
     if (e == cudaSuccess) e = cudaMemset(ly->ws + L.counts, 0, L.rho - L.counts);
+    // snapshot rows beyond a snapshot's slot count are read (and masked) by the
+    // tensor-core attention: keep them finite
+    if (e == cudaSuccess && L.rope > L.snap_k) e = cudaMemset(ly->ws + L.snap_k, 0, L.rope - L.snap_k);
     if (e != cudaSuccess) {
         g_err = std::string("kvm_layer_create: ") + cudaGetErrorString(e);
         delete ly;
@@ -325,6 +328,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         aa.r = c.rope_dims;
         aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
         aa.BH = BH;
+        aa.status = ly->at<int>(L.status);
         e = timed(ly, PH_ATTN, s, [&] { return kvm::launch_attn(aa, bf16, s); });
         if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
 

@@ -159,6 +159,7 @@ __global__ void ring_fill_kernel(RingFillArgs a) {
 
 cudaError_t launch_attn(const AttnArgs& a, bool bf16, cudaStream_t s) {
     if (a.N == 0) return cudaSuccess;
+    if (attn_tc_supported(a, bf16)) return launch_attn_tc(a, a.status, s);
     const int QB = (a.C % 64 == 0) ? 64 : (a.C % 32 == 0 ? 32 : 16);
     dim3 grid((unsigned)((a.N + QB - 1) / QB), (unsigned)a.BH);
     if (bf16)

@@ -101,6 +101,7 @@ struct AttnArgs {
     int r;
     float scale_log2;   // log2(e) / sqrt(D)
     int BH;
+    int* status;
 };
 
 struct DecodeArgs {
@@ -150,6 +151,8 @@ struct RenormArgs {
 // Host launchers (return the launch error).
 cudaError_t launch_fold(const FoldArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_attn(const AttnArgs& a, bool bf16, cudaStream_t s);
+bool attn_tc_supported(const AttnArgs& a, bool bf16);
+cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_ring_fill(const RingFillArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_renorm(const RenormArgs& a, bool bf16, cudaStream_t s);
