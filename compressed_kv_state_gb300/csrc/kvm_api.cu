@@ -8,22 +8,26 @@
 #include <vector>
 
 #include "../../include/kvm.h"
+#include "kvm_host.h"
 #include "kvm_internal.cuh"
 
 using kvm::D;
 using kvm::Sched;
 
-namespace {
-
+namespace kvm {
+namespace host {
 thread_local std::string g_err = "no error";
+}  // namespace host
+}  // namespace kvm
 
-constexpr size_t ALIGN = 256;
+using kvm::host::ALIGN;
+using kvm::host::g_err;
+using kvm::host::Layout;
+
+namespace kvm {
+namespace host {
+
 size_t align_up(size_t x) { return (x + ALIGN - 1) / ALIGN * ALIGN; }
-
-struct Layout {
-    size_t sum_k, sum_v, counts, rho, simdir, view_k, view_v;
-    size_t ring_k, ring_v, ring_g, snap_k, snap_v, rope, sched, status, total;
-};
 
 int64_t n_events_for(const kvm_config& c, int64_t N) {
     const int64_t nchunks = (N + c.chunk - 1) / c.chunk;
@@ -108,6 +112,17 @@ Layout layout_of(const kvm_config& c) {
     L.total = o;
     return L;
 }
+
+}  // namespace host
+}  // namespace kvm
+
+using kvm::host::capacity;
+using kvm::host::event_sched;
+using kvm::host::layout_of;
+using kvm::host::n_events_for;
+using kvm::host::validate;
+
+namespace {
 
 struct DeviceGuard {
     int prev = -1;

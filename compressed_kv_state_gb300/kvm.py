@@ -85,6 +85,8 @@ def _load():
     lib.kvm_layer_set_timing.argtypes = [P, ctypes.c_int]
     lib.kvm_layer_get_timing.restype = ctypes.c_int
     lib.kvm_layer_get_timing.argtypes = [P, P]
+    lib.kvm_prefill_noalloc.restype = ctypes.c_int
+    lib.kvm_prefill_noalloc.argtypes = [P, P, P, P, P, I64, P, P]
     lib.kvm_layer_destroy.restype = None
     lib.kvm_layer_destroy.argtypes = [P]
     return lib
@@ -158,6 +160,16 @@ def kvm_layer_get_timing(layer) -> dict:
     t = kvm_timing()
     _check(lib.kvm_layer_get_timing(layer, ctypes.byref(t)), layer)
     return {name: getattr(t, name) for name, _ in kvm_timing._fields_}
+
+
+KVM_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def kvm_prefill_noalloc(cfg: kvm_config, q, k, v, gate, n_tokens: int, out, stream=None):
+    """One-shot prefill with no allocation (scratch in the library's static device array)."""
+    st = lib.kvm_prefill_noalloc(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
+                                 int(n_tokens), _ptr(out), _stream(stream))
+    _check(st, None)
 
 
 def kvm_last_error(layer) -> str:

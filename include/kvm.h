@@ -195,6 +195,36 @@ kvm_status kvm_layer_set_timing(kvm_layer* layer, int enable);
 /* Wait for the recorded events and return the totals since timing was enabled. */
 kvm_status kvm_layer_get_timing(kvm_layer* layer, kvm_timing* out);
 
+/* Size of the static device scratch behind kvm_prefill_noalloc: 32 MiB. */
+#define KVM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* kvm_prefill_noalloc - a one-shot prefill that allocates no memory.
+ * This entry point has no counterpart in the paper; it exists for callers
+ * that may not allocate device memory themselves: a plugin running inside an
+ * inference server or host framework that owns all device memory through
+ * its own pool and forbids direct cudaMalloc/cudaFree, or a latency-critical
+ * loop that cannot afford the device synchronisation an allocation implies.
+ * Such callers cannot hand kvm_layer_create a workspace.
+ *
+ * Computes exactly what kvm_prefill computes into out (same kernels), for
+ * q, k, v, out: dtype [B, H, n_tokens, d] and gate fp32 [B, H, n_tokens]
+ * device buffers owned by the caller, but keeps no layer: nothing is left
+ * for a later decode, export or debug record.  Its scratch (state, read-view
+ * snapshots, RoPE and schedule tables) is a file-scope device array of
+ * KVM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library holds
+ * until the process exits.  A call whose scratch would exceed it (or that
+ * would fold more than 1024 chunks) returns KVM_ERR_WORKSPACE with the
+ * required size in kvm_last_error(NULL), before enqueuing anything.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any CUDA
+ * stream capture.  Every call reuses the same array and clears what must
+ * start at zero; calls whose GPU work overlaps in time (several streams or
+ * host threads) race on it and must be serialised by the caller.  Calls no
+ * cudaMalloc, cudaFree or other allocating routine.  Errors are reported
+ * through kvm_last_error(NULL); device-side status is not reported. */
+kvm_status kvm_prefill_noalloc(const kvm_config* cfg, const void* q, const void* k, const void* v,
+                               const float* gate, int64_t n_tokens, void* out, void* cuda_stream);
+
 /* Free the layer's host metadata.  The workspace stays the caller's. */
 void kvm_layer_destroy(kvm_layer* layer);
 
