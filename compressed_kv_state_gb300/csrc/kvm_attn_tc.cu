@@ -423,8 +423,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
+}  // namespace tc
+
 // 3-D bf16 map over [planes][rows][64] with a 128 x 64 box, 128-byte swizzle.
-static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes) {
+bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes) {
+    using namespace tc;
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[3] = {64, rows, planes};
@@ -437,8 +440,6 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t p
     return r == CUDA_SUCCESS;
 }
 
-}  // namespace tc
-
 bool attn_tc_supported(const AttnArgs& a, bool bf16) {
     return bf16 && a.C % 128 == 0 && a.N > 0;
 }
@@ -448,9 +449,10 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, msk, msv;
     const uint64_t BH = (uint64_t)a.BH;
     const uint64_t planes_snap = BH * (uint64_t)(a.snap_events > 0 ? a.snap_events : 1);
-    if (!make_map(&mq, a.q, (uint64_t)a.N, BH) || !make_map(&mk, a.k, (uint64_t)a.N, BH) ||
-        !make_map(&mv, a.v, (uint64_t)a.N, BH) || !make_map(&msk, a.snap_k, (uint64_t)a.M, planes_snap) ||
-        !make_map(&msv, a.snap_v, (uint64_t)a.M, planes_snap))
+    if (!make_tmap_bf16_3d(&mq, a.q, (uint64_t)a.N, BH) || !make_tmap_bf16_3d(&mk, a.k, (uint64_t)a.N, BH) ||
+        !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH) ||
+        !make_tmap_bf16_3d(&msk, a.snap_k, (uint64_t)a.M, planes_snap) ||
+        !make_tmap_bf16_3d(&msv, a.snap_v, (uint64_t)a.M, planes_snap))
         return cudaErrorInvalidValue;
     TcArgs t;
     t.N = a.N;
