@@ -423,7 +423,12 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="run the same workload with another batch size (profiling a smaller case)")
     args = ap.parse_args()
+    global W
+    if args.batch is not None:
+        W = W.with_(B=args.batch, name=W.name.replace(f"B{W.B}", f"B{args.batch}"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

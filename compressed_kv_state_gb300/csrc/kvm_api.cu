@@ -572,6 +572,7 @@ kvm_status kvm_layer_get_timing(kvm_layer* ly, kvm_timing* out) {
     return KVM_OK;
 }
 
+
 const char* kvm_last_error(const kvm_layer* ly) { return ly ? ly->err.c_str() : g_err.c_str(); }
 
 void kvm_layer_destroy(kvm_layer* ly) { delete ly; }

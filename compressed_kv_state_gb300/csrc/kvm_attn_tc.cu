@@ -11,22 +11,27 @@
 // in blocks of 128: first ceil(n/128) blocks of the state snapshot, then the
 // window from (c - W/C)*C up to the tile's end (the last block is causal).
 //
-// Persistent CTAs (one per SM, 256 threads) loop over tiles; warp roles:
-//   warp 0     TMA producer: Q tile (double-buffered), K/V blocks (3 stages)
+// Persistent CTAs (two per SM, 256 threads, 112 KB shared memory and 256
+// TMEM columns each, so the tensor core alternates between two tiles) loop
+// over tiles; warp roles:
+//   warp 0     TMA producer: Q tile, K/V blocks (2 stages)
 //   warp 1     tensor-memory owner and MMA issuer (one thread):
-//              S = Q K^T into one of two TMEM S buffers (128 fp32 columns),
+//              S = Q K^T into the TMEM S buffer (128 fp32 columns), issued for
+//              block j+1 as soon as the softmax has consumed block j;
 //              O += P V into the TMEM O accumulator (64 columns)
 //   warps 2-3  RoPE: rotate the Q tile and every window K block in shared
 //              memory (128-byte swizzled rows), then hand them to the MMA
-//   warps 4-7  softmax: thread i owns query row i (= TMEM lane i); online
-//              softmax with lazy rescaling of O (only when the running
-//              maximum grows by more than 2^8), P written to shared memory
-//              as bf16 in the swizzled K-major layout the MMA reads.
+//   warps 4-7  softmax: thread i owns query row i (= TMEM lane i); two passes
+//              over the S row in TMEM (block maximum, then exponentials), lazy
+//              rescaling of O (only when the running maximum grows by more than
+//              2^8), P written to shared memory as bf16 in the swizzled K-major
+//              layout the MMA reads.
 // All mbarrier waits are bounded (about two seconds); on expiry the CTA
 // raises the device status word, drains and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdio>
 #include <mutex>
 
 #include "kvm_internal.cuh"
@@ -36,16 +41,23 @@ namespace kvm {
 namespace tc {
 
 constexpr int NS = 3;                 // K/V pipeline stages
-constexpr int TILE_BYTES = 128 * 128; // one [128 x 64] bf16 tile
-constexpr int OFF_Q = 0;              // 2 Q buffers
-constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
-constexpr int OFF_V = OFF_K + NS * TILE_BYTES;
-constexpr int OFF_P = OFF_V + NS * TILE_BYTES;  // 2 P buffers of [128 x 128] bf16
-constexpr int OFF_BAR = OFF_P + 2 * 2 * TILE_BYTES;
-constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // barriers + alignment slack
-constexpr int TMEM_COLS = 512;
-constexpr int TM_S0 = 0, TM_O = 256;
+constexpr int KB = 64;                // keys per block
+constexpr int Q_BYTES = 128 * 128;    // Q tile [128 x 64] bf16
+constexpr int KV_BYTES = KB * 128;    // K or V block [64 x 64] bf16
+constexpr int P_BYTES = 128 * 128;    // P block [128 x 64] bf16
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_V = OFF_K + NS * KV_BYTES;
+constexpr int OFF_P = OFF_V + NS * KV_BYTES;    // 2 P buffers
+constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // 97.25 KB with alignment slack: two CTAs per SM
+constexpr int TMEM_COLS = 256;
+constexpr int TM_S = 0, TM_O = 128;             // S buffers at columns 0 and 64
 constexpr float TAU = 8.0f;  // lazy-rescale threshold (log2 units)
+
+#ifdef KVM_PROBE
+static __device__ unsigned long long g_probe_attn[64];
+#endif
 
 struct TcArgs {
     int64_t N;
@@ -72,10 +84,15 @@ __device__ __forceinline__ Tile tile_of(const TcArgs& a, int id) {
     t.e = (int)(c - Wc - 1);
     t.n = t.e >= 0 ? a.sched[t.e].n_after : 0;
     t.ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
-    t.nst = (t.n + 127) / 128;
-    t.nwin = (int)((t.q0 + 128 - t.ws) / 128);
+    t.nst = (t.n + KB - 1) / KB;
+    t.nwin = (int)((t.q0 + 128 - t.ws) / KB);
     t.nblk = t.nst + t.nwin;
     return t;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 // Rotate-half RoPE of one 128-byte swizzled bf16 row in shared memory.
@@ -94,28 +111,61 @@ __device__ __forceinline__ void rope_row(uint8_t* row, int row_idx, int64_t pos,
     }
 }
 
-__global__ void __launch_bounds__(256, 1)
+// Same rotation when half is a multiple of 8: dims [0, half) and [half, 2*half)
+// are whole 16-byte chunks, so a row is rotated with vector shared-memory
+// accesses and vector loads of the (cos, sin) table.
+__device__ __forceinline__ void rope_row_vec(uint8_t* row, int row_idx, int64_t pos, const float2* rope,
+                                             int half) {
+    const float4* tab = reinterpret_cast<const float4*>(rope + pos * half);
+    const int sw = row_idx & 7;
+    const int hc = half >> 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c >= hc) break;
+        uint4* pa = reinterpret_cast<uint4*>(row + ((c ^ sw) << 4));
+        uint4* pb = reinterpret_cast<uint4*>(row + (((c + hc) ^ sw) << 4));
+        // element e of the chunk is pair 8c + e: float4 4c + e/2 holds pairs 8c + 2(e/2) (x = cos,
+        // y = sin) and 8c + 2(e/2) + 1 (z = cos, w = sin)
+        const float4 t0 = tab[4 * c], t1 = tab[4 * c + 1], t2 = tab[4 * c + 2], t3 = tab[4 * c + 3];
+        const float ce[8] = {t0.x, t0.z, t1.x, t1.z, t2.x, t2.z, t3.x, t3.z};
+        const float se[8] = {t0.y, t0.w, t1.y, t1.w, t2.y, t2.w, t3.y, t3.w};
+        uint4 A = *pa, B = *pb;
+        __nv_bfloat162* a2 = reinterpret_cast<__nv_bfloat162*>(&A);
+        __nv_bfloat162* b2 = reinterpret_cast<__nv_bfloat162*>(&B);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 av = __bfloat1622float2(a2[u]), bv = __bfloat1622float2(b2[u]);
+            const float c0 = ce[2 * u], c1 = ce[2 * u + 1], s0 = se[2 * u], s1 = se[2 * u + 1];
+            a2[u] = __floats2bfloat162_rn(av.x * c0 - bv.x * s0, av.y * c1 - bv.y * s1);
+            b2[u] = __floats2bfloat162_rn(bv.x * c0 + av.x * s0, bv.y * c1 + av.y * s1);
+        }
+        *pa = A;
+        *pb = B;
+    }
+}
+
+__global__ void __launch_bounds__(256, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
                    const __grid_constant__ CUtensorMap tm_sv, const TcArgs a) {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned tiles for the 128-byte swizzle (the slack is part of the request)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    // barrier slots
     enum {
-        B_QFULL = 0,              // [2] TMA Q landed
-        B_QREADY = 2,             // [2] Q rotated (64 arrivals)
-        B_QEMPTY = 4,             // [2] last QK of the tile done
-        B_KFULL = 6,              // [NS] TMA K landed
-        B_VFULL = B_KFULL + NS,   // [NS] TMA V landed
-        B_KREADY = B_VFULL + NS,  // [NS] K rotated (64 arrivals)
-        B_KVEMPTY = B_KREADY + NS,// [NS] PV of the stage done
-        B_SFULL = B_KVEMPTY + NS, // [2] QK done
-        B_PFULL = B_SFULL + 2,    // [2] P written, O rescaled (128 arrivals)
-        B_PVDONE = B_PFULL + 2,   // [2] PV done
-        B_FINAL = B_PVDONE + 2,   // MMA drain
+        B_QFULL = 0,               // TMA Q landed
+        B_QREADY = 1,              // Q rotated (64 arrivals)
+        B_QEMPTY = 2,              // last QK of the tile done
+        B_KFULL = 3,               // [NS] TMA K landed
+        B_VFULL = B_KFULL + NS,    // [NS] TMA V landed
+        B_KREADY = B_VFULL + NS,   // [NS] K rotated (64 arrivals)
+        B_KVEMPTY = B_KREADY + NS, // [NS] PV of the stage done
+        B_SFULL = B_KVEMPTY + NS,  // [2] QK done
+        B_PFULL = B_SFULL + 2,     // [2] S consumed, P written, O rescaled (128 arrivals)
+        B_PVDONE = B_PFULL + 2,    // [2] PV done
+        B_FINAL = B_PVDONE + 2,    // MMA drain
         NBARS = B_FINAL + 1
     };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
@@ -123,10 +173,10 @@ __global__ void __launch_bounds__(256, 1)
     auto bar = [&](int i) { return smem_u32(bars + i); };
 
     if (tid == 0) {
+        mbar_init(bar(B_QFULL), 1);
+        mbar_init(bar(B_QREADY), 64);
+        mbar_init(bar(B_QEMPTY), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_QFULL + i), 1);
-            mbar_init(bar(B_QREADY + i), 64);
-            mbar_init(bar(B_QEMPTY + i), 1);
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_PFULL + i), 128);
             mbar_init(bar(B_PVDONE + i), 1);
@@ -146,6 +196,15 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+#ifdef KVM_PROBE
+    unsigned probe_sm = 0;
+    if (tid == 0) {
+        if (blockIdx.x == 0) g_probe_attn[31] = gridDim.x;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(probe_sm));
+        const unsigned long long now = atomicAdd(&g_probe_attn[32 + (probe_sm & 31)], 1ull) + 1;
+        atomicMax(&g_probe_attn[29], now);
+    }
+#endif
     const uint32_t tmem = *tmem_slot;
     const uint32_t sQ = smem_u32(smem + OFF_Q), sK = smem_u32(smem + OFF_K);
     const uint32_t sV = smem_u32(smem + OFF_V), sP = smem_u32(smem + OFF_P);
@@ -154,79 +213,91 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            KVM_PROBE_DECL(3)
+            KVM_PROBE_START()
             int g = 0, tt = 0;
             for (int id = blockIdx.x; id < a.ntiles; id += gridDim.x, ++tt) {
                 const Tile T = tile_of(a, id);
-                const int qb = tt & 1;
-                if (tt >= 2 && !mbar_wait(bar(B_QEMPTY + qb), ((tt >> 1) - 1) & 1, abort_flag, a.status)) break;
-                mbar_expect_tx(bar(B_QFULL + qb), TILE_BYTES);
-                tma_load_3d(sQ + qb * TILE_BYTES, &tm_q, 0, (int)T.q0, T.bh, bar(B_QFULL + qb));
+                KVM_PROBE_LAP(2)
+                if (tt >= 1 && !mbar_wait(bar(B_QEMPTY), (tt - 1) & 1, abort_flag, a.status)) break;
+                KVM_PROBE_LAP(0)
+                mbar_expect_tx(bar(B_QFULL), Q_BYTES);
+                tma_load_3d(sQ, &tm_q, 0, (int)T.q0, T.bh, bar(B_QFULL));
                 bool ok = true;
                 for (int j = 0; j < T.nblk; ++j, ++g) {
                     const int s = g % NS;
+                    KVM_PROBE_LAP(2)
                     if (g >= NS && !mbar_wait(bar(B_KVEMPTY + s), ((g / NS) - 1) & 1, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(B_KFULL + s), TILE_BYTES);
-                    mbar_expect_tx(bar(B_VFULL + s), TILE_BYTES);
+                    KVM_PROBE_LAP(1)
+                    mbar_expect_tx(bar(B_KFULL + s), KV_BYTES);
+                    mbar_expect_tx(bar(B_VFULL + s), KV_BYTES);
                     if (j < T.nst) {
                         const int plane = T.bh * a.snap_events + T.e;
-                        tma_load_3d(sK + s * TILE_BYTES, &tm_sk, 0, 128 * j, plane, bar(B_KFULL + s));
-                        tma_load_3d(sV + s * TILE_BYTES, &tm_sv, 0, 128 * j, plane, bar(B_VFULL + s));
+                        tma_load_3d(sK + s * KV_BYTES, &tm_sk, 0, KB * j, plane, bar(B_KFULL + s));
+                        tma_load_3d(sV + s * KV_BYTES, &tm_sv, 0, KB * j, plane, bar(B_VFULL + s));
                     } else {
-                        const int key0 = (int)(T.ws + 128 * (j - T.nst));
-                        tma_load_3d(sK + s * TILE_BYTES, &tm_k, 0, key0, T.bh, bar(B_KFULL + s));
-                        tma_load_3d(sV + s * TILE_BYTES, &tm_v, 0, key0, T.bh, bar(B_VFULL + s));
+                        const int key0 = (int)(T.ws + KB * (j - T.nst));
+                        tma_load_3d(sK + s * KV_BYTES, &tm_k, 0, key0, T.bh, bar(B_KFULL + s));
+                        tma_load_3d(sV + s * KV_BYTES, &tm_v, 0, key0, T.bh, bar(B_VFULL + s));
                     }
                 }
                 if (!ok) break;
             }
+            KVM_PROBE_LAP(2)
+            KVM_PROBE_FLUSH(g_probe_attn, 0, 3)
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
+            const uint32_t idesc_qk = idesc_bf16(128, KB, 0, 0);
             const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
+            const int ks_state = min(a.r / 16, 3);
+            KVM_PROBE_DECL(5)
+            KVM_PROBE_START()
             int g = 0, tt = 0;
             bool ok = true;
             for (int id = blockIdx.x; id < a.ntiles && ok; id += gridDim.x, ++tt) {
                 const Tile T = tile_of(a, id);
-                const int qb = tt & 1;
-                if (!mbar_wait(bar(B_QREADY + qb), (tt >> 1) & 1, abort_flag, a.status)) break;
+                KVM_PROBE_LAP(4)
+                if (!mbar_wait(bar(B_QREADY), tt & 1, abort_flag, a.status)) break;
+                KVM_PROBE_LAP(0)
                 tc_fence_after();
-                const int ks_state = min(a.r / 16, 3);
                 auto issue_qk = [&](int j, int gq) -> bool {
                     const int s = gq % NS, sb = gq & 1;
+                    KVM_PROBE_LAP(4)
                     if (!mbar_wait(bar(B_KREADY + s), (gq / NS) & 1, abort_flag, a.status)) return false;
+                    KVM_PROBE_LAP(1)
                     tc_fence_after();
                     const int ks0 = j < T.nst ? ks_state : 0;
                     for (int ks = ks0; ks < 4; ++ks) {
-                        const uint64_t ad = sdesc_sw128(sQ + qb * TILE_BYTES + ks * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(sK + s * TILE_BYTES + ks * 32, 16, 1024);
-                        mma_bf16_ss(tmem + TM_S0 + sb * 128, ad, bd, idesc_qk, ks > ks0);
+                        const uint64_t ad = sdesc_sw128(sQ + ks * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(sK + s * KV_BYTES + ks * 32, 16, 1024);
+                        mma_bf16_ss(tmem + TM_S + sb * KB, ad, bd, idesc_qk, ks > ks0);
                     }
                     mma_commit(bar(B_SFULL + sb));
                     return true;
                 };
                 if (!issue_qk(0, g)) { ok = false; break; }
                 for (int j = 0; j < T.nblk; ++j) {
-                    const int gj = g + j;
+                    const int gj = g + j, s = gj % NS, pb = gj & 1;
+                    // S buffer of block gj + 1 last held block gj - 1, consumed before its P was published
                     if (j + 1 < T.nblk) {
                         if (!issue_qk(j + 1, gj + 1)) { ok = false; break; }
                     } else {
-                        mma_commit(bar(B_QEMPTY + qb));
+                        mma_commit(bar(B_QEMPTY));
                     }
-                    const int s = gj % NS, pb = gj & 1;
-                    if (!mbar_wait(bar(B_PFULL + pb), (gj >> 1) & 1, abort_flag, a.status) ||
-                        !mbar_wait(bar(B_VFULL + s), (gj / NS) & 1, abort_flag, a.status)) {
-                        ok = false;
-                        break;
-                    }
+                    KVM_PROBE_LAP(4)
+                    if (!mbar_wait(bar(B_PFULL + pb), (gj >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                    KVM_PROBE_LAP(2)
+                    if (!mbar_wait(bar(B_VFULL + s), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
+                    KVM_PROBE_LAP(3)
                     tc_fence_after();
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint64_t ad = sdesc_sw128(sP + pb * 2 * TILE_BYTES + (ks >> 2) * TILE_BYTES + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(sV + s * TILE_BYTES + ks * 2048, TILE_BYTES, 1024);
+                    for (int ks = 0; ks < KB / 16; ++ks) {
+                        const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + ks * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(sV + s * KV_BYTES + ks * 2048, KV_BYTES, 1024);
                         mma_bf16_ss(tmem + TM_O, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(bar(B_PVDONE + pb));
@@ -234,38 +305,51 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 g += T.nblk;
             }
-            // drain: every MMA issued above has completed once this arrives
+            KVM_PROBE_LAP(4)
+            KVM_PROBE_FLUSH(g_probe_attn, 3, 5)
             mma_commit(bar(B_FINAL));
             mbar_wait(bar(B_FINAL), 0, abort_flag, nullptr);
         }
     } else if (warp < 4) {
         // --------------------------------------------------------------- RoPE
         const int rt = tid - 64;
+        KVM_PROBE_DECL(4)
+        KVM_PROBE_START()
         int g = 0, tt = 0;
         for (int id = blockIdx.x; id < a.ntiles; id += gridDim.x, ++tt) {
             const Tile T = tile_of(a, id);
-            const int qb = tt & 1;
-            if (!mbar_wait(bar(B_QFULL + qb), (tt >> 1) & 1, abort_flag, a.status)) break;
+            KVM_PROBE_LAP(3)
+            if (!mbar_wait(bar(B_QFULL), tt & 1, abort_flag, a.status)) break;
+            KVM_PROBE_LAP(0)
             if (half > 0) {
                 for (int row = rt; row < 128; row += 64) {
                     const int64_t pos = T.q0 + row;
-                    if (pos < a.N) rope_row(smem + OFF_Q + qb * TILE_BYTES + row * 128, row, pos, a.rope, half);
+                    if (pos < a.N) {
+                        if ((half & 7) == 0)
+                            rope_row_vec(smem + OFF_Q + row * 128, row, pos, a.rope, half);
+                        else
+                            rope_row(smem + OFF_Q + row * 128, row, pos, a.rope, half);
+                    }
                 }
             }
             fence_proxy_async();
-            mbar_arrive(bar(B_QREADY + qb));
+            mbar_arrive(bar(B_QREADY));
             bool ok = true;
             for (int j = 0; j < T.nblk; ++j, ++g) {
                 const int s = g % NS;
+                KVM_PROBE_LAP(2)
                 if (!mbar_wait(bar(B_KFULL + s), (g / NS) & 1, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
+                KVM_PROBE_LAP(1)
                 if (j >= T.nst && half > 0) {
-                    const int64_t key0 = T.ws + 128 * (j - T.nst);
-                    for (int row = rt; row < 128; row += 64) {
-                        const int64_t pos = key0 + row;
-                        if (pos < a.N) rope_row(smem + OFF_K + s * TILE_BYTES + row * 128, row, pos, a.rope, half);
+                    const int64_t pos = T.ws + KB * (j - T.nst) + rt;
+                    if (pos < a.N) {
+                        if ((half & 7) == 0)
+                            rope_row_vec(smem + OFF_K + s * KV_BYTES + rt * 128, rt, pos, a.rope, half);
+                        else
+                            rope_row(smem + OFF_K + s * KV_BYTES + rt * 128, rt, pos, a.rope, half);
                     }
                 }
                 fence_proxy_async();
@@ -273,10 +357,16 @@ __global__ void __launch_bounds__(256, 1)
             }
             if (!ok) break;
         }
+        KVM_PROBE_LAP(2)
+        if (rt == 0) KVM_PROBE_FLUSH(g_probe_attn, 8, 4)
     } else {
         // ------------------------------------------------------------ softmax
         const int row = tid - 128;                 // query row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tO = tmem + lane_base + TM_O;
+        const float sc = a.scale_log2;
+        KVM_PROBE_DECL(10)
+        KVM_PROBE_START()
         int g = 0;
         bool ok = true;
         for (int id = blockIdx.x; id < a.ntiles && ok; id += gridDim.x) {
@@ -285,29 +375,37 @@ __global__ void __launch_bounds__(256, 1)
             float m_used = -INFINITY, l = 0.0f;
             for (int j = 0; j < T.nblk; ++j) {
                 const int gj = g + j, sb = gj & 1;
+                KVM_PROBE_LAP(9)
                 if (!mbar_wait(bar(B_SFULL + sb), (gj >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                KVM_PROBE_LAP(0)
+#ifdef KVM_PROBE
+                probe_acc[8] += 1;
+#endif
                 tc_fence_after();
-                uint32_t sr[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + TM_S0 + sb * 128 + c * 32, sr[c]);
+                uint32_t v[2][32];
+                tmem_ld32(tmem + lane_base + TM_S + sb * KB, v[0]);
+                tmem_ld32(tmem + lane_base + TM_S + sb * KB + 32, v[1]);
                 tmem_wait_ld();
                 const bool is_state = j < T.nst;
-                const int64_t key0 = is_state ? 0 : T.ws + 128 * (j - T.nst);
-                // limit: columns < lim are valid
+                const int64_t key0 = is_state ? 0 : T.ws + KB * (j - T.nst);
+                // columns < lim are valid keys for this query (a causal block may have none)
                 int lim;
-                if (is_state) lim = min(128, T.n - 128 * j);
-                else lim = (p - key0 + 1) < 128 ? (int)(p - key0 + 1) : 128;
-                float mblk = -INFINITY;
+                if (is_state) {
+                    lim = min(KB, T.n - KB * j);
+                } else {
+                    const int64_t d = p - key0 + 1;
+                    lim = d < 0 ? 0 : (d < KB ? (int)d : KB);
+                }
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
-                        const int col = c * 32 + x;
-                        float v = __uint_as_float(sr[c][x]) * a.scale_log2;
-                        v = col < lim ? v : -INFINITY;
-                        sr[c][x] = __float_as_uint(v);
-                        mblk = fmaxf(mblk, v);
+                        const float val = h * 32 + x < lim ? __uint_as_float(v[h][x]) : -INFINITY;
+                        v[h][x] = __float_as_uint(val);
+                        mx[x & 3] = fmaxf(mx[x & 3], val);
                     }
+                const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
                 bool rescale = false;
                 float alpha = 1.0f;
                 if (mblk > m_used) {
@@ -320,81 +418,85 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 }
                 l *= alpha;
-                uint32_t pk[64];
-                float rs = 0.0f;
+                KVM_PROBE_LAP(1)
+                const float mneg = -m_used;
+                uint32_t pk[32];
+                float rs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int x = 0; x < 32; x += 2) {
-                        const float p0 = ex2(__uint_as_float(sr[c][x]) - m_used);
-                        const float p1 = ex2(__uint_as_float(sr[c][x + 1]) - m_used);
-                        rs += p0 + p1;
-                        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                        pk[(c * 32 + x) >> 1] = *reinterpret_cast<uint32_t*>(&h);
+                        const float p0 = ex2(fmaf(__uint_as_float(v[h][x]), sc, mneg));
+                        const float p1 = ex2(fmaf(__uint_as_float(v[h][x + 1]), sc, mneg));
+                        rs[(x >> 1) & 3] += p0 + p1;
+                        pk[(h * 32 + x) >> 1] = pack_bf16(p0, p1);
                     }
-                l += rs;
+                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+                KVM_PROBE_LAP(4)
                 if (rescale) {
-                    // O holds blocks < j: wait for the last PV, then scale it in place
+                    // O holds blocks < j: wait for their last PV, then scale it in place
                     if (!mbar_wait(bar(B_PVDONE + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
-                    uint32_t o[2][32];
-                    tmem_ld32(tmem + lane_base + TM_O, o[0]);
-                    tmem_ld32(tmem + lane_base + TM_O + 32, o[1]);
-                    tmem_wait_ld();
+                    uint32_t o[32];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(tO + h * 32, o);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) o[h][x] = __float_as_uint(__uint_as_float(o[h][x]) * alpha);
-                    tmem_st32(tmem + lane_base + TM_O, o[0]);
-                    tmem_st32(tmem + lane_base + TM_O + 32, o[1]);
+                        for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+                        tmem_st32(tO + h * 32, o);
+                    }
                     tmem_wait_st();
                 }
+                KVM_PROBE_LAP(3)
                 // the P buffer was last read by the PV of block gj - 2
                 if (gj >= 2 && !mbar_wait(bar(B_PVDONE + sb), ((gj - 2) >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-                uint8_t* prow = smem + OFF_P + sb * 2 * TILE_BYTES + row * 128;
+                KVM_PROBE_LAP(2)
+                uint8_t* prow = smem + OFF_P + sb * P_BYTES + row * 128;
 #pragma unroll
-                for (int ch = 0; ch < 16; ++ch) {
-                    const int hsub = ch >> 3, c8 = ch & 7;
-                    uint4 val = make_uint4(pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-                    *reinterpret_cast<uint4*>(prow + hsub * TILE_BYTES + ((c8 ^ (row & 7)) << 4)) = val;
-                }
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
                 fence_proxy_async();
                 tc_fence_before();
                 mbar_arrive(bar(B_PFULL + sb));
+                KVM_PROBE_LAP(4)
             }
             if (!ok) break;
             // epilogue: O / l for this tile
             const int gl = g + T.nblk - 1;
+            KVM_PROBE_LAP(9)
             if (!mbar_wait(bar(B_PVDONE + (gl & 1)), (gl >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+            KVM_PROBE_LAP(5)
             tc_fence_after();
-            uint32_t o[2][32];
-            tmem_ld32(tmem + lane_base + TM_O, o[0]);
-            tmem_ld32(tmem + lane_base + TM_O + 32, o[1]);
-            tmem_wait_ld();
-            tc_fence_before();
-            if (p < a.N) {
-                const float il = 1.0f / l;
-                uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)T.bh * a.N + p) * D);
+            const float il = 1.0f / l;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+            for (int h = 0; h < 2; ++h) {
+                uint32_t o[32];
+                tmem_ld32(tO + h * 32, o);
+                tmem_wait_ld();
+                if (p < a.N) {
+                    uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)T.bh * a.N + p) * D) + h * 4;
 #pragma unroll
-                    for (int x = 0; x < 32; x += 8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[h][x + 2 * u]) * il,
-                                                                      __uint_as_float(o[h][x + 2 * u + 1]) * il);
-                            w[u] = *reinterpret_cast<uint32_t*>(&b2);
-                        }
-                        dst[(h * 32 + x) >> 3] = make_uint4(w[0], w[1], w[2], w[3]);
-                    }
+                    for (int x = 0; x < 32; x += 8)
+                        dst[x >> 3] = make_uint4(pack_bf16(__uint_as_float(o[x]) * il, __uint_as_float(o[x + 1]) * il),
+                                                 pack_bf16(__uint_as_float(o[x + 2]) * il, __uint_as_float(o[x + 3]) * il),
+                                                 pack_bf16(__uint_as_float(o[x + 4]) * il, __uint_as_float(o[x + 5]) * il),
+                                                 pack_bf16(__uint_as_float(o[x + 6]) * il, __uint_as_float(o[x + 7]) * il));
+                }
             }
+            tc_fence_before();
             g += T.nblk;
+            KVM_PROBE_LAP(6)
         }
+        if (row == 0) KVM_PROBE_FLUSH(g_probe_attn, 12, 10)
     }
 
     tc_fence_before();
     __syncthreads();
+#ifdef KVM_PROBE
+    if (tid == 0) atomicAdd(&g_probe_attn[32 + (probe_sm & 31)], ~0ull);
+#endif
     if (*abort_flag) {
         // let copies still in flight land before the shared memory is released
         const long long t0 = clock64();
@@ -406,6 +508,8 @@ __global__ void __launch_bounds__(256, 1)
         tmem_dealloc(tmem, TMEM_COLS);
     }
 }
+
+KVM_PROBE_READOUT(kvm_probe_read_attn, g_probe_attn)
 
 // ------------------------------------------------------------------ host
 
@@ -425,14 +529,14 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 }  // namespace tc
 
-// 3-D bf16 map over [planes][rows][64] with a 128 x 64 box, 128-byte swizzle.
-bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes) {
+// 3-D bf16 map over [planes][rows][64] with a box_rows x 64 box, 128-byte swizzle.
+bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes, uint32_t box_rows) {
     using namespace tc;
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[3] = {64, rows, planes};
     cuuint64_t strides[2] = {64 * 2, rows * 64 * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -449,10 +553,10 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, msk, msv;
     const uint64_t BH = (uint64_t)a.BH;
     const uint64_t planes_snap = BH * (uint64_t)(a.snap_events > 0 ? a.snap_events : 1);
-    if (!make_tmap_bf16_3d(&mq, a.q, (uint64_t)a.N, BH) || !make_tmap_bf16_3d(&mk, a.k, (uint64_t)a.N, BH) ||
-        !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH) ||
-        !make_tmap_bf16_3d(&msk, a.snap_k, (uint64_t)a.M, planes_snap) ||
-        !make_tmap_bf16_3d(&msv, a.snap_v, (uint64_t)a.M, planes_snap))
+    if (!make_tmap_bf16_3d(&mq, a.q, (uint64_t)a.N, BH, 128) || !make_tmap_bf16_3d(&mk, a.k, (uint64_t)a.N, BH, KB) ||
+        !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH, KB) ||
+        !make_tmap_bf16_3d(&msk, a.snap_k, (uint64_t)a.M, planes_snap, KB) ||
+        !make_tmap_bf16_3d(&msv, a.snap_v, (uint64_t)a.M, planes_snap, KB))
         return cudaErrorInvalidValue;
     TcArgs t;
     t.N = a.N;
@@ -475,8 +579,40 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     }
-    const int grid = t.ntiles < nsm ? t.ntiles : nsm;
-    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+        // Two CTAs per SM fit (2 x 97 KB shared memory, 2 x 256 x 128 registers, 2 x 256
+        // TMEM columns), but the occupancy calculator reports one for this kernel.  CTAs
+        // of the persistent grid never wait on each other, so a grid of two per SM is
+        // correct whether or not both are resident.
+        per_sm = 2;
+#ifdef KVM_PROBE
+        {
+            int dev = 0, smem_sm = 0, resv = 0, regs_sm = 0, occ = -1;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+            cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+            cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_tc_kernel, 256, SMEM_BYTES);
+            cudaFuncAttributes fa;
+            cudaFuncGetAttributes(&fa, attn_tc_kernel);
+            for (int sz : {0, 16384, 49152, 65536, 81920, 99584}) {
+                int o2 = -1;
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, attn_tc_kernel, 256, sz);
+                int o3 = -1;
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o3, attn_tc_kernel, 128, sz);
+                fprintf(stderr, "[probe] dyn smem %d -> occupancy %d (256 thr) %d (128 thr)\n", sz, o2, o3);
+            }
+            fprintf(stderr, "[probe] attn occupancy %d (err %d %s) smem/SM %d reserved/block %d regs/SM %d "
+                    "kernel regs %d static smem %zu dyn %d maxdyn %d\n", occ, (int)oe, cudaGetErrorString(oe),
+                    smem_sm, resv, regs_sm, fa.numRegs, fa.sharedSizeBytes, SMEM_BYTES, fa.maxDynamicSharedSizeBytes);
+        }
+#endif
+    }
+    const int grid = t.ntiles < per_sm * nsm ? t.ntiles : per_sm * nsm;
     attn_tc_kernel<<<grid, 256, SMEM_BYTES, s>>>(mq, mk, mv, msk, msv, t);
     return cudaGetLastError();
 }

@@ -43,6 +43,7 @@ struct Misc {
     float pb[2][TOK], ps[2][TOK];
     int pa[2][TOK];
     int kind[TOK], slot[TOK], list[TOK];
+    int hist[4][MAXS];  // merged tokens per slot, per token warp
     int cnt[MAXS];
     float rho[MAXS];
     int cnt_new[MAXS];
@@ -54,6 +55,10 @@ struct Misc {
     int abort_flag;
 };
 constexpr int SMEM_BYTES = OFF_MISC + (int)sizeof(Misc) + 1024;
+
+#ifdef KVM_PROBE
+static __device__ unsigned long long g_probe_fold[16];
+#endif
 
 __device__ __forceinline__ int swz(int row, int ch) { return row * ROWB + (((ch ^ (row & 7)) & 7) << 4); }
 
@@ -77,19 +82,45 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// Sums over 64 registers with eight independent partial sums (short dependency chains).
+__device__ __forceinline__ float sum64(const float (&x)[64]) {
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[i] = x[i];
+#pragma unroll
+    for (int i = 8; i < 64; ++i) p[i & 7] += x[i];
+    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+}
+// sum over x of (x - c)^2, eight partial sums
+__device__ __forceinline__ float sqdev64(const float (&x)[64], float c, float scale) {
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float d = x[i] * scale - c;
+        p[i] = d * d;
+    }
+#pragma unroll
+    for (int i = 8; i < 64; ++i) {
+        const float d = x[i] * scale - c;
+        p[i & 7] = fmaf(d, d, p[i & 7]);
+    }
+    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+}
+// dot product of two 64-vectors, eight partial sums
+__device__ __forceinline__ float dot64(const float (&x)[64], const float (&y)[64]) {
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[i] = x[i] * y[i];
+#pragma unroll
+    for (int i = 8; i < 64; ++i) p[i & 7] = fmaf(x[i], y[i], p[i & 7]);
+    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+}
+
 // Owner-thread renormalisation of slot j from its key sums (registers): the
 // winner-take-all direction (hi/lo) and the read-view key.
 __device__ __forceinline__ void owner_view_k(int j, const float (&sk)[64], int cnt, int r, float eps, uint8_t* sm) {
-    float mean = 0.0f;
-#pragma unroll
-    for (int x = 0; x < 64; ++x) mean += sk[x];
-    mean *= (1.0f / 64.0f);
-    float ss = 0.0f;
-#pragma unroll
-    for (int x = 0; x < 64; ++x) {
-        const float c = sk[x] - mean;
-        ss = fmaf(c, c, ss);
-    }
+    const float mean = sum64(sk) * (1.0f / 64.0f);
+    const float ss = sqdev64(sk, mean, 1.0f);
     const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
@@ -106,17 +137,11 @@ __device__ __forceinline__ void owner_view_k(int j, const float (&sk)[64], int c
     }
     // read key: LayerNorm(sum_k / count), rotary dims zeroed
     const float ic = 1.0f / (float)cnt;
-    float mx = 0.0f;
+    float xs[64];
 #pragma unroll
-    for (int x = 0; x < 64; ++x) mx += sk[x] * ic;
-    mx *= (1.0f / 64.0f);
-    float var = 0.0f;
-#pragma unroll
-    for (int x = 0; x < 64; ++x) {
-        const float d = sk[x] * ic - mx;
-        var = fmaf(d, d, var);
-    }
-    var *= (1.0f / 64.0f);
+    for (int x = 0; x < 64; ++x) xs[x] = sk[x] * ic;
+    const float mx = sum64(xs) * (1.0f / 64.0f);
+    const float var = sqdev64(xs, mx, 1.0f) * (1.0f / 64.0f);
     const float rs = 1.0f / sqrtf(var + eps);
     uint4* vk = reinterpret_cast<uint4*>(sm + OFF_VK + j * ROWB);
 #pragma unroll
@@ -135,10 +160,7 @@ __device__ __forceinline__ void owner_view_k(int j, const float (&sk)[64], int c
 
 // Read-view value of slot j: rho * unit(sum_v).
 __device__ __forceinline__ void owner_view_v(int j, const float (&sv)[64], float rho, uint8_t* sm) {
-    float nv2 = 0.0f;
-#pragma unroll
-    for (int x = 0; x < 64; ++x) nv2 = fmaf(sv[x], sv[x], nv2);
-    const float nv = sqrtf(nv2);
+    const float nv = sqrtf(dot64(sv, sv));
     const float f = nv > 0.0f ? rho / nv : 0.0f;
     uint4* vv = reinterpret_cast<uint4*>(sm + OFF_VV + j * ROWB);
 #pragma unroll
@@ -251,6 +273,8 @@ __global__ void __launch_bounds__(256, 1)
     if (tid == 0 && a.e_begin < a.e_end) load_chunk(a.e_begin, 0);
     const uint32_t idesc = idesc_bf16(128, 256, 0, 0);
     int mma_count = 0;
+    KVM_PROBE_DECL(11)
+    KVM_PROBE_START()
 
     for (int e = a.e_begin, it = 0; e < a.e_end; ++e, ++it) {
         const int buf = it & 1;
@@ -261,6 +285,10 @@ __global__ void __launch_bounds__(256, 1)
         }
         __syncthreads();
         if (X.abort_flag) break;
+        KVM_PROBE_LAP(0)
+#ifdef KVM_PROBE
+        probe_acc[8] += 1;
+#endif
         const int64_t first_pos = (int64_t)e * C;
         const int64_t off = first_pos % a.src_len;
         const uint8_t* kch = sm + OFF_K + buf * TOK * ROWB;
@@ -285,17 +313,16 @@ __global__ void __launch_bounds__(256, 1)
             X.g[t] = a.g_src[(int64_t)bh * a.src_row + off + t];
             float kx[64];
             load_row_sw(kch, t, kx);
-            float nn = 0.0f;
-#pragma unroll
-            for (int x = 0; x < 64; ++x) nn = fmaf(kx[x], kx[x], nn);
-            X.kn[t] = sqrtf(nn);
+            X.kn[t] = sqrtf(dot64(kx, kx));
             const bool sink = first_pos + t < S;
             X.kind[t] = sink ? 2 : -1;
             X.slot[t] = sink ? (int)(first_pos + t) : -1;
         }
-        X.cnt_new[tid] = 0;
         X.slot_tok[tid] = -1;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) X.hist[w][tid] = 0;
         __syncthreads();
+        KVM_PROBE_LAP(1)
 
         // best / second / argmax over the mergeable slots [S, n0): each half of
         // the CTA scans 128 slot columns of every token row
@@ -303,32 +330,56 @@ __global__ void __launch_bounds__(256, 1)
             if (tid == 0 && !mbar_wait(bar_s, mma_count & 1, &X.abort_flag, a.status)) X.abort_flag = 1;
             __syncthreads();
             if (X.abort_flag) break;
+            KVM_PROBE_LAP(9)
             ++mma_count;
             tc_fence_after();
             const int half = tid >> 7, t = tid & 127;
             const int lo = max(S, half * 128), hi = min(n0, half * 128 + 128);
-            float b = -INFINITY, s2 = -INFINITY;
-            int ba = -1;
+            // four independent chains (one per 32-column chunk), merged in index order
+            float bq[4], sq[4];
+            int aq[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                bq[c] = -INFINITY;
+                sq[c] = -INFINITY;
+                aq[c] = -1;
+            }
             if (lo < hi) {
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(t_sim + half * 128 + c * 32, v);
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(t_sim + half * 128 + (2 * c2) * 32, v0);
+                    tmem_ld32(t_sim + half * 128 + (2 * c2 + 1) * 32, v1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int x = 0; x < 32; ++x) {
-                        const int j = half * 128 + c * 32 + x;
-                        const float val = __uint_as_float(v[x]);
-                        if (j >= lo && j < hi) {
-                            if (val > b) {
-                                s2 = b;
-                                b = val;
-                                ba = j;
-                            } else if (val > s2) {
-                                s2 = val;
-                            }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const int c = 2 * c2 + q;
+                            const int j = half * 128 + c * 32 + x;
+                            const float raw = __uint_as_float(q ? v1[x] : v0[x]);
+                            const float val = (j >= lo && j < hi) ? raw : -INFINITY;
+                            // branchless: a strictly larger value takes the lead (lower index kept on ties)
+                            const bool gt = val > bq[c];
+                            sq[c] = gt ? bq[c] : fmaxf(sq[c], val);
+                            aq[c] = gt ? j : aq[c];
+                            bq[c] = gt ? val : bq[c];
                         }
                     }
+                }
+            }
+            float b = bq[0], s2 = sq[0];
+            int ba = aq[0];
+#pragma unroll
+            for (int c = 1; c < 4; ++c) {
+                if (aq[c] < 0) continue;
+                if (ba < 0 || bq[c] > b) {  // a strictly larger value from a later chunk wins
+                    s2 = fmaxf(fmaxf(s2, sq[c]), ba < 0 ? -INFINITY : b);
+                    b = bq[c];
+                    ba = aq[c];
+                } else {
+                    s2 = fmaxf(s2, bq[c]);
+                    s2 = fmaxf(s2, sq[c]);
                 }
             }
             X.pb[half][t] = b;
@@ -337,6 +388,7 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_before();
             __syncthreads();
         }
+        KVM_PROBE_LAP(2)
         float best = -INFINITY, sec = -INFINITY;
         int barg = -1;
         const bool cand = tid < C && X.kind[tid] != 2;
@@ -365,6 +417,7 @@ __global__ void __launch_bounds__(256, 1)
             int rank = 0;
             if (cand) {
                 const float mt = X.m[tid];
+#pragma unroll 4
                 for (int u = 0; u < C; ++u) {
                     if (X.kind[u] == 2) continue;
                     const float mu = X.m[u];
@@ -385,6 +438,7 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         if (tid < C && X.kind[tid] != 0) X.slot_tok[X.slot[tid]] = tid;
         __syncthreads();
+        KVM_PROBE_LAP(3)
 
         if (na > 0) {
             // directions of the new slots (from their founding token), then the
@@ -395,24 +449,18 @@ __global__ void __launch_bounds__(256, 1)
                 float kx[64];
                 load_row_sw(kch, t, kx);
                 const float g = X.g[t];
-                float mean = 0.0f;
 #pragma unroll
-                for (int x = 0; x < 64; ++x) mean += g * kx[x];
-                mean *= (1.0f / 64.0f);
-                float ss = 0.0f;
-#pragma unroll
-                for (int x = 0; x < 64; ++x) {
-                    const float c = g * kx[x] - mean;
-                    ss = fmaf(c, c, ss);
-                }
+                for (int x = 0; x < 64; ++x) kx[x] = g * kx[x];
+                const float mean = sum64(kx) * (1.0f / 64.0f);
+                const float ss = sqdev64(kx, mean, 1.0f);
                 const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const float a0 = (g * kx[ch * 8 + 2 * u] - mean) * inv;
-                        const float a1 = (g * kx[ch * 8 + 2 * u + 1] - mean) * inv;
+                        const float a0 = (kx[ch * 8 + 2 * u] - mean) * inv;
+                        const float a1 = (kx[ch * 8 + 2 * u + 1] - mean) * inv;
                         const __nv_bfloat16 h0 = __float2bfloat16_rn(a0), h1 = __float2bfloat16_rn(a1);
                         hw[u] = pack2(__bfloat162float(h0), __bfloat162float(h1));
                         lw[u] = pack2(a0 - __bfloat162float(h0), a1 - __bfloat162float(h1));
@@ -429,9 +477,9 @@ __global__ void __launch_bounds__(256, 1)
                     float hx[64], lx[64];
                     load_row_sw(sm + OFF_UHI, jj, hx);
                     load_row_sw(sm + OFF_ULO, jj, lx);
-                    float s = 0.0f;
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) s = fmaf(kx[x], hx[x] + lx[x], s);
+                    for (int x = 0; x < 64; ++x) hx[x] += lx[x];
+                    const float s = dot64(kx, hx);
                     if (s > best) {
                         sec = best;
                         best = s;
@@ -460,30 +508,39 @@ __global__ void __launch_bounds__(256, 1)
         }
         __syncthreads();
 
-        // merge lists: merged tokens grouped by slot, position order inside a slot
-        int rank_in_slot = 0;
+        KVM_PROBE_LAP(4)
+        // merge lists: merged tokens grouped by slot, position order inside a slot.
+        // A token's rank among earlier tokens of its slot = earlier lanes of its
+        // warp with the same slot (match_any) + the same slot's count in earlier warps.
+        int rank_in_slot = 0, sj = -1;
         const bool merged = tid < C && X.kind[tid] == 0 && X.slot[tid] >= 0;
-        if (merged) {
-            const int sj = X.slot[tid];
-            atomicAdd(&X.cnt_new[sj], 1);
-            for (int u = 0; u < tid; ++u) rank_in_slot += (X.kind[u] == 0 && X.slot[u] == sj);
+        if (warp < 4) {
+            sj = merged ? X.slot[tid] : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, merged ? sj : MAXS + (tid & 31));
+            const int lane = tid & 31;
+            rank_in_slot = __popc(same & ((1u << lane) - 1u));
+            if (merged && rank_in_slot == 0) X.hist[warp][sj] = __popc(same);
         }
+        __syncthreads();
+        if (merged)
+            for (int w = 0; w < warp; ++w) rank_in_slot += X.hist[w][sj];
+        X.cnt_new[tid] = X.hist[0][tid] + X.hist[1][tid] + X.hist[2][tid] + X.hist[3][tid];
         __syncthreads();
         if (warp == 0) {
             const int lane = tid & 31;
-            int v8[8], s = 0;
+            int v8[8], sacc = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 v8[i] = X.cnt_new[lane * 8 + i];
-                s += v8[i];
+                sacc += v8[i];
             }
-            int incl = s;
+            int incl = sacc;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
-            int run = incl - s;
+            int run = incl - sacc;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 X.seg[lane * 8 + i] = run;
@@ -494,8 +551,9 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) bulk_wait_read();
         }
         __syncthreads();
-        if (merged) X.list[X.seg[X.slot[tid]] + rank_in_slot] = tid;
+        if (merged) X.list[X.seg[sj] + rank_in_slot] = tid;
         __syncthreads();
+        KVM_PROBE_LAP(5)
 
         // owner threads: founding and merging into their slot, then the new read view
         {
@@ -518,6 +576,7 @@ __global__ void __launch_bounds__(256, 1)
                         for (int x = 0; x < 64; ++x) x64[x] = g * tx[x];
                         cnt = 0;
                     }
+                    // merged tokens in position order
                     for (int i = b0; i < b0 + nm; ++i) {
                         const int t = X.list[i];
                         load_row_sw(kch, t, tx);
@@ -535,13 +594,9 @@ __global__ void __launch_bounds__(256, 1)
                     if (ft >= 0) {
                         load_row_sw(vch, ft, tx);
                         const float g = X.g[ft];
-                        float nv2 = 0.0f;
 #pragma unroll
-                        for (int x = 0; x < 64; ++x) {
-                            x64[x] = g * tx[x];
-                            nv2 = fmaf(tx[x], tx[x], nv2);
-                        }
-                        rho = sqrtf(nv2);
+                        for (int x = 0; x < 64; ++x) x64[x] = g * tx[x];
+                        rho = sqrtf(dot64(tx, tx));
                     }
                     for (int i = b0; i < b0 + nm; ++i) {
                         const int t = X.list[i];
@@ -558,6 +613,7 @@ __global__ void __launch_bounds__(256, 1)
                 tmem_wait_st();
             }
         }
+        KVM_PROBE_LAP(6)
         tc_fence_before();
         fence_proxy_async();
         __syncthreads();
@@ -572,6 +628,7 @@ __global__ void __launch_bounds__(256, 1)
             bulk_commit();
         }
         n = sc.n_after;
+        KVM_PROBE_LAP(7)
     }
 
     // write the state back for decode, export and the portable kernels
@@ -582,16 +639,8 @@ __global__ void __launch_bounds__(256, 1)
         float x64[64];
         tmem_ld64(t_sums, x64);
         if (wr) {
-            float mean = 0.0f;
-#pragma unroll
-            for (int x = 0; x < 64; ++x) mean += x64[x];
-            mean *= (1.0f / 64.0f);
-            float ss = 0.0f;
-#pragma unroll
-            for (int x = 0; x < 64; ++x) {
-                const float c = x64[x] - mean;
-                ss = fmaf(c, c, ss);
-            }
+            const float mean = sum64(x64) * (1.0f / 64.0f);
+            const float ss = sqdev64(x64, mean, 1.0f);
             const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
             float4* dk = reinterpret_cast<float4*>(g_sum_k + (int64_t)j * D);
             float4* ds = reinterpret_cast<float4*>(g_simdir + (int64_t)j * D);
@@ -620,6 +669,8 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
     }
+    KVM_PROBE_LAP(10)
+    if (tid == 0) KVM_PROBE_FLUSH(g_probe_fold, 0, 11)
     tc_fence_before();
     __syncthreads();
     if (X.abort_flag) {
@@ -635,12 +686,14 @@ __global__ void __launch_bounds__(256, 1)
 
 }  // namespace foldtc
 
+KVM_PROBE_READOUT(kvm_probe_read_fold, foldtc::g_probe_fold)
+
 bool fold_tc_supported(const FoldArgs& a, bool bf16) { return bf16 && a.C <= 128 && a.M <= foldtc::MAXS; }
 
 cudaError_t launch_fold_tc(const FoldArgs& a, cudaStream_t s) {
     CUtensorMap mk, mv;
-    if (!make_tmap_bf16_3d(&mk, a.k_src, (uint64_t)a.src_row, (uint64_t)a.BH) ||
-        !make_tmap_bf16_3d(&mv, a.v_src, (uint64_t)a.src_row, (uint64_t)a.BH))
+    if (!make_tmap_bf16_3d(&mk, a.k_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
+        !make_tmap_bf16_3d(&mv, a.v_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(foldtc::fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, foldtc::SMEM_BYTES);
     foldtc::fold_tc_kernel<<<a.BH, 256, foldtc::SMEM_BYTES, s>>>(mk, mv, a);

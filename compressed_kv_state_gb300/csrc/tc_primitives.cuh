@@ -8,6 +8,29 @@
 
 #include "kvm_internal.cuh"
 
+// Optional phase timers (compiled in only with -DKVM_PROBE): cycles spent per
+// role and per wait, summed over CTAs into a per-file device counter array.
+#ifdef KVM_PROBE
+#define KVM_PROBE_DECL(n) long long probe_acc[n] = {0}; long long probe_t = 0;
+#define KVM_PROBE_START() probe_t = clock64();
+#define KVM_PROBE_LAP(i) { long long _n = clock64(); probe_acc[i] += _n - probe_t; probe_t = _n; }
+#define KVM_PROBE_FLUSH(arr, base, n) { for (int _i = 0; _i < (n); ++_i) atomicAdd(&arr[(base) + _i], (unsigned long long)probe_acc[_i]); }
+#define KVM_PROBE_READOUT(fname, arr) \
+    extern "C" int fname(unsigned long long* host) { \
+        cudaDeviceSynchronize(); \
+        int e = (int)cudaMemcpyFromSymbol(host, arr, sizeof(arr)); \
+        unsigned long long z[sizeof(arr) / 8] = {0}; \
+        cudaMemcpyToSymbol(arr, z, sizeof(arr)); \
+        return e; \
+    }
+#else
+#define KVM_PROBE_DECL(n)
+#define KVM_PROBE_START() {}
+#define KVM_PROBE_LAP(i) {}
+#define KVM_PROBE_FLUSH(arr, base, n) {}
+#define KVM_PROBE_READOUT(fname, arr)
+#endif
+
 namespace kvm {
 namespace tc {
 
@@ -191,7 +214,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 }  // namespace tc
 
-// Host: 3-D bf16 tensor map over [planes][rows][64], 128 x 64 box, 128-byte swizzle.
-bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes);
+// Host: 3-D bf16 tensor map over [planes][rows][64], box_rows x 64 box, 128-byte swizzle.
+bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes, uint32_t box_rows);
 
 }  // namespace kvm
