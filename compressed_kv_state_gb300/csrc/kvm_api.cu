@@ -104,6 +104,7 @@ Layout layout_of(const kvm_config& c) {
     L.ring_k = take(BH * ring * d * es);
     L.ring_v = take(BH * ring * d * es);
     L.ring_g = take(BH * ring * 4);
+    L.ring_kr = take(BH * ring * d * es);
     L.snap_k = take(BH * E * M * d * es);
     L.snap_v = take(BH * E * M * d * es);
     L.rope = take((size_t)c.max_tokens * (c.rope_dims / 2) * sizeof(float2) + 16);
@@ -354,6 +355,9 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         ra.ring_k = ly->ws + L.ring_k;
         ra.ring_v = ly->ws + L.ring_v;
         ra.ring_g = ly->at<float>(L.ring_g);
+        ra.ring_kr = ly->ws + L.ring_kr;
+        ra.rope = ly->at<float2>(L.rope);
+        ra.r = c.rope_dims;
         ra.N = n_tokens;
         ra.first = E * c.chunk;
         ra.L = c.window + c.chunk;
@@ -428,6 +432,7 @@ kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const vo
     da.ring_k = ly->ws + L.ring_k;
     da.ring_v = ly->ws + L.ring_v;
     da.ring_g = ly->at<float>(L.ring_g);
+    da.ring_kr = ly->ws + L.ring_kr;
     da.view_k = ly->ws + L.view_k;
     da.view_v = ly->ws + L.view_v;
     da.M = c.max_slots;
@@ -439,6 +444,7 @@ kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const vo
     da.r = c.rope_dims;
     da.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     da.BH = BH;
+    da.status = ly->at<int>(L.status);
     cudaError_t e = timed(ly, PH_DECODE, s, [&] { return kvm::launch_decode(da, bf16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "decode launch");
     ly->n_slots = n;
@@ -514,6 +520,22 @@ kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda
     ra.BH = c.batch * c.heads;
     cudaError_t e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_renorm(ra, c.dtype == KVM_BF16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "renormalise launch");
+    // rotated copy of the imported window: tokens at positions [pos - (W + C), pos)
+    const int64_t Lr = (int64_t)c.window + c.chunk;
+    kvm::RingFillArgs rf{};
+    rf.ring_k = ly->ws + L.ring_k;
+    rf.ring_v = ly->ws + L.ring_v;
+    rf.ring_g = ly->at<float>(L.ring_g);
+    rf.ring_kr = ly->ws + L.ring_kr;
+    rf.rope = ly->at<float2>(L.rope);
+    rf.r = c.rope_dims;
+    rf.N = src->pos;
+    rf.first = src->pos > Lr ? src->pos - Lr : 0;
+    rf.L = (int)Lr;
+    rf.BH = c.batch * c.heads;
+    rf.rotate_only = 1;
+    e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_ring_fill(rf, c.dtype == KVM_BF16, s); });
+    if (e != cudaSuccess) return ly->cuda_fail(e, "ring rotation launch");
     ly->n_slots = src->n_slots;
     ly->n_overflow = src->n_overflow;
     ly->pos = src->pos;

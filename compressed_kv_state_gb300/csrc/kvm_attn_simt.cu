@@ -140,20 +140,38 @@ __global__ void __launch_bounds__(64) attn_simt_kernel(AttnArgs a, int QB) {
     }
 }
 
+// Window ring: tokens [first, N) of each row enter the ring (row = position mod L)
+// with their unrotated key (for folds and export), value, gate, and a copy of the
+// key rotated at the token's position (for decode attention).  rotate_only:
+// rebuild only the rotated copy from the ring's own keys.
 template <typename T>
 __global__ void ring_fill_kernel(RingFillArgs a) {
     const int bh = blockIdx.y;
+    const int half = a.r / 2;
     const int64_t cnt = a.N - a.first;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < cnt * D;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t tok = a.first + i / D;
         const int x = (int)(i % D);
         const int64_t slot = tok % a.L;
-        const int64_t src = ((int64_t)bh * a.N + tok) * D + x;
         const int64_t dst = ((int64_t)bh * a.L + slot) * D + x;
-        reinterpret_cast<T*>(a.ring_k)[dst] = reinterpret_cast<const T*>(a.k)[src];
-        reinterpret_cast<T*>(a.ring_v)[dst] = reinterpret_cast<const T*>(a.v)[src];
-        if (x == 0) a.ring_g[(int64_t)bh * a.L + slot] = a.g[(int64_t)bh * a.N + tok];
+        const T* krow;
+        if (a.rotate_only) {
+            krow = reinterpret_cast<const T*>(a.ring_k) + ((int64_t)bh * a.L + slot) * D;
+        } else {
+            const int64_t src = ((int64_t)bh * a.N + tok) * D;
+            krow = reinterpret_cast<const T*>(a.k) + src;
+            reinterpret_cast<T*>(a.ring_k)[dst] = krow[x];
+            reinterpret_cast<T*>(a.ring_v)[dst] = reinterpret_cast<const T*>(a.v)[src + x];
+            if (x == 0) a.ring_g[(int64_t)bh * a.L + slot] = a.g[(int64_t)bh * a.N + tok];
+        }
+        float kv = to_f<T>(krow[x]);
+        if (x < 2 * half) {
+            const int i2 = x < half ? x : x - half;
+            const float2 cs = a.rope[tok * half + i2];
+            kv = x < half ? kv * cs.x - to_f<T>(krow[x + half]) * cs.y : kv * cs.x + to_f<T>(krow[x - half]) * cs.y;
+        }
+        reinterpret_cast<T*>(a.ring_kr)[dst] = from_f<T>(kv);
     }
 }
 

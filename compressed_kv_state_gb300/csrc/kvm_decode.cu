@@ -11,14 +11,41 @@
 
 namespace kvm {
 
-constexpr int DEC_THREADS = 128;
+constexpr int DEC_WARPS = 4;
+constexpr int DEC_THREADS = DEC_WARPS * 32;
+constexpr int TK = 32;  // keys per tile
 
+__device__ __forceinline__ uint32_t dsmem_u32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+// bulk global -> shared copy completing on an mbarrier (16-byte aligned, multiple of 16 bytes)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+template <typename T> __device__ __forceinline__ float2 ld2s(const T* p);
+template <> __device__ __forceinline__ float2 ld2s<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+template <> __device__ __forceinline__ float2 ld2s<float>(const float* p) { return *reinterpret_cast<const float2*>(p); }
+
+// One CTA per (b, h), four warps.  Keys (state rows, then the window in
+// position order) are split into one contiguous range per warp; each warp
+// streams its range in tiles of 32 keys through two shared-memory stages of
+// its own, filled by bulk copies (a tile is at most three contiguous row runs:
+// state view, window up to the ring's end, window from the ring's start).
+// Scores are dim-parallel (lane = 2 dims) with a butterfly transpose-reduce
+// that leaves key i's score on lane i; P V is dim-parallel from shared memory;
+// online softmax per warp, warps combined at the end.
 template <typename T>
-__global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(DEC_THREADS, 3) decode_kernel(DecodeArgs a) {
+    constexpr int RB = 64 * (int)sizeof(T);  // bytes per key row
+    constexpr int TILE = TK * RB;            // bytes of one K (or V) tile
+    extern __shared__ __align__(128) uint8_t dsm[];
     __shared__ float qs[D];
-    __shared__ float kbuf[DEC_THREADS / 32][D];
-    __shared__ float accs[DEC_THREADS / 32][D];
-    __shared__ float ls[DEC_THREADS / 32], mxs[DEC_THREADS / 32];
+    __shared__ float red_m[DEC_WARPS], red_l[DEC_WARPS];
+    __shared__ float red_acc[DEC_WARPS][D];
+    __shared__ __align__(8) unsigned long long bars[DEC_WARPS][2];
     const int bh = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = a.W + a.C;
@@ -26,110 +53,176 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_kernel(DecodeArgs a) {
     const int half = a.r / 2;
     T* rk = reinterpret_cast<T*>(a.ring_k) + (int64_t)bh * L * D;
     T* rv = reinterpret_cast<T*>(a.ring_v) + (int64_t)bh * L * D;
+    T* rkr = reinterpret_cast<T*>(a.ring_kr) + (int64_t)bh * L * D;
 
-    // the new token enters the ring
+    // the new token enters the rings (its key also rotated at position p); rotated, scaled query
     if (tid < D) {
-        const int64_t sl = (p % L) * D + tid;
-        rk[sl] = reinterpret_cast<const T*>(a.k)[(int64_t)bh * D + tid];
-        rv[sl] = reinterpret_cast<const T*>(a.v)[(int64_t)bh * D + tid];
+        const int x = tid;
+        const T* k = reinterpret_cast<const T*>(a.k) + (int64_t)bh * D;
+        const T* q = reinterpret_cast<const T*>(a.q) + (int64_t)bh * D;
+        const int64_t sl = (p % L) * D + x;
+        rk[sl] = k[x];
+        rv[sl] = reinterpret_cast<const T*>(a.v)[(int64_t)bh * D + x];
+        float kx = to_f<T>(k[x]), qx = to_f<T>(q[x]);
+        if (x < 2 * half) {
+            const int i = x < half ? x : x - half;
+            const float2 cs = a.rope[p * half + i];
+            if (x < half) {
+                kx = kx * cs.x - to_f<T>(k[x + half]) * cs.y;
+                qx = qx * cs.x - to_f<T>(q[x + half]) * cs.y;
+            } else {
+                kx = kx * cs.x + to_f<T>(k[x - half]) * cs.y;
+                qx = qx * cs.x + to_f<T>(q[x - half]) * cs.y;
+            }
+        }
+        rkr[sl] = from_f<T>(kx);
+        qs[x] = qx * a.scale_log2;
     }
     if (tid == 0) a.ring_g[(int64_t)bh * L + p % L] = a.g[bh];
-    // rotated, scaled query
-    if (tid < D) {
-        const T* q = reinterpret_cast<const T*>(a.q) + (int64_t)bh * D;
-        float x = to_f<T>(q[tid]);
-        if (tid < 2 * half) {
-            const int i = tid < half ? tid : tid - half;
-            const float2 cs = a.rope[p * half + i];
-            x = tid < half ? x * cs.x - to_f<T>(q[tid + half]) * cs.y
-                           : x * cs.x + to_f<T>(q[tid - half]) * cs.y;
-        }
-        qs[tid] = x * a.scale_log2;
+    if (lane == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(dsmem_u32(&bars[warp][0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(dsmem_u32(&bars[warp][1])) : "memory");
     }
+    // the bulk copies below read the rows just written through the generic proxy
+    asm volatile("fence.proxy.async;" ::: "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     __syncthreads();
 
     const int64_t c = p / a.C, Wc = a.W / a.C;
     const int64_t ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
+    const int ws_slot = (int)(ws % L);
     const int n = a.n_slots;
-    const int64_t nkeys = n + (p - ws + 1);
+    const int nkeys = n + (int)(p - ws + 1);
     const T* vk = reinterpret_cast<const T*>(a.view_k) + (int64_t)bh * a.M * D;
     const T* vv = reinterpret_cast<const T*>(a.view_v) + (int64_t)bh * a.M * D;
+    const int per = ((nkeys + DEC_WARPS * TK - 1) / (DEC_WARPS * TK)) * TK;
+    const int beg = warp * per, end = min(nkeys, beg + per);
+    uint8_t* stage = dsm + warp * 2 * 2 * TILE;  // [2 stages][K tile, V tile]
 
-    // each warp takes keys warp, warp + 4, ...; lanes split the head dim (2 each)
-    float m = -INFINITY, l = 0.0f, acc0 = 0.0f, acc1 = 0.0f;
-    const float q0 = qs[lane], q1 = qs[lane + 32];
-    for (int64_t j = warp; j < nkeys; j += DEC_THREADS / 32) {
-        float k0, k1, v0, v1;
-        if (j < n) {
-            k0 = to_f<T>(vk[j * D + lane]);
-            k1 = to_f<T>(vk[j * D + lane + 32]);
-            v0 = to_f<T>(vv[j * D + lane]);
-            v1 = to_f<T>(vv[j * D + lane + 32]);
-        } else {
-            const int64_t kp = ws + (j - n);
-            const int64_t sl = (kp % L) * D;
-            k0 = to_f<T>(rk[sl + lane]);
-            k1 = to_f<T>(rk[sl + lane + 32]);
-            if (half > 0) {
-                // rotate-half RoPE at the key's own position: pair (i, i + half)
-                kbuf[warp][lane] = k0;
-                kbuf[warp][lane + 32] = k1;
-                __syncwarp();
-                const float2* rp = a.rope + kp * half;
-                if (lane < half) {
-                    const float2 cs = rp[lane];
-                    k0 = kbuf[warp][lane] * cs.x - kbuf[warp][lane + half] * cs.y;
-                } else if (lane < 2 * half) {
-                    const float2 cs = rp[lane - half];
-                    k0 = kbuf[warp][lane] * cs.x + kbuf[warp][lane - half] * cs.y;
-                }
-                const int x1 = lane + 32;
-                if (x1 < half) {
-                    const float2 cs = rp[x1];
-                    k1 = kbuf[warp][x1] * cs.x - kbuf[warp][x1 + half] * cs.y;
-                } else if (x1 < 2 * half) {
-                    const float2 cs = rp[x1 - half];
-                    k1 = kbuf[warp][x1] * cs.x + kbuf[warp][x1 - half] * cs.y;
-                }
-                __syncwarp();
-            }
-            v0 = to_f<T>(rv[sl + lane]);
-            v1 = to_f<T>(rv[sl + lane + 32]);
+    // issue the copies of keys [k0, k1) into stage b (lane 0 only)
+    auto issue = [&](int k0, int k1, int b) {
+        const uint32_t bar = dsmem_u32(&bars[warp][b]);
+        const uint32_t sk = dsmem_u32(stage + b * 2 * TILE), sv = sk + TILE;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"((uint32_t)((k1 - k0) * RB * 2)) : "memory");
+        int kk = k0;
+        if (kk < n) {  // state rows
+            const int e = min(k1, n);
+            bulk_g2s(sk, vk + (int64_t)kk * D, (uint32_t)((e - kk) * RB), bar);
+            bulk_g2s(sv, vv + (int64_t)kk * D, (uint32_t)((e - kk) * RB), bar);
+            kk = e;
         }
-        const float s = warp_sum(q0 * k0 + q1 * k1);
-        const float mnew = fmaxf(m, s);
+        while (kk < k1) {  // window rows, contiguous up to the ring's end
+            int slot = ws_slot + (kk - n);
+            if (slot >= L) slot -= L;
+            const int e = min(k1, kk + (L - slot));
+            const uint32_t o = (uint32_t)((kk - k0) * RB);
+            bulk_g2s(sk + o, rkr + (int64_t)slot * D, (uint32_t)((e - kk) * RB), bar);
+            bulk_g2s(sv + o, rv + (int64_t)slot * D, (uint32_t)((e - kk) * RB), bar);
+            kk = e;
+        }
+    };
+
+    float m = -INFINITY, l = 0.0f, acc0 = 0.0f, acc1 = 0.0f;
+    const float2 qv = make_float2(qs[2 * lane], qs[2 * lane + 1]);
+    int it = 0;
+    if (lane == 0 && beg < end) issue(beg, min(end, beg + TK), 0);
+    __syncwarp();
+    for (int k0 = beg; k0 < end; k0 += TK, ++it) {
+        const int b = it & 1;
+        const int cnt = min(TK, end - k0);
+        if (lane == 0 && k0 + TK < end) issue(k0 + TK, min(end, k0 + 2 * TK), b ^ 1);
+        // wait for this tile: lane 0 polls (bounded: a copy that never lands latches a
+        // timeout), the warp barrier orders the other lanes' reads after its acquire
+        {
+            uint32_t ok = 1;
+            if (lane == 0) {
+                const uint32_t bar = dsmem_u32(&bars[warp][b]);
+                const uint32_t par = (it >> 1) & 1;
+                long long t0 = -1;
+                for (;;) {
+                    asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+                                 : "=r"(ok) : "r"(bar), "r"(par) : "memory");
+                    if (ok) break;
+                    if (t0 < 0) t0 = clock64();
+                    if (clock64() - t0 > (1ll << 32)) {
+                        if (a.status) atomicOr(a.status, STATUS_TIMEOUT);
+                        break;
+                    }
+                }
+            }
+            __syncwarp();
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
+        const T* kt = reinterpret_cast<const T*>(stage + b * 2 * TILE);
+        const T* vt = reinterpret_cast<const T*>(stage + b * 2 * TILE + TILE);
+        // partial dot products of this lane's two dims with every key of the tile
+        float v[TK];
+#pragma unroll
+        for (int j = 0; j < TK; ++j) {
+            const float2 kx = ld2s<T>(kt + j * D + 2 * lane);
+            v[j] = qv.x * kx.x + qv.y * kx.y;
+        }
+        // butterfly transpose-reduce: afterwards lane i holds key i's score
+#pragma unroll
+        for (int off = 16, w = TK; off >= 1; off >>= 1, w >>= 1) {
+            const bool upper = (lane & off) != 0;
+#pragma unroll
+            for (int i = 0; i < w / 2; ++i) {
+                const float send = upper ? v[i] : v[i + w / 2];
+                const float keep = upper ? v[i + w / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+            }
+        }
+        const float sc = lane < cnt ? v[0] : -INFINITY;
+        const float mnew = fmaxf(m, warp_max(sc));
         const float corr = exp2f(m - mnew);
-        const float pj = exp2f(s - mnew);
-        l = l * corr + pj;
-        acc0 = acc0 * corr + pj * v0;
-        acc1 = acc1 * corr + pj * v1;
+        const float pj = exp2f(sc - mnew);
+        l = l * corr + warp_sum(pj);
+        acc0 *= corr;
+        acc1 *= corr;
         m = mnew;
+#pragma unroll
+        for (int j = 0; j < TK; ++j) {
+            const float pk = __shfl_sync(0xffffffffu, pj, j);  // 0 past the tile's keys
+            if (j < cnt) {
+                const float2 vx = ld2s<T>(vt + j * D + 2 * lane);
+                acc0 = fmaf(pk, vx.x, acc0);
+                acc1 = fmaf(pk, vx.y, acc1);
+            }
+        }
+        __syncwarp();
     }
     if (lane == 0) {
-        mxs[warp] = m;
-        ls[warp] = l;
+        red_m[warp] = m;
+        red_l[warp] = l;
     }
-    accs[warp][lane] = acc0;
-    accs[warp][lane + 32] = acc1;
+    red_acc[warp][2 * lane] = acc0;
+    red_acc[warp][2 * lane + 1] = acc1;
     __syncthreads();
     if (tid < D) {
         float M = -INFINITY;
-        for (int w = 0; w < DEC_THREADS / 32; ++w) M = fmaxf(M, mxs[w]);
+        for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, red_m[w]);
         float L2 = 0.0f, o = 0.0f;
-        for (int w = 0; w < DEC_THREADS / 32; ++w) {
-            const float f = mxs[w] == -INFINITY ? 0.0f : exp2f(mxs[w] - M);
-            L2 += ls[w] * f;
-            o += accs[w][tid] * f;
+        for (int w = 0; w < DEC_WARPS; ++w) {
+            const float f = red_m[w] == -INFINITY ? 0.0f : exp2f(red_m[w] - M);
+            L2 += red_l[w] * f;
+            o += red_acc[w][tid] * f;
         }
         reinterpret_cast<T*>(a.out)[(int64_t)bh * D + tid] = from_f<T>(o / L2);
     }
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s) {
-    if (bf16)
-        decode_kernel<__nv_bfloat16><<<a.BH, DEC_THREADS, 0, s>>>(a);
-    else
-        decode_kernel<float><<<a.BH, DEC_THREADS, 0, s>>>(a);
+    if (bf16) {
+        const int smem = DEC_WARPS * 2 * 2 * TK * 64 * 2;
+        cudaFuncSetAttribute(decode_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        decode_kernel<__nv_bfloat16><<<a.BH, DEC_THREADS, smem, s>>>(a);
+    } else {
+        const int smem = DEC_WARPS * 2 * 2 * TK * 64 * 4;
+        cudaFuncSetAttribute(decode_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        decode_kernel<float><<<a.BH, DEC_THREADS, smem, s>>>(a);
+    }
     return cudaGetLastError();
 }
 

@@ -117,43 +117,35 @@ __device__ __forceinline__ float dot64(const float (&x)[64], const float (&y)[64
 }
 
 // Owner-thread renormalisation of slot j from its key sums (registers): the
-// winner-take-all direction (hi/lo) and the read-view key.
+// winner-take-all direction u = c / |c| (as bf16 hi + lo terms) and the
+// read-view key LayerNorm(sum / count) = c / sqrt(|c|^2 / 64 + eps * count^2),
+// both from the centred sums c = sum - mean(sum); rotary dims of the key are 0.
 __device__ __forceinline__ void owner_view_k(int j, const float (&sk)[64], int cnt, int r, float eps, uint8_t* sm) {
     const float mean = sum64(sk) * (1.0f / 64.0f);
-    const float ss = sqdev64(sk, mean, 1.0f);
+    float c[64];
+#pragma unroll
+    for (int x = 0; x < 64; ++x) c[x] = sk[x] - mean;
+    const float ss = dot64(c, c);
     const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float a0 = (sk[ch * 8 + 2 * u] - mean) * inv, a1 = (sk[ch * 8 + 2 * u + 1] - mean) * inv;
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(a0), h1 = __float2bfloat16_rn(a1);
-            hi[u] = pack2(__bfloat162float(h0), __bfloat162float(h1));
-            lo[u] = pack2(a0 - __bfloat162float(h0), a1 - __bfloat162float(h1));
-        }
-        *reinterpret_cast<uint4*>(sm + OFF_UHI + swz(j, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sm + OFF_ULO + swz(j, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    // read key: LayerNorm(sum_k / count), rotary dims zeroed
-    const float ic = 1.0f / (float)cnt;
-    float xs[64];
-#pragma unroll
-    for (int x = 0; x < 64; ++x) xs[x] = sk[x] * ic;
-    const float mx = sum64(xs) * (1.0f / 64.0f);
-    const float var = sqdev64(xs, mx, 1.0f) * (1.0f / 64.0f);
-    const float rs = 1.0f / sqrtf(var + eps);
+    const float fc = (float)cnt;
+    const float rs = 1.0f / sqrtf(ss * (1.0f / 64.0f) + eps * fc * fc);
     uint4* vk = reinterpret_cast<uint4*>(sm + OFF_VK + j * ROWB);
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
-        uint32_t wk[4];
+        uint32_t hi[4], lo[4], wk[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int x0 = ch * 8 + 2 * u, x1 = x0 + 1;
-            const float k0 = x0 < r ? 0.0f : (sk[x0] * ic - mx) * rs;
-            const float k1 = x1 < r ? 0.0f : (sk[x1] * ic - mx) * rs;
-            wk[u] = pack2(k0, k1);
+            const int x0 = ch * 8 + 2 * u;
+            const float a0 = c[x0] * inv, a1 = c[x0 + 1] * inv;
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+            const float2 hf = __bfloat1622float2(h);
+            const __nv_bfloat162 lw = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
+            hi[u] = *reinterpret_cast<const uint32_t*>(&h);
+            lo[u] = *reinterpret_cast<const uint32_t*>(&lw);
+            wk[u] = (x0 + 1 < r) ? 0u : pack2(x0 < r ? 0.0f : c[x0] * rs, c[x0 + 1] * rs);
         }
+        *reinterpret_cast<uint4*>(sm + OFF_UHI + swz(j, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sm + OFF_ULO + swz(j, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         vk[ch] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
     }
 }
@@ -265,7 +257,6 @@ __global__ void __launch_bounds__(256, 1)
 
     auto load_chunk = [&](int e, int buf) {
         const int64_t off = ((int64_t)e * C) % a.src_len;
-        fence_proxy_async();
         mbar_expect_tx(smem_u32(&X.bar_k[buf]), 2 * TOK * ROWB);
         tma_load_3d(sK + buf * TOK * ROWB, &tm_k, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
         tma_load_3d(sV + buf * TOK * ROWB, &tm_v, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
@@ -273,15 +264,23 @@ __global__ void __launch_bounds__(256, 1)
     if (tid == 0 && a.e_begin < a.e_end) load_chunk(a.e_begin, 0);
     const uint32_t idesc = idesc_bf16(128, 256, 0, 0);
     int mma_count = 0;
-    KVM_PROBE_DECL(11)
+    KVM_PROBE_DECL(13)
     KVM_PROBE_START()
 
+    // the next event's schedule entry and gates are loaded one event ahead, off the chain
+    Sched sc_nx = a.sched ? a.sched[a.e_begin] : a.sched0;
+    float g_nx = 0.0f;
+    if (tid < C && a.e_begin < a.e_end)
+        g_nx = a.g_src[(int64_t)bh * a.src_row + ((int64_t)a.e_begin * C) % a.src_len + tid];
     for (int e = a.e_begin, it = 0; e < a.e_end; ++e, ++it) {
         const int buf = it & 1;
-        const Sched sc = a.sched ? a.sched[e] : a.sched0;
-        if (tid == 0) {
-            if (e + 1 < a.e_end) load_chunk(e + 1, buf ^ 1);
-            if (!mbar_wait(smem_u32(&X.bar_k[buf]), (it >> 1) & 1, &X.abort_flag, a.status)) X.abort_flag = 1;
+        const Sched sc = sc_nx;
+        const float g_here = g_nx;
+        if (tid == 0 && !mbar_wait(smem_u32(&X.bar_k[buf]), (it >> 1) & 1, &X.abort_flag, a.status))
+            X.abort_flag = 1;
+        if (e + 1 < a.e_end) {
+            sc_nx = a.sched ? a.sched[e + 1] : a.sched0;
+            if (tid < C) g_nx = a.g_src[(int64_t)bh * a.src_row + ((int64_t)(e + 1) * C) % a.src_len + tid];
         }
         __syncthreads();
         if (X.abort_flag) break;
@@ -290,7 +289,6 @@ __global__ void __launch_bounds__(256, 1)
         probe_acc[8] += 1;
 #endif
         const int64_t first_pos = (int64_t)e * C;
-        const int64_t off = first_pos % a.src_len;
         const uint8_t* kch = sm + OFF_K + buf * TOK * ROWB;
         const uint8_t* vch = sm + OFF_V + buf * TOK * ROWB;
         const int n0 = sc.n0, na = sc.a;
@@ -307,10 +305,12 @@ __global__ void __launch_bounds__(256, 1)
                 }
             mma_commit(bar_s);
         }
+        // the next chunk's keys and values load while this event runs
+        if (tid == 0 && e + 1 < a.e_end) load_chunk(e + 1, buf ^ 1);
         // per-token set-up
         if (tid < C) {
             const int t = tid;
-            X.g[t] = a.g_src[(int64_t)bh * a.src_row + off + t];
+            X.g[t] = g_here;
             float kx[64];
             load_row_sw(kch, t, kx);
             X.kn[t] = sqrtf(dot64(kx, kx));
@@ -345,25 +345,32 @@ __global__ void __launch_bounds__(256, 1)
                 aq[c] = -1;
             }
             if (lo < hi) {
+                uint32_t va[4][32];
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(t_sim + half * 128 + (2 * c2) * 32, v0);
-                    tmem_ld32(t_sim + half * 128 + (2 * c2 + 1) * 32, v1);
-                    tmem_wait_ld();
+                for (int c = 0; c < 4; ++c) tmem_ld32(t_sim + half * 128 + c * 32, va[c]);
+                tmem_wait_ld();
+                KVM_PROBE_LAP(11)
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
+                for (int c = 0; c < 4; ++c) {
+                    const int base = half * 128 + c * 32;
+                    // branchless running best / second best / argmax (strictly larger
+                    // values take the lead, so ties keep the lower slot index)
+                    if (base >= lo && base + 32 <= hi) {
 #pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            const int c = 2 * c2 + q;
-                            const int j = half * 128 + c * 32 + x;
-                            const float raw = __uint_as_float(q ? v1[x] : v0[x]);
-                            const float val = (j >= lo && j < hi) ? raw : -INFINITY;
-                            // branchless: a strictly larger value takes the lead (lower index kept on ties)
-                            const bool gt = val > bq[c];
-                            sq[c] = gt ? bq[c] : fmaxf(sq[c], val);
-                            aq[c] = gt ? j : aq[c];
-                            bq[c] = gt ? val : bq[c];
+                        for (int x = 0; x < 32; ++x) {
+                            const float val = __uint_as_float(va[c][x]);
+                            aq[c] = val > bq[c] ? base + x : aq[c];
+                            sq[c] = fmaxf(sq[c], fminf(val, bq[c]));
+                            bq[c] = fmaxf(bq[c], val);
+                        }
+                    } else if (base + 32 > lo && base < hi) {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            const int j = base + x;
+                            const float val = (j >= lo && j < hi) ? __uint_as_float(va[c][x]) : -INFINITY;
+                            aq[c] = val > bq[c] ? j : aq[c];
+                            sq[c] = fmaxf(sq[c], fminf(val, bq[c]));
+                            bq[c] = fmaxf(bq[c], val);
                         }
                     }
                 }
@@ -382,6 +389,7 @@ __global__ void __launch_bounds__(256, 1)
                     s2 = fmaxf(s2, sq[c]);
                 }
             }
+            KVM_PROBE_LAP(12)
             X.pb[half][t] = b;
             X.ps[half][t] = s2;
             X.pa[half][t] = ba;
@@ -670,7 +678,7 @@ __global__ void __launch_bounds__(256, 1)
         }
     }
     KVM_PROBE_LAP(10)
-    if (tid == 0) KVM_PROBE_FLUSH(g_probe_fold, 0, 11)
+    if (tid == 0) KVM_PROBE_FLUSH(g_probe_fold, 0, 13)
     tc_fence_before();
     __syncthreads();
     if (X.abort_flag) {

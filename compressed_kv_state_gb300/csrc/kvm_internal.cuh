@@ -113,6 +113,7 @@ struct DecodeArgs {
     void* ring_k;
     void* ring_v;
     float* ring_g;
+    void* ring_kr;  // window keys with RoPE applied at their own positions
     const void* view_k;
     const void* view_v;
     int M, n_slots, C, W;
@@ -121,18 +122,23 @@ struct DecodeArgs {
     int r;
     float scale_log2;
     int BH;
+    int* status;
 };
 
 struct RingFillArgs {
-    const void* k;
+    const void* k;      // source keys [BH, N, D] (unrotated)
     const void* v;
     const float* g;
     void* ring_k;
     void* ring_v;
     float* ring_g;
+    void* ring_kr;      // rotated copy of the ring keys
+    const float2* rope;
+    int r;
     int64_t N, first;  // copy tokens [first, N) of each row
     int L;             // ring length W + C
     int BH;
+    int rotate_only;   // 1: only recompute ring_kr from ring_k for positions [first, N)
 };
 
 struct RenormArgs {
