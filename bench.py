@@ -208,6 +208,24 @@ def cpu_oracle_sample(w, heads_per_thread=1):
                        f"{w.name}, one row per thread, {dt:.1f} s wall")
 
 
+# ------------------------------------------------------------- multi-rank
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own rows (weak scaling)."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 # ------------------------------------------------------------------ ours
 
 def run_ours(args, rank, world, local_rank):
@@ -252,13 +270,9 @@ def run_ours(args, rank, world, local_rank):
     tm = kvm.kvm_layer_get_timing(layer.handle)
     kvm.kvm_layer_set_timing(layer.handle, False)
     layer.sync()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
-    value = world * W.B * W.N / (ms_step / 1e3)
+    value = job_throughput(W.B * W.N, world, ms_step)
 
     # end to end through the C ABI: pinned host inputs in, output back to host
     hq = torch.from_numpy(q).bfloat16().pin_memory()

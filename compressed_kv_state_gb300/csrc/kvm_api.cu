@@ -320,6 +320,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             fa.dbg_m = dbg->max_sim;
             fa.dbg_gap = dbg->gap;
             fa.dbg_events = (int)(dbg->max_events < E ? dbg->max_events : E);
+            fa.test_stall = dbg->test_stall;
         }
         fa.status = ly->at<int>(L.status);
         fa.BH = BH;

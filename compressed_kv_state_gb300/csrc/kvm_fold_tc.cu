@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_3d(sK + buf * TOK * ROWB, &tm_k, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
         tma_load_3d(sV + buf * TOK * ROWB, &tm_v, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
     };
-    if (tid == 0 && a.e_begin < a.e_end) load_chunk(a.e_begin, 0);
+    if (tid == 0 && a.e_begin < a.e_end && !a.test_stall) load_chunk(a.e_begin, 0);
     const uint32_t idesc = idesc_bf16(128, 256, 0, 0);
     int mma_count = 0;
     KVM_PROBE_DECL(13)

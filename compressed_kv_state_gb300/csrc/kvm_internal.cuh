@@ -81,6 +81,7 @@ struct FoldArgs {
     float* dbg_m;
     float* dbg_gap;
     int dbg_events;
+    int test_stall;  // wait for a chunk copy that is never issued (bounded-wait test)
     int* status;
     int BH;
 };

@@ -44,7 +44,7 @@ class kvm_state_bufs(ctypes.Structure):
 class kvm_debug(ctypes.Structure):
     _fields_ = [("assign", ctypes.c_void_p), ("kind", ctypes.c_void_p),
                 ("max_sim", ctypes.c_void_p), ("gap", ctypes.c_void_p),
-                ("max_events", ctypes.c_int64)]
+                ("max_events", ctypes.c_int64), ("test_stall", ctypes.c_int32)]
 
 
 class kvm_timing(ctypes.Structure):

@@ -124,6 +124,12 @@ typedef struct {
     float* max_sim;
     float* gap;
     int64_t max_events;
+    /* Test hook of the failure path: when nonzero, the on-chip fold chain (bf16,
+     * chunk <= 128, max_slots <= 256) waits for a chunk copy that is never
+     * issued; its bounded wait expires after about two seconds, the kernel
+     * drains and exits, and kvm_layer_sync reports KVM_ERR_TIMEOUT.  The
+     * prefill's outputs are then meaningless; the context stays usable. */
+    int32_t test_stall;
 } kvm_debug;
 
 /* Bytes of device workspace a layer with this config needs (0 if the config

@@ -45,7 +45,7 @@ def test_struct_sizes_match_header(kvm):
     # 15 four-byte fields, no padding
     assert ctypes.sizeof(kvm.kvm_config) == 60
     assert ctypes.sizeof(kvm.kvm_state_bufs) == 7 * 8 + 3 * 8
-    assert ctypes.sizeof(kvm.kvm_debug) == 5 * 8
+    assert ctypes.sizeof(kvm.kvm_debug) == 5 * 8 + 8  # + int32 test hook, padded
 
 
 @pytest.mark.parametrize("field,value,msg", [
