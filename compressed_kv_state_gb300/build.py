@@ -46,7 +46,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
-    deps = glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
+    deps = (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
+            glob.glob(os.path.join(INCLUDE, "*.h")))
     jobs = []
     objs = []
     for src in sources():

@@ -109,7 +109,7 @@ Layout layout_of(const kvm_config& c) {
     L.snap_v = take(BH * E * M * d * es);
     L.rope = take((size_t)c.max_tokens * (c.rope_dims / 2) * sizeof(float2) + 16);
     L.sched = take((E + 1) * sizeof(Sched));
-    L.status = take(16);
+    L.status = take(256);  // status word at 0, attention tile-range counters at TILE_CTR_OFF
     L.total = o;
     return L;
 }
@@ -158,11 +158,19 @@ struct kvm_layer {
     size_t used = 0;
     double acc_ms[4] = {0, 0, 0, 0};
     int64_t acc_n[4] = {0, 0, 0, 0};
+    int64_t kernels = 0;
+    // overlapped prefill (kvm_layer_set_overlap)
+    int overlap_segs = -1;
+    int last_segs = 0;
+    bool part_tried = false;
+    kvm::host::Partition part;
+    std::string part_why;
     ~kvm_layer() {
         for (auto& t : pool) {
             cudaEventDestroy(t.a);
             cudaEventDestroy(t.b);
         }
+        if (part.ok) kvm::host::partition_free(&part);
     }
 
     template <typename P> P* at(size_t off) const { return reinterpret_cast<P*>(ws + off); }
@@ -289,82 +297,164 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     const Layout& L = ly->L;
     cudaError_t e = cudaSuccess;
 
-    if (E > 0) {
-        kvm::FoldArgs fa{};
-        fa.sum_k = ly->at<float>(L.sum_k);
-        fa.sum_v = ly->at<float>(L.sum_v);
-        fa.counts = ly->at<int>(L.counts);
-        fa.rho = ly->at<float>(L.rho);
-        fa.simdir = ly->at<float>(L.simdir);
-        fa.view_k = ly->ws + L.view_k;
-        fa.view_v = ly->ws + L.view_v;
-        fa.M = c.max_slots;
-        fa.C = c.chunk;
-        fa.S = c.n_sinks;
-        fa.r = c.rope_dims;
-        fa.ln_eps = c.ln_eps;
-        fa.k_src = k;
-        fa.v_src = v;
-        fa.g_src = gate;
-        fa.src_row = n_tokens;
-        fa.src_len = INT64_MAX / 4;
-        fa.e_begin = 0;
-        fa.e_end = (int)E;
-        fa.sched = ly->at<Sched>(L.sched);
-        fa.snap_k = ly->ws + L.snap_k;
-        fa.snap_v = ly->ws + L.snap_v;
-        fa.snap_events = (int)ly->E_max;
-        if (dbg) {
-            fa.dbg_assign = dbg->assign;
-            fa.dbg_kind = dbg->kind;
-            fa.dbg_m = dbg->max_sim;
-            fa.dbg_gap = dbg->gap;
-            fa.dbg_events = (int)(dbg->max_events < E ? dbg->max_events : E);
-            fa.test_stall = dbg->test_stall;
-        }
-        fa.status = ly->at<int>(L.status);
-        fa.BH = BH;
-        e = timed(ly, PH_FOLD, s, [&] { return kvm::launch_fold(fa, bf16, s); });
-        if (e != cudaSuccess) return ly->cuda_fail(e, "fold chain launch");
+    kvm::FoldArgs fa{};
+    fa.sum_k = ly->at<float>(L.sum_k);
+    fa.sum_v = ly->at<float>(L.sum_v);
+    fa.counts = ly->at<int>(L.counts);
+    fa.rho = ly->at<float>(L.rho);
+    fa.simdir = ly->at<float>(L.simdir);
+    fa.view_k = ly->ws + L.view_k;
+    fa.view_v = ly->ws + L.view_v;
+    fa.M = c.max_slots;
+    fa.C = c.chunk;
+    fa.S = c.n_sinks;
+    fa.r = c.rope_dims;
+    fa.ln_eps = c.ln_eps;
+    fa.k_src = k;
+    fa.v_src = v;
+    fa.g_src = gate;
+    fa.src_row = n_tokens;
+    fa.src_len = INT64_MAX / 4;
+    fa.e_begin = 0;
+    fa.e_end = (int)E;
+    fa.sched = ly->at<Sched>(L.sched);
+    fa.snap_k = ly->ws + L.snap_k;
+    fa.snap_v = ly->ws + L.snap_v;
+    fa.snap_events = (int)ly->E_max;
+    if (dbg) {
+        fa.dbg_assign = dbg->assign;
+        fa.dbg_kind = dbg->kind;
+        fa.dbg_m = dbg->max_sim;
+        fa.dbg_gap = dbg->gap;
+        fa.dbg_events = (int)(dbg->max_events < E ? dbg->max_events : E);
+        fa.test_stall = dbg->test_stall;
     }
-    if (n_tokens > 0) {
-        kvm::AttnArgs aa{};
-        aa.q = q;
-        aa.k = k;
-        aa.v = v;
-        aa.out = out;
-        aa.N = n_tokens;
-        aa.C = c.chunk;
-        aa.W = c.window;
-        aa.snap_k = ly->ws + L.snap_k;
-        aa.snap_v = ly->ws + L.snap_v;
-        aa.snap_events = (int)ly->E_max;
-        aa.M = c.max_slots;
-        aa.sched = ly->at<Sched>(L.sched);
-        aa.rope = ly->at<float2>(L.rope);
-        aa.r = c.rope_dims;
-        aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
-        aa.BH = BH;
-        aa.status = ly->at<int>(L.status);
-        e = timed(ly, PH_ATTN, s, [&] { return kvm::launch_attn(aa, bf16, s); });
-        if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
+    fa.status = ly->at<int>(L.status);
+    fa.BH = BH;
 
-        kvm::RingFillArgs ra{};
-        ra.k = k;
-        ra.v = v;
-        ra.g = gate;
-        ra.ring_k = ly->ws + L.ring_k;
-        ra.ring_v = ly->ws + L.ring_v;
-        ra.ring_g = ly->at<float>(L.ring_g);
-        ra.ring_kr = ly->ws + L.ring_kr;
-        ra.rope = ly->at<float2>(L.rope);
-        ra.r = c.rope_dims;
-        ra.N = n_tokens;
-        ra.first = E * c.chunk;
-        ra.L = c.window + c.chunk;
-        ra.BH = BH;
+    kvm::AttnArgs aa{};
+    aa.q = q;
+    aa.k = k;
+    aa.v = v;
+    aa.out = out;
+    aa.N = n_tokens;
+    aa.C = c.chunk;
+    aa.W = c.window;
+    aa.snap_k = ly->ws + L.snap_k;
+    aa.snap_v = ly->ws + L.snap_v;
+    aa.snap_events = (int)ly->E_max;
+    aa.M = c.max_slots;
+    aa.sched = ly->at<Sched>(L.sched);
+    aa.rope = ly->at<float2>(L.rope);
+    aa.r = c.rope_dims;
+    aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    aa.BH = BH;
+    aa.status = ly->at<int>(L.status);
+
+    kvm::RingFillArgs ra{};
+    ra.k = k;
+    ra.v = v;
+    ra.g = gate;
+    ra.ring_k = ly->ws + L.ring_k;
+    ra.ring_v = ly->ws + L.ring_v;
+    ra.ring_g = ly->at<float>(L.ring_g);
+    ra.ring_kr = ly->ws + L.ring_kr;
+    ra.rope = ly->at<float2>(L.rope);
+    ra.r = c.rope_dims;
+    ra.N = n_tokens;
+    ra.first = E * c.chunk;
+    ra.L = c.window + c.chunk;
+    ra.BH = BH;
+    const bool ring_work = n_tokens > ra.first;
+
+    // overlapped prefill: fold segments on one SM partition, the attention of
+    // the chunks each segment has made ready on the other
+    int segs = 0;
+    if (ly->overlap_segs != 0 && !dbg && E >= 2 && kvm::fold_tc_supported(fa, bf16) &&
+        kvm::attn_tc_supported(aa, bf16) && c.chunk == 128) {
+        if (!ly->part_tried) {
+            ly->part_tried = true;
+            kvm::host::partition_make(ly->device, BH, &ly->part, ly->part_why);
+        }
+        if (ly->part.ok) {
+            segs = ly->overlap_segs > 0 ? ly->overlap_segs : 4;
+            if (segs > kvm::host::Partition::MAX_SEGS) segs = kvm::host::Partition::MAX_SEGS;
+            if (segs > E) segs = (int)E;
+        }
+    }
+    ly->last_segs = segs;
+
+    if (segs > 0) {
+        kvm::host::Partition& P = ly->part;
+        int* ctr = reinterpret_cast<int*>(ly->ws + L.status + kvm::host::TILE_CTR_OFF);
+        const int64_t tph = (n_tokens + 127) / 128, Wc = c.window / c.chunk, tpc = c.chunk / 128;
+        // tiles (all rows) of the chunks whose state is complete once events < e_done are folded
+        auto ready = [&](int64_t e_done) {
+            int64_t t = (e_done + Wc + 1) * tpc;
+            return (int)((t < tph ? t : tph) * BH);
+        };
+        // range 0: chunks that need no fold; range k + 1: the chunks segment k makes ready
+        aa.n_ranges = segs + 1;
+        aa.range_end[0] = ready(0);
+        for (int sg = 0; sg < segs; ++sg) aa.range_end[sg + 1] = ready(E * (sg + 1) / segs);
+        e = cudaMemsetAsync(ctr, 0, sizeof(int) * aa.n_ranges, s);
+        if (e == cudaSuccess) e = cudaEventRecord(P.ev_fork, s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(P.s_fold, P.ev_fork, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(P.s_attn, P.ev_fork, 0);
+        if (e != cudaSuccess) return ly->cuda_fail(e, "overlap set-up");
+        aa.tile_ctr = ctr;
+        // attention launches on the second partition may claim only ready ranges
+        const int all_ranges = aa.n_ranges;
+        aa.grid = 2 * P.sm_attn;
+        aa.n_ranges = 1;
+        e = timed(ly, PH_ATTN, P.s_attn, [&] { return kvm::launch_attn(aa, bf16, P.s_attn); });
+        if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
+        ly->kernels += 1;
+        e = timed(ly, PH_FOLD, P.s_fold, [&] {
+            for (int sg = 0; sg < segs; ++sg) {
+                fa.e_begin = (int)(E * sg / segs);
+                fa.e_end = (int)(E * (sg + 1) / segs);
+                cudaError_t r = kvm::launch_fold(fa, bf16, P.s_fold);
+                if (r == cudaSuccess) r = cudaEventRecord(P.ev_seg[sg], P.s_fold);
+                if (r != cudaSuccess) return r;
+                ly->kernels += 1;
+                if (sg + 1 < segs) {
+                    r = cudaStreamWaitEvent(P.s_attn, P.ev_seg[sg], 0);
+                    aa.n_ranges = sg + 2;
+                    if (r == cudaSuccess) r = timed(ly, PH_ATTN, P.s_attn, [&] { return kvm::launch_attn(aa, bf16, P.s_attn); });
+                    if (r != cudaSuccess) return r;
+                    ly->kernels += 1;
+                }
+            }
+            return cudaSuccess;
+        });
+        if (e != cudaSuccess) return ly->cuda_fail(e, "overlapped fold / attention launch");
+        // what is left of the attention on every SM, once the chain is done
+        e = cudaStreamWaitEvent(s, P.ev_seg[segs - 1], 0);
+        aa.n_ranges = all_ranges;
+        aa.grid = 2 * P.sm_all;
+        if (e == cudaSuccess) e = timed(ly, PH_ATTN, s, [&] { return kvm::launch_attn(aa, bf16, s); });
+        if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
+        ly->kernels += 1;
+        e = cudaEventRecord(P.ev_attn, P.s_attn);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, P.ev_attn, 0);
+        if (e != cudaSuccess) return ly->cuda_fail(e, "overlap join");
+    } else {
+        if (E > 0) {
+            e = timed(ly, PH_FOLD, s, [&] { return kvm::launch_fold(fa, bf16, s); });
+            if (e != cudaSuccess) return ly->cuda_fail(e, "fold chain launch");
+            ly->kernels += 1;
+        }
+        if (n_tokens > 0) {
+            e = timed(ly, PH_ATTN, s, [&] { return kvm::launch_attn(aa, bf16, s); });
+            if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
+            ly->kernels += 1;
+        }
+    }
+    if (ring_work) {
         e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_ring_fill(ra, bf16, s); });
         if (e != cudaSuccess) return ly->cuda_fail(e, "ring fill launch");
+        ly->kernels += 1;
     }
     ly->n_slots = E > 0 ? ly->sched[E - 1].n_after : 0;
     ly->n_overflow = E * c.chunk;
@@ -421,6 +511,7 @@ kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const vo
         fa.BH = BH;
         cudaError_t e = timed(ly, PH_FOLD, s, [&] { return kvm::launch_fold(fa, bf16, s); });
         if (e != cudaSuccess) return ly->cuda_fail(e, "decode fold launch");
+        ly->kernels += 1;
         n = sc.n_after;
         t += c.chunk;
     }
@@ -448,6 +539,7 @@ kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const vo
     da.status = ly->at<int>(L.status);
     cudaError_t e = timed(ly, PH_DECODE, s, [&] { return kvm::launch_decode(da, bf16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "decode launch");
+    ly->kernels += 1;
     ly->n_slots = n;
     ly->n_overflow = t;
     ly->pos = p + 1;
@@ -521,6 +613,7 @@ kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda
     ra.BH = c.batch * c.heads;
     cudaError_t e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_renorm(ra, c.dtype == KVM_BF16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "renormalise launch");
+    if (ra.n > 0) ly->kernels += 1;
     // rotated copy of the imported window: tokens at positions [pos - (W + C), pos)
     const int64_t Lr = (int64_t)c.window + c.chunk;
     kvm::RingFillArgs rf{};
@@ -537,6 +630,7 @@ kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda
     rf.rotate_only = 1;
     e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_ring_fill(rf, c.dtype == KVM_BF16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "ring rotation launch");
+    if (rf.N > rf.first) ly->kernels += 1;
     ly->n_slots = src->n_slots;
     ly->n_overflow = src->n_overflow;
     ly->pos = src->pos;
@@ -563,6 +657,7 @@ kvm_status kvm_layer_set_timing(kvm_layer* ly, int enable) {
     if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
     ly->timing = enable != 0;
     ly->used = 0;
+    ly->kernels = 0;
     for (int i = 0; i < 4; ++i) {
         ly->acc_ms[i] = 0.0;
         ly->acc_n[i] = 0;
@@ -592,6 +687,20 @@ kvm_status kvm_layer_get_timing(kvm_layer* ly, kvm_timing* out) {
     out->attn_launches = ly->acc_n[PH_ATTN];
     out->decode_launches = ly->acc_n[PH_DECODE];
     out->other_launches = ly->acc_n[PH_OTHER];
+    out->kernels = ly->kernels;
+    return KVM_OK;
+}
+
+kvm_status kvm_layer_set_overlap(kvm_layer* ly, int32_t segments) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    ly->overlap_segs = segments < 0 ? -1 : segments;
+    return KVM_OK;
+}
+
+kvm_status kvm_layer_get_overlap(const kvm_layer* ly, int32_t* last_segments) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    if (!last_segments) return const_cast<kvm_layer*>(ly)->fail(KVM_ERR_INVALID_ARG, "last_segments is NULL");
+    *last_segments = ly->last_segs;
     return KVM_OK;
 }
 

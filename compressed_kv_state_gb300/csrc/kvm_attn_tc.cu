@@ -8,24 +8,24 @@
 //
 // Work unit: a tile of 128 consecutive queries of one (b, h) row (chunks are
 // multiples of 128, so a tile never spans two chunks).  The tile's keys come
-// in blocks of 128: first ceil(n/128) blocks of the state snapshot, then the
+// in blocks of 64: first ceil(n/64) blocks of the state snapshot, then the
 // window from (c - W/C)*C up to the tile's end (the last block is causal).
 //
-// Persistent CTAs (two per SM, 256 threads, 112 KB shared memory and 256
-// TMEM columns each, so the tensor core alternates between two tiles) loop
-// over tiles; warp roles:
-//   warp 0     TMA producer: Q tile, K/V blocks (2 stages)
+// Persistent CTAs (two per SM, 256 threads, 97 KB shared memory and 256 TMEM
+// columns each, so the tensor core alternates between two tiles) take tiles in
+// turns, either statically strided or claimed from a counter shared by several
+// launches; warp roles:
+//   warp 0     TMA producer: claims the tile, loads Q and the K/V blocks
+//              (3 stages)
 //   warp 1     tensor-memory owner and MMA issuer (one thread):
-//              S = Q K^T into the TMEM S buffer (128 fp32 columns), issued for
-//              block j+1 as soon as the softmax has consumed block j;
-//              O += P V into the TMEM O accumulator (64 columns)
+//              S = Q K^T into one of two 64-column TMEM S buffers, issued for
+//              block j+1 before O += P V of block j (O: 64 columns)
 //   warps 2-3  RoPE: rotate the Q tile and every window K block in shared
 //              memory (128-byte swizzled rows), then hand them to the MMA
-//   warps 4-7  softmax: thread i owns query row i (= TMEM lane i); two passes
-//              over the S row in TMEM (block maximum, then exponentials), lazy
-//              rescaling of O (only when the running maximum grows by more than
-//              2^8), P written to shared memory as bf16 in the swizzled K-major
-//              layout the MMA reads.
+//   warps 4-7  softmax: thread i owns query row i (= TMEM lane i); one pass
+//              over the 64-column S row, lazy rescaling of O (only when the
+//              running maximum grows by more than 2^8), P written to shared
+//              memory as bf16 in the swizzled K-major layout the MMA reads.
 // All mbarrier waits are bounded (about two seconds); on expiry the CTA
 // raises the device status word, drains and exits.
 #include <cuda.h>
@@ -63,6 +63,9 @@ struct TcArgs {
     int64_t N;
     int BH, C, W, M, r;
     int tiles_per_head, ntiles;
+    int* tile_ctr;   // dynamic claiming: one counter per range (nullptr: static striding)
+    int n_ranges;
+    int range_end[AttnArgs::MAX_RANGES];
     int snap_events;
     const Sched* sched;
     const float2* rope;
@@ -76,10 +79,13 @@ struct Tile {
     int64_t q0, ws;
 };
 
+// Tiles are numbered query-tile-major: number id is query tile id / BH of row
+// id % BH, so every prefix of the numbering is a set of whole chunks of all rows
+// (the order in which the fold chain makes their state snapshots available).
 __device__ __forceinline__ Tile tile_of(const TcArgs& a, int id) {
     Tile t;
-    t.bh = id / a.tiles_per_head;
-    t.q0 = (int64_t)(id % a.tiles_per_head) * 128;
+    t.bh = id % a.BH;
+    t.q0 = (int64_t)(id / a.BH) * 128;
     const int64_t c = t.q0 / a.C, Wc = a.W / a.C;
     t.e = (int)(c - Wc - 1);
     t.n = t.e >= 0 ? a.sched[t.e].n_after : 0;
@@ -88,6 +94,25 @@ __device__ __forceinline__ Tile tile_of(const TcArgs& a, int id) {
     t.nwin = (int)((t.q0 + 128 - t.ws) / KB);
     t.nblk = t.nst + t.nwin;
     return t;
+}
+
+// The tile a CTA processes in its tt-th turn, or -1 when it is done.  Dynamic
+// claiming: the next tile of the first range (from the CTA's cursor *range on)
+// that is not exhausted, one atomicAdd per claim (a compare-and-swap loop on a
+// shared counter collapses under contention from hundreds of CTAs).  Static:
+// blockIdx.x + tt * gridDim.x.
+__device__ __forceinline__ int next_tile(const TcArgs& a, int tt, int* range) {
+    if (a.tile_ctr) {
+        for (; *range < a.n_ranges; ++*range) {
+            const int r = *range;
+            const int lo = r > 0 ? a.range_end[r - 1] : 0;
+            const int id = lo + atomicAdd(a.tile_ctr + r, 1);
+            if (id < a.range_end[r]) return id;
+        }
+        return -1;
+    }
+    const int64_t id = blockIdx.x + (int64_t)tt * gridDim.x;
+    return id < a.ntiles ? (int)id : -1;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -166,11 +191,22 @@ __global__ void __launch_bounds__(256, 2)
         B_PFULL = B_SFULL + 2,     // [2] S consumed, P written, O rescaled (128 arrivals)
         B_PVDONE = B_PFULL + 2,    // [2] PV done
         B_FINAL = B_PVDONE + 2,    // MMA drain
-        NBARS = B_FINAL + 1
+        B_TILE = B_FINAL + 1,      // [4] tile number of turn tt published (ring of 4)
+        NBARS = B_TILE + 4
     };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* tile_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
     auto bar = [&](int i) { return smem_u32(bars + i); };
+    // The producer publishes the tile of turn tt in ring slot tt % 4; the other roles
+    // read it after the slot's barrier.  A slot is rewritten four turns later, when
+    // every role has moved past that turn: the producer claims turn tt only after the
+    // last QK MMA of turn tt - 1, which follows the rotation of its Q (RoPE warps in
+    // turn tt - 1) and the softmax of a block of turn tt - 2 or later.
+    auto tile_wait = [&](int tt) -> int {
+        if (!mbar_wait(bar(B_TILE + (tt & 3)), (tt >> 2) & 1, abort_flag, a.status)) return -1;
+        return tile_ring[tt & 3];
+    };
 
     if (tid == 0) {
         mbar_init(bar(B_QFULL), 1);
@@ -188,6 +224,7 @@ __global__ void __launch_bounds__(256, 2)
             mbar_init(bar(B_KVEMPTY + s), 1);
         }
         mbar_init(bar(B_FINAL), 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(B_TILE + i), 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async();
@@ -215,12 +252,16 @@ __global__ void __launch_bounds__(256, 2)
         if (lane == 0) {
             KVM_PROBE_DECL(3)
             KVM_PROBE_START()
-            int g = 0, tt = 0;
-            for (int id = blockIdx.x; id < a.ntiles; id += gridDim.x, ++tt) {
-                const Tile T = tile_of(a, id);
+            int g = 0, range = 0;
+            for (int tt = 0;; ++tt) {
                 KVM_PROBE_LAP(2)
                 if (tt >= 1 && !mbar_wait(bar(B_QEMPTY), (tt - 1) & 1, abort_flag, a.status)) break;
                 KVM_PROBE_LAP(0)
+                const int id = next_tile(a, tt, &range);
+                tile_ring[tt & 3] = id;
+                mbar_arrive(bar(B_TILE + (tt & 3)));
+                if (id < 0) break;
+                const Tile T = tile_of(a, id);
                 mbar_expect_tx(bar(B_QFULL), Q_BYTES);
                 tma_load_3d(sQ, &tm_q, 0, (int)T.q0, T.bh, bar(B_QFULL));
                 bool ok = true;
@@ -257,9 +298,11 @@ __global__ void __launch_bounds__(256, 2)
             const int ks_state = min(a.r / 16, 3);
             KVM_PROBE_DECL(5)
             KVM_PROBE_START()
-            int g = 0, tt = 0;
+            int g = 0;
             bool ok = true;
-            for (int id = blockIdx.x; id < a.ntiles && ok; id += gridDim.x, ++tt) {
+            for (int tt = 0; ok; ++tt) {
+                const int id = tile_wait(tt);
+                if (id < 0) break;
                 const Tile T = tile_of(a, id);
                 KVM_PROBE_LAP(4)
                 if (!mbar_wait(bar(B_QREADY), tt & 1, abort_flag, a.status)) break;
@@ -315,8 +358,10 @@ __global__ void __launch_bounds__(256, 2)
         const int rt = tid - 64;
         KVM_PROBE_DECL(4)
         KVM_PROBE_START()
-        int g = 0, tt = 0;
-        for (int id = blockIdx.x; id < a.ntiles; id += gridDim.x, ++tt) {
+        int g = 0;
+        for (int tt = 0;; ++tt) {
+            const int id = tile_wait(tt);
+            if (id < 0) break;
             const Tile T = tile_of(a, id);
             KVM_PROBE_LAP(3)
             if (!mbar_wait(bar(B_QFULL), tt & 1, abort_flag, a.status)) break;
@@ -369,7 +414,9 @@ __global__ void __launch_bounds__(256, 2)
         KVM_PROBE_START()
         int g = 0;
         bool ok = true;
-        for (int id = blockIdx.x; id < a.ntiles && ok; id += gridDim.x) {
+        for (int tt = 0; ok; ++tt) {
+            const int id = tile_wait(tt);
+            if (id < 0) break;
             const Tile T = tile_of(a, id);
             const int64_t p = T.q0 + row;
             float m_used = -INFINITY, l = 0.0f;
@@ -544,6 +591,20 @@ bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
     return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_f32_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes, uint32_t box_rows) {
+    using namespace tc;
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {64, rows, planes};
+    cuuint64_t strides[2] = {64 * 4, rows * 64 * 4};
+    cuuint32_t box[3] = {32, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool attn_tc_supported(const AttnArgs& a, bool bf16) {
     return bf16 && a.C % 128 == 0 && a.N > 0;
 }
@@ -567,6 +628,12 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     t.r = a.r;
     t.tiles_per_head = (int)((a.N + 127) / 128);
     t.ntiles = t.tiles_per_head * a.BH;
+    t.tile_ctr = a.tile_ctr;
+    t.n_ranges = a.n_ranges < AttnArgs::MAX_RANGES ? a.n_ranges : AttnArgs::MAX_RANGES;
+    for (int r = 0; r < AttnArgs::MAX_RANGES; ++r) {
+        const int e = r < t.n_ranges ? a.range_end[r] : t.ntiles;
+        t.range_end[r] = e < t.ntiles ? e : t.ntiles;
+    }
     t.snap_events = a.snap_events;
     t.sched = a.sched;
     t.rope = a.rope;
@@ -612,7 +679,8 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
         }
 #endif
     }
-    const int grid = t.ntiles < per_sm * nsm ? t.ntiles : per_sm * nsm;
+    int grid = a.grid > 0 ? a.grid : per_sm * nsm;
+    if (!a.tile_ctr && grid > t.ntiles) grid = t.ntiles;
     attn_tc_kernel<<<grid, 256, SMEM_BYTES, s>>>(mq, mk, mv, msk, msv, t);
     return cudaGetLastError();
 }

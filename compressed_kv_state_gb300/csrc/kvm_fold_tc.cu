@@ -4,21 +4,25 @@
 // "Key-Value Means" (gist.science technical summary), Core mechanisms 1-3
 // and 5; lay part "smart merge".  Same rule as the portable fold chain
 // (kvm_fold.cu); this kernel keeps one (b, h) row's whole state on one SM
-// for the entire chain:
+// for the entire chain, with 512 threads:
 //   - raw fp32 sums in tensor memory: slot j lives in TMEM lane j % 128 of
-//     column block j / 128 (64 columns of sum_k, 64 of sum_v); thread j of the
-//     CTA owns slot j and is the only one that reads or writes it;
+//     column block j / 128 (64 columns of sum_k, 64 of sum_v); thread j owns
+//     the key sums of slot j and thread 256 + j its value sums (the same TMEM
+//     lane: warps w and w + 8 address the same lane quarter), and nobody else
+//     reads or writes them;
 //   - the winner-take-all direction u_j = unit(sum_k_j - mean) in shared
 //     memory as two bf16 terms hi + lo (the K-major B operand of the MMA);
 //   - the similarity of the 128 chunk keys to all 256 slots is one tcgen05
 //     MMA chain S = k (u_hi + u_lo)^T into the other 256 TMEM columns (keys
 //     are exactly bf16; the two-term split keeps the cosine to about 1e-6);
+//     four threads scan each token's row (64 slot columns each);
 //   - the read view (LayerNorm'd keys with the rotary dims zeroed, values at
 //     the read radius) in shared memory, recomputed only for slots the event
 //     touched, and bulk-copied asynchronously to the event's snapshot;
 //   - the next chunk's keys and values arrive by TMA while an event runs.
-// The merge is deterministic: each slot's owner thread adds its tokens in
-// position order.
+// The merge is deterministic: each slot's owner threads add its tokens in
+// position order.  Rows are accumulated 8 dims at a time from shared memory
+// so that every thread stays within 128 registers.
 #include "kvm_internal.cuh"
 #include "tc_primitives.cuh"
 
@@ -29,6 +33,7 @@ using namespace tc;
 
 constexpr int MAXS = 256;  // slots held on chip
 constexpr int TOK = 128;   // token rows of the MMA tile
+constexpr int NT = 512;    // threads: key owner j and value owner 256 + j of every slot j
 constexpr int ROWB = 128;  // bytes of one 64-dim bf16 row
 constexpr int OFF_UHI = 0;                      // [256][128 B] swizzled (MMA B operand)
 constexpr int OFF_ULO = OFF_UHI + MAXS * ROWB;  // [256][128 B] swizzled
@@ -40,17 +45,18 @@ constexpr int OFF_MISC = OFF_VV + MAXS * ROWB;
 
 struct Misc {
     float g[TOK], kn[TOK], m[TOK];
-    float pb[2][TOK], ps[2][TOK];
-    int pa[2][TOK];
+    float pb[4][TOK], ps[4][TOK];  // best / second best of each 64-slot quarter
+    int pa[4][TOK];                // argmax of each quarter
     int kind[TOK], slot[TOK], list[TOK];
     int hist[4][MAXS];  // merged tokens per slot, per token warp
-    int cnt[MAXS];
-    float rho[MAXS];
+    int cnt[MAXS];      // written by key owners
+    float rho[MAXS];    // written by value owners
     int cnt_new[MAXS];
     int seg[MAXS + 1];
     int slot_tok[MAXS];
     unsigned long long bar_k[2];
     unsigned long long bar_s;
+    unsigned long long bar_st;  // state rows staged by TMA
     uint32_t tmem_slot;
     int abort_flag;
 };
@@ -62,19 +68,70 @@ static __device__ unsigned long long g_probe_fold[16];
 
 __device__ __forceinline__ int swz(int row, int ch) { return row * ROWB + (((ch ^ (row & 7)) & 7) << 4); }
 
-// 64 bf16 of a swizzled row -> fp32
-__device__ __forceinline__ void load_row_sw(const uint8_t* base, int row, float (&x)[64]) {
+// fp32 state rows move between global memory and shared memory by TMA through
+// staging tiles: half h (floats [32h, 32h + 32)) of row j at
+// h * 32 KB + j * 128 B, 16-byte chunk c at (c ^ (j & 7)) * 16 (the 128-byte
+// swizzle, so that the row-per-thread accesses below are conflict-free).
+constexpr int STAGE_ROWS = 64;  // rows per TMA box (fewer when max_slots is smaller)
+__device__ __forceinline__ uint32_t stage_off(int j, int q) {
+    const int h = q >> 3, c = q & 7;
+    return (uint32_t)(h * 32768 + j * 128 + ((c ^ (j & 7)) << 4));
+}
+
+__device__ __forceinline__ float2 bf2(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+// x = g * row, for the 64 bf16 of a swizzled row
+__device__ __forceinline__ void set_row_sw(const uint8_t* base, int row, float g, float (&x)[64]) {
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
         const uint4 w = *reinterpret_cast<const uint4*>(base + swz(row, ch));
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const float2 f = __bfloat1622float2(h[u]);
-            x[ch * 8 + 2 * u] = f.x;
-            x[ch * 8 + 2 * u + 1] = f.y;
+            const float2 f = bf2(wv[u]);
+            x[ch * 8 + 2 * u] = g * f.x;
+            x[ch * 8 + 2 * u + 1] = g * f.y;
         }
     }
+}
+// x += g * row
+__device__ __forceinline__ void add_row_sw(const uint8_t* base, int row, float g, float (&x)[64]) {
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(base + swz(row, ch));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 f = bf2(wv[u]);
+            x[ch * 8 + 2 * u] = fmaf(g, f.x, x[ch * 8 + 2 * u]);
+            x[ch * 8 + 2 * u + 1] = fmaf(g, f.y, x[ch * 8 + 2 * u + 1]);
+        }
+    }
+}
+// sum of squares of the dims [8 c0, 8 (c0 + nc)) of a swizzled row, partial
+// sums by dim mod 8 in increasing dim order (the order of dot64 below)
+template <int NC>
+__device__ __forceinline__ float sq_row_sw(const uint8_t* base, int row, int c0) {
+    float p[8];
+#pragma unroll
+    for (int ch = 0; ch < NC; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(base + swz(row, c0 + ch));
+        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 f = bf2(wv[u]);
+            if (ch == 0) {
+                p[2 * u] = f.x * f.x;
+                p[2 * u + 1] = f.y * f.y;
+            } else {
+                p[2 * u] = fmaf(f.x, f.x, p[2 * u]);
+                p[2 * u + 1] = fmaf(f.y, f.y, p[2 * u + 1]);
+            }
+        }
+    }
+    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
@@ -91,21 +148,6 @@ __device__ __forceinline__ float sum64(const float (&x)[64]) {
     for (int i = 8; i < 64; ++i) p[i & 7] += x[i];
     return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
-// sum over x of (x - c)^2, eight partial sums
-__device__ __forceinline__ float sqdev64(const float (&x)[64], float c, float scale) {
-    float p[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float d = x[i] * scale - c;
-        p[i] = d * d;
-    }
-#pragma unroll
-    for (int i = 8; i < 64; ++i) {
-        const float d = x[i] * scale - c;
-        p[i & 7] = fmaf(d, d, p[i & 7]);
-    }
-    return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
-}
 // dot product of two 64-vectors, eight partial sums
 __device__ __forceinline__ float dot64(const float (&x)[64], const float (&y)[64]) {
     float p[8];
@@ -116,15 +158,14 @@ __device__ __forceinline__ float dot64(const float (&x)[64], const float (&y)[64
     return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
-// Owner-thread renormalisation of slot j from its key sums (registers): the
-// winner-take-all direction u = c / |c| (as bf16 hi + lo terms) and the
+// Key owner's renormalisation of slot j from its key sums (centred in place):
+// the winner-take-all direction u = c / |c| (as bf16 hi + lo terms) and the
 // read-view key LayerNorm(sum / count) = c / sqrt(|c|^2 / 64 + eps * count^2),
 // both from the centred sums c = sum - mean(sum); rotary dims of the key are 0.
-__device__ __forceinline__ void owner_view_k(int j, const float (&sk)[64], int cnt, int r, float eps, uint8_t* sm) {
-    const float mean = sum64(sk) * (1.0f / 64.0f);
-    float c[64];
+__device__ __forceinline__ void key_view_inplace(int j, float (&c)[64], int cnt, int r, float eps, uint8_t* sm) {
+    const float mean = sum64(c) * (1.0f / 64.0f);
 #pragma unroll
-    for (int x = 0; x < 64; ++x) c[x] = sk[x] - mean;
+    for (int x = 0; x < 64; ++x) c[x] -= mean;
     const float ss = dot64(c, c);
     const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
     const float fc = (float)cnt;
@@ -150,8 +191,8 @@ __device__ __forceinline__ void owner_view_k(int j, const float (&sk)[64], int c
     }
 }
 
-// Read-view value of slot j: rho * unit(sum_v).
-__device__ __forceinline__ void owner_view_v(int j, const float (&sv)[64], float rho, uint8_t* sm) {
+// Value owner's read view of slot j: rho * unit(sum_v).
+__device__ __forceinline__ void value_view(int j, const float (&sv)[64], float rho, uint8_t* sm) {
     const float nv = sqrtf(dot64(sv, sv));
     const float f = nv > 0.0f ? rho / nv : 0.0f;
     uint4* vv = reinterpret_cast<uint4*>(sm + OFF_VV + j * ROWB);
@@ -186,13 +227,54 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const float (&x)[64]) 
     tmem_st32(taddr + 32, b);
 }
 
-__global__ void __launch_bounds__(256, 1)
+// Running best / second best / argmax over 32 slot columns starting at slot
+// base, restricted to [lo, hi); strictly larger values take the lead, so ties
+// keep the lower slot index.
+__device__ __forceinline__ void scan32(const uint32_t (&v)[32], int base, int lo, int hi, float& b, float& s,
+                                       int& arg) {
+    if (base >= lo && base + 32 <= hi) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+            const float val = __uint_as_float(v[x]);
+            arg = val > b ? base + x : arg;
+            s = fmaxf(s, fminf(val, b));
+            b = fmaxf(b, val);
+        }
+    } else if (base + 32 > lo && base < hi) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+            const int j = base + x;
+            const float val = (j >= lo && j < hi) ? __uint_as_float(v[x]) : -INFINITY;
+            arg = val > b ? j : arg;
+            s = fmaxf(s, fminf(val, b));
+            b = fmaxf(b, val);
+        }
+    }
+}
+
+// (b, s, arg) <- combination with a later (higher slot index) partial result.
+__device__ __forceinline__ void merge_later(float& b, float& s, int& arg, float b2, float s2, int a2) {
+    if (a2 < 0) return;
+    if (arg < 0 || b2 > b) {
+        s = fmaxf(fmaxf(s, s2), arg < 0 ? -INFINITY : b);
+        b = b2;
+        arg = a2;
+    } else {
+        s = fmaxf(s, b2);
+        s = fmaxf(s, s2);
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1)
     fold_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_sk, const __grid_constant__ CUtensorMap tm_sv,
                    const FoldArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Misc& X = *reinterpret_cast<Misc*>(sm + OFF_MISC);
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int j = tid & (MAXS - 1);  // owned slot
+    const bool vside = tid >= MAXS;  // value owner (else key owner)
     const int bh = blockIdx.x;
     const int C = a.C, S = a.S, M = a.M;
 
@@ -200,55 +282,93 @@ __global__ void __launch_bounds__(256, 1)
     float* g_sum_v = a.sum_v + (int64_t)bh * M * D;
     int* g_counts = a.counts + (int64_t)bh * M;
     float* g_rho = a.rho + (int64_t)bh * M;
-    float* g_simdir = a.simdir + (int64_t)bh * M * D;
     uint8_t* g_view_k = reinterpret_cast<uint8_t*>(a.view_k) + (int64_t)bh * M * ROWB;
     uint8_t* g_view_v = reinterpret_cast<uint8_t*>(a.view_v) + (int64_t)bh * M * ROWB;
 
+    // state before the first event (non-empty for a decode-boundary fold or a later segment)
+    const Sched sc_first = a.sched ? a.sched[a.e_begin] : a.sched0;
+    int n = sc_first.n_before;
+    const int srows = a.stage_rows;
+    const int nblk_st = (n + srows - 1) / srows;
     if (tid == 0) {
         mbar_init(smem_u32(&X.bar_k[0]), 1);
         mbar_init(smem_u32(&X.bar_k[1]), 1);
         mbar_init(smem_u32(&X.bar_s), 1);
+        mbar_init(smem_u32(&X.bar_st), 1);
         X.abort_flag = 0;
         fence_barrier_init();
+        // key sums staged in the direction area, value sums in the read-view area
+        if (nblk_st > 0) {
+            const uint32_t bst = smem_u32(&X.bar_st);
+            mbar_expect_tx(bst, 2 * 2 * nblk_st * srows * 128);
+            for (int h = 0; h < 2; ++h)
+                for (int b = 0; b < nblk_st; ++b) {
+                    const uint32_t o = h * 32768 + b * srows * 128;
+                    tma_load_3d(smem_u32(sm + OFF_UHI) + o, &tm_sk, 32 * h, b * srows, bh, bst);
+                    tma_load_3d(smem_u32(sm + OFF_VK) + o, &tm_sv, 32 * h, b * srows, bh, bst);
+                }
+        }
     }
     if (warp == 0) tmem_alloc(smem_u32(&X.tmem_slot), 512);
-    for (int i = tid; i < 2 * MAXS * ROWB / 16; i += 256) {
-        reinterpret_cast<uint4*>(sm + OFF_UHI)[i] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(sm + OFF_VK)[i] = make_uint4(0, 0, 0, 0);
+    if (!vside) {
+        X.cnt[j] = 0;
+        X.rho[j] = 0.0f;
     }
-    X.cnt[tid] = 0;
-    X.rho[tid] = 0.0f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = X.tmem_slot;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int blk = tid >> 7;  // slot block of the owner thread
-    const uint32_t t_sums = tmem + lane_base + blk * 128;
+    // this thread's sums: slot block j / 128, key columns [0, 64) or value columns [64, 128)
+    const uint32_t t_own = tmem + lane_base + (j >> 7) * 128 + (vside ? 64 : 0);
     const uint32_t t_sim = tmem + lane_base + 256;
     const uint32_t sK = smem_u32(sm + OFF_K), sV = smem_u32(sm + OFF_V);
     const uint32_t sUH = smem_u32(sm + OFF_UHI), sUL = smem_u32(sm + OFF_ULO);
     const uint32_t bar_s = smem_u32(&X.bar_s);
 
-    // state before the first event (non-empty for a decode-boundary fold)
-    const Sched sc_first = a.sched ? a.sched[a.e_begin] : a.sched0;
-    int n = sc_first.n_before;
     {
-        const int j = tid;
-        float x64[64];
-        if (j < n) {
-            X.cnt[j] = g_counts[j];
-            X.rho[j] = g_rho[j];
+        float x[64];
+        if (nblk_st > 0) {
+            if (tid == 0 && !mbar_wait(smem_u32(&X.bar_st), 0, &X.abort_flag, a.status)) X.abort_flag = 1;
+            __syncthreads();
         }
+        const uint8_t* stage = sm + (vside ? OFF_VK : OFF_UHI);
 #pragma unroll
-        for (int x = 0; x < 64; ++x) x64[x] = j < n ? g_sum_k[(int64_t)j * D + x] : 0.0f;
-        if (j < n) owner_view_k(j, x64, X.cnt[j], a.r, a.ln_eps, sm);
-        tmem_st64(t_sums, x64);
-#pragma unroll
-        for (int x = 0; x < 64; ++x) x64[x] = j < n ? g_sum_v[(int64_t)j * D + x] : 0.0f;
-        if (j < n) owner_view_v(j, x64, X.rho[j], sm);
-        tmem_st64(t_sums + 64, x64);
+        for (int q = 0; q < 16; ++q) {
+            const float4 f = (j < n && !X.abort_flag) ? *reinterpret_cast<const float4*>(stage + stage_off(j, q))
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[4 * q] = f.x;
+            x[4 * q + 1] = f.y;
+            x[4 * q + 2] = f.z;
+            x[4 * q + 3] = f.w;
+        }
+        __syncthreads();  // the staging areas are free again
+        tmem_st64(t_own, x);
         tmem_wait_st();
+        if (j < n) {
+            if (!vside) {
+                const int cnt = g_counts[j];
+                X.cnt[j] = cnt;
+                key_view_inplace(j, x, cnt, a.r, a.ln_eps, sm);
+            } else {
+                const float rho = g_rho[j];
+                X.rho[j] = rho;
+                value_view(j, x, rho, sm);
+            }
+        } else {
+            // slots not founded yet: zero direction (S = 0) and zero read view
+            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                if (!vside) {
+                    *reinterpret_cast<uint4*>(sm + OFF_UHI + swz(j, ch)) = z;
+                    *reinterpret_cast<uint4*>(sm + OFF_ULO + swz(j, ch)) = z;
+                    *reinterpret_cast<uint4*>(sm + OFF_VK + j * ROWB + ch * 16) = z;
+                } else {
+                    *reinterpret_cast<uint4*>(sm + OFF_VV + j * ROWB + ch * 16) = z;
+                }
+            }
+        }
     }
     tc_fence_before();
     fence_proxy_async();
@@ -295,37 +415,42 @@ __global__ void __launch_bounds__(256, 1)
         const bool do_mma = n0 > S;
 
         // similarity of the chunk's keys to every slot direction
-        if (do_mma && tid == 0) {
-            tc_fence_after();
-            for (int ks = 0; ks < 4; ++ks)
-                for (int part = 0; part < 2; ++part) {
-                    const uint64_t ad = sdesc_sw128(sK + buf * TOK * ROWB + ks * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128((part ? sUL : sUH) + ks * 32, 16, 1024);
-                    mma_bf16_ss(tmem + 256, ad, bd, idesc, (ks | part) ? 1u : 0u);
-                }
-            mma_commit(bar_s);
+        if (tid == 0) {
+            if (do_mma) {
+                tc_fence_after();
+                for (int ks = 0; ks < 4; ++ks)
+                    for (int part = 0; part < 2; ++part) {
+                        const uint64_t ad = sdesc_sw128(sK + buf * TOK * ROWB + ks * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128((part ? sUL : sUH) + ks * 32, 16, 1024);
+                        mma_bf16_ss(tmem + 256, ad, bd, idesc, (ks | part) ? 1u : 0u);
+                    }
+                mma_commit(bar_s);
+            }
+            // the next chunk's keys and values load while this event runs
+            if (e + 1 < a.e_end) load_chunk(e + 1, buf ^ 1);
         }
-        // the next chunk's keys and values load while this event runs
-        if (tid == 0 && e + 1 < a.e_end) load_chunk(e + 1, buf ^ 1);
-        // per-token set-up
-        if (tid < C) {
-            const int t = tid;
-            X.g[t] = g_here;
-            float kx[64];
-            load_row_sw(kch, t, kx);
-            X.kn[t] = sqrtf(dot64(kx, kx));
-            const bool sink = first_pos + t < S;
-            X.kind[t] = sink ? 2 : -1;
-            X.slot[t] = sink ? (int)(first_pos + t) : -1;
+        if (tid < C) X.g[tid] = g_here;
+        // per-token set-up: two threads per token (warps 8-15), 32 dims each
+        if (vside) {
+            const int t = (tid - MAXS) >> 1, h = tid & 1;
+            float ss = t < C ? sq_row_sw<4>(kch, t, 4 * h) : 0.0f;
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            if (t < C && h == 0) {
+                X.kn[t] = sqrtf(ss);
+                const bool sink = first_pos + t < S;
+                X.kind[t] = sink ? 2 : -1;
+                X.slot[t] = sink ? (int)(first_pos + t) : -1;
+            }
+        } else {
+            X.slot_tok[j] = -1;
         }
-        X.slot_tok[tid] = -1;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) X.hist[w][tid] = 0;
+        X.hist[tid >> 8][j] = 0;
+        X.hist[2 + (tid >> 8)][j] = 0;
         __syncthreads();
         KVM_PROBE_LAP(1)
 
-        // best / second / argmax over the mergeable slots [S, n0): each half of
-        // the CTA scans 128 slot columns of every token row
+        // best / second / argmax over the mergeable slots [S, n0): each quarter of
+        // the CTA scans 64 slot columns of every token row (token = TMEM lane)
         if (do_mma) {
             if (tid == 0 && !mbar_wait(bar_s, mma_count & 1, &X.abort_flag, a.status)) X.abort_flag = 1;
             __syncthreads();
@@ -333,66 +458,24 @@ __global__ void __launch_bounds__(256, 1)
             KVM_PROBE_LAP(9)
             ++mma_count;
             tc_fence_after();
-            const int half = tid >> 7, t = tid & 127;
-            const int lo = max(S, half * 128), hi = min(n0, half * 128 + 128);
-            // four independent chains (one per 32-column chunk), merged in index order
-            float bq[4], sq[4];
-            int aq[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                bq[c] = -INFINITY;
-                sq[c] = -INFINITY;
-                aq[c] = -1;
-            }
+            const int q = tid >> 7, t = tid & 127;
+            const int lo = max(S, q * 64), hi = min(n0, q * 64 + 64);
+            float b0 = -INFINITY, s0 = -INFINITY, b1 = -INFINITY, s1 = -INFINITY;
+            int a0 = -1, a1 = -1;
             if (lo < hi) {
-                uint32_t va[4][32];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(t_sim + half * 128 + c * 32, va[c]);
+                uint32_t va[32], vb[32];
+                tmem_ld32(t_sim + q * 64, va);
+                tmem_ld32(t_sim + q * 64 + 32, vb);
                 tmem_wait_ld();
                 KVM_PROBE_LAP(11)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int base = half * 128 + c * 32;
-                    // branchless running best / second best / argmax (strictly larger
-                    // values take the lead, so ties keep the lower slot index)
-                    if (base >= lo && base + 32 <= hi) {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) {
-                            const float val = __uint_as_float(va[c][x]);
-                            aq[c] = val > bq[c] ? base + x : aq[c];
-                            sq[c] = fmaxf(sq[c], fminf(val, bq[c]));
-                            bq[c] = fmaxf(bq[c], val);
-                        }
-                    } else if (base + 32 > lo && base < hi) {
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) {
-                            const int j = base + x;
-                            const float val = (j >= lo && j < hi) ? __uint_as_float(va[c][x]) : -INFINITY;
-                            aq[c] = val > bq[c] ? j : aq[c];
-                            sq[c] = fmaxf(sq[c], fminf(val, bq[c]));
-                            bq[c] = fmaxf(bq[c], val);
-                        }
-                    }
-                }
+                scan32(va, q * 64, lo, hi, b0, s0, a0);
+                scan32(vb, q * 64 + 32, lo, hi, b1, s1, a1);
             }
-            float b = bq[0], s2 = sq[0];
-            int ba = aq[0];
-#pragma unroll
-            for (int c = 1; c < 4; ++c) {
-                if (aq[c] < 0) continue;
-                if (ba < 0 || bq[c] > b) {  // a strictly larger value from a later chunk wins
-                    s2 = fmaxf(fmaxf(s2, sq[c]), ba < 0 ? -INFINITY : b);
-                    b = bq[c];
-                    ba = aq[c];
-                } else {
-                    s2 = fmaxf(s2, bq[c]);
-                    s2 = fmaxf(s2, sq[c]);
-                }
-            }
+            merge_later(b0, s0, a0, b1, s1, a1);
             KVM_PROBE_LAP(12)
-            X.pb[half][t] = b;
-            X.ps[half][t] = s2;
-            X.pa[half][t] = ba;
+            X.pb[q][t] = b0;
+            X.ps[q][t] = s0;
+            X.pa[q][t] = a0;
             tc_fence_before();
             __syncthreads();
         }
@@ -401,20 +484,8 @@ __global__ void __launch_bounds__(256, 1)
         int barg = -1;
         const bool cand = tid < C && X.kind[tid] != 2;
         if (cand && do_mma) {
-            const int t = tid;
-            const float b0 = X.pb[0][t], s0 = X.ps[0][t], b1 = X.pb[1][t], s1 = X.ps[1][t];
-            const int a0 = X.pa[0][t], a1 = X.pa[1][t];
-            if (a0 >= 0 && (a1 < 0 || b0 >= b1)) {
-                best = b0;
-                barg = a0;
-                sec = fmaxf(s0, a1 >= 0 ? b1 : -INFINITY);
-                sec = fmaxf(sec, s1);
-            } else if (a1 >= 0) {
-                best = b1;
-                barg = a1;
-                sec = fmaxf(s1, a0 >= 0 ? b0 : -INFINITY);
-                sec = fmaxf(sec, s0);
-            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) merge_later(best, sec, barg, X.pb[q][tid], X.ps[q][tid], X.pa[q][tid]);
         }
         const float kn = tid < C ? X.kn[tid] : 0.0f;
         if (cand) X.m[tid] = barg < 0 ? -INFINITY : (kn > 0.0f ? best / kn : 0.0f);
@@ -451,24 +522,22 @@ __global__ void __launch_bounds__(256, 1)
         if (na > 0) {
             // directions of the new slots (from their founding token), then the
             // remaining tokens also compare against them
-            const int j = tid;
-            if (j >= n0 && j < n0 + na) {
+            if (!vside && j >= n0 && j < n0 + na) {
                 const int t = X.slot_tok[j];
                 float kx[64];
-                load_row_sw(kch, t, kx);
-                const float g = X.g[t];
-#pragma unroll
-                for (int x = 0; x < 64; ++x) kx[x] = g * kx[x];
+                set_row_sw(kch, t, X.g[t], kx);
                 const float mean = sum64(kx) * (1.0f / 64.0f);
-                const float ss = sqdev64(kx, mean, 1.0f);
+#pragma unroll
+                for (int x = 0; x < 64; ++x) kx[x] -= mean;
+                const float ss = dot64(kx, kx);
                 const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const float a0 = (kx[ch * 8 + 2 * u] - mean) * inv;
-                        const float a1 = (kx[ch * 8 + 2 * u + 1] - mean) * inv;
+                        const float a0 = kx[ch * 8 + 2 * u] * inv;
+                        const float a1 = kx[ch * 8 + 2 * u + 1] * inv;
                         const __nv_bfloat16 h0 = __float2bfloat16_rn(a0), h1 = __float2bfloat16_rn(a1);
                         hw[u] = pack2(__bfloat162float(h0), __bfloat162float(h1));
                         lw[u] = pack2(a0 - __bfloat162float(h0), a1 - __bfloat162float(h1));
@@ -480,14 +549,29 @@ __global__ void __launch_bounds__(256, 1)
             __syncthreads();
             if (tid < C && X.kind[tid] == 0) {
                 float kx[64];
-                load_row_sw(kch, tid, kx);
+                set_row_sw(kch, tid, 1.0f, kx);
                 for (int jj = n0; jj < n0 + na; ++jj) {
-                    float hx[64], lx[64];
-                    load_row_sw(sm + OFF_UHI, jj, hx);
-                    load_row_sw(sm + OFF_ULO, jj, lx);
+                    // k . (u_hi + u_lo), partial sums by dim mod 8 in dim order
+                    float p[8];
 #pragma unroll
-                    for (int x = 0; x < 64; ++x) hx[x] += lx[x];
-                    const float s = dot64(kx, hx);
+                    for (int ch = 0; ch < 8; ++ch) {
+                        const uint4 hw = *reinterpret_cast<const uint4*>(sm + OFF_UHI + swz(jj, ch));
+                        const uint4 lw = *reinterpret_cast<const uint4*>(sm + OFF_ULO + swz(jj, ch));
+                        const uint32_t hv[4] = {hw.x, hw.y, hw.z, hw.w}, lv[4] = {lw.x, lw.y, lw.z, lw.w};
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float2 hf = bf2(hv[u]), lf = bf2(lv[u]);
+                            const float u0 = hf.x + lf.x, u1 = hf.y + lf.y;
+                            if (ch == 0) {
+                                p[2 * u] = kx[2 * u] * u0;
+                                p[2 * u + 1] = kx[2 * u + 1] * u1;
+                            } else {
+                                p[2 * u] = fmaf(kx[ch * 8 + 2 * u], u0, p[2 * u]);
+                                p[2 * u + 1] = fmaf(kx[ch * 8 + 2 * u + 1], u1, p[2 * u + 1]);
+                            }
+                        }
+                    }
+                    const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
                     if (s > best) {
                         sec = best;
                         best = s;
@@ -532,7 +616,7 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         if (merged)
             for (int w = 0; w < warp; ++w) rank_in_slot += X.hist[w][sj];
-        X.cnt_new[tid] = X.hist[0][tid] + X.hist[1][tid] + X.hist[2][tid] + X.hist[3][tid];
+        if (!vside) X.cnt_new[j] = X.hist[0][j] + X.hist[1][j] + X.hist[2][j] + X.hist[3][j];
         __syncthreads();
         if (warp == 0) {
             const int lane = tid & 31;
@@ -563,62 +647,45 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         KVM_PROBE_LAP(5)
 
-        // owner threads: founding and merging into their slot, then the new read view
+        // owners: founding and merging into their slot (key owner: key sums and
+        // count; value owner: value sums and read radius), then the new read view
         {
-            const int j = tid;
             const int ft = X.slot_tok[j];
             const int nm = X.cnt_new[j];
             const bool touched = ft >= 0 || nm > 0;
             if (__any_sync(0xffffffffu, touched)) {
                 const int b0 = X.seg[j];
-                int cnt = X.cnt[j];
-                float rho = X.rho[j];
-                float x64[64], tx[64];
-                // keys
-                tmem_ld64(t_sums, x64);
+                const uint8_t* rows = vside ? vch : kch;
+                float x[64];
+                tmem_ld64(t_own, x);
+                int cnt = 0;
+                float rho = 0.0f;
                 if (touched) {
+                    if (!vside) cnt = X.cnt[j];
+                    else rho = X.rho[j];
                     if (ft >= 0) {
-                        load_row_sw(kch, ft, tx);
-                        const float g = X.g[ft];
-#pragma unroll
-                        for (int x = 0; x < 64; ++x) x64[x] = g * tx[x];
+                        set_row_sw(rows, ft, X.g[ft], x);
                         cnt = 0;
+                        if (vside) rho = sqrtf(sq_row_sw<8>(vch, ft, 0));
                     }
                     // merged tokens in position order
                     for (int i = b0; i < b0 + nm; ++i) {
                         const int t = X.list[i];
-                        load_row_sw(kch, t, tx);
-                        const float g = X.g[t];
-#pragma unroll
-                        for (int x = 0; x < 64; ++x) x64[x] = fmaf(g, tx[x], x64[x]);
+                        add_row_sw(rows, t, X.g[t], x);
                     }
                     cnt += nm + (ft >= 0 ? 1 : 0);
-                    owner_view_k(j, x64, cnt, a.r, a.ln_eps, sm);
                 }
-                tmem_st64(t_sums, x64);
-                // values
-                tmem_ld64(t_sums + 64, x64);
-                if (touched) {
-                    if (ft >= 0) {
-                        load_row_sw(vch, ft, tx);
-                        const float g = X.g[ft];
-#pragma unroll
-                        for (int x = 0; x < 64; ++x) x64[x] = g * tx[x];
-                        rho = sqrtf(dot64(tx, tx));
-                    }
-                    for (int i = b0; i < b0 + nm; ++i) {
-                        const int t = X.list[i];
-                        load_row_sw(vch, t, tx);
-                        const float g = X.g[t];
-#pragma unroll
-                        for (int x = 0; x < 64; ++x) x64[x] = fmaf(g, tx[x], x64[x]);
-                    }
-                    owner_view_v(j, x64, rho, sm);
-                    X.cnt[j] = cnt;
-                    X.rho[j] = rho;
-                }
-                tmem_st64(t_sums + 64, x64);
+                tmem_st64(t_own, x);
                 tmem_wait_st();
+                if (touched) {
+                    if (!vside) {
+                        X.cnt[j] = cnt;
+                        key_view_inplace(j, x, cnt, a.r, a.ln_eps, sm);
+                    } else {
+                        X.rho[j] = rho;
+                        value_view(j, x, rho, sm);
+                    }
+                }
             }
         }
         KVM_PROBE_LAP(6)
@@ -639,43 +706,37 @@ __global__ void __launch_bounds__(256, 1)
         KVM_PROBE_LAP(7)
     }
 
-    // write the state back for decode, export and the portable kernels
+    // write the state back for decode, export and later segments: the sums go
+    // through swizzled staging tiles (key sums in the direction area, value sums
+    // in the chunk area) and leave by TMA; the read view leaves by bulk copy
     if (tid == 0) bulk_wait_all();
     {
-        const int j = tid;
-        const bool wr = j < n && !X.abort_flag;
-        float x64[64];
-        tmem_ld64(t_sums, x64);
-        if (wr) {
-            const float mean = sum64(x64) * (1.0f / 64.0f);
-            const float ss = sqdev64(x64, mean, 1.0f);
-            const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
-            float4* dk = reinterpret_cast<float4*>(g_sum_k + (int64_t)j * D);
-            float4* ds = reinterpret_cast<float4*>(g_simdir + (int64_t)j * D);
+        float x[64];
+        tmem_ld64(t_own, x);
+        uint8_t* stage = sm + (vside ? OFF_K : OFF_UHI);
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                dk[x] = make_float4(x64[4 * x], x64[4 * x + 1], x64[4 * x + 2], x64[4 * x + 3]);
-                ds[x] = make_float4((x64[4 * x] - mean) * inv, (x64[4 * x + 1] - mean) * inv,
-                                    (x64[4 * x + 2] - mean) * inv, (x64[4 * x + 3] - mean) * inv);
-            }
+        for (int q = 0; q < 16; ++q)
+            *reinterpret_cast<float4*>(stage + stage_off(j, q)) =
+                make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        if (j < n && !X.abort_flag) {
+            if (!vside) g_counts[j] = X.cnt[j];
+            else g_rho[j] = X.rho[j];
         }
-        tmem_ld64(t_sums + 64, x64);
-        if (wr) {
-            float4* dv = reinterpret_cast<float4*>(g_sum_v + (int64_t)j * D);
-#pragma unroll
-            for (int x = 0; x < 16; ++x) dv[x] = make_float4(x64[4 * x], x64[4 * x + 1], x64[4 * x + 2], x64[4 * x + 3]);
-            g_counts[j] = X.cnt[j];
-            g_rho[j] = X.rho[j];
-            const uint4* vk = reinterpret_cast<const uint4*>(sm + OFF_VK + j * ROWB);
-            const uint4* vv = reinterpret_cast<const uint4*>(sm + OFF_VV + j * ROWB);
-            uint4* gk = reinterpret_cast<uint4*>(g_view_k + (int64_t)j * ROWB);
-            uint4* gv = reinterpret_cast<uint4*>(g_view_v + (int64_t)j * ROWB);
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                gk[ch] = vk[ch];
-                gv[ch] = vv[ch];
+    }
+    fence_proxy_async();
+    __syncthreads();
+    if (tid == 0 && n > 0 && !X.abort_flag) {
+        const int nb = (n + srows - 1) / srows;
+        for (int h = 0; h < 2; ++h)
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t o = h * 32768 + b * srows * 128;
+                tma_store_3d(&tm_sk, smem_u32(sm + OFF_UHI) + o, 32 * h, b * srows, bh);
+                tma_store_3d(&tm_sv, smem_u32(sm + OFF_K) + o, 32 * h, b * srows, bh);
             }
-        }
+        bulk_store(g_view_k, smem_u32(sm + OFF_VK), (uint32_t)n * ROWB);
+        bulk_store(g_view_v, smem_u32(sm + OFF_VV), (uint32_t)n * ROWB);
+        bulk_commit();
+        bulk_wait_all();
     }
     KVM_PROBE_LAP(10)
     if (tid == 0) KVM_PROBE_FLUSH(g_probe_fold, 0, 13)
@@ -698,13 +759,17 @@ KVM_PROBE_READOUT(kvm_probe_read_fold, foldtc::g_probe_fold)
 
 bool fold_tc_supported(const FoldArgs& a, bool bf16) { return bf16 && a.C <= 128 && a.M <= foldtc::MAXS; }
 
-cudaError_t launch_fold_tc(const FoldArgs& a, cudaStream_t s) {
-    CUtensorMap mk, mv;
+cudaError_t launch_fold_tc(const FoldArgs& args, cudaStream_t s) {
+    FoldArgs a = args;
+    a.stage_rows = a.M < foldtc::STAGE_ROWS ? a.M : foldtc::STAGE_ROWS;
+    CUtensorMap mk, mv, msk, msv;
     if (!make_tmap_bf16_3d(&mk, a.k_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
-        !make_tmap_bf16_3d(&mv, a.v_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128))
+        !make_tmap_bf16_3d(&mv, a.v_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
+        !make_tmap_f32_3d(&msk, a.sum_k, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows) ||
+        !make_tmap_f32_3d(&msv, a.sum_v, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows))
         return cudaErrorInvalidValue;
     cudaFuncSetAttribute(foldtc::fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, foldtc::SMEM_BYTES);
-    foldtc::fold_tc_kernel<<<a.BH, 256, foldtc::SMEM_BYTES, s>>>(mk, mv, a);
+    foldtc::fold_tc_kernel<<<a.BH, foldtc::NT, foldtc::SMEM_BYTES, s>>>(mk, mv, msk, msv, a);
     return cudaGetLastError();
 }
 

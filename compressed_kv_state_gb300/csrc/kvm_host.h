@@ -31,5 +31,27 @@ Sched event_sched(const kvm_config& c, int64_t first_pos, int64_t n, int64_t t);
 bool validate(const kvm_config* c, std::string& why);
 Layout layout_of(const kvm_config& c);
 
+// Byte offset, inside the status region, of the attention's tile-range counters.
+constexpr size_t TILE_CTR_OFF = 128;
+
+// Two disjoint SM partitions (green contexts) with a stream each, for the
+// overlapped prefill; defined in kvm_partition.cu.
+struct Partition {
+    static constexpr int MAX_SEGS = 16;
+    bool ok = false;
+    int sm_fold = 0, sm_attn = 0, sm_all = 0;
+    void* g_fold = nullptr;  // CUgreenCtx
+    void* g_attn = nullptr;
+    cudaStream_t s_fold = nullptr, s_attn = nullptr;
+    cudaEvent_t ev_fork = nullptr;              // primary context
+    cudaEvent_t ev_seg[MAX_SEGS] = {};          // fold partition: end of segment k
+    cudaEvent_t ev_attn = nullptr;              // attention partition: end of its work
+};
+// fold_rows SMs (rounded up to the split granularity) for the fold chain, the
+// rest for attention.  False (with the reason) when the device or driver
+// cannot provide both.
+bool partition_make(int device, int fold_rows, Partition* p, std::string& why);
+void partition_free(Partition* p);
+
 }  // namespace host
 }  // namespace kvm

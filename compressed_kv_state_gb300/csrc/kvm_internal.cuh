@@ -84,6 +84,7 @@ struct FoldArgs {
     int test_stall;  // wait for a chunk copy that is never issued (bounded-wait test)
     int* status;
     int BH;
+    int stage_rows;  // on-chip chain: rows per TMA box of the state sums (set by its launcher)
 };
 
 // ------------------------------------------------------------- attention
@@ -103,6 +104,18 @@ struct AttnArgs {
     float scale_log2;   // log2(e) / sqrt(D)
     int BH;
     int* status;
+    // Tensor-core path only.  Tiles (128 queries of one row) are numbered
+    // query-tile-major and split into ranges r = [range_end[r-1], range_end[r])
+    // (range_end[-1] = 0).  tile_ctr != nullptr: CTAs claim tiles of ranges
+    // 0 .. n_ranges-1 in order, tile range_end[r-1] + atomicAdd(&tile_ctr[r], 1),
+    // so launches on several streams share one numbering and every tile is
+    // taken once (a counter overshoots only once its range is exhausted).
+    // nullptr: every tile, statically strided over the CTAs.
+    static constexpr int MAX_RANGES = 24;
+    int* tile_ctr;
+    int n_ranges;
+    int range_end[MAX_RANGES];
+    int grid;           // CTAs to launch; 0 = two per SM of the device
 };
 
 struct DecodeArgs {

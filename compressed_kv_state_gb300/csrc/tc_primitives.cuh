@@ -98,6 +98,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Tiled store of one box from shared memory (bulk-group completion: commit,
+// then wait before the shared memory is reused or the CTA exits).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -216,5 +225,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Host: 3-D bf16 tensor map over [planes][rows][64], box_rows x 64 box, 128-byte swizzle.
 bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes, uint32_t box_rows);
+// 3-D fp32 map over [planes][rows][64] with a box of 32 floats x box_rows, 128-byte swizzle.
+bool make_tmap_f32_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t planes, uint32_t box_rows);
 
 }  // namespace kvm

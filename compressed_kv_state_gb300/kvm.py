@@ -51,7 +51,8 @@ class kvm_timing(ctypes.Structure):
     _fields_ = [("fold_ms", ctypes.c_double), ("attn_ms", ctypes.c_double),
                 ("decode_ms", ctypes.c_double), ("other_ms", ctypes.c_double),
                 ("fold_launches", ctypes.c_int64), ("attn_launches", ctypes.c_int64),
-                ("decode_launches", ctypes.c_int64), ("other_launches", ctypes.c_int64)]
+                ("decode_launches", ctypes.c_int64), ("other_launches", ctypes.c_int64),
+                ("kernels", ctypes.c_int64)]
 
 
 class KvmError(RuntimeError):
@@ -85,6 +86,10 @@ def _load():
     lib.kvm_layer_set_timing.argtypes = [P, ctypes.c_int]
     lib.kvm_layer_get_timing.restype = ctypes.c_int
     lib.kvm_layer_get_timing.argtypes = [P, P]
+    lib.kvm_layer_set_overlap.restype = ctypes.c_int
+    lib.kvm_layer_set_overlap.argtypes = [P, ctypes.c_int32]
+    lib.kvm_layer_get_overlap.restype = ctypes.c_int
+    lib.kvm_layer_get_overlap.argtypes = [P, P]
     lib.kvm_prefill_noalloc.restype = ctypes.c_int
     lib.kvm_prefill_noalloc.argtypes = [P, P, P, P, P, I64, P, P]
     lib.kvm_layer_destroy.restype = None
@@ -160,6 +165,18 @@ def kvm_layer_get_timing(layer) -> dict:
     t = kvm_timing()
     _check(lib.kvm_layer_get_timing(layer, ctypes.byref(t)), layer)
     return {name: getattr(t, name) for name, _ in kvm_timing._fields_}
+
+
+def kvm_layer_set_overlap(layer, segments: int):
+    """0: sequential prefill; n > 0: n fold segments overlapped with attention; < 0: automatic."""
+    _check(lib.kvm_layer_set_overlap(layer, int(segments)), layer)
+
+
+def kvm_layer_get_overlap(layer) -> int:
+    """Fold segments of the layer's last prefill (0: it ran sequentially)."""
+    n = ctypes.c_int32(0)
+    _check(lib.kvm_layer_get_overlap(layer, ctypes.byref(n)), layer)
+    return n.value
 
 
 KVM_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024

@@ -185,13 +185,17 @@ const char* kvm_last_error(const kvm_layer* layer);
  * events recorded on the launch stream immediately before and after each
  * kernel: a phase's time is its kernels' device duration (the start event
  * completes only when the stream reaches the kernel, so queueing behind earlier
- * work is not counted). */
+ * work is not counted).  In an overlapped prefill (kvm_layer_set_overlap) one
+ * fold interval spans the whole chain, from the start of its first segment to
+ * the end of its last, and the attention, split over several launches that
+ * run beside the chain, is not timed. */
 typedef struct {
     double fold_ms;      /* fold-chain kernels (prefill chains and decode-boundary folds) */
-    double attn_ms;      /* prefill attention kernels */
+    double attn_ms;      /* prefill attention kernels (sequential prefill only) */
     double decode_ms;    /* decode attention kernels */
     double other_ms;     /* ring fill, state renormalisation */
-    int64_t fold_launches, attn_launches, decode_launches, other_launches;
+    int64_t fold_launches, attn_launches, decode_launches, other_launches;  /* timed intervals */
+    int64_t kernels;     /* every kernel the layer launched, timed or not */
 } kvm_timing;
 
 /* Enable (1) or disable (0) per-kernel timing; enabling resets the totals.
@@ -200,6 +204,29 @@ kvm_status kvm_layer_set_timing(kvm_layer* layer, int enable);
 
 /* Wait for the recorded events and return the totals since timing was enabled. */
 kvm_status kvm_layer_get_timing(kvm_layer* layer, kvm_timing* out);
+
+/* Overlapped prefill.  The fold chain runs one CTA per (b,h) row, each on an SM
+ * of its own, for the whole chain, while the attention of chunk c needs only
+ * the fold events before it ("Key-Value Means", technical summary, Core
+ * mechanism 4: attention of a chunk overlaps the state update from the chunk
+ * that left the window).  With overlap on, kvm_prefill splits the GPU's SMs
+ * into two disjoint partitions (CUDA green contexts): the chain runs in
+ * `segments` launches on the first (at least B*H SMs), and after each segment
+ * the attention of every chunk it has made ready runs on the second; what is
+ * left of the attention then runs on all SMs.  Results are identical to the
+ * sequential prefill (same kernels, same per-tile arithmetic).
+ *
+ * segments: 0 = never overlap; n > 0 = n fold segments (at most 16, at most
+ * the number of fold events); < 0 = automatic (the default).  Overlap applies
+ * only to the tensor-core paths (bf16, chunk a multiple of 128 and <= 128,
+ * max_slots <= 256), without a debug record, with at least 2 fold events, and
+ * when the device leaves at least one SM partition beside B*H SMs; otherwise
+ * the prefill runs sequentially.  The partition is made on first use and
+ * released by kvm_layer_destroy. */
+kvm_status kvm_layer_set_overlap(kvm_layer* layer, int32_t segments);
+
+/* Fold segments the layer's last kvm_prefill ran with (0: sequential). */
+kvm_status kvm_layer_get_overlap(const kvm_layer* layer, int32_t* last_segments);
 
 /* Size of the static device scratch behind kvm_prefill_noalloc: 32 MiB. */
 #define KVM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
