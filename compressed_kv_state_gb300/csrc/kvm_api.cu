@@ -377,7 +377,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             kvm::host::partition_make(ly->device, BH, &ly->part, ly->part_why);
         }
         if (ly->part.ok) {
-            segs = ly->overlap_segs > 0 ? ly->overlap_segs : 4;
+            segs = ly->overlap_segs > 0 ? ly->overlap_segs : 3;
             if (segs > kvm::host::Partition::MAX_SEGS) segs = kvm::host::Partition::MAX_SEGS;
             if (segs > E) segs = (int)E;
         }

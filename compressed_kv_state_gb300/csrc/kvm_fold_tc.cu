@@ -227,9 +227,11 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const float (&x)[64]) 
     tmem_st32(taddr + 32, b);
 }
 
-// Running best / second best / argmax over 32 slot columns starting at slot
-// base, restricted to [lo, hi); strictly larger values take the lead, so ties
-// keep the lower slot index.
+// Running best / argmax (and, with GAP, second best) over 32 slot columns
+// starting at slot base, restricted to [lo, hi); strictly larger values take
+// the lead, so ties keep the lower slot index.  The second best only feeds the
+// debug record's top-2 gap.
+template <bool GAP>
 __device__ __forceinline__ void scan32(const uint32_t (&v)[32], int base, int lo, int hi, float& b, float& s,
                                        int& arg) {
     if (base >= lo && base + 32 <= hi) {
@@ -237,7 +239,7 @@ __device__ __forceinline__ void scan32(const uint32_t (&v)[32], int base, int lo
         for (int x = 0; x < 32; ++x) {
             const float val = __uint_as_float(v[x]);
             arg = val > b ? base + x : arg;
-            s = fmaxf(s, fminf(val, b));
+            if (GAP) s = fmaxf(s, fminf(val, b));
             b = fmaxf(b, val);
         }
     } else if (base + 32 > lo && base < hi) {
@@ -246,7 +248,7 @@ __device__ __forceinline__ void scan32(const uint32_t (&v)[32], int base, int lo
             const int j = base + x;
             const float val = (j >= lo && j < hi) ? __uint_as_float(v[x]) : -INFINITY;
             arg = val > b ? j : arg;
-            s = fmaxf(s, fminf(val, b));
+            if (GAP) s = fmaxf(s, fminf(val, b));
             b = fmaxf(b, val);
         }
     }
@@ -265,6 +267,7 @@ __device__ __forceinline__ void merge_later(float& b, float& s, int& arg, float 
     }
 }
 
+template <bool GAP>
 __global__ void __launch_bounds__(NT, 1)
     fold_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_sk, const __grid_constant__ CUtensorMap tm_sv,
@@ -468,8 +471,8 @@ __global__ void __launch_bounds__(NT, 1)
                 tmem_ld32(t_sim + q * 64 + 32, vb);
                 tmem_wait_ld();
                 KVM_PROBE_LAP(11)
-                scan32(va, q * 64, lo, hi, b0, s0, a0);
-                scan32(vb, q * 64 + 32, lo, hi, b1, s1, a1);
+                scan32<GAP>(va, q * 64, lo, hi, b0, s0, a0);
+                scan32<GAP>(vb, q * 64 + 32, lo, hi, b1, s1, a1);
             }
             merge_later(b0, s0, a0, b1, s1, a1);
             KVM_PROBE_LAP(12)
@@ -592,7 +595,7 @@ __global__ void __launch_bounds__(NT, 1)
             if (a.dbg_assign) a.dbg_assign[o] = X.slot[tid];
             if (a.dbg_kind) a.dbg_kind[o] = kd;
             if (a.dbg_m) a.dbg_m[o] = kd == 2 ? __int_as_float(0x7fc00000) : X.m[tid];
-            if (a.dbg_gap) {
+            if (GAP && a.dbg_gap) {
                 float gp = __int_as_float(0x7fc00000);
                 if (kd == 0) gp = sec == -INFINITY ? INFINITY : (kn > 0.0f ? (best - sec) / kn : 0.0f);
                 a.dbg_gap[o] = gp;
@@ -768,8 +771,10 @@ cudaError_t launch_fold_tc(const FoldArgs& args, cudaStream_t s) {
         !make_tmap_f32_3d(&msk, a.sum_k, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows) ||
         !make_tmap_f32_3d(&msv, a.sum_v, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows))
         return cudaErrorInvalidValue;
-    cudaFuncSetAttribute(foldtc::fold_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, foldtc::SMEM_BYTES);
-    foldtc::fold_tc_kernel<<<a.BH, foldtc::NT, foldtc::SMEM_BYTES, s>>>(mk, mv, msk, msv, a);
+    // the second-best similarity is tracked only when the debug record wants the top-2 gap
+    auto kern = a.dbg_gap ? foldtc::fold_tc_kernel<true> : foldtc::fold_tc_kernel<false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, foldtc::SMEM_BYTES);
+    kern<<<a.BH, foldtc::NT, foldtc::SMEM_BYTES, s>>>(mk, mv, msk, msv, a);
     return cudaGetLastError();
 }
 
