@@ -110,6 +110,7 @@ Layout layout_of(const kvm_config& c) {
     L.rope = take((size_t)c.max_tokens * (c.rope_dims / 2) * sizeof(float2) + 16);
     L.sched = take((E + 1) * sizeof(Sched));
     L.status = take(256);  // status word at 0, attention tile-range counters at TILE_CTR_OFF
+    L.k_rot = take(c.dtype == KVM_BF16 && c.rope_dims > 0 ? BH * (size_t)c.max_tokens * d * es : 0);
     L.total = o;
     return L;
 }
@@ -148,6 +149,7 @@ struct kvm_layer {
     int device;
     int64_t n_slots, n_overflow, pos;
     int64_t E_max;
+    int nsm = 0;               // SMs of the device
     std::vector<Sched> sched;  // prefill-from-empty schedule (host copy)
     cudaStream_t last_stream;
     std::string err;
@@ -241,6 +243,8 @@ kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t b
     ly->E_max = n_events_for(*cfg, cfg->max_tokens);
     ly->last_stream = nullptr;
     DeviceGuard g(ly->device);
+    cudaDeviceGetAttribute(&ly->nsm, cudaDevAttrMultiProcessorCount, ly->device);
+    if (ly->nsm <= 0) ly->nsm = 1;
     // growth schedule of a prefill from the empty state
     ly->sched.resize((size_t)ly->E_max + 1);
     int64_t n = 0, t = 0;
@@ -367,6 +371,17 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     ra.BH = BH;
     const bool ring_work = n_tokens > ra.first;
 
+    // tensor-core attention: keys rotated once, before it, instead of per tile
+    kvm::RopeKeysArgs ka{};
+    ka.k = k;
+    ka.k_rot = ly->ws + L.k_rot;
+    ka.rope = ly->at<float2>(L.rope);
+    ka.r = c.rope_dims;
+    ka.N = n_tokens;
+    ka.BH = BH;
+    const bool pre_rotate = bf16 && c.rope_dims > 0 && n_tokens > 0 && kvm::attn_tc_supported(aa, bf16);
+    if (pre_rotate) aa.k_rot = ka.k_rot;
+
     // overlapped prefill: fold segments on one SM partition, the attention of
     // the chunks each segment has made ready on the other
     int segs = 0;
@@ -403,6 +418,12 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         if (e == cudaSuccess) e = cudaStreamWaitEvent(P.s_attn, P.ev_fork, 0);
         if (e != cudaSuccess) return ly->cuda_fail(e, "overlap set-up");
         aa.tile_ctr = ctr;
+        if (pre_rotate) {
+            ka.grid = 8 * P.sm_attn;
+            e = timed(ly, PH_OTHER, P.s_attn, [&] { return kvm::launch_rope_keys(ka, P.s_attn); });
+            if (e != cudaSuccess) return ly->cuda_fail(e, "key rotation launch");
+            ly->kernels += 1;
+        }
         // attention launches on the second partition may claim only ready ranges
         const int all_ranges = aa.n_ranges;
         aa.grid = 2 * P.sm_attn;
@@ -443,6 +464,12 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         if (E > 0) {
             e = timed(ly, PH_FOLD, s, [&] { return kvm::launch_fold(fa, bf16, s); });
             if (e != cudaSuccess) return ly->cuda_fail(e, "fold chain launch");
+            ly->kernels += 1;
+        }
+        if (pre_rotate) {
+            ka.grid = 8 * ly->nsm;
+            e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_rope_keys(ka, s); });
+            if (e != cudaSuccess) return ly->cuda_fail(e, "key rotation launch");
             ly->kernels += 1;
         }
         if (n_tokens > 0) {

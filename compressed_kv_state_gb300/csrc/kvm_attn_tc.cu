@@ -63,6 +63,7 @@ struct TcArgs {
     int64_t N;
     int BH, C, W, M, r;
     int tiles_per_head, ntiles;
+    int k_rotated;   // window keys arrive rotated (no RoPE on K in the kernel)
     int* tile_ctr;   // dynamic claiming: one counter per range (nullptr: static striding)
     int n_ranges;
     int range_end[AttnArgs::MAX_RANGES];
@@ -388,7 +389,7 @@ __global__ void __launch_bounds__(256, 2)
                     break;
                 }
                 KVM_PROBE_LAP(1)
-                if (j >= T.nst && half > 0) {
+                if (j >= T.nst && half > 0 && !a.k_rotated) {
                     const int64_t pos = T.ws + KB * (j - T.nst) + rt;
                     if (pos < a.N) {
                         if ((half & 7) == 0)
@@ -444,14 +445,22 @@ __global__ void __launch_bounds__(256, 2)
                     lim = d < 0 ? 0 : (d < KB ? (int)d : KB);
                 }
                 float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (lim == KB) {
+                    // a full block: every column is a valid key
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                    for (int h = 0; h < 2; ++h)
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        const float val = h * 32 + x < lim ? __uint_as_float(v[h][x]) : -INFINITY;
-                        v[h][x] = __float_as_uint(val);
-                        mx[x & 3] = fmaxf(mx[x & 3], val);
-                    }
+                        for (int x = 0; x < 32; ++x) mx[x & 3] = fmaxf(mx[x & 3], __uint_as_float(v[h][x]));
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            const float val = h * 32 + x < lim ? __uint_as_float(v[h][x]) : -INFINITY;
+                            v[h][x] = __float_as_uint(val);
+                            mx[x & 3] = fmaxf(mx[x & 3], val);
+                        }
+                }
                 const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
                 bool rescale = false;
                 float alpha = 1.0f;
@@ -614,7 +623,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, msk, msv;
     const uint64_t BH = (uint64_t)a.BH;
     const uint64_t planes_snap = BH * (uint64_t)(a.snap_events > 0 ? a.snap_events : 1);
-    if (!make_tmap_bf16_3d(&mq, a.q, (uint64_t)a.N, BH, 128) || !make_tmap_bf16_3d(&mk, a.k, (uint64_t)a.N, BH, KB) ||
+    if (!make_tmap_bf16_3d(&mq, a.q, (uint64_t)a.N, BH, 128) || !make_tmap_bf16_3d(&mk, a.k_rot ? a.k_rot : a.k, (uint64_t)a.N, BH, KB) ||
         !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH, KB) ||
         !make_tmap_bf16_3d(&msk, a.snap_k, (uint64_t)a.M, planes_snap, KB) ||
         !make_tmap_bf16_3d(&msv, a.snap_v, (uint64_t)a.M, planes_snap, KB))
@@ -628,6 +637,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     t.r = a.r;
     t.tiles_per_head = (int)((a.N + 127) / 128);
     t.ntiles = t.tiles_per_head * a.BH;
+    t.k_rotated = a.k_rot != nullptr;
     t.tile_ctr = a.tile_ctr;
     t.n_ranges = a.n_ranges < AttnArgs::MAX_RANGES ? a.n_ranges : AttnArgs::MAX_RANGES;
     for (int r = 0; r < AttnArgs::MAX_RANGES; ++r) {

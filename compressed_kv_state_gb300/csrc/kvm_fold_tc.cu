@@ -281,8 +281,6 @@ __global__ void __launch_bounds__(NT, 1)
     const int bh = blockIdx.x;
     const int C = a.C, S = a.S, M = a.M;
 
-    float* g_sum_k = a.sum_k + (int64_t)bh * M * D;
-    float* g_sum_v = a.sum_v + (int64_t)bh * M * D;
     int* g_counts = a.counts + (int64_t)bh * M;
     float* g_rho = a.rho + (int64_t)bh * M;
     uint8_t* g_view_k = reinterpret_cast<uint8_t*>(a.view_k) + (int64_t)bh * M * ROWB;

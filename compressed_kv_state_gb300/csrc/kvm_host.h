@@ -19,7 +19,9 @@ constexpr size_t ALIGN = 256;
 // Byte offsets of every array inside a layer's workspace.
 struct Layout {
     size_t sum_k, sum_v, counts, rho, simdir, view_k, view_v;
-    size_t ring_k, ring_v, ring_g, ring_kr, snap_k, snap_v, rope, sched, status, total;
+    size_t ring_k, ring_v, ring_g, ring_kr, snap_k, snap_v, rope, sched, status;
+    size_t k_rot;  // keys rotated at their own positions (bf16 layers with rope_dims > 0; else empty)
+    size_t total;
 };
 
 extern thread_local std::string g_err;

@@ -116,6 +116,22 @@ struct AttnArgs {
     int n_ranges;
     int range_end[MAX_RANGES];
     int grid;           // CTAs to launch; 0 = two per SM of the device
+    // Tensor-core path: keys already rotated at their own positions (launch_rope_keys),
+    // read instead of k for the window; nullptr = rotate window keys in the kernel.
+    const void* k_rot;
+};
+
+// Keys rotated once at their own positions (rotate-half RoPE on dims [0, r)),
+// so that the attention need not rotate every window key for every tile that
+// sees it.  bf16 [BH, N, D] in and out.
+struct RopeKeysArgs {
+    const void* k;
+    void* k_rot;
+    const float2* rope;  // [max_tokens, r/2] (cos, sin)
+    int r;
+    int64_t N;
+    int BH;
+    int grid;            // CTAs to launch (a multiple of the SM count of the launch's partition)
 };
 
 struct DecodeArgs {
@@ -177,6 +193,7 @@ bool attn_tc_supported(const AttnArgs& a, bool bf16);
 cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_ring_fill(const RingFillArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_rope_keys(const RopeKeysArgs& a, cudaStream_t s);
 cudaError_t launch_renorm(const RenormArgs& a, bool bf16, cudaStream_t s);
 
 }  // namespace kvm

@@ -182,27 +182,41 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         fa.BH = BH;
         e = kvm::launch_fold(fa, bf16, s);
     }
-    if (e == cudaSuccess) {
-        kvm::AttnArgs aa{};
-        aa.q = q;
-        aa.k = k;
-        aa.v = v;
-        aa.out = out;
-        aa.N = n_tokens;
-        aa.C = c.chunk;
-        aa.W = c.window;
-        aa.snap_k = ws + L.snap_k;
-        aa.snap_v = ws + L.snap_v;
-        aa.snap_events = (int)E;
-        aa.M = c.max_slots;
-        aa.sched = reinterpret_cast<const kvm::Sched*>(ws + L.sched);
-        aa.rope = reinterpret_cast<const float2*>(ws + L.rope);
-        aa.r = c.rope_dims;
-        aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kvm::D));
-        aa.BH = BH;
-        aa.status = reinterpret_cast<int*>(ws + L.status);
-        e = kvm::launch_attn(aa, bf16, s);
+    kvm::AttnArgs aa{};
+    aa.q = q;
+    aa.k = k;
+    aa.v = v;
+    aa.out = out;
+    aa.N = n_tokens;
+    aa.C = c.chunk;
+    aa.W = c.window;
+    aa.snap_k = ws + L.snap_k;
+    aa.snap_v = ws + L.snap_v;
+    aa.snap_events = (int)E;
+    aa.M = c.max_slots;
+    aa.sched = reinterpret_cast<const kvm::Sched*>(ws + L.sched);
+    aa.rope = reinterpret_cast<const float2*>(ws + L.rope);
+    aa.r = c.rope_dims;
+    aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)kvm::D));
+    aa.BH = BH;
+    aa.status = reinterpret_cast<int*>(ws + L.status);
+    // tensor-core attention: keys rotated once, before it
+    if (e == cudaSuccess && bf16 && c.rope_dims > 0 && kvm::attn_tc_supported(aa, bf16)) {
+        int dev = 0, nsm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        kvm::RopeKeysArgs ka{};
+        ka.k = k;
+        ka.k_rot = ws + L.k_rot;
+        ka.rope = aa.rope;
+        ka.r = c.rope_dims;
+        ka.N = n_tokens;
+        ka.BH = BH;
+        ka.grid = 8 * (nsm > 0 ? nsm : 1);
+        e = kvm::launch_rope_keys(ka, s);
+        aa.k_rot = ka.k_rot;
     }
+    if (e == cudaSuccess) e = kvm::launch_attn(aa, bf16, s);
     if (e != cudaSuccess) {
         g_err = std::string("kvm_prefill_noalloc: ") + cudaGetErrorString(e);
         return KVM_ERR_CUDA;
