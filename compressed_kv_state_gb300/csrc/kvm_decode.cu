@@ -132,27 +132,24 @@ __global__ void __launch_bounds__(DEC_THREADS, 3) decode_kernel(DecodeArgs a) {
         const int b = it & 1;
         const int cnt = min(TK, end - k0);
         if (lane == 0 && k0 + TK < end) issue(k0 + TK, min(end, k0 + 2 * TK), b ^ 1);
-        // wait for this tile: lane 0 polls (bounded: a copy that never lands latches a
-        // timeout), the warp barrier orders the other lanes' reads after its acquire
+        // wait for this tile: every lane waits on the stage's barrier (try_wait suspends
+        // the warp in hardware; bounded: a copy that never lands latches a timeout)
         {
-            uint32_t ok = 1;
-            if (lane == 0) {
-                const uint32_t bar = dsmem_u32(&bars[warp][b]);
-                const uint32_t par = (it >> 1) & 1;
-                long long t0 = -1;
-                for (;;) {
-                    asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
-                                 : "=r"(ok) : "r"(bar), "r"(par) : "memory");
-                    if (ok) break;
-                    if (t0 < 0) t0 = clock64();
-                    if (clock64() - t0 > (1ll << 32)) {
-                        if (a.status) atomicOr(a.status, STATUS_TIMEOUT);
-                        break;
-                    }
+            const uint32_t bar = dsmem_u32(&bars[warp][b]);
+            const uint32_t par = (it >> 1) & 1;
+            uint32_t ok = 0;
+            long long t0 = -1;
+            for (;;) {
+                asm volatile("{\n\t.reg .pred q;\n\tmbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\tselp.u32 %0, 1, 0, q;\n\t}\n"
+                             : "=r"(ok) : "r"(bar), "r"(par) : "memory");
+                if (ok) break;
+                if (t0 < 0) t0 = clock64();
+                if (clock64() - t0 > (1ll << 32)) {
+                    if (lane == 0 && a.status) atomicOr(a.status, STATUS_TIMEOUT);
+                    break;
                 }
             }
-            __syncwarp();
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            if (!__all_sync(0xffffffffu, ok)) break;
         }
         const T* kt = reinterpret_cast<const T*>(stage + b * 2 * TILE);
         const T* vt = reinterpret_cast<const T*>(stage + b * 2 * TILE + TILE);
@@ -182,13 +179,23 @@ __global__ void __launch_bounds__(DEC_THREADS, 3) decode_kernel(DecodeArgs a) {
         acc0 *= corr;
         acc1 *= corr;
         m = mnew;
+        if (cnt == TK) {
 #pragma unroll
-        for (int j = 0; j < TK; ++j) {
-            const float pk = __shfl_sync(0xffffffffu, pj, j);  // 0 past the tile's keys
-            if (j < cnt) {
+            for (int j = 0; j < TK; ++j) {
+                const float pk = __shfl_sync(0xffffffffu, pj, j);
                 const float2 vx = ld2s<T>(vt + j * D + 2 * lane);
                 acc0 = fmaf(pk, vx.x, acc0);
                 acc1 = fmaf(pk, vx.y, acc1);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < TK; ++j) {
+                const float pk = __shfl_sync(0xffffffffu, pj, j);  // 0 past the tile's keys
+                if (j < cnt) {
+                    const float2 vx = ld2s<T>(vt + j * D + 2 * lane);
+                    acc0 = fmaf(pk, vx.x, acc0);
+                    acc1 = fmaf(pk, vx.y, acc1);
+                }
             }
         }
         __syncwarp();
