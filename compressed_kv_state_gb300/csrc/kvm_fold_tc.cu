@@ -397,14 +397,14 @@ __global__ void __launch_bounds__(NT, 1)
         const int buf = it & 1;
         const Sched sc = sc_nx;
         const float g_here = g_nx;
-        if (tid == 0 && !mbar_wait(smem_u32(&X.bar_k[buf]), (it >> 1) & 1, &X.abort_flag, a.status))
-            X.abort_flag = 1;
+        // every thread waits for the chunk itself (nothing of the previous event is
+        // read after its last barrier, so the set-up below needs no barrier first);
+        // a failed wait is carried to the next barrier, which all threads leave together
+        bool fail = !mbar_wait(smem_u32(&X.bar_k[buf]), (it >> 1) & 1, &X.abort_flag, a.status);
         if (e + 1 < a.e_end) {
             sc_nx = a.sched ? a.sched[e + 1] : a.sched0;
             if (tid < C) g_nx = a.g_src[(int64_t)bh * a.src_row + ((int64_t)(e + 1) * C) % a.src_len + tid];
         }
-        __syncthreads();
-        if (X.abort_flag) break;
         KVM_PROBE_LAP(0)
 #ifdef KVM_PROBE
         probe_acc[8] += 1;
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(NT, 1)
         const bool do_mma = n0 > S;
 
         // similarity of the chunk's keys to every slot direction
-        if (tid == 0) {
+        if (tid == 0 && !fail) {
             if (do_mma) {
                 tc_fence_after();
                 for (int ks = 0; ks < 4; ++ks)
@@ -447,15 +447,12 @@ __global__ void __launch_bounds__(NT, 1)
         }
         X.hist[tid >> 8][j] = 0;
         X.hist[2 + (tid >> 8)][j] = 0;
-        __syncthreads();
         KVM_PROBE_LAP(1)
 
         // best / second / argmax over the mergeable slots [S, n0): each quarter of
         // the CTA scans 64 slot columns of every token row (token = TMEM lane)
         if (do_mma) {
-            if (tid == 0 && !mbar_wait(bar_s, mma_count & 1, &X.abort_flag, a.status)) X.abort_flag = 1;
-            __syncthreads();
-            if (X.abort_flag) break;
+            fail = fail || !mbar_wait(bar_s, mma_count & 1, &X.abort_flag, a.status);
             KVM_PROBE_LAP(9)
             ++mma_count;
             tc_fence_after();
@@ -463,7 +460,7 @@ __global__ void __launch_bounds__(NT, 1)
             const int lo = max(S, q * 64), hi = min(n0, q * 64 + 64);
             float b0 = -INFINITY, s0 = -INFINITY, b1 = -INFINITY, s1 = -INFINITY;
             int a0 = -1, a1 = -1;
-            if (lo < hi) {
+            if (lo < hi && !__any_sync(0xffffffffu, fail)) {
                 uint32_t va[32], vb[32];
                 tmem_ld32(t_sim + q * 64, va);
                 tmem_ld32(t_sim + q * 64 + 32, vb);
@@ -478,8 +475,8 @@ __global__ void __launch_bounds__(NT, 1)
             X.ps[q][t] = s0;
             X.pa[q][t] = a0;
             tc_fence_before();
-            __syncthreads();
         }
+        if (__syncthreads_or(fail)) break;
         KVM_PROBE_LAP(2)
         float best = -INFINITY, sec = -INFINITY;
         int barg = -1;
@@ -490,7 +487,11 @@ __global__ void __launch_bounds__(NT, 1)
         }
         const float kn = tid < C ? X.kn[tid] : 0.0f;
         if (cand) X.m[tid] = barg < 0 ? -INFINITY : (kn > 0.0f ? best / kn : 0.0f);
-        __syncthreads();
+        // events that append slots or found sinks exchange per-token results; the
+        // others (every token merges) touch only their own token's entries until
+        // the merge lists below
+        const bool slow = na > 0 || first_pos < S;
+        if (slow) __syncthreads();
 
         // surprise selection: the a lowest scores (ties to the lower position) are appended
         if (na > 0) {
@@ -515,9 +516,11 @@ __global__ void __launch_bounds__(NT, 1)
         } else if (cand) {
             X.kind[tid] = 0;
         }
-        __syncthreads();
-        if (tid < C && X.kind[tid] != 0) X.slot_tok[X.slot[tid]] = tid;
-        __syncthreads();
+        if (slow) {
+            __syncthreads();
+            if (tid < C && X.kind[tid] != 0) X.slot_tok[X.slot[tid]] = tid;
+            __syncthreads();
+        }
         KVM_PROBE_LAP(3)
 
         if (na > 0) {
@@ -599,7 +602,6 @@ __global__ void __launch_bounds__(NT, 1)
                 a.dbg_gap[o] = gp;
             }
         }
-        __syncthreads();
 
         KVM_PROBE_LAP(4)
         // merge lists: merged tokens grouped by slot, position order inside a slot.
@@ -617,14 +619,15 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         if (merged)
             for (int w = 0; w < warp; ++w) rank_in_slot += X.hist[w][sj];
-        if (!vside) X.cnt_new[j] = X.hist[0][j] + X.hist[1][j] + X.hist[2][j] + X.hist[3][j];
-        __syncthreads();
         if (warp == 0) {
+            // merged tokens per slot, then their exclusive scan (list offsets)
             const int lane = tid & 31;
             int v8[8], sacc = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                v8[i] = X.cnt_new[lane * 8 + i];
+                const int jj = lane * 8 + i;
+                v8[i] = X.hist[0][jj] + X.hist[1][jj] + X.hist[2][jj] + X.hist[3][jj];
+                X.cnt_new[jj] = v8[i];
                 sacc += v8[i];
             }
             int incl = sacc;
