@@ -83,6 +83,7 @@ bool validate(const kvm_config* c, std::string& why) {
     if (!(c->ln_eps > 0.0f)) { why = "ln_eps must be > 0"; return false; }
     if (c->dtype != KVM_BF16 && c->dtype != KVM_FP32) { why = "unknown dtype"; return false; }
     if (c->max_tokens < 1 || c->max_tokens > (1 << 22)) { why = "max_tokens must be in [1, 2^22]"; return false; }
+    if (c->flags & ~KVM_FLAG_NO_VALUE_NORM) { why = "unknown flags"; return false; }
     return true;
 }
 
@@ -314,6 +315,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     fa.S = c.n_sinks;
     fa.r = c.rope_dims;
     fa.ln_eps = c.ln_eps;
+    fa.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
     fa.k_src = k;
     fa.v_src = v;
     fa.g_src = gate;
@@ -525,6 +527,8 @@ kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const vo
         fa.S = c.n_sinks;
         fa.r = c.rope_dims;
         fa.ln_eps = c.ln_eps;
+        fa.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
+    fa.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
         fa.k_src = ly->ws + L.ring_k;
         fa.v_src = ly->ws + L.ring_v;
         fa.g_src = ly->at<float>(L.ring_g);
@@ -637,6 +641,7 @@ kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda
     ra.n = (int)src->n_slots;
     ra.r = c.rope_dims;
     ra.ln_eps = c.ln_eps;
+    ra.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
     ra.BH = c.batch * c.heads;
     cudaError_t e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_renorm(ra, c.dtype == KVM_BF16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "renormalise launch");

@@ -26,7 +26,8 @@ constexpr int UTILE = 32;  // slot directions staged per shared-memory tile
 // Recompute the read view and the similarity direction of slot j (one warp).
 template <typename T>
 __device__ __forceinline__ void renorm_slot(const float* sk, const float* sv, int cnt, float rho,
-                                            float* sd, T* vk, T* vv, int r, float eps, int lane) {
+                                            float* sd, T* vk, T* vv, int r, float eps, int lane,
+                                            int no_vnorm) {
     float s0 = sk[lane], s1 = sk[lane + 32];
     // similarity direction: unit(s - mean(s)); the cosine against LayerNorm(s / count)
     // equals the cosine against this (LayerNorm centres and scales only)
@@ -45,10 +46,10 @@ __device__ __forceinline__ void renorm_slot(const float* sk, const float* sv, in
     float rs = 1.0f / sqrtf(var + eps);
     vk[lane] = from_f<T>(lane < r ? 0.0f : d0 * rs);
     vk[lane + 32] = from_f<T>(lane + 32 < r ? 0.0f : d1 * rs);
-    // read value: rho * unit(sum_v)
+    // read value: rho * unit(sum_v) (ablation: the member mean sum_v / count)
     float v0 = sv[lane], v1 = sv[lane + 32];
     float nv = sqrtf(warp_sum(v0 * v0 + v1 * v1));
-    float f = nv > 0.0f ? rho / nv : 0.0f;
+    float f = no_vnorm ? ic : (nv > 0.0f ? rho / nv : 0.0f);
     vv[lane] = from_f<T>(v0 * f);
     vv[lane + 32] = from_f<T>(v1 * f);
 }
@@ -326,7 +327,7 @@ __global__ void __launch_bounds__(FOLD_THREADS, 1) fold_chain_kernel(FoldArgs a)
             const int j = touched[i];
             renorm_slot<T>(sum_k + (int64_t)j * D, sum_v + (int64_t)j * D, counts[j], rho[j],
                            simdir + (int64_t)j * D, view_k + (int64_t)j * D,
-                           view_v + (int64_t)j * D, a.r, a.ln_eps, lane);
+                           view_v + (int64_t)j * D, a.r, a.ln_eps, lane, a.no_vnorm);
         }
         __syncthreads();
 
@@ -358,7 +359,7 @@ __global__ void renorm_all_kernel(RenormArgs a) {
     const int64_t row = bh * a.M + j;
     renorm_slot<T>(a.sum_k + row * D, a.sum_v + row * D, a.counts[row], a.rho[row],
                    a.simdir + row * D, reinterpret_cast<T*>(a.view_k) + row * D,
-                   reinterpret_cast<T*>(a.view_v) + row * D, a.r, a.ln_eps, lane);
+                   reinterpret_cast<T*>(a.view_v) + row * D, a.r, a.ln_eps, lane, a.no_vnorm);
 }
 
 static size_t fold_smem_bytes(int C) {

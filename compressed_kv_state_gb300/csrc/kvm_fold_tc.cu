@@ -51,6 +51,7 @@ struct Misc {
     int hist[4][MAXS];  // merged tokens per slot, per token warp
     int cnt[MAXS];      // written by key owners
     float rho[MAXS];    // written by value owners
+    int cntv[MAXS];     // value owners' copy of the counts (read value of the no-norm ablation)
     int cnt_new[MAXS];
     int seg[MAXS + 1];
     int slot_tok[MAXS];
@@ -191,10 +192,11 @@ __device__ __forceinline__ void key_view_inplace(int j, float (&c)[64], int cnt,
     }
 }
 
-// Value owner's read view of slot j: rho * unit(sum_v).
+// Value owner's read view of slot j: rho * unit(sum_v) (with the no-norm
+// ablation, the member mean sum_v / count: rho < 0 carries -1 / count).
 __device__ __forceinline__ void value_view(int j, const float (&sv)[64], float rho, uint8_t* sm) {
     const float nv = sqrtf(dot64(sv, sv));
-    const float f = nv > 0.0f ? rho / nv : 0.0f;
+    const float f = rho < 0.0f ? -rho : (nv > 0.0f ? rho / nv : 0.0f);
     uint4* vv = reinterpret_cast<uint4*>(sm + OFF_VV + j * ROWB);
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
@@ -314,6 +316,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (!vside) {
         X.cnt[j] = 0;
         X.rho[j] = 0.0f;
+        X.cntv[j] = 0;
     }
     tc_fence_before();
     __syncthreads();
@@ -353,8 +356,10 @@ __global__ void __launch_bounds__(NT, 1)
                 key_view_inplace(j, x, cnt, a.r, a.ln_eps, sm);
             } else {
                 const float rho = g_rho[j];
+                const int cnt = g_counts[j];
                 X.rho[j] = rho;
-                value_view(j, x, rho, sm);
+                X.cntv[j] = cnt;
+                value_view(j, x, a.no_vnorm ? -1.0f / (float)cnt : rho, sm);
             }
         } else {
             // slots not founded yet: zero direction (S = 0) and zero read view
@@ -666,7 +671,10 @@ __global__ void __launch_bounds__(NT, 1)
                 float rho = 0.0f;
                 if (touched) {
                     if (!vside) cnt = X.cnt[j];
-                    else rho = X.rho[j];
+                    else {
+                        rho = X.rho[j];
+                        cnt = X.cntv[j];
+                    }
                     if (ft >= 0) {
                         set_row_sw(rows, ft, X.g[ft], x);
                         cnt = 0;
@@ -687,7 +695,8 @@ __global__ void __launch_bounds__(NT, 1)
                         key_view_inplace(j, x, cnt, a.r, a.ln_eps, sm);
                     } else {
                         X.rho[j] = rho;
-                        value_view(j, x, rho, sm);
+                        X.cntv[j] = cnt;
+                        value_view(j, x, a.no_vnorm ? -1.0f / (float)cnt : rho, sm);
                     }
                 }
             }

@@ -62,6 +62,7 @@ struct FoldArgs {
     void* view_v;
     int M, C, S, r;
     float ln_eps;
+    int no_vnorm;  // ablation: read value = sum_v / count instead of rho * unit(sum_v)
     // tokens: row bh, token i of event e sits at src + bh*src_row + ((e*C) % src_len + i)
     const void* k_src;
     const void* v_src;
@@ -181,6 +182,7 @@ struct RenormArgs {
     void* view_v;
     int M, n, r;
     float ln_eps;
+    int no_vnorm;  // ablation: read value = sum_v / count
     int BH;
 };
 

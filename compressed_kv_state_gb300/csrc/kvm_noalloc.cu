@@ -167,6 +167,7 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         fa.S = c.n_sinks;
         fa.r = c.rope_dims;
         fa.ln_eps = c.ln_eps;
+        fa.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
         fa.k_src = k;
         fa.v_src = v;
         fa.g_src = gate;

@@ -17,6 +17,7 @@ KVM_OK, KVM_ERR_INVALID_ARG, KVM_ERR_UNSUPPORTED, KVM_ERR_CAPACITY = 0, 1, 2, 3
 KVM_ERR_WORKSPACE, KVM_ERR_CUDA, KVM_ERR_TIMEOUT, KVM_ERR_DEVICE = 4, 5, 6, 7
 KVM_BF16, KVM_FP32 = 0, 1
 KVM_SCHED_FIXED, KVM_SCHED_POWER = 0, 1
+KVM_FLAG_NO_VALUE_NORM = 1
 STATUS_NAMES = {0: "KVM_OK", 1: "KVM_ERR_INVALID_ARG", 2: "KVM_ERR_UNSUPPORTED",
                 3: "KVM_ERR_CAPACITY", 4: "KVM_ERR_WORKSPACE", 5: "KVM_ERR_CUDA",
                 6: "KVM_ERR_TIMEOUT", 7: "KVM_ERR_DEVICE"}
@@ -30,7 +31,7 @@ class kvm_config(ctypes.Structure):
                 ("sched", ctypes.c_int32), ("max_slots", ctypes.c_int32),
                 ("coef", ctypes.c_float), ("expo", ctypes.c_float),
                 ("ln_eps", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("max_tokens", ctypes.c_int32)]
+                ("max_tokens", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class kvm_state_bufs(ctypes.Structure):
@@ -201,9 +202,9 @@ def kvm_layer_destroy(layer):
 
 def make_config(*, batch, heads, head_dim=64, rope_dims=32, rope_theta=10000.0, chunk=128,
                 window=512, n_sinks=16, sched=KVM_SCHED_FIXED, max_slots=256, coef=4.0, expo=0.5,
-                ln_eps=1e-5, dtype=KVM_BF16, max_tokens=8192) -> kvm_config:
+                ln_eps=1e-5, dtype=KVM_BF16, max_tokens=8192, flags=0) -> kvm_config:
     return kvm_config(batch, heads, head_dim, rope_dims, rope_theta, chunk, window, n_sinks, sched,
-                      max_slots, coef, expo, ln_eps, dtype, max_tokens)
+                      max_slots, coef, expo, ln_eps, dtype, max_tokens, flags)
 
 
 class KvmLayer:

@@ -65,6 +65,14 @@ typedef enum { KVM_BF16 = 0, KVM_FP32 = 1 } kvm_dtype;
  * (the "sqrt" state is expo = 0.5, coef = 4).  Capacities count sink slots. */
 typedef enum { KVM_SCHED_FIXED = 0, KVM_SCHED_POWER = 1 } kvm_sched;
 
+/* Ablation switches ("Key-Value Means", technical summary, Experimental
+ * results, ablation studies: removing the value-length normalisation, the sink
+ * protection or the merge gate).  KVM_FLAG_NO_VALUE_NORM: the state's read
+ * value is the mean of its gate-weighted members, sum_v / count, instead of
+ * rho * unit(sum_v).  No sink protection is n_sinks = 0 (every overflowed token
+ * is an ordinary merge or append candidate); no merge gate is a gate of ones. */
+#define KVM_FLAG_NO_VALUE_NORM 1
+
 typedef struct {
     int32_t batch;       /* B >= 1 */
     int32_t heads;       /* H >= 1; one state per (batch, head) */
@@ -80,6 +88,7 @@ typedef struct {
     float ln_eps;        /* LayerNorm epsilon for the state keys, e.g. 1e-5 */
     int32_t dtype;       /* kvm_dtype of q, k, v, out and the window ring */
     int32_t max_tokens;  /* longest sequence the layer will see (prefill + decode) */
+    int32_t flags;       /* KVM_FLAG_* ablation switches; 0 = the method as described */
 } kvm_config;
 
 typedef struct kvm_layer kvm_layer;

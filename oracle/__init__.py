@@ -46,7 +46,7 @@ class _Cfg(ctypes.Structure):
         ("sched", ctypes.c_int32), ("max_slots", ctypes.c_int32),
         ("coef", ctypes.c_double), ("expo", ctypes.c_double),
         ("ln_eps", ctypes.c_double), ("merge_pre_append", ctypes.c_int32),
-        ("cos_nope_only", ctypes.c_int32),
+        ("cos_nope_only", ctypes.c_int32), ("no_value_norm", ctypes.c_int32),
     ]
 
 
@@ -67,11 +67,12 @@ class OracleConfig:
     ln_eps: float = 1e-5
     merge_pre_append: int = 0
     cos_nope_only: int = 0
+    no_value_norm: int = 0    # ablation: read value = sum_v / count
 
     def c(self) -> _Cfg:
         return _Cfg(self.head_dim, self.rope_dims, self.rope_theta, self.chunk, self.window,
                     self.n_sinks, self.sched, self.max_slots, self.coef, self.expo,
-                    self.ln_eps, self.merge_pre_append, self.cos_nope_only)
+                    self.ln_eps, self.merge_pre_append, self.cos_nope_only, self.no_value_norm)
 
 
 _lib = None

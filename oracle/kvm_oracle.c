@@ -59,6 +59,7 @@ typedef struct {
     double ln_eps;         /* LayerNorm epsilon */
     int32_t merge_pre_append;  /* alternative reading: merge targets = pre-append slots only */
     int32_t cos_nope_only;     /* alternative reading: cosine over dims [r, d) only */
+    int32_t no_value_norm;     /* ablation: read value = sum_v / count (no value-length norm) */
 } kvo_config;
 
 enum { KVO_MERGED = 0, KVO_APPENDED = 1, KVO_SINK = 2 };
@@ -294,7 +295,9 @@ int kvo_fold_event(const kvo_config* cfg, int64_t* n_slots, int64_t* t,
 /*
  * Just-in-time read view of n slots (KVM summary, Core mechanisms 2 and 4):
  * key_view = LayerNorm(sum_k / count) with dims [0, r) set to zero;
- * val_view = rho * sum_v / ||sum_v||  (zero when sum_v is zero).
+ * val_view = rho * sum_v / ||sum_v||  (zero when sum_v is zero);
+ * with the value-length normalisation removed (the pages' ablation, technical
+ * summary, Experimental results), val_view = sum_v / count.
  */
 void kvo_state_view(const kvo_config* cfg, int64_t n, const double* sum_k, const double* sum_v,
                     const int64_t* count, const double* rho, double* key_view, double* val_view) {
@@ -303,8 +306,12 @@ void kvo_state_view(const kvo_config* cfg, int64_t n, const double* sum_k, const
         state_key_full(cfg, sum_k, count, j, key_view + j * d);
         for (int x = 0; x < r; ++x) key_view[j * d + x] = 0.0;
         double nv = norm2(sum_v + j * d, d);
-        for (int x = 0; x < d; ++x)
-            val_view[j * d + x] = nv == 0.0 ? 0.0 : rho[j] * sum_v[j * d + x] / nv;
+        for (int x = 0; x < d; ++x) {
+            if (cfg->no_value_norm)
+                val_view[j * d + x] = sum_v[j * d + x] / (double)count[j];
+            else
+                val_view[j * d + x] = nv == 0.0 ? 0.0 : rho[j] * sum_v[j * d + x] / nv;
+        }
     }
 }
 

@@ -21,7 +21,8 @@ TOL_FP32 = 1e-4
 def oracle_cfg(w) -> oracle.OracleConfig:
     return oracle.OracleConfig(head_dim=w.d, rope_dims=w.rope_dims, rope_theta=w.rope_theta,
                                chunk=w.chunk, window=w.window, n_sinks=w.n_sinks, sched=w.sched,
-                               max_slots=w.max_slots, coef=w.coef, expo=w.expo, ln_eps=w.ln_eps)
+                               max_slots=w.max_slots, coef=w.coef, expo=w.expo, ln_eps=w.ln_eps,
+                               no_value_norm=int(w.flags & 1))
 
 
 def tol_of(w) -> float:
@@ -35,7 +36,7 @@ def make_layer(w, max_tokens=None):
                           n_sinks=w.n_sinks, sched=w.sched, max_slots=w.max_slots, coef=w.coef,
                           expo=w.expo, ln_eps=w.ln_eps,
                           dtype=kvm.KVM_BF16 if w.dtype == "bf16" else kvm.KVM_FP32,
-                          max_tokens=max_tokens or max(w.N, 1))
+                          max_tokens=max_tokens or max(w.N, 1), flags=w.flags)
     return kvm.KvmLayer(cfg)
 
 

@@ -42,8 +42,8 @@ def test_headers_cover_the_boundary():
 
 
 def test_struct_sizes_match_header(kvm):
-    # 15 four-byte fields, no padding
-    assert ctypes.sizeof(kvm.kvm_config) == 60
+    # 16 four-byte fields, no padding
+    assert ctypes.sizeof(kvm.kvm_config) == 64
     assert ctypes.sizeof(kvm.kvm_state_bufs) == 7 * 8 + 3 * 8
     assert ctypes.sizeof(kvm.kvm_debug) == 5 * 8 + 8  # + int32 test hook, padded
 
@@ -60,6 +60,7 @@ def test_struct_sizes_match_header(kvm):
     ("sched", 5, "schedule"),
     ("batch", 0, "batch"),
     ("max_tokens", 0, "max_tokens"),
+    ("flags", 2, "flags"),
 ])
 def test_invalid_configs_rejected(kvm, field, value, msg):
     cfg = kvm.make_config(batch=1, heads=2)

@@ -43,6 +43,21 @@ SMALL = [
                        n_sinks=16, sched=1, dtype="fp32", keys="neardup20")),
     wl.Workload("fixed_C128_ragged", B=1, H=2, N=1337, chunk=128, window=256, n_sinks=16,
                 max_slots=64, keys="repeat5"),
+    # other power-law growth schedules (exponent 0.75, coefficient 1; exponent 0.25)
+    _sized(wl.Workload("pow075_B1H3N2000_C128W256", B=1, H=3, N=2000, chunk=128, window=256,
+                       n_sinks=16, sched=1, coef=1.0, expo=0.75, keys="repeat5")),
+    _sized(wl.Workload("pow025_fp32_B1H2N900_C32W64", B=1, H=2, N=900, chunk=32, window=64,
+                       n_sinks=4, sched=1, coef=8.0, expo=0.25, dtype="fp32", keys="needles10")),
+    # the pages' ablations: no value-length normalisation (on-chip and portable chains),
+    # no sink protection, no merge gate
+    wl.Workload("ablate_novnorm_B2H2N3000_C128W256", B=2, H=2, N=3000, chunk=128, window=256,
+                n_sinks=16, max_slots=128, keys="repeat5", flags=1),
+    _sized(wl.Workload("ablate_novnorm_fp32_B1H2N1500_C64W128", B=1, H=2, N=1500, chunk=64,
+                       window=128, n_sinks=8, sched=1, dtype="fp32", keys="neardup20", flags=1)),
+    wl.Workload("ablate_nosinks_B1H3N2500_C128W256", B=1, H=3, N=2500, chunk=128, window=256,
+                n_sinks=0, max_slots=96, keys="repeat5"),
+    wl.Workload("ablate_nogate_B1H3N2500_C128W256", B=1, H=3, N=2500, chunk=128, window=256,
+                n_sinks=16, max_slots=96, keys="repeat5", gate="ones"),
 ]
 
 
@@ -202,6 +217,8 @@ def _decode_from_prefill(w, N0, steps):
                  dtype="fp32"), 100, 140),
     (wl.Workload("dec_from_start", B=1, H=2, N=0, chunk=16, window=32, n_sinks=16, max_slots=30),
      0, 120),
+    (wl.Workload("dec_novnorm", B=1, H=2, N=0, chunk=64, window=128, n_sinks=8, max_slots=40,
+                 keys="repeat5", flags=1), 300, 150),
 ])
 def test_decode_matches_prefill_and_oracle(w, N0, steps):
     """Decoding token by token equals the last rows of one longer prefill

@@ -105,14 +105,15 @@ def test_every_token_appended_closed_form(N, C, W, S):
 
 # ---------------------------------------------------------------- invariants
 
-def _random_run(seed=5, N=600, sched=1, M=64, C=16, W=32, S=4, d=16, r=8, dup=0.3):
+def _random_run(seed=5, N=600, sched=1, M=64, C=16, W=32, S=4, d=16, r=8, dup=0.3, coef=2.0,
+                expo=0.5):
     rng = np.random.default_rng(seed)
     q, k, v, g = _inputs(seed, N, d)
     for t in range(1, N):               # some near-duplicate keys so merges happen
         if rng.random() < dup:
             k[t] = k[rng.integers(0, t)] + 0.1 * rng.standard_normal(d)
     cfg = oracle.OracleConfig(head_dim=d, rope_dims=r, chunk=C, window=W, n_sinks=S,
-                              sched=sched, max_slots=M, coef=2.0, expo=0.5)
+                              sched=sched, max_slots=M, coef=coef, expo=expo)
     return cfg, (q, k, v, g), _run(cfg, q, k, v, g)
 
 
@@ -136,13 +137,17 @@ def test_read_radius_preserved(sched, M):
     assert (kv[:, :cfg.rope_dims] == 0).all()
 
 
-@pytest.mark.parametrize("sched,M", [(0, 24), (1, 64)])
-def test_counts_sums_and_growth(sched, M):
+@pytest.mark.parametrize("sched,M,coef,expo", [(0, 24, 2.0, 0.5), (1, 64, 2.0, 0.5),
+                                                (1, 128, 1.0, 0.75), (1, 80, 8.0, 0.25),
+                                                (1, 200, 0.3, 1.0)])
+def test_counts_sums_and_growth(sched, M, coef, expo):
     """Counts sum to the number of overflowed tokens; the slot count follows
     the schedule: after each fold n = min(cap(t), n_before + candidates) and
     never exceeds cap(t); sums equal the gate-weighted sum of their members
-    (KVM summary, Core mechanisms 2 and 3; lay part 'smart merge')."""
-    cfg, (q, k, v, g), (_, st, dbg) = _random_run(sched=sched, M=M)
+    (KVM summary, Core mechanisms 2 and 3; lay part 'smart merge').  Power-law
+    growth with other exponents and coefficients than the sqrt schedule
+    (Core mechanism 3 names power-law growth in general)."""
+    cfg, (q, k, v, g), (_, st, dbg) = _random_run(sched=sched, M=M, coef=coef, expo=expo)
     E = dbg["assign"].shape[0]
     C, S = cfg.chunk, cfg.n_sinks
     assert st.t == E * C
@@ -172,6 +177,53 @@ def test_counts_sums_and_growth(sched, M):
     np.testing.assert_array_equal(cnt, st.count)
     np.testing.assert_allclose(st.sum_k, members_k, atol=1e-12)
     np.testing.assert_allclose(st.sum_v, members_v, atol=1e-12)
+
+
+@pytest.mark.parametrize("coef,expo", [(4.0, 0.5), (1.0, 0.75), (8.0, 0.25), (0.3, 1.0), (2.5, 0.6)])
+def test_power_law_capacity_closed_form(coef, expo):
+    """cap(t) = S + ceil(coef * t^expo) for t > 0 and S at t = 0 (power-law
+    growth, KVM summary Core mechanism 3), checked against exact rational
+    arithmetic where t^expo is rational, else against math.pow."""
+    import fractions
+    import math
+    S = 16
+    cfg = oracle.OracleConfig(n_sinks=S, sched=1, max_slots=10**6, coef=coef, expo=expo)
+    assert oracle.capacity(cfg, 0) == S
+    for t in (1, 2, 3, 16, 100, 127, 128, 1000, 7552, 64256):
+        want = S + math.ceil(coef * math.pow(t, expo))
+        if expo == 1.0:
+            want = S + math.ceil(fractions.Fraction(coef) * t)
+        assert oracle.capacity(cfg, t) == want, (t, oracle.capacity(cfg, t), want)
+    # monotone in t
+    caps = [oracle.capacity(cfg, t) for t in range(0, 3000, 7)]
+    assert all(b >= a for a, b in zip(caps, caps[1:]))
+
+
+@pytest.mark.parametrize("sched,M", [(0, 24), (1, 64)])
+def test_no_value_norm_ablation_reads_member_means(sched, M):
+    """Ablation of the value-length normalisation (KVM summary, Experimental
+    results, ablation studies): the fold decisions and sums are unchanged, the
+    read value becomes sum_v / count (the gate-weighted member mean), the read
+    key is unchanged, and the outputs differ from the normalised read."""
+    cfg, (q, k, v, g), (out, st, dbg) = _random_run(sched=sched, M=M)
+    cfg_a = oracle.OracleConfig(**{**cfg.__dict__, "no_value_norm": 1})
+    out_a, st_a, dbg_a = _run(cfg_a, q, k, v, g)
+    np.testing.assert_array_equal(dbg_a["assign"], dbg["assign"])
+    np.testing.assert_array_equal(dbg_a["kind"], dbg["kind"])
+    np.testing.assert_array_equal(st_a.count, st.count)
+    np.testing.assert_array_equal(st_a.sum_v, st.sum_v)
+    kv, vv = oracle.state_view(cfg, st)
+    kv_a, vv_a = oracle.state_view(cfg_a, st_a)
+    np.testing.assert_array_equal(kv_a, kv)
+    n = st.n
+    np.testing.assert_allclose(vv_a, st.sum_v[:n] / st.count[:n, None], rtol=0, atol=1e-15)
+    # members of each slot, gate-weighted, averaged over the count
+    mem = np.zeros((M, cfg.head_dim))
+    for e in range(dbg["assign"].shape[0]):
+        for i in range(cfg.chunk):
+            mem[dbg["assign"][e, i]] += g[e * cfg.chunk + i] * v[e * cfg.chunk + i]
+    np.testing.assert_allclose(vv_a, mem[:n] / st.count[:n, None], atol=1e-12)
+    assert np.abs(out_a - out).max() > 1e-3
 
 
 def test_workload_slot_literals_match_schedule():
@@ -284,6 +336,7 @@ TINY = [
     dict(N=64, C=4, W=8, S=0, r=4, d=8, sched=0, M=6),
     dict(N=130, C=16, W=32, S=16, r=8, d=16, sched=1, M=64),
     dict(N=7, C=4, W=4, S=1, r=2, d=4, sched=0, M=3),
+    dict(N=120, C=8, W=16, S=2, r=4, d=8, sched=1, M=60, coef=1.0, expo=0.75),
     dict(N=200, C=8, W=24, S=4, r=8, d=16, sched=0, M=8),
 ]
 
@@ -299,12 +352,13 @@ def test_oracle_matches_bruteforce(case, seed):
     for t in range(1, c["N"]):
         if rng.random() < 0.25:
             k[t] = k[rng.integers(0, t)] + 0.2 * rng.standard_normal(c["d"])
+    coef, expo = c.get("coef", 2.0), c.get("expo", 0.5)
     cfg = oracle.OracleConfig(head_dim=c["d"], rope_dims=c["r"], chunk=c["C"], window=c["W"],
-                              n_sinks=c["S"], sched=c["sched"], max_slots=c["M"], coef=2.0,
-                              expo=0.5)
+                              n_sinks=c["S"], sched=c["sched"], max_slots=c["M"], coef=coef,
+                              expo=expo)
     out, st, dbg = _run(cfg, q, k, v, g)
     bout, bst, bev = bf_prefill(q, k, v, g, C=c["C"], W=c["W"], S=c["S"], r=c["r"],
-                                sched=c["sched"], M=c["M"], coef=2.0, expo=0.5)
+                                sched=c["sched"], M=c["M"], coef=coef, expo=expo)
     assert len(bev) == dbg["assign"].shape[0]
     for e, (a, kd) in enumerate(bev):
         np.testing.assert_array_equal(dbg["assign"][e], a)
