@@ -382,7 +382,20 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     ka.N = n_tokens;
     ka.BH = BH;
     const bool pre_rotate = bf16 && c.rope_dims > 0 && n_tokens > 0 && kvm::attn_tc_supported(aa, bf16);
-    if (pre_rotate) aa.k_rot = ka.k_rot;
+    if (pre_rotate) {
+        aa.k_rot = ka.k_rot;
+        // the window ring is filled in the same pass
+        if (ring_work) {
+            ka.v = v;
+            ka.g = gate;
+            ka.ring_k = ra.ring_k;
+            ka.ring_v = ra.ring_v;
+            ka.ring_g = ra.ring_g;
+            ka.ring_kr = ra.ring_kr;
+            ka.first = ra.first;
+            ka.L = ra.L;
+        }
+    }
 
     // overlapped prefill: fold segments on one SM partition, the attention of
     // the chunks each segment has made ready on the other
@@ -480,7 +493,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             ly->kernels += 1;
         }
     }
-    if (ring_work) {
+    if (ring_work && !pre_rotate) {
         e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_ring_fill(ra, bf16, s); });
         if (e != cudaSuccess) return ly->cuda_fail(e, "ring fill launch");
         ly->kernels += 1;

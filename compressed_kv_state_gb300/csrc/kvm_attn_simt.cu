@@ -177,60 +177,80 @@ __global__ void ring_fill_kernel(RingFillArgs a) {
 
 // One thread per 16-byte chunk (8 dims) of a key row: chunks inside the rotary
 // dims are rotated with their rotate-half partner chunk (vector path when r/2
-// is a multiple of 8, one dim at a time otherwise); the rest are copied.
+// is a multiple of 8, one dim at a time otherwise); the rest are copied.  Rows
+// (b, h) are strided over gridDim.y and chunks of a row over gridDim.x, so the
+// position of a chunk needs no division.
 __global__ void rope_keys_kernel(RopeKeysArgs a) {
     const int half = a.r / 2;
-    const int64_t total = (int64_t)a.BH * a.N * 8;
-    const uint4* src = reinterpret_cast<const uint4*>(a.k);
-    uint4* dst = reinterpret_cast<uint4*>(a.k_rot);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t row = i >> 3;
-        const int c = (int)(i & 7);
-        const int64_t p = row % a.N;
-        uint4 w = src[i];
-        if (8 * c < a.r) {
-            if ((half & 7) == 0) {
-                const int hc = half >> 3;
-                const bool low = c < hc;  // dims [0, half) pair with [half, r)
-                const uint4 o = src[row * 8 + (low ? c + hc : c - hc)];
-                const float4* tab = reinterpret_cast<const float4*>(a.rope + p * half + (low ? c : c - hc) * 8);
-                const float4 t[4] = {tab[0], tab[1], tab[2], tab[3]};
-                const float ce[8] = {t[0].x, t[0].z, t[1].x, t[1].z, t[2].x, t[2].z, t[3].x, t[3].z};
-                const float se[8] = {t[0].y, t[0].w, t[1].y, t[1].w, t[2].y, t[2].w, t[3].y, t[3].w};
-                __nv_bfloat162* m2 = reinterpret_cast<__nv_bfloat162*>(&w);
-                const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+    const int64_t per_row = a.N * 8;
+    for (int bh = blockIdx.y; bh < a.BH; bh += gridDim.y) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.k) + (int64_t)bh * per_row;
+        uint4* dst = reinterpret_cast<uint4*>(a.k_rot) + (int64_t)bh * per_row;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per_row;
+             i += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t p = i >> 3;
+            const int c = (int)(i & 7);
+            uint4 w = src[i];
+            const bool ring = a.ring_k && p >= a.first;
+            int64_t rrow = 0;
+            if (ring) {
+                const int64_t slot = p - (p / a.L) * a.L;
+                rrow = (int64_t)bh * a.L + slot;
+                reinterpret_cast<uint4*>(a.ring_k)[rrow * 8 + c] = w;
+                reinterpret_cast<uint4*>(a.ring_v)[rrow * 8 + c] =
+                    reinterpret_cast<const uint4*>(a.v)[(int64_t)bh * per_row + i];
+                if (c == 0) a.ring_g[rrow] = a.g[(int64_t)bh * a.N + p];
+            }
+            if (8 * c < a.r) {
+                if ((half & 7) == 0) {
+                    const int hc = half >> 3;
+                    const bool low = c < hc;  // dims [0, half) pair with [half, r)
+                    const uint4 o = src[p * 8 + (low ? c + hc : c - hc)];
+                    const float4* tab = reinterpret_cast<const float4*>(a.rope + p * half + (low ? c : c - hc) * 8);
+                    const float4 t[4] = {tab[0], tab[1], tab[2], tab[3]};
+                    const float ce[8] = {t[0].x, t[0].z, t[1].x, t[1].z, t[2].x, t[2].z, t[3].x, t[3].z};
+                    const float se[8] = {t[0].y, t[0].w, t[1].y, t[1].w, t[2].y, t[2].w, t[3].y, t[3].w};
+                    __nv_bfloat162* m2 = reinterpret_cast<__nv_bfloat162*>(&w);
+                    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 mv = __bfloat1622float2(m2[u]), ov = __bfloat1622float2(o2[u]);
-                    const float c0 = ce[2 * u], c1 = ce[2 * u + 1], s0 = se[2 * u], s1 = se[2 * u + 1];
-                    m2[u] = low ? __floats2bfloat162_rn(mv.x * c0 - ov.x * s0, mv.y * c1 - ov.y * s1)
-                                : __floats2bfloat162_rn(mv.x * c0 + ov.x * s0, mv.y * c1 + ov.y * s1);
-                }
-            } else {
-                const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(src + row * 8);
-                __nv_bfloat16* m = reinterpret_cast<__nv_bfloat16*>(&w);
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 mv = __bfloat1622float2(m2[u]), ov = __bfloat1622float2(o2[u]);
+                        const float c0 = ce[2 * u], c1 = ce[2 * u + 1], s0 = se[2 * u], s1 = se[2 * u + 1];
+                        m2[u] = low ? __floats2bfloat162_rn(mv.x * c0 - ov.x * s0, mv.y * c1 - ov.y * s1)
+                                    : __floats2bfloat162_rn(mv.x * c0 + ov.x * s0, mv.y * c1 + ov.y * s1);
+                    }
+                } else {
+                    const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(src + p * 8);
+                    __nv_bfloat16* m = reinterpret_cast<__nv_bfloat16*>(&w);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int x = 8 * c + e;
-                    if (x < 2 * half) {
-                        const int i2 = x < half ? x : x - half;
-                        const float2 cs = a.rope[p * half + i2];
-                        const float kv = __bfloat162float(krow[x]);
-                        const float r2 = x < half ? kv * cs.x - __bfloat162float(krow[x + half]) * cs.y
-                                                  : kv * cs.x + __bfloat162float(krow[x - half]) * cs.y;
-                        m[e] = __float2bfloat16_rn(r2);
+                    for (int e = 0; e < 8; ++e) {
+                        const int x = 8 * c + e;
+                        if (x < 2 * half) {
+                            const int i2 = x < half ? x : x - half;
+                            const float2 cs = a.rope[p * half + i2];
+                            const float kv = __bfloat162float(krow[x]);
+                            const float r2 = x < half ? kv * cs.x - __bfloat162float(krow[x + half]) * cs.y
+                                                      : kv * cs.x + __bfloat162float(krow[x - half]) * cs.y;
+                            m[e] = __float2bfloat16_rn(r2);
+                        }
                     }
                 }
             }
+            dst[i] = w;
+            if (ring) reinterpret_cast<uint4*>(a.ring_kr)[rrow * 8 + c] = w;
         }
-        dst[i] = w;
     }
 }
 
 cudaError_t launch_rope_keys(const RopeKeysArgs& a, cudaStream_t s) {
     if (a.N <= 0 || a.r <= 0) return cudaSuccess;
-    rope_keys_kernel<<<a.grid, 256, 0, s>>>(a);
+    // a.grid CTAs in total, spread over rows (y) and the chunks of a row (x)
+    const int gy = a.BH < 65535 ? a.BH : 65535;
+    int gx = a.grid / gy;
+    const int64_t need = (a.N * 8 + 255) / 256;
+    if (gx < 1) gx = 1;
+    if (gx > need) gx = (int)need;
+    rope_keys_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(a);
     return cudaGetLastError();
 }
 

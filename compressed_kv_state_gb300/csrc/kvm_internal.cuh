@@ -133,6 +133,17 @@ struct RopeKeysArgs {
     int64_t N;
     int BH;
     int grid;            // CTAs to launch (a multiple of the SM count of the launch's partition)
+    // optional window ring fill in the same pass (ring_k == nullptr: none): tokens
+    // [first, N) enter the ring at row position mod L with their unrotated key,
+    // value, gate and the rotated key (the same values as ring_fill_kernel writes)
+    const void* v;
+    const float* g;
+    void* ring_k;
+    void* ring_v;
+    float* ring_g;
+    void* ring_kr;
+    int64_t first;
+    int L;
 };
 
 struct DecodeArgs {
