@@ -489,7 +489,9 @@ __global__ void __launch_bounds__(256, 2)
                     }
                 l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
                 KVM_PROBE_LAP(4)
-                if (rescale) {
+                // tensor-memory loads and stores are warp-wide (.sync.aligned): the whole
+                // warp rescales when any of its rows must (the others scale by alpha = 1)
+                if (__any_sync(0xffffffffu, rescale)) {
                     // O holds blocks < j: wait for their last PV, then scale it in place
                     if (!mbar_wait(bar(B_PVDONE + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
@@ -592,6 +594,23 @@ bool make_tmap_bf16_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t
     if (!enc) return false;
     cuuint64_t dims[3] = {64, rows, planes};
     cuuint64_t strides[2] = {64 * 2, rows * 64 * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over [planes][rows][row_elems] with a 64 x box_rows box, 128-byte swizzle
+// (row_elems a multiple of 8: rows start on 16-byte boundaries).
+bool make_tmap_bf16_rows(CUtensorMap* m, const void* base, uint64_t row_elems, uint64_t rows, uint64_t planes,
+                         uint32_t box_rows) {
+    using namespace tc;
+    auto enc = get_encode();
+    if (!enc || row_elems % 8) return false;
+    cuuint64_t dims[3] = {row_elems, rows, planes};
+    cuuint64_t strides[2] = {row_elems * 2, rows * row_elems * 2};
     cuuint32_t box[3] = {64, box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,

@@ -58,6 +58,9 @@ SMALL = [
                 n_sinks=0, max_slots=96, keys="repeat5"),
     wl.Workload("ablate_nogate_B1H3N2500_C128W256", B=1, H=3, N=2500, chunk=128, window=256,
                 n_sinks=16, max_slots=96, keys="repeat5", gate="ones"),
+    # queries that spike on one key: a few rows of a warp rescale their output
+    wl.Workload("qspike_B2H2N3000_C128W512", B=2, H=2, N=3000, chunk=128, window=512,
+                n_sinks=16, max_slots=128, keys="qspike5"),
 ]
 
 
