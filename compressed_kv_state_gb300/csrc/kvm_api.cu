@@ -159,8 +159,8 @@ struct kvm_layer {
     bool timing = false;
     std::vector<Timed> pool;
     size_t used = 0;
-    double acc_ms[4] = {0, 0, 0, 0};
-    int64_t acc_n[4] = {0, 0, 0, 0};
+    double acc_ms[5] = {0, 0, 0, 0, 0};
+    int64_t acc_n[5] = {0, 0, 0, 0, 0};
     int64_t kernels = 0;
     // overlapped prefill (kvm_layer_set_overlap)
     int overlap_segs = -1;
@@ -187,7 +187,7 @@ struct kvm_layer {
     }
 };
 
-enum { PH_FOLD = 0, PH_ATTN = 1, PH_DECODE = 2, PH_OTHER = 3 };
+enum { PH_FOLD = 0, PH_ATTN = 1, PH_DECODE = 2, PH_OTHER = 3, PH_PROJ = 4 };
 
 // Launch through f(), bracketed by timing events on s when timing is on.
 template <class F>
@@ -703,7 +703,7 @@ kvm_status kvm_layer_set_timing(kvm_layer* ly, int enable) {
     ly->timing = enable != 0;
     ly->used = 0;
     ly->kernels = 0;
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 5; ++i) {
         ly->acc_ms[i] = 0.0;
         ly->acc_n[i] = 0;
     }
@@ -733,6 +733,96 @@ kvm_status kvm_layer_get_timing(kvm_layer* ly, kvm_timing* out) {
     out->decode_launches = ly->acc_n[PH_DECODE];
     out->other_launches = ly->acc_n[PH_OTHER];
     out->kernels = ly->kernels;
+    out->proj_ms = ly->acc_ms[PH_PROJ];
+    out->proj_launches = ly->acc_n[PH_PROJ];
+    return KVM_OK;
+}
+
+namespace {
+// offsets of q, k, v, o and gate inside the forward scratch
+struct FwdScratch {
+    size_t q, k, v, o, gate, total;
+};
+FwdScratch fwd_scratch_of(const kvm_config& c, int64_t n_tokens) {
+    FwdScratch f;
+    const size_t rows = (size_t)c.batch * c.heads * (size_t)n_tokens;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = kvm::host::align_up(o + bytes); return at; };
+    f.q = take(rows * D * 2);
+    f.k = take(rows * D * 2);
+    f.v = take(rows * D * 2);
+    f.o = take(rows * D * 2);
+    f.gate = take(rows * 4);
+    f.total = o;
+    return f;
+}
+}  // namespace
+
+size_t kvm_forward_scratch_bytes(const kvm_config* cfg, int32_t d_model, int64_t n_tokens) {
+    std::string why;
+    if (!validate(cfg, why)) { g_err = why; return 0; }
+    if (cfg->dtype != KVM_BF16 || d_model < 64 || d_model % 64 || n_tokens < 1 || n_tokens > cfg->max_tokens) {
+        g_err = "kvm_forward_scratch_bytes: bf16 layer, d_model a positive multiple of 64, 1 <= n_tokens <= max_tokens";
+        return 0;
+    }
+    return fwd_scratch_of(*cfg, n_tokens).total;
+}
+
+kvm_status kvm_layer_forward(kvm_layer* ly, int32_t d_model, const void* x, const void* w_in, const void* w_out,
+                             int64_t n_tokens, void* y, void* scratch, size_t scratch_bytes, void* cuda_stream) {
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    const kvm_config& c = ly->cfg;
+    if (c.dtype != KVM_BF16) return ly->fail(KVM_ERR_UNSUPPORTED, "kvm_layer_forward needs a bf16 layer");
+    if (d_model < 64 || d_model % 64) return ly->fail(KVM_ERR_INVALID_ARG, "d_model must be a positive multiple of 64");
+    if (n_tokens < 1 || n_tokens > c.max_tokens) return ly->fail(KVM_ERR_INVALID_ARG, "n_tokens must be in [1, max_tokens]");
+    if (!x || !w_in || !w_out || !y || !scratch)
+        return ly->fail(KVM_ERR_INVALID_ARG, "x, w_in, w_out, y and scratch must be non-NULL");
+    for (const void* p : {x, w_in, w_out, (const void*)y})
+        if (reinterpret_cast<uintptr_t>(p) % 16) return ly->fail(KVM_ERR_INVALID_ARG, "x, w_in, w_out and y must be 16-byte aligned");
+    const FwdScratch F = fwd_scratch_of(c, n_tokens);
+    if (reinterpret_cast<uintptr_t>(scratch) % ALIGN || scratch_bytes < F.total)
+        return ly->fail(KVM_ERR_WORKSPACE, "scratch missing, misaligned or smaller than kvm_forward_scratch_bytes");
+    DeviceGuard g(ly->device);
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    ly->last_stream = s;
+    char* sc = static_cast<char*>(scratch);
+    const int H = c.heads;
+    kvm::GemmSpec in{};
+    in.a = x;
+    in.w = w_in;
+    in.B = c.batch;
+    in.N = n_tokens;
+    in.H = H;
+    in.K = d_model;
+    in.Nout = 3 * H * D + H;
+    in.a_heads = 0;
+    in.epi = 0;
+    in.q = sc + F.q;
+    in.k = sc + F.k;
+    in.v = sc + F.v;
+    in.gate = reinterpret_cast<float*>(sc + F.gate);
+    in.status = ly->at<int>(ly->L.status);
+    cudaError_t e = timed(ly, PH_PROJ, s, [&] { return kvm::launch_gemm_tc(in, s); });
+    if (e != cudaSuccess) return ly->cuda_fail(e, "input projection launch");
+    ly->kernels += 1;
+    kvm_status st = kvm_prefill(ly, sc + F.q, sc + F.k, sc + F.v, reinterpret_cast<const float*>(sc + F.gate),
+                                n_tokens, sc + F.o, cuda_stream, nullptr);
+    if (st != KVM_OK) return st;
+    kvm::GemmSpec outp{};
+    outp.a = sc + F.o;
+    outp.w = w_out;
+    outp.B = c.batch;
+    outp.N = n_tokens;
+    outp.H = H;
+    outp.K = H * D;
+    outp.Nout = d_model;
+    outp.a_heads = 1;
+    outp.epi = 1;
+    outp.y = y;
+    outp.status = ly->at<int>(ly->L.status);
+    e = timed(ly, PH_PROJ, s, [&] { return kvm::launch_gemm_tc(outp, s); });
+    if (e != cudaSuccess) return ly->cuda_fail(e, "output projection launch");
+    ly->kernels += 1;
     return KVM_OK;
 }
 

@@ -197,6 +197,25 @@ struct RenormArgs {
     int BH;
 };
 
+// Projection GEMM of the whole layer: C = A * W^T, A [rows, K] bf16 (or the
+// attention output [B*H, N, 64] read head by head when a_heads), W [Nout, K]
+// bf16; epi 0 scatters q/k/v [B,H,N,64] bf16 and sigmoid gates [B,H,N] fp32,
+// epi 1 writes y [B, N, Nout] bf16.  K a multiple of 64.
+struct GemmSpec {
+    const void* a;
+    const void* w;
+    int B;
+    int64_t N;
+    int H, K, Nout;
+    int a_heads, epi;
+    void* q;
+    void* k;
+    void* v;
+    float* gate;
+    void* y;
+    int* status;
+};
+
 // Host launchers (return the launch error).
 cudaError_t launch_fold(const FoldArgs& a, bool bf16, cudaStream_t s);
 bool fold_tc_supported(const FoldArgs& a, bool bf16);
@@ -207,6 +226,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_ring_fill(const RingFillArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_rope_keys(const RopeKeysArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_tc(const GemmSpec& g, cudaStream_t s);
 cudaError_t launch_renorm(const RenormArgs& a, bool bf16, cudaStream_t s);
 
 }  // namespace kvm

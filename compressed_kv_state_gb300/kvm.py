@@ -53,7 +53,8 @@ class kvm_timing(ctypes.Structure):
                 ("decode_ms", ctypes.c_double), ("other_ms", ctypes.c_double),
                 ("fold_launches", ctypes.c_int64), ("attn_launches", ctypes.c_int64),
                 ("decode_launches", ctypes.c_int64), ("other_launches", ctypes.c_int64),
-                ("kernels", ctypes.c_int64)]
+                ("kernels", ctypes.c_int64), ("proj_ms", ctypes.c_double),
+                ("proj_launches", ctypes.c_int64)]
 
 
 class KvmError(RuntimeError):
@@ -87,6 +88,10 @@ def _load():
     lib.kvm_layer_set_timing.argtypes = [P, ctypes.c_int]
     lib.kvm_layer_get_timing.restype = ctypes.c_int
     lib.kvm_layer_get_timing.argtypes = [P, P]
+    lib.kvm_forward_scratch_bytes.restype = ctypes.c_size_t
+    lib.kvm_forward_scratch_bytes.argtypes = [P, ctypes.c_int32, I64]
+    lib.kvm_layer_forward.restype = ctypes.c_int
+    lib.kvm_layer_forward.argtypes = [P, ctypes.c_int32, P, P, P, I64, P, P, ctypes.c_size_t, P]
     lib.kvm_layer_set_overlap.restype = ctypes.c_int
     lib.kvm_layer_set_overlap.argtypes = [P, ctypes.c_int32]
     lib.kvm_layer_get_overlap.restype = ctypes.c_int
@@ -166,6 +171,20 @@ def kvm_layer_get_timing(layer) -> dict:
     t = kvm_timing()
     _check(lib.kvm_layer_get_timing(layer, ctypes.byref(t)), layer)
     return {name: getattr(t, name) for name, _ in kvm_timing._fields_}
+
+
+def kvm_forward_scratch_bytes(cfg: kvm_config, d_model: int, n_tokens: int) -> int:
+    n = lib.kvm_forward_scratch_bytes(ctypes.byref(cfg), int(d_model), int(n_tokens))
+    if n == 0:
+        raise KvmError(KVM_ERR_INVALID_ARG, kvm_last_error(None))
+    return n
+
+
+def kvm_layer_forward(layer, d_model: int, x, w_in, w_out, n_tokens: int, y, scratch, stream=None):
+    """Whole-layer forward: projections (tensor cores) around the KVM attention."""
+    st = lib.kvm_layer_forward(layer, int(d_model), _ptr(x), _ptr(w_in), _ptr(w_out), int(n_tokens), _ptr(y),
+                               _ptr(scratch), int(scratch.numel() * scratch.element_size()), _stream(stream))
+    _check(st, layer)
 
 
 def kvm_layer_set_overlap(layer, segments: int):
@@ -281,6 +300,31 @@ class KvmLayer:
     def import_state(self, t, stream=None):
         b = self._bufs(t, t["n_slots"], t["n_overflow"], t["pos"])
         kvm_state_import(self.handle, b, stream)
+
+    def forward(self, x, w_in, w_out, stream=None):
+        """Whole-layer forward of x [B, N, d_model] bf16; returns y and the
+        scratch views q, k, v, o [B, H, N, 64] bf16 and gate [B, H, N] fp32."""
+        import torch
+        c = self.cfg
+        B, N, d_model = x.shape
+        for t, shp in ((x, (c.batch, N, d_model)), (w_in, (3 * c.heads * 64 + c.heads, d_model)),
+                       (w_out, (d_model, c.heads * 64))):
+            self._io(t, shp, torch.bfloat16)
+        nbytes = kvm_forward_scratch_bytes(c, d_model, N)
+        scratch = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+        y = torch.empty((c.batch, N, d_model), dtype=torch.bfloat16, device=x.device)
+        kvm_layer_forward(self.handle, d_model, x, w_in, w_out, N, y, scratch, stream)
+        rows = c.batch * c.heads * N
+        al = lambda n: (n + 255) // 256 * 256
+        off, parts = 0, {}
+        for name, nb in (("q", rows * 128), ("k", rows * 128), ("v", rows * 128), ("o", rows * 128),
+                         ("gate", rows * 4)):
+            parts[name] = scratch[off:off + nb]
+            off = al(off + nb)
+        shp = (c.batch, c.heads, N, 64)
+        inter = {n: parts[n].view(torch.bfloat16).view(shp) for n in ("q", "k", "v", "o")}
+        inter["gate"] = parts["gate"].view(torch.float32).view(c.batch, c.heads, N)
+        return y, inter
 
     def sync(self):
         kvm_layer_sync(self.handle)

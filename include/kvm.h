@@ -205,6 +205,8 @@ typedef struct {
     double other_ms;     /* ring fill, state renormalisation */
     int64_t fold_launches, attn_launches, decode_launches, other_launches;  /* timed intervals */
     int64_t kernels;     /* every kernel the layer launched, timed or not */
+    double proj_ms;      /* projection GEMMs of kvm_layer_forward */
+    int64_t proj_launches;
 } kvm_timing;
 
 /* Enable (1) or disable (0) per-kernel timing; enabling resets the totals.
@@ -236,6 +238,27 @@ kvm_status kvm_layer_set_overlap(kvm_layer* layer, int32_t segments);
 
 /* Fold segments the layer's last kvm_prefill ran with (0: sequential). */
 kvm_status kvm_layer_get_overlap(const kvm_layer* layer, int32_t* last_segments);
+
+/* Whole-layer forward ("Key-Value Means", technical summary, Methodology: the
+ * layer's own projections around the KVM attention; the merge gate is produced
+ * inside the layer from its input).  For x [B, n_tokens, d_model] bf16:
+ *   [q | k | v | gate_logit] = x * w_in^T, w_in [3*H*64 + H, d_model] bf16
+ *     (rows: q of heads 0..H-1, then k, then v, each 64 rows per head, then one
+ *     gate row per head); gate = sigmoid(gate_logit), fused in the GEMM epilogue;
+ *   o = the KVM attention of this layer (kvm_prefill) on q, k, v, gate;
+ *   y = o_flat * w_out^T, o_flat [B, n_tokens, H*64] (head-major features),
+ *     w_out [d_model, H*64] bf16, y [B, n_tokens, d_model] bf16.
+ * Only for bf16 layers; d_model a positive multiple of 64; x, w_in, w_out and y
+ * 16-byte aligned.  The projections run on the tensor cores (tcgen05, fp32
+ * accumulation).  scratch (device, 256-byte aligned, at least
+ * kvm_forward_scratch_bytes) receives, in order and each 256-byte aligned:
+ * q, k, v, o (bf16 [B, H, n_tokens, 64]) and gate (fp32 [B, H, n_tokens]); they
+ * stay readable after the call.  The layer's state afterwards is that of
+ * kvm_prefill.  Asynchronous on the stream; 0 on invalid arguments. */
+size_t kvm_forward_scratch_bytes(const kvm_config* cfg, int32_t d_model, int64_t n_tokens);
+kvm_status kvm_layer_forward(kvm_layer* layer, int32_t d_model, const void* x, const void* w_in,
+                             const void* w_out, int64_t n_tokens, void* y, void* scratch,
+                             size_t scratch_bytes, void* cuda_stream);
 
 /* Size of the static device scratch behind kvm_prefill_noalloc: 32 MiB. */
 #define KVM_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

@@ -289,3 +289,57 @@ class OracleDecoder:
 __all__ = ["OracleConfig", "OracleState", "OracleDecoder", "OracleError", "capacity",
            "fold_event", "state_view", "attend_query", "prefill", "n_events", "build",
            "MERGED", "APPENDED", "SINK"]
+
+
+# ------------------------------------------------------------- whole layer
+#
+# The layer around the KVM attention (KVM summary, Methodology: queries, keys,
+# values and a data-dependent merge gate are projections of the layer input;
+# the heads are projected back).  Weight layouts follow the linear layer's
+# [out_features, in_features] convention: w_in rows are q of heads 0..H-1 (64
+# rows per head), then k, then v, then one merge-gate row per head; w_out is
+# [d_model, H * 64] over head-major features.  Plain fp64 matrix products.
+
+def bf16_round(a):
+    """Round float64 values to the nearest bf16 value (8 significant bits, ties to
+    even), exactly, returned as float64 (normal range)."""
+    a = np.asarray(a, dtype=np.float64)
+    m, e = np.frexp(a)                        # a = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)
+
+
+def layer_project_in(x, w_in, H: int, d: int = 64):
+    """q, k, v [B, H, N, d] and gate = sigmoid(logit) [B, H, N] from x [B, N, d_model]."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w_in, dtype=np.float64)
+    B, N, _ = x.shape
+    z = x @ w.T                               # [B, N, 3*H*d + H]
+    Hd = H * d
+    heads = lambda part: part.reshape(B, N, H, d).transpose(0, 2, 1, 3)
+    q, k, v = heads(z[..., :Hd]), heads(z[..., Hd:2 * Hd]), heads(z[..., 2 * Hd:3 * Hd])
+    gate = 1.0 / (1.0 + np.exp(-z[..., 3 * Hd:3 * Hd + H])).transpose(0, 2, 1)
+    return q, k, v, gate
+
+
+def layer_project_out(o, w_out):
+    """y [B, N, d_model] from the attention output o [B, H, N, d]."""
+    o = np.asarray(o, dtype=np.float64)
+    B, H, N, d = o.shape
+    flat = o.transpose(0, 2, 1, 3).reshape(B, N, H * d)
+    return flat @ np.asarray(w_out, dtype=np.float64).T
+
+
+def layer_forward(cfg: OracleConfig, x, w_in, w_out, H: int, threads: int | None = None):
+    """Whole-layer forward.  The projected q, k, v are rounded to bf16 before the
+    attention: they are bf16 tensors between the layer's operations, and the
+    fold's winner-take-all decisions are taken on those values."""
+    q, k, v, gate = layer_project_in(x, w_in, H, cfg.head_dim)
+    B, _, N, d = q.shape
+    q, k, v = bf16_round(q), bf16_round(k), bf16_round(v)
+    o = np.empty_like(q)
+    dbgs = []
+    for b in range(B):
+        out, _, dbg = prefill(cfg, q[b], k[b], v[b], gate[b], threads=threads)
+        o[b] = out
+        dbgs.append(dbg)
+    return layer_project_out(o, w_out), (q, k, v, gate, o), dbgs

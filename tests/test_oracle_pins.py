@@ -407,3 +407,67 @@ def test_decode_equals_prefill_rows(N0, steps):
     dec = oracle.OracleDecoder(cfg, st, N0, k[F:N0], v[F:N0], g[F:N0])
     outs = [dec.step(q[p], k[p], v[p], g[p]) for p in range(N0, N)]
     np.testing.assert_allclose(np.stack(outs), full[N0:], rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ whole layer
+
+def test_bf16_round_ties_to_even_and_matches_torch():
+    """The oracle's bf16 rounding (8 significant bits, ties to even) against hand
+    values and torch's float32 -> bfloat16 conversion."""
+    import torch
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 1.0 + 3 * 2 ** -9, -3.0, 0.0, 2.0 ** -20 * 1.5])
+    want = np.array([1.0, 1.0, 1.0 + 2 ** -6, 1.0 + 2 ** -7, -3.0, 0.0, 2.0 ** -20 * 1.5])
+    np.testing.assert_array_equal(oracle.bf16_round(x), want)
+    r = np.random.default_rng(3).standard_normal(20000).astype(np.float32) * 7
+    ref = torch.from_numpy(r).bfloat16().double().numpy()
+    np.testing.assert_array_equal(oracle.bf16_round(r.astype(np.float64)), ref)
+
+
+def test_layer_projections_index_convention_bruteforce():
+    """Projection layouts by explicit loops: q/k/v of head h, dim x are rows
+    h*64+x of the q, k, v blocks of w_in; the gate of head h is the sigmoid of
+    row 3*H*64+h; y[n, j] sums o[h, n, x] * w_out[j, h*64+x] (KVM summary,
+    Methodology: per-head projections of the layer input, heads projected back)."""
+    rng = np.random.default_rng(11)
+    B, N, H, d, dm = 2, 3, 2, 64, 5
+    x = rng.standard_normal((B, N, dm))
+    w_in = rng.standard_normal((3 * H * d + H, dm))
+    w_out = rng.standard_normal((dm, H * d))
+    q, k, v, g = oracle.layer_project_in(x, w_in, H, d)
+    for b in range(B):
+        for n in range(N):
+            for h in range(H):
+                for part, arr in ((0, q), (1, k), (2, v)):
+                    for xx in (0, 17, 63):
+                        row = part * H * d + h * d + xx
+                        want = sum(x[b, n, i] * w_in[row, i] for i in range(dm))
+                        assert arr[b, h, n, xx] == pytest.approx(want, abs=1e-12)
+                logit = sum(x[b, n, i] * w_in[3 * H * d + h, i] for i in range(dm))
+                assert g[b, h, n] == pytest.approx(1.0 / (1.0 + np.exp(-logit)), abs=1e-14)
+    o = rng.standard_normal((B, H, N, d))
+    y = oracle.layer_project_out(o, w_out)
+    for b in range(B):
+        for n in range(N):
+            for j in range(dm):
+                want = sum(o[b, h, n, xx] * w_out[j, h * d + xx] for h in range(H) for xx in range(d))
+                assert y[b, n, j] == pytest.approx(want, abs=1e-10)
+
+
+def test_layer_with_identity_projections_reduces_to_the_attention():
+    """With w_in = [I; I; I; 0] (q = k = v = the head slices of x, gate logit 0 so
+    the gate is 1/2) and w_out = I, the whole layer is the pinned KVM attention
+    on those inputs, heads laid out back along the features."""
+    H, d, N = 2, 64, 700
+    dm = H * d
+    cfg = oracle.OracleConfig(head_dim=d, rope_dims=32, chunk=64, window=128, n_sinks=4,
+                              max_slots=24)
+    rng = np.random.default_rng(5)
+    x = oracle.bf16_round(rng.standard_normal((1, N, dm)))
+    eye = np.eye(dm)
+    w_in = np.concatenate([eye, eye, eye, np.zeros((H, dm))])
+    y, (q, k, v, gate, o), _ = oracle.layer_forward(cfg, x, w_in, eye, H)
+    xh = x[0].reshape(N, H, d).transpose(1, 0, 2)
+    np.testing.assert_array_equal(q[0], xh)
+    np.testing.assert_array_equal(gate, 0.5)
+    out, _, _ = oracle.prefill(cfg, xh, xh, xh, np.full((H, N), 0.5))
+    np.testing.assert_allclose(y[0], out.transpose(1, 0, 2).reshape(N, dm), rtol=0, atol=1e-12)
