@@ -320,6 +320,7 @@ def run_ours(args, rank, world, local_rank):
     d2h = hout.numel() * hout.element_size()
 
     decode = None if args.no_decode else run_decode(dev, stream)
+    layer_fwd = None if args.no_layer else run_layer(dev, stream, max(3, args.steps // 2))
     clk = clocks.stop()
 
     peaks = _peaks()
@@ -378,8 +379,56 @@ def run_ours(args, rank, world, local_rank):
                             "folded chunks on the other, the rest on all SMs"},
         "clocks": clk,
         "decode": decode,
+        "layer_forward": layer_fwd,
     }
     return line
+
+
+def run_layer(dev, stream, steps, d_model=768):
+    """Whole-layer forward of the same workload as a d_model = 768 layer (12 heads of
+    64, the pages' 120M-like shape): tensor-core input projection with fused gate,
+    the KVM attention, output projection.  Random bf16 weights; inputs in HBM."""
+    import torch
+    from compressed_kv_state_gb300 import kvm
+    peaks = _peaks()
+    x, w_in, w_out = wl.layer_inputs(W, d_model)
+    tx = torch.from_numpy(x).to(dev).bfloat16()
+    tin = torch.from_numpy(w_in).to(dev).bfloat16()
+    tout = torch.from_numpy(w_out).to(dev).bfloat16()
+    cfg = kvm.make_config(batch=W.B, heads=W.H, rope_dims=W.rope_dims, chunk=W.chunk, window=W.window,
+                          n_sinks=W.n_sinks, sched=W.sched, max_slots=W.max_slots, max_tokens=W.N)
+    layer = kvm.KvmLayer(cfg, device=dev)
+    y = torch.empty((W.B, W.N, d_model), dtype=torch.bfloat16, device=dev)
+    scratch = torch.empty(kvm.kvm_forward_scratch_bytes(cfg, d_model, W.N), dtype=torch.uint8, device=dev)
+
+    def step():
+        kvm.kvm_layer_forward(layer.handle, d_model, tx, tin, tout, W.N, y, scratch, stream)
+
+    for _ in range(3):
+        step()
+    layer.sync()
+    kvm.kvm_layer_set_timing(layer.handle, True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    tm = kvm.kvm_layer_get_timing(layer.handle)
+    kvm.kvm_layer_set_timing(layer.handle, False)
+    layer.sync()
+    Hd = W.H * W.d
+    proj_flops = 2.0 * W.B * W.N * d_model * (3 * Hd + W.H) + 2.0 * W.B * W.N * Hd * d_model
+    proj_ms = tm["proj_ms"] / max(1, steps)
+    tf = proj_flops / (proj_ms / 1e3) / 1e12
+    layer.close()
+    return {"d_model": d_model, "value": W.B * W.N / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "projections": {"ms_per_step": proj_ms, "flops_per_step": proj_flops, "tflops": tf,
+                            "frac_of_bf16_peak": tf / peaks["bf16"], "peak": peaks["bf16"],
+                            "note": "two launches per step (input and output projection), "
+                                    "times summed; measured bf16 burst peak"}}
 
 
 def run_decode(dev, stream):
@@ -467,6 +516,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-layer", action="store_true", help="skip the whole-layer forward line")
     ap.add_argument("--segments", type=int, default=-1,
                     help="fold segments of the overlapped prefill (0: sequential, <0: automatic)")
     ap.add_argument("--no-cpu", action="store_true")
