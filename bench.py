@@ -320,7 +320,7 @@ def run_ours(args, rank, world, local_rank):
     d2h = hout.numel() * hout.element_size()
 
     decode = None if args.no_decode else run_decode(dev, stream)
-    layer_fwd = None if args.no_layer else run_layer(dev, stream, max(3, args.steps // 2))
+    layer_fwd = None if args.no_layer else run_layer(dev, stream, max(3, args.steps // 2), args.segments)
     clk = clocks.stop()
 
     peaks = _peaks()
@@ -384,7 +384,7 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-def run_layer(dev, stream, steps, d_model=768):
+def run_layer(dev, stream, steps, segments=-1, d_model=768):
     """Whole-layer forward of the same workload as a d_model = 768 layer (12 heads of
     64, the pages' 120M-like shape): tensor-core input projection with fused gate,
     the KVM attention, output projection.  Random bf16 weights; inputs in HBM."""
@@ -398,6 +398,7 @@ def run_layer(dev, stream, steps, d_model=768):
     cfg = kvm.make_config(batch=W.B, heads=W.H, rope_dims=W.rope_dims, chunk=W.chunk, window=W.window,
                           n_sinks=W.n_sinks, sched=W.sched, max_slots=W.max_slots, max_tokens=W.N)
     layer = kvm.KvmLayer(cfg, device=dev)
+    kvm.kvm_layer_set_overlap(layer.handle, segments)
     y = torch.empty((W.B, W.N, d_model), dtype=torch.bfloat16, device=dev)
     scratch = torch.empty(kvm.kvm_forward_scratch_bytes(cfg, d_model, W.N), dtype=torch.uint8, device=dev)
 
