@@ -290,34 +290,71 @@ def run_ours(args, rank, world, local_rank):
     ms_step = ms / args.steps
     value = job_throughput(W.B * W.N, world, ms_step)
 
-    # end to end through the C ABI: pinned host inputs in, output back to host
+    # end to end through the C ABI: pinned host inputs in, output back to host, every
+    # step.  Pipelined like a server: step i+1's host-to-device copies (three copy
+    # streams) and step i-1's device-to-host read overlap step i's prefill; device
+    # inputs and outputs are double-buffered, and events order every reuse.
     hq = torch.from_numpy(q).bfloat16().pin_memory()
     hk = torch.from_numpy(k).bfloat16().pin_memory()
     hv = torch.from_numpy(v).bfloat16().pin_memory()
     hg = torch.from_numpy(g).pin_memory()
-    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    houts = [torch.empty(out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dins = [(dq, dk, dv, dg), tuple(torch.empty_like(t) for t in (dq, dk, dv, dg))]
+    douts = [out, torch.empty_like(out)]
+    s_in = [torch.cuda.Stream(dev) for _ in range(3)]
+    s_out = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    ev_in = [[ev() for _ in range(3)] for _ in range(2)]     # inputs of set b landed
+    ev_used = [ev() for _ in range(2)]                         # prefill of set b done
+    ev_read = [ev() for _ in range(2)]                         # output of set b read back
+    started = [False, False]
 
-    def e2e_step():
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dg.copy_(hg, non_blocking=True)
-        kvm.kvm_prefill(layer.handle, dq, dk, dv, dg, W.N, out, stream)
-        hout.copy_(out, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        tq, tk, tv, tg = dins[b]
+        for j, (src, dst) in enumerate(((hq, tq), (hk, tk), ((hv, hg), (tv, tg)))):
+            st = s_in[j]
+            if started[b]:
+                st.wait_event(ev_used[b])  # the previous prefill on this set read its inputs
+            with torch.cuda.stream(st):
+                if j < 2:
+                    dst.copy_(src, non_blocking=True)
+                else:
+                    dst[0].copy_(src[0], non_blocking=True)
+                    dst[1].copy_(src[1], non_blocking=True)
+            ev_in[b][j].record(st)
+        for j in range(3):
+            stream.wait_event(ev_in[b][j])
+        if started[b]:
+            stream.wait_event(ev_read[b])  # the previous output of this set was read back
+        kvm.kvm_prefill(layer.handle, tq, tk, tv, tg, W.N, douts[b], stream)
+        ev_used[b].record(stream)
+        s_out.wait_event(ev_used[b])
+        with torch.cuda.stream(s_out):
+            houts[b].copy_(douts[b], non_blocking=True)
+        ev_read[b].record(s_out)
+        started[b] = True
 
-    for _ in range(2):
-        e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize(dev)
+    ke2e = max(3, args.steps // 2)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    ke2e = max(3, args.steps // 2)
-    for _ in range(ke2e):
-        e2e_step()
+    for j in range(3):
+        s_in[j].wait_event(e0)
+    for i in range(ke2e):
+        e2e_step(i)
+    for b in range(2):
+        stream.wait_event(ev_read[b])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = e0.elapsed_time(e1) / ke2e
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
-    d2h = hout.numel() * hout.element_size()
+    d2h = houts[0].numel() * houts[0].element_size()
+    # the pipelined outputs equal the device-resident step's output
+    e2e_same = bool(torch.equal(houts[(ke2e - 1) & 1], out.cpu())) if ke2e > 0 else None
+    del dins, douts
 
     decode = None if args.no_decode else run_decode(dev, stream)
     layer_fwd = None if args.no_layer else run_layer(dev, stream, max(3, args.steps // 2), args.segments)
@@ -372,7 +409,10 @@ def run_ours(args, rank, world, local_rank):
         "algorithmic_flops_per_step": {"attention": aw["flops"], "attention_4d_count": aw["flops_4d"],
                                        "fold_similarity": ffl},
         "e2e": {"value": W.B * W.N / (ms_e2e / 1e3), "unit": UNIT, "ms_per_step": ms_e2e,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "pipelined": "step i+1's host-to-device copies and step i-1's read-back overlap "
+                             "step i's prefill (double-buffered device inputs and outputs)",
+                "output_matches_device_step": e2e_same},
         "gpu_launches": int(launches),
         "overlap": {"fold_segments": segments,
                     "note": "fold segments on one SM partition (green context), attention of "
