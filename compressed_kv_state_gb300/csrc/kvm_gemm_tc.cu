@@ -11,13 +11,13 @@
 //     merge-gate logits of head h, written as sigmoid(logit) fp32 [B, H, N];
 //   - output projection: A is the attention output [B, H, N, 64] read
 //     head by head (K-block h = head h), C is written bf16 [B, N, Nout].
-// Persistent: one CTA per SM walks its share of the 128 x 128 output tiles.
-// Warp 0 lane 0 issues the TMA loads (128-byte swizzle, a ring of 5 stages of
+// Persistent: one CTA per SM walks its share of the 128 x 256 output tiles.
+// Warp 0 lane 0 issues the TMA loads (128-byte swizzle, a ring of 4 stages of
 // 64-wide K blocks, running across tile boundaries), warp 1 lane 0 issues the
-// tcgen05 MMAs into one of two TMEM accumulators (tile i uses accumulator
-// i % 2), and warps 2-5 drain the other accumulator meanwhile (thread = output
-// row = TMEM lane), so a tile's epilogue overlaps the next tile's MMAs.  Every
-// wait is bounded.
+// tcgen05 MMAs (M 128, N 256) into one of two TMEM accumulators (tile i uses
+// accumulator i % 2; together they fill the 512 columns), and warps 2-5 drain
+// the other accumulator meanwhile (thread = output row = TMEM lane), so a
+// tile's epilogue overlaps the next tile's MMAs.  Every wait is bounded.
 #include <cuda.h>
 
 #include "kvm_internal.cuh"
@@ -28,7 +28,7 @@ namespace gemm {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 128, BK = 64, NSTAGE = 5;
+constexpr int BM = 128, BN = 256, BK = 64, NSTAGE = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
