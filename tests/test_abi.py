@@ -91,3 +91,23 @@ def test_null_handles_are_rejected(kvm):
     assert kvm.lib.kvm_layer_create(ctypes.byref(cfg), None, 0, ctypes.byref(out)) == \
         kvm.KVM_ERR_WORKSPACE
     assert out.value is None
+
+
+def test_forward_scratch_bytes_validates_and_sizes(kvm):
+    cfg = kvm.make_config(batch=2, heads=3, max_tokens=1000)
+    rows = 2 * 3 * 700
+    al = lambda n: (n + 255) // 256 * 256
+    want = 4 * al(rows * 64 * 2) + al(rows * 4)
+    assert kvm.lib.kvm_forward_scratch_bytes(ctypes.byref(cfg), 128, 700) == want
+    for d_model, n in ((100, 700), (0, 700), (128, 0), (128, 1001)):
+        assert kvm.lib.kvm_forward_scratch_bytes(ctypes.byref(cfg), d_model, n) == 0
+    cfg32 = kvm.make_config(batch=2, heads=3, max_tokens=1000, dtype=kvm.KVM_FP32)
+    assert kvm.lib.kvm_forward_scratch_bytes(ctypes.byref(cfg32), 128, 700) == 0
+
+
+def test_overlap_and_forward_entry_points_reject_null_layers(kvm):
+    assert kvm.lib.kvm_layer_set_overlap(None, 3) == kvm.KVM_ERR_INVALID_ARG
+    n = ctypes.c_int32(5)
+    assert kvm.lib.kvm_layer_get_overlap(None, ctypes.byref(n)) == kvm.KVM_ERR_INVALID_ARG
+    assert kvm.lib.kvm_layer_forward(None, 128, None, None, None, 1, None, None, 0, None) == \
+        kvm.KVM_ERR_INVALID_ARG
