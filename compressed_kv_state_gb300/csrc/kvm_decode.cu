@@ -11,7 +11,7 @@
 
 namespace kvm {
 
-constexpr int DEC_WARPS = 4;
+constexpr int DEC_WARPS = 3;
 constexpr int DEC_THREADS = DEC_WARPS * 32;
 constexpr int TK = 32;  // keys per tile
 
@@ -29,7 +29,8 @@ template <> __device__ __forceinline__ float2 ld2s<__nv_bfloat16>(const __nv_bfl
 }
 template <> __device__ __forceinline__ float2 ld2s<float>(const float* p) { return *reinterpret_cast<const float2*>(p); }
 
-// One CTA per (b, h), four warps.  Keys (state rows, then the window in
+// One CTA per (b, h), three warps (48 KB of stages: four CTAs per SM, so the
+// 1024 rows of the decode sweep take two waves).  Keys (state rows, then the window in
 // position order) are split into one contiguous range per warp; each warp
 // streams its range in tiles of 32 keys through two shared-memory stages of
 // its own, filled by bulk copies (a tile is at most three contiguous row runs:
@@ -38,7 +39,7 @@ template <> __device__ __forceinline__ float2 ld2s<float>(const float* p) { retu
 // that leaves key i's score on lane i; P V is dim-parallel from shared memory;
 // online softmax per warp, warps combined at the end.
 template <typename T>
-__global__ void __launch_bounds__(DEC_THREADS, 3) decode_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
     constexpr int RB = 64 * (int)sizeof(T);  // bytes per key row
     constexpr int TILE = TK * RB;            // bytes of one K (or V) tile
     extern __shared__ __align__(128) uint8_t dsm[];
