@@ -6,10 +6,13 @@
 // needs.  Work launched on ordinary streams may still use every SM.
 //
 // Driver entry points are resolved at run time through the runtime, so the
-// library links no driver library.
+// library links no driver library.  No partition is made while a CUDA
+// injection library (a profiler) is attached: kernel profilers do not handle
+// launches into green contexts, so under one the prefill runs sequentially.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -80,6 +83,8 @@ bool events_in(const Driver& d, CUgreenCtx g, cudaEvent_t* ev, int n) {
 
 bool partition_make(int device, int fold_rows, Partition* p, std::string& why) {
     *p = Partition{};
+    const char* inj = std::getenv("CUDA_INJECTION64_PATH");
+    if (inj != nullptr && inj[0] != '\0') { why = "a CUDA injection library (profiler) is attached"; return false; }
     const Driver& d = driver();
     if (!d.ok) { why = "green-context driver entry points unavailable"; return false; }
     CUdevice dev;
