@@ -438,6 +438,10 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             e = timed(ly, PH_OTHER, P.s_attn, [&] { return kvm::launch_rope_keys(ka, P.s_attn); });
             if (e != cudaSuccess) return ly->cuda_fail(e, "key rotation launch");
             ly->kernels += 1;
+            // the last attention launch (on s) reads the rotated keys as well
+            e = cudaEventRecord(P.ev_attn, P.s_attn);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s, P.ev_attn, 0);
+            if (e != cudaSuccess) return ly->cuda_fail(e, "key rotation join");
         }
         // attention launches on the second partition may claim only ready ranges
         const int all_ranges = aa.n_ranges;
@@ -541,7 +545,6 @@ kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const vo
         fa.r = c.rope_dims;
         fa.ln_eps = c.ln_eps;
         fa.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
-    fa.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
         fa.k_src = ly->ws + L.ring_k;
         fa.v_src = ly->ws + L.ring_v;
         fa.g_src = ly->at<float>(L.ring_g);
