@@ -399,11 +399,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": W.name, "batch": W.B, "heads": W.H, "seq_len": W.N,
-                   "head_dim": W.d, "chunk": W.chunk, "window": W.window,
-                   "slots": W.max_slots, "sinks": W.n_sinks, "rope_dims": W.rope_dims,
-                   "keys": "5% repeated keys", "l2": "inputs larger than L2 (302 MB), no flush",
-                   "parallelism": f"rows (batch x head) independent, {world} replica(s)"},
+        "config": bench_config(world),
         "roofline": roofline,
         "kernels": kernels,
         "algorithmic_flops_per_step": {"attention": aw["flops"], "attention_4d_count": aw["flops_4d"],
@@ -527,6 +523,17 @@ def run_decode(dev, stream):
 
 # ------------------------------------------------------------- reference
 
+def bench_config(world):
+    """The workload both arms report (the reference arm times a sample of it)."""
+    in_bytes = W.B * W.H * W.N * (3 * W.d * 2 + 4)  # bf16 q, k, v and the fp32 gate
+    return {"workload": W.name, "batch": W.B, "heads": W.H, "seq_len": W.N,
+            "head_dim": W.d, "chunk": W.chunk, "window": W.window,
+            "slots": W.max_slots, "sinks": W.n_sinks, "rope_dims": W.rope_dims,
+            "keys": "5% repeated keys",
+            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB), no flush",
+            "parallelism": f"rows (batch x head) independent, {world} replica(s)"}
+
+
 def run_reference(args):
     """The oracle as it stands, on the host cores: each step is a bounded sample
     of the same workload (one full-length row per core)."""
@@ -544,8 +551,7 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": W.name, "batch": W.B, "heads": W.H,
-                                            "seq_len": W.N},
+            "data": "synthetic", "config": bench_config(int(os.environ.get("WORLD_SIZE", "1"))),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
