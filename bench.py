@@ -188,7 +188,7 @@ def _ncu_traffic(kernel_file):
 
 # ------------------------------------------------------------- CPU oracle
 
-def cpu_oracle_sample(w, heads_per_thread=1):
+def cpu_oracle_sample(w, heads_per_thread=1, one_thread=True):
     """Time the fp64 oracle on a bounded sample of the workload: one full-length
     (batch, head) row per host core, all cores in parallel.  Returns tokens/s in
     the layer's unit (a layer token needs all H heads)."""
@@ -206,9 +206,17 @@ def cpu_oracle_sample(w, heads_per_thread=1):
     oracle.prefill(ocfg, q, k, v, g, threads=cores)
     dt = time.perf_counter() - t0
     layer_tokens = w.N * q.shape[0] / w.H
-    return dict(value=layer_tokens / dt, unit=UNIT, cores=min(cores, q.shape[0]), kind="oracle",
-                sample=f"{q.shape[0]} of {w.B * w.H} (batch, head) rows x {w.N} tokens of "
-                       f"{w.name}, one row per thread, {dt:.1f} s wall")
+    r = dict(value=layer_tokens / dt, unit=UNIT, cores=min(cores, q.shape[0]), kind="oracle",
+             sample=f"{q.shape[0]} of {w.B * w.H} (batch, head) rows x {w.N} tokens of "
+                    f"{w.name}, one row per thread, {dt:.1f} s wall")
+    r["seconds"] = dt
+    if one_thread:  # the same oracle on one thread, one row
+        t1 = time.perf_counter()
+        oracle.prefill(ocfg, q[:1], k[:1], v[:1], g[:1], threads=1)
+        dt1 = time.perf_counter() - t1
+        r["one_thread"] = {"value": w.N / w.H / dt1, "unit": UNIT, "cores": 1,
+                           "sample": f"1 (batch, head) row x {w.N} tokens, {dt1:.1f} s wall"}
+    return r
 
 
 # ------------------------------------------------------------- multi-rank
@@ -538,13 +546,12 @@ def run_reference(args):
     """The oracle as it stands, on the host cores: each step is a bounded sample
     of the same workload (one full-length row per core)."""
     for _ in range(args.warmup):
-        cpu_oracle_sample(W)
-    vals, walls = [], []
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        r = cpu_oracle_sample(W)
-        vals.append(r["value"])
-    wall = time.perf_counter() - t0
+        cpu_oracle_sample(W, one_thread=False)
+    secs = []
+    for _ in range(args.steps):  # timed: the oracle call of each step (not its input generation)
+        r = cpu_oracle_sample(W, one_thread=False)
+        secs.append(r.pop("seconds"))
+    wall = sum(secs)
     tokens_per_step = W.N * r["cores"] / W.H
     value = tokens_per_step * args.steps / wall
     cb = dict(value=value, unit=UNIT, cores=r["cores"], kind="oracle", sample=r["sample"])
@@ -589,6 +596,7 @@ def main():
     if rank == 0:
         if world == 1 and not args.no_cpu:
             line["cpu_baseline"] = cpu_oracle_sample(W)
+            line["cpu_baseline"].pop("seconds")
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
