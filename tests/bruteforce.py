@@ -59,7 +59,17 @@ class BFState:
         return len(self.sk)
 
 
-def bf_fold(st: BFState, first_pos, k, v, g, *, S, sched, M, coef, expo, eps, C):
+class NoMergeTarget(ValueError):
+    """A token must merge but the state has no mergeable slot (possible only
+    when merge targets are restricted to the slots before the chunk's appends)."""
+
+
+def bf_fold(st: BFState, first_pos, k, v, g, *, S, sched, M, coef, expo, eps, C,
+            r=0, pre_append=False, nope_only=False):
+    """One fold event.  Alternative readings: ``pre_append`` restricts merge
+    targets to the slots that existed before this chunk's appends;
+    ``nope_only`` takes the cosine over the non-rotary dims [r, d) only."""
+    lo_dim = r if nope_only else 0
     idx = np.arange(first_pos, first_pos + C)
     assign = np.full(C, -1)
     kind = np.full(C, -1)
@@ -73,7 +83,7 @@ def bf_fold(st: BFState, first_pos, k, v, g, *, S, sched, M, coef, expo, eps, C)
     n0 = st.n
     if n0 > S and cand.size:
         kh = ln(np.array(st.sk[S:]) / np.array(st.cnt[S:])[:, None], eps)
-        m = cos_matrix(k[cand], kh).max(axis=1)
+        m = cos_matrix(k[cand][:, lo_dim:], kh[:, lo_dim:]).max(axis=1)
     else:
         m = np.full(cand.size, -np.inf)
     a = int(np.clip(cap_of(st.t, S, sched, M, coef, expo) - n0, 0, cand.size))
@@ -85,8 +95,12 @@ def bf_fold(st: BFState, first_pos, k, v, g, *, S, sched, M, coef, expo, eps, C)
         assign[i] = st.n - 1; kind[i] = 1
     rest = np.array([i for i in cand if i not in set(chosen.tolist())], dtype=np.int64)
     if rest.size:
-        kh = ln(np.array(st.sk[S:]) / np.array(st.cnt[S:])[:, None], eps)
-        tgt = np.argmax(cos_matrix(k[rest], kh), axis=1) + S   # first maximum = lowest index
+        hi = n0 if pre_append else st.n
+        if hi <= S:
+            raise NoMergeTarget(f"event at position {first_pos}: no slot to merge into")
+        kh = ln(np.array(st.sk[S:hi]) / np.array(st.cnt[S:hi])[:, None], eps)
+        # first maximum = lowest index
+        tgt = np.argmax(cos_matrix(k[rest][:, lo_dim:], kh[:, lo_dim:]), axis=1) + S
         for i, j in zip(rest, tgt):
             assign[i] = j; kind[i] = 0
         for i, j in zip(rest, tgt):
@@ -96,19 +110,21 @@ def bf_fold(st: BFState, first_pos, k, v, g, *, S, sched, M, coef, expo, eps, C)
     return assign, kind
 
 
-def bf_view(st: BFState, r, eps):
+def bf_view(st: BFState, r, eps, no_vnorm=False):
     if st.n == 0:
         return np.zeros((0, 0)), np.zeros((0, 0))
     kh = ln(np.array(st.sk) / np.array(st.cnt)[:, None], eps)
     kh[:, :r] = 0.0
     sv = np.array(st.sv)
+    if no_vnorm:  # ablation without the value-length normalisation: the member mean
+        return kh, sv / np.array(st.cnt, dtype=np.float64)[:, None]
     nv = np.linalg.norm(sv, axis=1, keepdims=True)
     vh = np.where(nv > 0, np.array(st.rho)[:, None] * sv / np.where(nv > 0, nv, 1.0), 0.0)
     return kh, vh
 
 
 def bf_prefill(q, k, v, g, *, C, W, S, r, sched=0, M=32, coef=4.0, expo=0.5, eps=1e-5,
-               theta=10000.0):
+               theta=10000.0, pre_append=False, nope_only=False, no_vnorm=False):
     """One head: q, k, v [N, d] float64, g [N]. Returns out [N, d], state, assignments."""
     q, k, v, g = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g))
     N, d = q.shape
@@ -123,8 +139,9 @@ def bf_prefill(q, k, v, g, *, C, W, S, r, sched=0, M=32, coef=4.0, expo=0.5, eps
             e = c - W // C - 1
             sl = slice(e * C, (e + 1) * C)
             events.append(bf_fold(st, e * C, k[sl], v[sl], g[sl], S=S, sched=sched, M=M,
-                                  coef=coef, expo=expo, eps=eps, C=C))
-        kh, vh = bf_view(st, r, eps)
+                                  coef=coef, expo=expo, eps=eps, C=C, r=r,
+                                  pre_append=pre_append, nope_only=nope_only))
+        kh, vh = bf_view(st, r, eps, no_vnorm)
         ws = max(0, (c - W // C) * C)
         for p in range(c * C, min(N, (c + 1) * C)):
             s_state = (q[p] @ kh.T) if st.n else np.zeros(0)

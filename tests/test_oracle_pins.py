@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from bruteforce import bf_prefill, ln, rope_complex
+from bruteforce import NoMergeTarget, bf_prefill, ln, rope_complex
 from compressed_kv_state_gb300 import workloads as wl
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -370,6 +370,69 @@ def test_oracle_matches_bruteforce(case, seed):
         np.testing.assert_allclose(st.sum_v[:st.n], np.array(bst.sv), atol=1e-12)
         np.testing.assert_array_equal(st.count[:st.n], bst.cnt)
         np.testing.assert_allclose(st.rho[:st.n], bst.rho, rtol=1e-14)
+
+
+VARIANTS = [
+    dict(merge_pre_append=1),
+    dict(cos_nope_only=1),
+    dict(no_value_norm=1),
+    dict(merge_pre_append=1, cos_nope_only=1, no_value_norm=1),
+]
+
+
+@pytest.mark.parametrize("case", TINY)
+@pytest.mark.parametrize("var", VARIANTS)
+def test_alternative_readings_match_bruteforce(case, var):
+    """The oracle's alternative readings (merge targets before the chunk's
+    appends, cosine over the non-rotary dims only) and the no-value-norm
+    ablation agree with the brute force.  Where the pre-append reading leaves a
+    token without any slot to merge into, both sides refuse the input."""
+    c = dict(case)
+    rng = np.random.default_rng(7)
+    q, k, v, g = _inputs(21, c["N"], c["d"])
+    for t in range(1, c["N"]):
+        if rng.random() < 0.25:
+            k[t] = k[rng.integers(0, t)] + 0.2 * rng.standard_normal(c["d"])
+    coef, expo = c.get("coef", 2.0), c.get("expo", 0.5)
+    cfg = oracle.OracleConfig(head_dim=c["d"], rope_dims=c["r"], chunk=c["C"], window=c["W"],
+                              n_sinks=c["S"], sched=c["sched"], max_slots=c["M"], coef=coef,
+                              expo=expo, **var)
+    kw = dict(C=c["C"], W=c["W"], S=c["S"], r=c["r"], sched=c["sched"], M=c["M"], coef=coef,
+              expo=expo, pre_append=bool(var.get("merge_pre_append")),
+              nope_only=bool(var.get("cos_nope_only")), no_vnorm=bool(var.get("no_value_norm")))
+    try:
+        bout, bst, bev = bf_prefill(q, k, v, g, **kw)
+    except NoMergeTarget:
+        with pytest.raises(oracle.OracleError):
+            _run(cfg, q, k, v, g)
+        return
+    out, st, dbg = _run(cfg, q, k, v, g)
+    assert len(bev) == dbg["assign"].shape[0]
+    for e, (a, kd) in enumerate(bev):
+        np.testing.assert_array_equal(dbg["assign"][e], a)
+        np.testing.assert_array_equal(dbg["kind"][e], kd)
+    np.testing.assert_allclose(out, bout, rtol=0, atol=1e-10)
+    assert st.n == bst.n and st.t == bst.t
+    if bst.n:
+        np.testing.assert_array_equal(st.count[:st.n], bst.cnt)
+        np.testing.assert_allclose(st.sum_k[:st.n], np.array(bst.sk), atol=1e-12)
+
+
+def test_alternative_readings_change_decisions():
+    """Each alternative reading decides differently from the main one on some
+    input, so the pins above would notice a flag that the oracle ignores."""
+    # sqrt growth: every event appends a few slots and merges the rest
+    c = dict(N=400, C=8, W=8, S=2, r=8, d=16, sched=1, M=200)
+    q, k, v, g = _inputs(5, c["N"], c["d"])
+    base = dict(head_dim=c["d"], rope_dims=c["r"], chunk=c["C"], window=c["W"], n_sinks=c["S"],
+                sched=c["sched"], max_slots=c["M"])
+    _, _, d0 = _run(oracle.OracleConfig(**base), q, k, v, g)
+    for var in (dict(merge_pre_append=1), dict(cos_nope_only=1)):
+        _, _, d1 = _run(oracle.OracleConfig(**base, **var), q, k, v, g)
+        assert (d1["assign"] != d0["assign"]).any(), var
+    o0, _, _ = _run(oracle.OracleConfig(**base), q, k, v, g)
+    o1, _, _ = _run(oracle.OracleConfig(**base, no_value_norm=1), q, k, v, g)
+    assert np.abs(o1 - o0).max() > 1e-3
 
 
 def test_empty_prefill():
