@@ -31,8 +31,9 @@
  *     only host-side metadata.
  *   - Calls enqueue work on the given CUDA stream (NULL = legacy default
  *     stream) and return without synchronising.  Arguments are validated
- *     before anything is enqueued; a call that returns an error enqueued
- *     nothing.  Errors raised on the device are latched in a status word in
+ *     before anything is enqueued: a call that fails validation enqueued
+ *     nothing; one that returns KVM_ERR_CUDA may have enqueued its earlier
+ *     launches.  Errors raised on the device are latched in a status word in
  *     the workspace and reported by kvm_layer_sync.
  *   - No entry point aborts the process.  kvm_last_error gives a message.
  *   - A layer may be used from one host thread at a time.
@@ -178,7 +179,7 @@ kvm_status kvm_state_export(const kvm_layer* layer, kvm_state_bufs* dst, void* c
 
 /* Replace the layer's state and window ring by src (device-to-device, async)
  * and recompute the state's read view.  src->n_slots <= max_slots,
- * src->pos < max_tokens, counts >= 1 for rows < n_slots. */
+ * 0 <= src->n_overflow <= src->pos <= max_tokens, counts >= 1 for rows < n_slots. */
 kvm_status kvm_state_import(kvm_layer* layer, const kvm_state_bufs* src, void* cuda_stream);
 
 /* Wait for the layer's last stream, then report (and clear) the device-side
@@ -231,8 +232,9 @@ kvm_status kvm_layer_get_timing(kvm_layer* layer, kvm_timing* out);
  * the number of fold events); < 0 = automatic (the default).  Overlap applies
  * only to the tensor-core paths (bf16, chunk a multiple of 128 and <= 128,
  * max_slots <= 256), without a debug record, with at least 2 fold events, and
- * when the device leaves at least one SM partition beside B*H SMs; otherwise
- * the prefill runs sequentially.  The partition is made on first use and
+ * when the device leaves at least one SM partition beside B*H SMs, and not
+ * while a CUDA injection library (a profiler) is attached; otherwise the
+ * prefill runs sequentially.  The partition is made on first use and
  * released by kvm_layer_destroy. */
 kvm_status kvm_layer_set_overlap(kvm_layer* layer, int32_t segments);
 
