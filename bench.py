@@ -412,6 +412,12 @@ def run_ours(args, rank, world, local_rank):
         "kernels": kernels,
         "algorithmic_flops_per_step": {"attention": aw["flops"], "attention_4d_count": aw["flops_4d"],
                                        "fold_similarity": ffl},
+        # the whole step against the tensor roofline: attention + similarity FLOPs per step time
+        "step_tensor_roofline": {"flops": aw["flops"] + ffl, "ms_per_step": ms_step,
+                                 "achieved": (aw["flops"] + ffl) / (ms_step / 1e3) / 1e12,
+                                 "peak": peaks["bf16"], "unit": "TFLOP/s",
+                                 "frac": (aw["flops"] + ffl) / (ms_step / 1e3) / 1e12 / peaks["bf16"],
+                                 "peak_source": f"{peaks['src']} bf16 burst"},
         "e2e": {"value": W.B * W.N / (ms_e2e / 1e3), "unit": UNIT, "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "step i+1's host-to-device copies and step i-1's read-back overlap "
