@@ -8,6 +8,8 @@ bit; the sequential prefill with a debug record is checked against the oracle
 elsewhere, and here the overlapped outputs of sampled heads are also compared
 with the oracle directly (rows before the first event with an oracle near tie).
 """
+import os
+
 import numpy as np
 import pytest
 
@@ -21,6 +23,20 @@ MID = wl.Workload("fixed_B2H3N4096_C128W512", B=2, H=3, N=4096, chunk=128, windo
                   n_sinks=16, max_slots=256, keys="repeat5")
 RAGGED = wl.Workload("fixed_B1H4N3000_C128W256_ragged", B=1, H=4, N=3000, chunk=128, window=256,
                      n_sinks=16, max_slots=96, keys="repeat5")
+
+
+# Under a CUDA injection library (a profiler or tracer) the library makes no SM
+# partition and every prefill runs sequentially.
+PROFILED = bool(os.environ.get("CUDA_INJECTION64_PATH"))
+
+
+def _overlap_ran(used, want=None):
+    if PROFILED:
+        assert used == 0, "the overlap must stay off under an injection library"
+        return
+    assert used > 0, "overlapped prefill did not run (no SM partition?)"
+    if want is not None:
+        assert used == want
 
 
 def _run(w, inputs, segs, debug=False):
@@ -52,10 +68,7 @@ def test_overlapped_equals_sequential(w):
     _same_state(st_d, st_s)
     for segs in (-1, 1, 3, 16):
         out_o, _, st_o, used = _run(w, inputs, segs)
-        want = min(segs, E) if segs > 0 else None
-        assert used > 0, "overlapped prefill did not run (no SM partition?)"
-        if want is not None:
-            assert used == want
+        _overlap_ran(used, min(segs, E) if segs > 0 else None)
         np.testing.assert_array_equal(out_o, out_s, err_msg=f"segments={segs}")
         _same_state(st_o, st_s)
 
@@ -67,7 +80,7 @@ def test_overlapped_outputs_match_oracle(w):
     inputs = wl.prefill_inputs(w)
     q, k, v, g = inputs
     out, _, _, used = _run(w, inputs, -1)
-    assert used > 0
+    _overlap_ran(used)
     hs = [(0, 0), (w.B - 1, w.H - 1)]
     ocfg = oracle_cfg(w)
     oout, _, odbg = oracle.prefill(ocfg, np.stack([q[b, h] for b, h in hs]),
