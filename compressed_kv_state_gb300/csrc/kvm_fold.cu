@@ -54,8 +54,10 @@ __device__ __forceinline__ void renorm_slot(const float* sk, const float* sv, in
     vv[lane + 32] = from_f<T>(v1 * f);
 }
 
+// Two CTAs per SM (at most 128 registers a thread, no spills): a fold at a decode
+// step's chunk boundary runs one CTA for each of up to thousands of (b, h) rows.
 template <typename T>
-__global__ void __launch_bounds__(FOLD_THREADS, 1) fold_chain_kernel(FoldArgs a) {
+__global__ void __launch_bounds__(FOLD_THREADS, 2) fold_chain_kernel(FoldArgs a) {
     extern __shared__ float4 smem4[];
     float* smem = reinterpret_cast<float*>(smem4);
     const int C = a.C, S = a.S, M = a.M;
