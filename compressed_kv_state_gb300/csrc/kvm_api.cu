@@ -63,7 +63,7 @@ Sched event_sched(const kvm_config& c, int64_t first_pos, int64_t n, int64_t t) 
 bool validate(const kvm_config* c, std::string& why) {
     if (!c) { why = "config is NULL"; return false; }
     if (c->batch < 1 || c->heads < 1) { why = "batch and heads must be >= 1"; return false; }
-    if (c->head_dim != D) { why = "head_dim must be 64 in this build"; return false; }
+    if (c->head_dim != D) { why = "head_dim must be 64 (the only head size this library supports)"; return false; }
     if (c->rope_dims < 0 || c->rope_dims > c->head_dim || (c->rope_dims & 1)) {
         why = "rope_dims must be even and in [0, head_dim]"; return false;
     }

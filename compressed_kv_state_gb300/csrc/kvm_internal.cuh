@@ -1,5 +1,5 @@
 // Internal declarations shared by the translation units of libkvm.so.
-// Device code for sm_103a; head_dim is fixed at 64 in this build.
+// Device code for sm_103a; head_dim is fixed at 64 throughout the library.
 #pragma once
 
 #include <cuda_bf16.h>

@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
     KVM_OK = 0,
     KVM_ERR_INVALID_ARG = 1,   /* bad pointer, size, shape or config value */
-    KVM_ERR_UNSUPPORTED = 2,   /* valid config this build does not implement */
+    KVM_ERR_UNSUPPORTED = 2,   /* valid config this library does not implement */
     KVM_ERR_CAPACITY = 3,      /* the growth schedule would exceed max_slots / max_tokens */
     KVM_ERR_WORKSPACE = 4,     /* workspace too small or misaligned */
     KVM_ERR_CUDA = 5,          /* a CUDA runtime call failed */
@@ -77,7 +77,7 @@ typedef enum { KVM_SCHED_FIXED = 0, KVM_SCHED_POWER = 1 } kvm_sched;
 typedef struct {
     int32_t batch;       /* B >= 1 */
     int32_t heads;       /* H >= 1; one state per (batch, head) */
-    int32_t head_dim;    /* d; this build supports 64 */
+    int32_t head_dim;    /* d; this library supports 64 */
     int32_t rope_dims;   /* r: RoPE on dims [0, r), rotate-half pairs (i, i + r/2); even, 0..d */
     float rope_theta;    /* RoPE base, e.g. 10000 */
     int32_t chunk;       /* C: multiple of 16, 16..256 */
