@@ -285,6 +285,19 @@ def test_hand_worked_fold():
     np.testing.assert_allclose(kv[2], E["key_view_slot2"], atol=1e-8)
 
 
+def test_hand_worked_attention():
+    """Hand-derived outputs of every position (tests/golden/attention_hand_example.json):
+    window extent, fold timing, the state's read view and the single softmax."""
+    G = json.load(open(os.path.join(GOLDEN, "attention_hand_example.json")))
+    c = G["config"]
+    cfg = oracle.OracleConfig(head_dim=c["head_dim"], rope_dims=c["rope_dims"], chunk=c["chunk"],
+                              window=c["window"], n_sinks=c["n_sinks"], sched=c["sched"],
+                              max_slots=c["max_slots"], ln_eps=c["ln_eps"], rope_theta=c["rope_theta"])
+    q, k, v, g = (np.array(G[x], float) for x in ("q", "k", "v", "g"))
+    out, _, _ = _run(cfg, q, k, v, g)
+    np.testing.assert_allclose(out, np.array(G["expect_out"]), rtol=0, atol=1e-12)
+
+
 def test_ties_go_to_lowest_index_and_lowest_position():
     """Surprise ties append the lower positions; argmax ties go to the lowest
     slot index."""
