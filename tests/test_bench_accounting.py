@@ -73,3 +73,26 @@ def test_decode_bytes_by_parts():
                + (d + d) * 2                      # q, out
                + (d + d) * 2 + 4)                 # new k, v into the ring; gate
     assert bench.decode_bytes(dw, rin, n) == per_row * 64 * 16
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_fold_flops_by_enumeration(w):
+    """Similarity work of every fold event from the oracle's per-token kinds: each
+    candidate (not a sink founder) against every mergeable slot that existed before
+    the event, and each merged token against the slots the event appended."""
+    rng = np.random.default_rng(3)
+    q, k, v = rng.standard_normal((3, 1, w.N, w.d))
+    g = np.full((1, w.N), 0.5)
+    cfg = oracle.OracleConfig(head_dim=w.d, rope_dims=w.rope_dims, chunk=w.chunk, window=w.window,
+                              n_sinks=w.n_sinks, sched=w.sched, max_slots=w.max_slots,
+                              coef=w.coef, expo=w.expo)
+    _, _, dbg = oracle.prefill(cfg, q, k, v, g, threads=1)
+    pairs, n = 0, 0
+    for kinds in dbg["kind"][0]:
+        sinks = int((kinds == oracle.SINK).sum())
+        appended = int((kinds == oracle.APPENDED).sum())
+        merged = int((kinds == oracle.MERGED).sum())
+        mergeable_before = n + sinks - w.n_sinks
+        pairs += (appended + merged) * max(0, mergeable_before) + merged * appended
+        n += sinks + appended
+    assert bench.fold_work(w) == 2 * w.d * pairs
