@@ -72,14 +72,18 @@ def test_rope_relative_position():
 
 # -------------------------------------------------------------- closed form
 
-@pytest.mark.parametrize("N,C,W,S", [(70, 8, 16, 3), (64, 4, 8, 1), (33, 8, 8, 0)])
-def test_every_token_appended_closed_form(N, C, W, S):
+@pytest.mark.parametrize("r", [0, 8, 16])
+@pytest.mark.parametrize("N,C,W,S", [(70, 8, 16, 3), (64, 4, 8, 1), (33, 8, 8, 0), (41, 8, 0, 2)])
+def test_every_token_appended_closed_form(N, C, W, S, r):
     """Capacity >= N: every overflowed token founds its own slot (count 1),
     so the state read is keys LN(g k) with the RoPE dims zeroed and values
     rho * unit(g v) = v (g > 0).  The layer output is then one softmax over
     [tokens before the window, keyed by LN(g k) against the unrotated query]
-    and [the window, RoPE on both sides] (KVM summary, Core mechanisms 2-4)."""
-    d, r = 16, 8
+    and [the window, RoPE on both sides] (KVM summary, Core mechanisms 2-4).
+    Also at the degenerate settings: no window (W = 0: a chunk sees itself and
+    the state), no rotary dims (r = 0) and all dims rotary (r = d: the state
+    keys are all zero, so every state row scores 0)."""
+    d = 16
     cfg = oracle.OracleConfig(head_dim=d, rope_dims=r, chunk=C, window=W, n_sinks=S,
                               max_slots=max(N, S + 1))
     q, k, v, g = _inputs(2, N, d)
