@@ -289,6 +289,40 @@ def test_hand_worked_fold():
     np.testing.assert_allclose(kv[2], E["key_view_slot2"], atol=1e-8)
 
 
+def test_hand_worked_merge_into_slot_appended_by_the_same_event():
+    """Hand-derived fold (tests/golden/fold_post_append_example.json): a token
+    merges into the slot its own chunk just appended; surprise scores, sums,
+    counts, read radii, read views and every output row."""
+    G = json.load(open(os.path.join(GOLDEN, "fold_post_append_example.json")))
+    c = G["config"]
+    cfg = oracle.OracleConfig(head_dim=c["head_dim"], rope_dims=c["rope_dims"], chunk=c["chunk"],
+                              window=c["window"], n_sinks=c["n_sinks"], sched=c["sched"],
+                              max_slots=c["max_slots"], ln_eps=c["ln_eps"])
+    k, v, g = np.array(G["k"], float), np.array(G["v"], float), np.array(G["g"], float)
+    out, st, dbg = _run(cfg, np.zeros_like(k), k, v, g)
+    E = G["expect"]
+    assert st.n == E["n_slots"] and st.t == E["t"]
+    np.testing.assert_array_equal(dbg["assign"], np.array(E["assign"]))
+    np.testing.assert_array_equal(dbg["kind"], np.array(E["kind"]))
+    np.testing.assert_allclose(dbg["max_sim"][1], E["max_sim_event1"], rtol=0, atol=1e-12)
+    assert np.isneginf(dbg["max_sim"][0]).all()
+    np.testing.assert_array_equal(st.count[:st.n], E["count"])
+    np.testing.assert_allclose(st.sum_k[:st.n], E["sum_k"], atol=0)
+    np.testing.assert_allclose(st.sum_v[:st.n], E["sum_v"], atol=0)
+    np.testing.assert_allclose(st.rho[:st.n], E["rho"], atol=0)
+    kv, vv = oracle.state_view(cfg, st)
+    np.testing.assert_allclose(vv[2], E["val_view_slot2"], atol=1e-12)
+    np.testing.assert_allclose(kv[2], E["key_view_slot2"], atol=1e-12)
+    np.testing.assert_allclose(out, np.array(E["out"]), rtol=0, atol=1e-12)
+    # the alternative reading (merge targets before the appends) sends token 2 to
+    # slot 0 (tie between slots 0 and 1 at -0.2887, lowest index)
+    alt = oracle.OracleConfig(head_dim=c["head_dim"], rope_dims=c["rope_dims"], chunk=c["chunk"],
+                              window=c["window"], n_sinks=c["n_sinks"], sched=c["sched"],
+                              max_slots=c["max_slots"], ln_eps=c["ln_eps"], merge_pre_append=1)
+    _, _, dbg_alt = _run(alt, np.zeros_like(k), k, v, g)
+    assert dbg_alt["assign"][1].tolist() == [0, 2]
+
+
 def test_hand_worked_attention():
     """Hand-derived outputs of every position (tests/golden/attention_hand_example.json):
     window extent, fold timing, the state's read view and the single softmax."""
