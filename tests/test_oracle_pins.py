@@ -321,6 +321,16 @@ def test_hand_worked_merge_into_slot_appended_by_the_same_event():
                               max_slots=c["max_slots"], ln_eps=c["ln_eps"], merge_pre_append=1)
     _, _, dbg_alt = _run(alt, np.zeros_like(k), k, v, g)
     assert dbg_alt["assign"][1].tolist() == [0, 2]
+    # the no-value-norm ablation reads the member mean: slot 2 = (0,0,1,6)/2, slots 0
+    # and 1 = their single members' gate-weighted values; decisions unchanged
+    abl = oracle.OracleConfig(head_dim=c["head_dim"], rope_dims=c["rope_dims"], chunk=c["chunk"],
+                              window=c["window"], n_sinks=c["n_sinks"], sched=c["sched"],
+                              max_slots=c["max_slots"], ln_eps=c["ln_eps"], no_value_norm=1)
+    out_a, st_a, dbg_a = _run(abl, np.zeros_like(k), k, v, g)
+    np.testing.assert_array_equal(dbg_a["assign"], np.array(E["assign"]))
+    np.testing.assert_allclose(oracle.state_view(abl, st_a)[1][2], [0, 0, 0.5, 3.0], atol=1e-15)
+    np.testing.assert_allclose(out_a[6], np.array([3, 3, 2.5, 4]) / 6, atol=1e-15)
+    np.testing.assert_allclose(out_a[7], np.array([3, 4, 2.5, 5]) / 7, atol=1e-15)
 
 
 def test_hand_worked_attention():
