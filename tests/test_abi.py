@@ -48,6 +48,30 @@ def test_struct_sizes_match_header(kvm):
     assert ctypes.sizeof(kvm.kvm_debug) == 5 * 8 + 8  # + int32 test hook, padded
 
 
+def test_struct_layouts_match_the_c_compiler(kvm, tmp_path):
+    """Every field offset and struct size of the ctypes binding equals what a C
+    compiler makes of include/kvm.h (gcc, this host's ABI)."""
+    structs = {"kvm_config": kvm.kvm_config, "kvm_state_bufs": kvm.kvm_state_bufs,
+               "kvm_debug": kvm.kvm_debug, "kvm_timing": kvm.kvm_timing}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "kvm.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for fname, _ in cls._fields_:
+            lines.append(f'printf("{name} {fname} %zu\\n", offsetof({name}, {fname}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.check_call(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split("\n")
+    got = {tuple(l.split()[:2]): int(l.split()[2]) for l in out if l.strip()}
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for fname, _ in cls._fields_:
+            assert got[(name, fname)] == getattr(cls, fname).offset, (name, fname)
+
+
 @pytest.mark.parametrize("field,value,msg", [
     ("head_dim", 32, "head_dim"),
     ("chunk", 24, "chunk"),
