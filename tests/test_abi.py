@@ -48,6 +48,24 @@ def test_struct_sizes_match_header(kvm):
     assert ctypes.sizeof(kvm.kvm_debug) == 5 * 8 + 8  # + int32 test hook, padded
 
 
+def test_binding_argument_counts_match_the_header(kvm):
+    """Each function the binding declares takes as many arguments as its
+    prototype in include/kvm.h."""
+    text = open(os.path.join(ROOT, "include", "kvm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = dict(re.findall(r"\b(kvm_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S))
+    lib = kvm.lib
+    checked = 0
+    for name, args in protos.items():
+        argtypes = getattr(lib, name).argtypes
+        if argtypes is None:
+            continue
+        n = 0 if args.strip() in ("", "void") else args.count(",") + 1
+        assert len(argtypes) == n, (name, n, len(argtypes))
+        checked += 1
+    assert checked >= 15
+
+
 def test_struct_layouts_match_the_c_compiler(kvm, tmp_path):
     """Every field offset and struct size of the ctypes binding equals what a C
     compiler makes of include/kvm.h (gcc, this host's ABI)."""
