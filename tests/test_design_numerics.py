@@ -69,3 +69,27 @@ def test_lazy_rescaling_is_exact_softmax_and_bounds_p():
         got, pmax = _lazy_online_softmax(s, v.astype(np.float32), tau=8.0)
         np.testing.assert_allclose(got, exact, rtol=0, atol=2e-5 * np.abs(v).max())
         assert pmax <= 2.0 ** 8 * (1 + 1e-6)
+
+
+def test_decode_butterfly_leaves_key_i_on_lane_i():
+    """The decode kernel's transpose-reduce of per-lane partial dot products (32
+    lanes x 32 keys): at offsets 16, 8, 4, 2, 1 each lane keeps the half of its
+    live entries on its side of the offset bit and adds its partner's other
+    half; afterwards lane i holds the full sum for key i.  Emulated lane by lane
+    with distinct integer partials, so any index slip shows."""
+    rng = np.random.default_rng(2)
+    part = rng.integers(-1000, 1000, size=(32, 32))  # [lane, key]
+    v = part.copy()
+    off, w = 16, 32
+    while off >= 1:
+        nv = v.copy()
+        for lane in range(32):
+            partner = lane ^ off
+            up, pup = (lane & off) != 0, (partner & off) != 0
+            for i in range(w // 2):
+                keep = v[lane, i + w // 2] if up else v[lane, i]
+                recv = v[partner, i] if pup else v[partner, i + w // 2]
+                nv[lane, i] = keep + recv
+        v = nv
+        off, w = off >> 1, w >> 1
+    np.testing.assert_array_equal(v[:, 0], part.sum(axis=0))
