@@ -595,3 +595,36 @@ def test_layer_with_identity_projections_reduces_to_the_attention():
     np.testing.assert_array_equal(gate, 0.5)
     out, _, _ = oracle.prefill(cfg, xh, xh, xh, np.full((H, N), 0.5))
     np.testing.assert_allclose(y[0], out.transpose(1, 0, 2).reshape(N, dm), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("w,n_tokens", [
+    (wl.TINY_FP32, None),
+    (wl.FIXED_8K, 2048),
+    (wl.SQRT_8K, 2048),
+    (wl.LONG_64K, 3072),
+], ids=lambda x: getattr(x, "name", str(x)))
+def test_oracle_matches_bruteforce_on_the_workload_shapes(w, n_tokens):
+    """The brute force and the C oracle on the workloads' own shapes and key
+    structure (head dim 64, RoPE on 32 dims, their chunk, window, sinks and
+    schedule; the large ones truncated to their first tokens, one head each):
+    assignments exactly, outputs and sums to rounding."""
+    N = w.N if n_tokens is None else n_tokens
+    q, k, v, g = wl.prefill_inputs(w.with_(B=1, H=min(w.H, 2)))
+    heads = range(q.shape[1]) if n_tokens is None else [0]
+    cfg = oracle.OracleConfig(head_dim=w.d, rope_dims=w.rope_dims, chunk=w.chunk, window=w.window,
+                              n_sinks=w.n_sinks, sched=w.sched, max_slots=w.max_slots,
+                              coef=w.coef, expo=w.expo)
+    for h in heads:
+        qh, kh, vh = (x[0, h, :N].astype(np.float64) for x in (q, k, v))
+        gh = g[0, h, :N].astype(np.float64)
+        out, st, dbg = _run(cfg, qh, kh, vh, gh)
+        bout, bst, bev = bf_prefill(qh, kh, vh, gh, C=w.chunk, W=w.window, S=w.n_sinks, r=w.rope_dims,
+                                    sched=w.sched, M=w.max_slots, coef=w.coef, expo=w.expo)
+        assert len(bev) == dbg["assign"].shape[0] > 0
+        for e, (a, kd) in enumerate(bev):
+            np.testing.assert_array_equal(dbg["assign"][e], a)
+            np.testing.assert_array_equal(dbg["kind"][e], kd)
+        np.testing.assert_allclose(out, bout, rtol=0, atol=1e-9)
+        assert st.n == bst.n
+        np.testing.assert_allclose(st.sum_k[:st.n], np.array(bst.sk), atol=1e-9)
+        np.testing.assert_array_equal(st.count[:st.n], bst.cnt)
