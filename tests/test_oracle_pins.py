@@ -628,3 +628,61 @@ def test_oracle_matches_bruteforce_on_the_workload_shapes(w, n_tokens):
         assert st.n == bst.n
         np.testing.assert_allclose(st.sum_k[:st.n], np.array(bst.sk), atol=1e-9)
         np.testing.assert_array_equal(st.count[:st.n], bst.cnt)
+
+
+def test_oracle_decoder_matches_bruteforce_on_the_decode_sweep_shape():
+    """Decode from an imported state (the decode sweep's shape: head dim 64, RoPE
+    on 32 dims, W 512, C 128, 16 sinks, a full fixed state of 256 slots), over 130
+    steps that cross two chunk boundaries: the oracle's decoder against a brute
+    force built from the independent restatement (fold, read view, complex RoPE,
+    torch softmax)."""
+    from bruteforce import BFState, bf_fold, bf_view
+    from compressed_kv_state_gb300.workloads import DecodeWorkload, decode_inputs
+    dw = DecodeWorkload("dec_pin", B=1, H=1, n_slots=256, steps=130)
+    state, (wk, wv, wg), (q, k, v, g) = decode_inputs(dw)
+    d, r, C, W, S, n = dw.d, dw.rope_dims, dw.chunk, dw.window, dw.n_sinks, dw.n_slots
+    cfg = oracle.OracleConfig(head_dim=d, rope_dims=r, chunk=C, window=W, n_sinks=S, sched=0,
+                              max_slots=n)
+    ost = oracle.OracleState(cfg)
+    ost.n, ost.t = n, state["t"]
+    ost.sum_k[:n] = state["sum_k"][0, 0]
+    ost.sum_v[:n] = state["sum_v"][0, 0]
+    ost.count[:n] = state["counts"][0, 0]
+    ost.rho[:n] = state["rho"][0, 0]
+    dec = oracle.OracleDecoder(cfg, ost, state["pos"], wk[0, 0], wv[0, 0], wg[0, 0])
+
+    bst = BFState()
+    bst.sk = [np.array(x, np.float64) for x in state["sum_k"][0, 0]]
+    bst.sv = [np.array(x, np.float64) for x in state["sum_v"][0, 0]]
+    bst.cnt = [int(x) for x in state["counts"][0, 0]]
+    bst.rho = [float(x) for x in state["rho"][0, 0]]
+    bst.t = state["t"]
+    win_k = [np.array(x, np.float64) for x in wk[0, 0]]
+    win_v = [np.array(x, np.float64) for x in wv[0, 0]]
+    win_g = [float(x) for x in wg[0, 0]]
+    pos = state["pos"]
+    for s in range(dw.steps):
+        p = pos + s
+        c = p // C
+        if p % C == 0 and c >= W // C + 1:
+            first = (c - W // C - 1) * C
+            bf_fold(bst, first, np.stack(win_k[:C]), np.stack(win_v[:C]), np.array(win_g[:C]),
+                    S=S, sched=0, M=n, coef=4.0, expo=0.5, eps=1e-5, C=C, r=r)
+            del win_k[:C], win_v[:C], win_g[:C]
+        qs, ks, vs, gs = (np.array(x[s, 0, 0], np.float64) for x in (q, k, v, g))
+        win_k.append(ks)
+        win_v.append(vs)
+        win_g.append(float(gs))
+        kh, vh = bf_view(bst, r, 1e-5)
+        w_first = p - len(win_k) + 1
+        assert w_first == max(0, (c - W // C) * C)
+        pos_w = np.arange(w_first, p + 1)
+        kr = rope_complex(np.stack(win_k), pos_w, r, 1e4)
+        qr = rope_complex(qs[None], np.array([p]), r, 1e4)[0]
+        sc = np.concatenate([kh @ qs, kr @ qr]) / math.sqrt(d)
+        wts = torch.softmax(torch.as_tensor(sc), 0).numpy()
+        want = wts @ np.concatenate([vh, np.stack(win_v)])
+        got = dec.step(q[s, 0, 0], k[s, 0, 0], v[s, 0, 0], g[s, 0, 0])
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-10, err_msg=f"step {s}")
+    assert dec.st.n == len(bst.sk) == n
+    np.testing.assert_array_equal(dec.st.count[:n], bst.cnt)
