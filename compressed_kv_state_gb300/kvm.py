@@ -226,6 +226,31 @@ def make_config(*, batch, heads, head_dim=64, rope_dims=32, rope_theta=10000.0, 
                       max_slots, coef, expo, ln_eps, dtype, max_tokens, flags)
 
 
+def state_spec(cfg: kvm_config) -> dict:
+    """Shape and torch dtype of every state buffer of kvm_state_bufs (include/kvm.h)."""
+    import torch
+    B, H, M, d, L = cfg.batch, cfg.heads, cfg.max_slots, cfg.head_dim, cfg.window + cfg.chunk
+    io = torch.bfloat16 if cfg.dtype == KVM_BF16 else torch.float32
+    return dict(sum_k=((B, H, M, d), torch.float32), sum_v=((B, H, M, d), torch.float32),
+                counts=((B, H, M), torch.int32), rho=((B, H, M), torch.float32),
+                ring_k=((B, H, L, d), io), ring_v=((B, H, L, d), io), ring_g=((B, H, L), torch.float32))
+
+
+def check_state_tensors(cfg: kvm_config, t: dict, require_cuda: bool = True) -> None:
+    """Raise ValueError unless t holds every state buffer with the layer's shape and
+    dtype, contiguous (and on a CUDA device): the library copies fixed byte counts
+    from and to these pointers."""
+    for name, (shape, dtype) in state_spec(cfg).items():
+        x = t.get(name)
+        if x is None or not hasattr(x, "data_ptr"):
+            raise ValueError(f"state buffer {name!r} missing")
+        if tuple(x.shape) != shape or x.dtype != dtype or not x.is_contiguous():
+            raise ValueError(f"state buffer {name!r}: expected contiguous {dtype} {shape}, got "
+                             f"{x.dtype} {tuple(x.shape)}")
+        if require_cuda and not x.is_cuda:
+            raise ValueError(f"state buffer {name!r} must be on a CUDA device")
+
+
 class KvmLayer:
     """Owns one layer handle and its device workspace (a torch uint8 tensor)."""
 
@@ -274,15 +299,8 @@ class KvmLayer:
     def state_buffers(self, device="cuda"):
         """Fresh caller-owned tensors shaped for export/import."""
         import torch
-        c = self.cfg
-        B, H, M, d, L = c.batch, c.heads, c.max_slots, c.head_dim, c.window + c.chunk
-        return dict(sum_k=torch.zeros(B, H, M, d, device=device),
-                    sum_v=torch.zeros(B, H, M, d, device=device),
-                    counts=torch.zeros(B, H, M, dtype=torch.int32, device=device),
-                    rho=torch.zeros(B, H, M, device=device),
-                    ring_k=torch.zeros(B, H, L, d, dtype=self.io_dtype, device=device),
-                    ring_v=torch.zeros(B, H, L, d, dtype=self.io_dtype, device=device),
-                    ring_g=torch.zeros(B, H, L, device=device))
+        return {name: torch.zeros(shape, dtype=dtype, device=device)
+                for name, (shape, dtype) in state_spec(self.cfg).items()}
 
     @staticmethod
     def _bufs(t, n_slots=0, n_overflow=0, pos=0) -> kvm_state_bufs:
@@ -292,12 +310,14 @@ class KvmLayer:
 
     def export_state(self, stream=None):
         t = self.state_buffers(self.ws.device)
+        check_state_tensors(self.cfg, t)
         b = self._bufs(t)
         kvm_state_export(self.handle, b, stream)
         t.update(n_slots=b.n_slots, n_overflow=b.n_overflow, pos=b.pos)
         return t
 
     def import_state(self, t, stream=None):
+        check_state_tensors(self.cfg, t)
         b = self._bufs(t, t["n_slots"], t["n_overflow"], t["pos"])
         kvm_state_import(self.handle, b, stream)
 

@@ -153,3 +153,27 @@ def test_overlap_and_forward_entry_points_reject_null_layers(kvm):
     assert kvm.lib.kvm_layer_get_overlap(None, ctypes.byref(n)) == kvm.KVM_ERR_INVALID_ARG
     assert kvm.lib.kvm_layer_forward(None, 128, None, None, None, 1, None, None, 0, None) == \
         kvm.KVM_ERR_INVALID_ARG
+
+
+def test_state_buffers_are_checked_before_the_library_copies_them(kvm):
+    """The binding rejects state tensors whose size, type or layout differs from
+    what kvm_state_export / kvm_state_import copy (fixed byte counts)."""
+    import torch
+    cfg = kvm.make_config(batch=2, heads=3, chunk=64, window=128, max_slots=40)
+    spec = kvm.state_spec(cfg)
+    assert spec["sum_k"][0] == (2, 3, 40, 64) and spec["ring_k"][0] == (2, 3, 192, 64)
+    assert spec["ring_k"][1] == torch.bfloat16 and spec["counts"][1] == torch.int32
+    good = {n: torch.zeros(s, dtype=d) for n, (s, d) in spec.items()}
+    kvm.check_state_tensors(cfg, good, require_cuda=False)
+    bad_cases = [
+        ("sum_k", torch.zeros(2, 3, 39, 64)),                         # too few slots
+        ("counts", torch.zeros(2, 3, 40, dtype=torch.int64)),          # wrong type
+        ("ring_k", torch.zeros(2, 3, 64, 192, dtype=torch.bfloat16).transpose(2, 3)),  # strided
+    ]
+    for name, t in bad_cases:
+        with pytest.raises(ValueError):
+            kvm.check_state_tensors(cfg, dict(good, **{name: t}), require_cuda=False)
+    with pytest.raises(ValueError):
+        kvm.check_state_tensors(cfg, {k: v for k, v in good.items() if k != "rho"}, require_cuda=False)
+    with pytest.raises(ValueError):
+        kvm.check_state_tensors(cfg, good)  # CPU tensors where device memory is required
