@@ -46,3 +46,25 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.job_throughput(1000, 1, 1.0) == pytest.approx(1e6)
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    """Under torchrun the reference arm (the oracle on the host cores) runs and
+    prints on rank 0; the other ranks exit 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+           "--steps", "1", "--warmup", "1"]
+    env1 = dict(os.environ, RANK="1", LOCAL_RANK="1", WORLD_SIZE="2")
+    r1 = subprocess.run(cmd, env=env1, capture_output=True, text=True, timeout=300)
+    assert r1.returncode == 0 and r1.stdout.strip() == ""
+    env0 = dict(os.environ, RANK="0", LOCAL_RANK="0", WORLD_SIZE="2")
+    r0 = subprocess.run(cmd, env=env0, capture_output=True, text=True, timeout=300)
+    assert r0.returncode == 0, r0.stderr
+    lines = [l for l in r0.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["config"]["workload"] == "fixed256_B8H12N8192"
