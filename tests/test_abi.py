@@ -177,3 +177,17 @@ def test_state_buffers_are_checked_before_the_library_copies_them(kvm):
         kvm.check_state_tensors(cfg, {k: v for k, v in good.items() if k != "rho"}, require_cuda=False)
     with pytest.raises(ValueError):
         kvm.check_state_tensors(cfg, good)  # CPU tensors where device memory is required
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No fallback: importing the binding without libkvm.so raises (run in a fresh
+    interpreter against a copy of the package whose library is absent)."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = os.path.join(ROOT, "compressed_kv_state_gb300")
+    dst = tmp_path / "compressed_kv_state_gb300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("lib", "__pycache__", "csrc"))
+    r = subprocess.run([sys.executable, "-c", "import compressed_kv_state_gb300.kvm"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0 and "libkvm.so not built" in r.stderr
