@@ -130,3 +130,68 @@ def compare_event_teacher_forced(w, st_before, first_pos, k, v, g, gpu_assign, g
                         f"{r['kind'][toks].tolist()} gaps {r['gap'][toks].tolist()}")
         n_ex = len(toks)
     return r, n_ex
+
+
+def chain_with_resync(w, layer, inputs, dbg, heads, max_resyncs=None):
+    """Compare every fold event of the sampled heads' chains, GPU against the
+    oracle, event by event.  The oracle folds from its own state; where the two
+    disagree (which must be a near tie, else AssertionError), the oracle's state
+    is replaced by the GPU's exported state after that event, so a near-tie flip
+    cannot cascade and every later event is still checked exactly.
+
+    Returns {(b, h): dict(first_divergent_event, exempt_events, exempt_tokens)}.
+    """
+    q, k, v, g = inputs
+    ocfg = oracle_cfg(w)
+    C, Wc = w.chunk, w.window // w.chunk
+    E = oracle.n_events(ocfg, w.N)
+    if max_resyncs is None:
+        max_resyncs = max(2, E // 10)
+    gpu_states = {}
+
+    def gpu_state_after(e):
+        if e not in gpu_states:
+            _, _, st = gpu_prefill(layer, w, q, k, v, g, n_tokens=min(w.N, (e + Wc + 2) * C),
+                                   debug=False)
+            gpu_states[e] = st
+        return gpu_states[e]
+
+    res = {}
+    for b, h in heads:
+        st = oracle.OracleState(ocfg)
+        first, ex_events, ex_tokens = None, 0, 0
+        for e in range(E):
+            sl = slice(e * C, (e + 1) * C)
+            r = oracle.fold_event(ocfg, st, e * C, k[b, h, sl], v[b, h, sl], g[b, h, sl])
+            ga, gk = dbg["assign"][b, h, e], dbg["kind"][b, h, e]
+            bad = (ga != r["assign"]) | (gk != r["kind"])
+            if not bad.any():
+                continue
+            toks = np.nonzero(bad)[0]
+            exempt = r["sel_margin"] < NEAR_TIE or all(
+                r["kind"][t] == oracle.MERGED and r["gap"][t] < NEAR_TIE for t in toks)
+            assert exempt, (f"(b={b}, h={h}) event {e}: tokens {toks.tolist()} gpu "
+                            f"{ga[toks].tolist()}/{gk[toks].tolist()} oracle "
+                            f"{r['assign'][toks].tolist()}/{r['kind'][toks].tolist()} gaps "
+                            f"{r['gap'][toks].tolist()} sel_margin {r['sel_margin']}")
+            first = e if first is None else first
+            ex_events += 1
+            ex_tokens += len(toks)
+            assert ex_events <= max_resyncs, f"(b={b}, h={h}): more than {max_resyncs} near-tie events"
+            st = state_to_oracle(w, gpu_state_after(e), b, h)
+        res[(b, h)] = dict(first_divergent_event=first, exempt_events=ex_events,
+                           exempt_tokens=ex_tokens)
+    return res
+
+
+# ------------------------------------------------------------ near-tie report
+#
+# The parity tests record, per workload, how many tokens and events were exempt
+# as near ties and where the first divergence fell; the session writes them to
+# tests/reports/near_ties.json (the GPU run regenerates it).
+
+REPORT = {}
+
+
+def report_near_ties(workload: str, entry: dict):
+    REPORT.setdefault(workload, []).append(entry)
