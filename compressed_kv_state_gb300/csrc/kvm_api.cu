@@ -117,6 +117,37 @@ Layout layout_of(const kvm_config& c) {
 }
 
 }  // namespace host
+
+namespace {
+struct RopeFreqs {
+    int half;
+    double f[32];  // theta^(-2i/r), computed on the host in double
+};
+
+// cos/sin of p * theta^(-2i/r), evaluated in double precision, stored as float2
+__global__ void rope_table_kernel(const RopeFreqs fr, int64_t n_pos, float2* out) {
+    const int64_t total = n_pos * fr.half;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t p = i / fr.half;
+        const int x = (int)(i % fr.half);
+        const double ang = (double)p * fr.f[x];
+        out[i] = make_float2((float)cos(ang), (float)sin(ang));
+    }
+}
+}  // namespace
+
+cudaError_t launch_rope_table(int rope_dims, float rope_theta, int64_t n_pos, float2* out, cudaStream_t s) {
+    RopeFreqs fr;
+    fr.half = rope_dims / 2;
+    if (fr.half <= 0 || n_pos <= 0) return cudaSuccess;
+    if (fr.half > 32) return cudaErrorInvalidValue;
+    for (int i = 0; i < fr.half; ++i) fr.f[i] = std::pow((double)rope_theta, -2.0 * i / (double)rope_dims);
+    const int64_t total = n_pos * fr.half;
+    const int blocks = (int)((total + 255) / 256 < 1024 ? (total + 255) / 256 : 1024);
+    rope_table_kernel<<<blocks, 256, 0, s>>>(fr, n_pos, out);
+    return cudaGetLastError();
+}
+
 }  // namespace kvm
 
 using kvm::host::capacity;
@@ -254,17 +285,10 @@ kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t b
         n = ly->sched[ev].n_after;
         t += cfg->chunk;
     }
-    // RoPE table: angle p * theta^(-2i/r) for pair i, computed in double
-    const int half = cfg->rope_dims / 2;
-    std::vector<float2> rope((size_t)cfg->max_tokens * half + 2);
-    for (int64_t p = 0; p < cfg->max_tokens; ++p)
-        for (int i = 0; i < half; ++i) {
-            const double f = std::pow((double)cfg->rope_theta, -2.0 * i / (double)cfg->rope_dims);
-            const double ang = (double)p * f;
-            rope[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
-        }
-    e = cudaMemcpy(ly->ws + L.rope, rope.data(), (size_t)cfg->max_tokens * half * sizeof(float2),
-                   cudaMemcpyHostToDevice);
+    // RoPE table: angle p * theta^(-2i/r) for pair i, computed in double on the device
+    e = kvm::launch_rope_table(cfg->rope_dims, cfg->rope_theta, cfg->max_tokens,
+                               reinterpret_cast<float2*>(ly->ws + L.rope), nullptr);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
     if (e == cudaSuccess)
         e = cudaMemcpy(ly->ws + L.sched, ly->sched.data(), ly->sched.size() * sizeof(Sched),
                        cudaMemcpyHostToDevice);

@@ -228,5 +228,10 @@ cudaError_t launch_ring_fill(const RingFillArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_rope_keys(const RopeKeysArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_tc(const GemmSpec& g, cudaStream_t s);
 cudaError_t launch_renorm(const RenormArgs& a, bool bf16, cudaStream_t s);
+// RoPE table [n_pos, r/2] of (cos, sin) of p * theta^(-2i/r), built on the device
+// (angles and their cosine and sine in double precision, stored as float): every
+// entry point that needs the table builds it with this one kernel, so their
+// tables are identical bit for bit.
+cudaError_t launch_rope_table(int rope_dims, float rope_theta, int64_t n_pos, float2* out, cudaStream_t s);
 
 }  // namespace kvm

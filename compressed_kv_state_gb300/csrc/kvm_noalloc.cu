@@ -43,22 +43,6 @@ __global__ void sched_upload_kernel(const SchedUpload u, kvm::Sched* dst) {
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < u.n; i += gridDim.x * blockDim.x) dst[i] = u.s[i];
 }
 
-struct RopeFreqs {
-    int half;
-    double f[32];
-};
-
-// cos/sin of p * theta^(-2i/r), evaluated in double precision, stored as float2
-__global__ void rope_table_kernel(const RopeFreqs fr, int64_t n_pos, float2* out) {
-    const int64_t total = n_pos * fr.half;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t p = i / fr.half;
-        const int x = (int)(i % fr.half);
-        const double ang = (double)p * fr.f[x];
-        out[i] = make_float2((float)cos(ang), (float)sin(ang));
-    }
-}
-
 // Device address of the static array on the current device (looked up once per device).
 cudaError_t scratch_address(void** out) {
     int dev = 0;
@@ -106,6 +90,29 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         g_err = "q, k, v, gate and out must be non-NULL";
         return KVM_ERR_INVALID_ARG;
     }
+    // every buffer must be device memory of the current device (the one whose
+    // scratch array and stream this call uses); cudaPointerGetAttributes allocates nothing
+    {
+        int dev = -1;
+        cudaError_t de = cudaGetDevice(&dev);
+        if (de != cudaSuccess) {
+            g_err = std::string("kvm_prefill_noalloc: cudaGetDevice: ") + cudaGetErrorString(de);
+            return KVM_ERR_CUDA;
+        }
+        const void* ptrs[5] = {q, k, v, gate, out};
+        const char* names[5] = {"q", "k", "v", "gate", "out"};
+        for (int i = 0; i < 5; ++i) {
+            cudaPointerAttributes at;
+            const cudaError_t pe = cudaPointerGetAttributes(&at, ptrs[i]);
+            if (pe != cudaSuccess) cudaGetLastError();
+            if (pe != cudaSuccess ||
+                (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) || at.device != dev) {
+                g_err = std::string("kvm_prefill_noalloc: ") + names[i] +
+                        " is not device memory of the current device " + std::to_string(dev);
+                return KVM_ERR_INVALID_ARG;
+            }
+        }
+    }
     const int64_t E = n_events_for(c, n_tokens);
     if (E > MAX_EVENTS) {
         g_err = "kvm_prefill_noalloc: at most 1024 fold events per call";
@@ -123,10 +130,6 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         g_err = "growth schedule exceeds max_slots for this n_tokens";
         return KVM_ERR_CAPACITY;
     }
-    RopeFreqs fr;
-    fr.half = c.rope_dims / 2;
-    for (int i = 0; i < fr.half; ++i) fr.f[i] = std::pow((double)c.rope_theta, -2.0 * i / (double)c.rope_dims);
-
     void* base = nullptr;
     cudaError_t e = scratch_address(&base);
     if (e != cudaSuccess) {
@@ -147,12 +150,8 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         sched_upload_kernel<<<1, 256, 0, s>>>(up, reinterpret_cast<kvm::Sched*>(ws + L.sched));
         e = cudaGetLastError();
     }
-    if (e == cudaSuccess && fr.half > 0) {
-        const int64_t total = n_tokens * fr.half;
-        const int blocks = (int)((total + 255) / 256 < 1024 ? (total + 255) / 256 : 1024);
-        rope_table_kernel<<<blocks, 256, 0, s>>>(fr, n_tokens, reinterpret_cast<float2*>(ws + L.rope));
-        e = cudaGetLastError();
-    }
+    if (e == cudaSuccess)
+        e = kvm::launch_rope_table(c.rope_dims, c.rope_theta, n_tokens, reinterpret_cast<float2*>(ws + L.rope), s);
     if (e == cudaSuccess && E > 0) {
         kvm::FoldArgs fa{};
         fa.sum_k = reinterpret_cast<float*>(ws + L.sum_k);

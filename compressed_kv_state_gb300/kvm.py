@@ -202,8 +202,34 @@ def kvm_layer_get_overlap(layer) -> int:
 KVM_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 
-def kvm_prefill_noalloc(cfg: kvm_config, q, k, v, gate, n_tokens: int, out, stream=None):
-    """One-shot prefill with no allocation (scratch in the library's static device array)."""
+def check_prefill_tensors(cfg: kvm_config, q, k, v, gate, n_tokens: int, out) -> None:
+    """Raise ValueError unless q, k, v, out are contiguous [B, H, n_tokens, d] tensors
+    of the config's dtype and gate a contiguous fp32 [B, H, n_tokens] tensor, all on
+    the current CUDA device: the library reads and writes n_tokens rows through
+    these pointers."""
+    import torch
+    io = torch.bfloat16 if cfg.dtype == KVM_BF16 else torch.float32
+    n_tokens = int(n_tokens)
+    shp = (cfg.batch, cfg.heads, n_tokens, cfg.head_dim)
+    cur = torch.cuda.current_device() if torch.cuda.is_available() else None
+    for name, t, want, dt in (("q", q, shp, io), ("k", k, shp, io), ("v", v, shp, io),
+                              ("gate", gate, shp[:3], torch.float32), ("out", out, shp, io)):
+        if t is None or not hasattr(t, "data_ptr"):
+            raise ValueError(f"{name} must be a tensor")
+        if tuple(t.shape) != want or t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name}: expected contiguous {dt} {want}, got {t.dtype} "
+                             f"{tuple(t.shape)}")
+        if not t.is_cuda or t.device.index != cur:
+            raise ValueError(f"{name} must be on the current CUDA device (cuda:{cur})")
+
+
+def kvm_prefill_noalloc(cfg: kvm_config, q, k, v, gate, n_tokens: int, out, stream=None,
+                        check: bool = True):
+    """One-shot prefill with no allocation (scratch in the library's static device array).
+    The tensors are checked first (check=False passes raw pointers through, for
+    the library's own argument validation)."""
+    if check:
+        check_prefill_tensors(cfg, q, k, v, gate, n_tokens, out)
     st = lib.kvm_prefill_noalloc(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(gate),
                                  int(n_tokens), _ptr(out), _stream(stream))
     _check(st, None)

@@ -273,13 +273,18 @@ kvm_status kvm_layer_forward(kvm_layer* layer, int32_t d_model, const void* x, c
  * loop that cannot afford the device synchronisation an allocation implies.
  * Such callers cannot hand kvm_layer_create a workspace.
  *
- * Computes exactly what kvm_prefill computes into out (same kernels), for
- * q, k, v, out: dtype [B, H, n_tokens, d] and gate fp32 [B, H, n_tokens]
- * device buffers owned by the caller, but keeps no layer: nothing is left
- * for a later decode, export or debug record.  Its scratch (state, read-view
- * snapshots, RoPE and schedule tables) is a file-scope device array of
- * KVM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library holds
- * until the process exits.  A call whose scratch would exceed it (or that
+ * Computes what kvm_prefill computes into out, with the same kernels and the
+ * same RoPE and schedule tables, so the outputs are identical bit for bit,
+ * for q, k, v, out: dtype [B, H, n_tokens, d] and gate fp32 [B, H, n_tokens]
+ * buffers owned by the caller, but keeps no layer: nothing is left for a
+ * later decode, export or debug record.  The call runs on the CURRENT device
+ * (cudaGetDevice): every buffer must be device memory of that device, else
+ * KVM_ERR_INVALID_ARG before anything is enqueued.  Its scratch (state,
+ * read-view snapshots, RoPE and schedule tables) is a file-scope device array
+ * of KVM_NOALLOC_SCRATCH_BYTES bytes that every GPU loading this library
+ * holds until the process exits; with CUDA's lazy module loading the array
+ * may be reserved only when this library's device code is first used on the
+ * device (possibly this call).  A call whose scratch would exceed it (or that
  * would fold more than 1024 chunks) returns KVM_ERR_WORKSPACE with the
  * required size in kvm_last_error(NULL), before enqueuing anything.
  * The first call on a device looks up the array's device address (once per
@@ -288,7 +293,8 @@ kvm_status kvm_layer_forward(kvm_layer* layer, int32_t d_model, const void* x, c
  * start at zero; calls whose GPU work overlaps in time (several streams or
  * host threads) race on it and must be serialised by the caller.  Calls no
  * cudaMalloc, cudaFree or other allocating routine.  Errors are reported
- * through kvm_last_error(NULL); device-side status is not reported. */
+ * through kvm_last_error(NULL); device-side status (a bounded wait that
+ * expired) is not reported, and the outputs of such a call are undefined. */
 kvm_status kvm_prefill_noalloc(const kvm_config* cfg, const void* q, const void* k, const void* v,
                                const float* gate, int64_t n_tokens, void* out, void* cuda_stream);
 

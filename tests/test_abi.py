@@ -179,6 +179,32 @@ def test_state_buffers_are_checked_before_the_library_copies_them(kvm):
         kvm.check_state_tensors(cfg, good)  # CPU tensors where device memory is required
 
 
+def test_noalloc_tensors_are_checked_before_the_library_is_called(kvm, monkeypatch):
+    """kvm_prefill_noalloc's binding rejects tensors of the wrong shape, type, layout
+    or device (and n_tokens beyond them) with ValueError before calling the library."""
+    import torch
+    calls = []
+    monkeypatch.setattr(kvm, "lib", type("L", (), {"kvm_prefill_noalloc": lambda *a: calls.append(a) or 0})())
+    cfg = kvm.make_config(batch=1, heads=2, chunk=64, window=128, max_slots=24, max_tokens=300)
+    shp = (1, 2, 300, 64)
+    q, k, v, out = (torch.zeros(shp, dtype=torch.bfloat16) for _ in range(4))
+    g = torch.zeros(shp[:3])
+    cases = [
+        dict(q=torch.zeros(1, 2, 299, 64, dtype=torch.bfloat16)),        # wrong shape
+        dict(k=torch.zeros(shp)),                                        # wrong dtype
+        dict(v=torch.zeros(1, 2, 64, 300, dtype=torch.bfloat16).transpose(2, 3)),  # strided
+        dict(gate=torch.zeros(shp[:3], dtype=torch.bfloat16)),           # gate not fp32
+        dict(n_tokens=301),                                              # beyond the tensors
+        dict(),                                                          # CPU tensors
+    ]
+    for bad in cases:
+        a = dict(q=q, k=k, v=v, gate=g, n_tokens=300, out=out)
+        a.update(bad)
+        with pytest.raises(ValueError):
+            kvm.kvm_prefill_noalloc(cfg, a["q"], a["k"], a["v"], a["gate"], a["n_tokens"], a["out"])
+    assert not calls
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     """No fallback: importing the binding without libkvm.so raises (run in a fresh
     interpreter against a copy of the package whose library is absent)."""
