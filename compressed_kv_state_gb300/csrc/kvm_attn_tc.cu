@@ -20,8 +20,11 @@
 //   warp 1     tensor-memory owner and MMA issuer (one thread):
 //              S = Q K^T into one of two 64-column TMEM S buffers, issued for
 //              block j+1 before O += P V of block j (O: 64 columns)
-//   warps 2-3  RoPE: rotate the Q tile and every window K block in shared
-//              memory (128-byte swizzled rows), then hand them to the MMA
+//   warps 2-3  RoPE: rotate the Q tile in shared memory (128-byte swizzled
+//              rows) and hand it to the MMA; window keys normally arrive
+//              already rotated (k_rot, rotated once per key by
+//              rope_keys_kernel), and only without that copy do these warps
+//              rotate each window K block as well
 //   warps 4-7  softmax: thread i owns query row i (= TMEM lane i); one pass
 //              over the 64-column S row, lazy rescaling of O (only when the
 //              running maximum grows by more than 2^8), P written to shared

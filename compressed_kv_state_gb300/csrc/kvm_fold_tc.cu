@@ -329,11 +329,18 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t sK = smem_u32(sm + OFF_K), sV = smem_u32(sm + OFF_V);
     const uint32_t sUH = smem_u32(sm + OFF_UHI), sUL = smem_u32(sm + OFF_ULO);
     const uint32_t bar_s = smem_u32(&X.bar_s);
+    // thread 0's record of asynchronous work it issued that no wait has seen
+    // complete yet (phase parity, or -1): drained before the CTA releases its
+    // tensor memory after an abort
+    int pend_st = -1, pend_ld[2] = {-1, -1}, pend_mma = -1;
 
     {
         float x[64];
         if (nblk_st > 0) {
-            if (tid == 0 && !mbar_wait(smem_u32(&X.bar_st), 0, &X.abort_flag, a.status)) X.abort_flag = 1;
+            if (tid == 0 && !mbar_wait(smem_u32(&X.bar_st), 0, &X.abort_flag, a.status)) {
+                X.abort_flag = 1;
+                pend_st = 0;
+            }
             __syncthreads();
         }
         const uint8_t* stage = sm + (vside ? OFF_VK : OFF_UHI);
@@ -382,6 +389,7 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_after();
 
     auto load_chunk = [&](int e, int buf) {
+        pend_ld[buf] = ((e - a.e_begin) >> 1) & 1;
         const int64_t off = ((int64_t)e * C) % a.src_len;
         mbar_expect_tx(smem_u32(&X.bar_k[buf]), 2 * TOK * ROWB);
         tma_load_3d(sK + buf * TOK * ROWB, &tm_k, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
@@ -406,6 +414,7 @@ __global__ void __launch_bounds__(NT, 1)
         // read after its last barrier, so the set-up below needs no barrier first);
         // a failed wait is carried to the next barrier, which all threads leave together
         bool fail = !mbar_wait(smem_u32(&X.bar_k[buf]), (it >> 1) & 1, &X.abort_flag, a.status);
+        if (!fail) pend_ld[buf] = -1;
         if (e + 1 < a.e_end) {
             sc_nx = a.sched ? a.sched[e + 1] : a.sched0;
             if (tid < C) g_nx = a.g_src[(int64_t)bh * a.src_row + ((int64_t)(e + 1) * C) % a.src_len + tid];
@@ -431,6 +440,7 @@ __global__ void __launch_bounds__(NT, 1)
                         mma_bf16_ss(tmem + 256, ad, bd, idesc, (ks | part) ? 1u : 0u);
                     }
                 mma_commit(bar_s);
+                pend_mma = mma_count & 1;
             }
             // the next chunk's keys and values load while this event runs
             if (e + 1 < a.e_end) load_chunk(e + 1, buf ^ 1);
@@ -458,6 +468,7 @@ __global__ void __launch_bounds__(NT, 1)
         // the CTA scans 64 slot columns of every token row (token = TMEM lane)
         if (do_mma) {
             fail = fail || !mbar_wait(bar_s, mma_count & 1, &X.abort_flag, a.status);
+            if (!fail) pend_mma = -1;
             KVM_PROBE_LAP(9)
             ++mma_count;
             tc_fence_after();
@@ -753,13 +764,22 @@ __global__ void __launch_bounds__(NT, 1)
     }
     KVM_PROBE_LAP(10)
     if (tid == 0) KVM_PROBE_FLUSH(g_probe_fold, 0, 13)
+    // after an abort: let the copies and MMAs this CTA issued land before its shared
+    // and tensor memory are released (each wait bounded; they depend on nothing else)
+    if (tid == 0 && X.abort_flag) {
+        auto drain = [&](uint32_t bar, int parity) {
+            if (parity < 0) return;
+            const long long t0 = clock64();
+            while (!mbar_try(bar, (uint32_t)parity) && clock64() - t0 < (1ll << 28)) {
+            }
+        };
+        drain(smem_u32(&X.bar_st), pend_st);
+        drain(smem_u32(&X.bar_k[0]), pend_ld[0]);
+        drain(smem_u32(&X.bar_k[1]), pend_ld[1]);
+        drain(bar_s, pend_mma);
+    }
     tc_fence_before();
     __syncthreads();
-    if (X.abort_flag) {
-        const long long t0 = clock64();
-        while (clock64() - t0 < (1ll << 22)) {
-        }
-    }
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
