@@ -10,6 +10,11 @@ folded chunks beside them.  A second, untimed-for-the-headline pass runs the
 sequential prefill to report each kernel's own duration.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload fixed8k|sqrt8k|long64k]
+
+--workload picks the headline prefill workload (default fixed8k, the line the
+metric is quoted on); the other two prefill workloads (sqrt-growth 8k, 64k long
+prefill) are timed in the same run and reported under "workloads".
 
 Under torchrun (N > 1) every rank runs its own copy of the workload on its
 GPU (the (batch, head) rows are independent: no collective on the data path),
@@ -36,6 +41,7 @@ from compressed_kv_state_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "KVM layer prefill tokens/s @8k (1 GB300)"
 UNIT = "tokens/s"
+PREFILL = {"fixed8k": wl.FIXED_8K, "sqrt8k": wl.SQRT_8K, "long64k": wl.LONG_64K}
 W = wl.FIXED_8K
 
 
@@ -188,22 +194,34 @@ def _ncu_traffic(kernel_file):
 
 # ------------------------------------------------------------- CPU oracle
 
+def _oracle_cfg(w):
+    import oracle
+    return oracle.OracleConfig(head_dim=w.d, rope_dims=w.rope_dims, chunk=w.chunk,
+                               window=w.window, n_sinks=w.n_sinks, sched=w.sched,
+                               max_slots=w.max_slots, coef=w.coef, expo=w.expo)
+
+
+def _sample_workload(w, rows):
+    """The bounded CPU sample of a workload: `rows` full-length (batch, head) rows,
+    drawn as a workload of batch 1 and `rows` heads with the same recipe."""
+    return w.with_(B=1, H=rows, name=f"{w.name}[sample B1H{rows}]")
+
+
 def cpu_oracle_sample(w, heads_per_thread=1, one_thread=True):
     """Time the fp64 oracle on a bounded sample of the workload: one full-length
-    (batch, head) row per host core, all cores in parallel.  Returns tokens/s in
-    the layer's unit (a layer token needs all H heads)."""
+    (batch, head) row per host core, all cores in parallel.  Returns (record,
+    sample) where record's value is tokens/s in the layer's unit (a layer token
+    needs all H heads) and sample = (sample workload, oracle debug record)."""
     import oracle
     oracle.build()
     cores = len(os.sched_getaffinity(0))
     nh = min(w.B * w.H, cores * heads_per_thread)
-    sub = w.with_(B=1, H=nh) if nh <= w.H else w
-    q, k, v, g = wl.prefill_inputs(sub.with_(B=1, H=min(nh, sub.H)))
+    sub = _sample_workload(w, nh)
+    q, k, v, g = wl.prefill_inputs(sub)
     q, k, v, g = q[0], k[0], v[0], g[0]
-    ocfg = oracle.OracleConfig(head_dim=w.d, rope_dims=w.rope_dims, chunk=w.chunk,
-                               window=w.window, n_sinks=w.n_sinks, sched=w.sched,
-                               max_slots=w.max_slots, coef=w.coef, expo=w.expo)
+    ocfg = _oracle_cfg(w)
     t0 = time.perf_counter()
-    oracle.prefill(ocfg, q, k, v, g, threads=cores)
+    _, _, odbg = oracle.prefill(ocfg, q, k, v, g, threads=cores)
     dt = time.perf_counter() - t0
     layer_tokens = w.N * q.shape[0] / w.H
     r = dict(value=layer_tokens / dt, unit=UNIT, cores=min(cores, q.shape[0]), kind="oracle",
@@ -216,7 +234,56 @@ def cpu_oracle_sample(w, heads_per_thread=1, one_thread=True):
         dt1 = time.perf_counter() - t1
         r["one_thread"] = {"value": w.N / w.H / dt1, "unit": UNIT, "cores": 1,
                            "sample": f"1 (batch, head) row x {w.N} tokens, {dt1:.1f} s wall"}
-    return r
+    return r, (sub, odbg)
+
+
+NEAR_TIE = 1e-5
+
+
+def near_tie_counts(sub, odbg, dev):
+    """Fold decisions of the GPU against the oracle on the CPU sample's rows (the
+    same seeded inputs, one GPU prefill with a debug record): per row the first
+    event where they differ (if any), and whether every differing token there is
+    a near tie (oracle top-2 cosine gap, or the event's surprise selection margin,
+    below 1e-5).  Counts only; nothing is asserted here."""
+    import torch
+    import oracle
+    from compressed_kv_state_gb300 import kvm
+    q, k, v, g = wl.prefill_inputs(sub)
+    E = oracle.n_events(_oracle_cfg(sub), sub.N)
+    layer = kvm.KvmLayer(layer_config(kvm, sub), device=dev)
+    shp = (sub.B, sub.H, max(E, 1), sub.chunk)
+    assign = torch.full(shp, -7, dtype=torch.int32, device=dev)
+    kind = torch.full(shp, -7, dtype=torch.int32, device=dev)
+    dbg = kvm.kvm_debug(assign.data_ptr(), kind.data_ptr(), None, None, E)
+    t = lambda a: torch.from_numpy(a).to(dev)
+    layer.prefill(t(q).bfloat16(), t(k).bfloat16(), t(v).bfloat16(), t(g), dbg=dbg)
+    layer.sync()
+    ga, gk = assign.cpu().numpy()[0], kind.cpu().numpy()[0]
+    layer.close()
+    rows = []
+    for h in range(sub.H):
+        first, n_tok, near = None, 0, True
+        for e in range(E):
+            bad = (ga[h, e] != odbg["assign"][h, e]) | (gk[h, e] != odbg["kind"][h, e])
+            if bad.any():
+                toks = np.nonzero(bad)[0]
+                first, n_tok = e, len(toks)
+                near = bool(odbg["sel_margin"][h, e] < NEAR_TIE or all(
+                    odbg["kind"][h, e, t] == oracle.MERGED and odbg["gap"][h, e, t] < NEAR_TIE
+                    for t in toks))
+                break
+        rows.append((first, n_tok, near))
+    div = [r for r in rows if r[0] is not None]
+    return {"rows": sub.H, "events_per_row": E, "rows_identical": len(rows) - len(div),
+            "rows_diverged": len(div),
+            "first_divergent_events": sorted(r[0] for r in div),
+            "tokens_differing_at_first_divergence": sum(r[1] for r in div),
+            "all_divergences_near_ties": all(r[2] for r in div),
+            "sample": sub.name,
+            "rule": "assignments and kinds compared event by event from event 0; a row stops "
+                    "at its first differing event; near tie = oracle top-2 gap (or surprise "
+                    "selection margin) < 1e-5"}
 
 
 # ------------------------------------------------------------- multi-rank
@@ -239,35 +306,34 @@ def job_throughput(tokens_per_rank: int, world: int, ms_per_step: float) -> floa
 
 # ------------------------------------------------------------------ ours
 
-def run_ours(args, rank, world, local_rank):
+def layer_config(kvm, w):
+    return kvm.make_config(batch=w.B, heads=w.H, rope_dims=w.rope_dims, chunk=w.chunk,
+                           window=w.window, n_sinks=w.n_sinks, sched=w.sched,
+                           max_slots=w.max_slots, coef=w.coef, expo=w.expo, max_tokens=w.N)
+
+
+def time_prefill(w, dev, stream, steps, warmup, segments, world=1):
+    """Device-resident prefill of workload w: warm-up, then `steps` prefills
+    between CUDA events on the launch stream (barrier and synchronize on both
+    sides), then a sequential pass that times each kernel on its own."""
     import torch
     from compressed_kv_state_gb300 import kvm
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    q, k, v, g = wl.prefill_inputs(W)
+    q, k, v, g = wl.prefill_inputs(w)
     dq = torch.from_numpy(q).to(dev).bfloat16()
     dk = torch.from_numpy(k).to(dev).bfloat16()
     dv = torch.from_numpy(v).to(dev).bfloat16()
     dg = torch.from_numpy(g).to(dev)
-    cfg = kvm.make_config(batch=W.B, heads=W.H, rope_dims=W.rope_dims, chunk=W.chunk,
-                          window=W.window, n_sinks=W.n_sinks, sched=W.sched,
-                          max_slots=W.max_slots, max_tokens=W.N)
-    layer = kvm.KvmLayer(cfg, device=dev)
+    layer = kvm.KvmLayer(layer_config(kvm, w), device=dev)
     out = torch.empty_like(dq)
-    stream = torch.cuda.current_stream(dev)
 
     def step():
-        kvm.kvm_prefill(layer.handle, dq, dk, dv, dg, W.N, out, stream)
+        kvm.kvm_prefill(layer.handle, dq, dk, dv, dg, w.N, out, stream)
 
-    kvm.kvm_layer_set_overlap(layer.handle, args.segments)
-    for _ in range(args.warmup):
+    kvm.kvm_layer_set_overlap(layer.handle, segments)
+    for _ in range(warmup):
         step()
     layer.sync()
-    segments = kvm.kvm_layer_get_overlap(layer.handle)
-    clocks = Clocks(local_rank)
-    clocks.start()
-    time.sleep(0.3)
+    used_segments = kvm.kvm_layer_get_overlap(layer.handle)
     kvm.kvm_layer_set_timing(layer.handle, True)
     if world > 1:
         import torch.distributed as dist
@@ -275,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     ev1.record(stream)
     torch.cuda.synchronize(dev)
@@ -289,13 +355,84 @@ def run_ours(args, rank, world, local_rank):
     step()
     layer.sync()
     kvm.kvm_layer_set_timing(layer.handle, True)
-    for _ in range(max(3, args.steps // 2)):
+    for _ in range(max(3, steps // 2)):
         step()
     tseq = kvm.kvm_layer_get_timing(layer.handle)
     kvm.kvm_layer_set_timing(layer.handle, False)
     layer.sync()
-    kvm.kvm_layer_set_overlap(layer.handle, args.segments)
-    ms_step = ms / args.steps
+    kvm.kvm_layer_set_overlap(layer.handle, segments)
+    return dict(ms_step=ms / steps, tm=tm, tseq=tseq, segments=used_segments, layer=layer,
+                host=(q, k, v, g), dev=(dq, dk, dv, dg), out=out, step=step)
+
+
+def prefill_report(w, t, peaks):
+    """tokens/s, per-kernel times of the sequential pass, the dominant kernel's
+    roofline in the timed step and the whole step against the tensor roofline."""
+    aw = attention_work(w)
+    ffl = fold_work(w)
+    tm, tseq = t["tm"], t["tseq"]
+    s_attn = tseq["attn_ms"] / max(1, tseq["attn_launches"])
+    s_fold = tseq["fold_ms"] / max(1, tseq["fold_launches"])
+    s_other = tseq["other_ms"] / max(1, tseq["other_launches"])
+    s_tot = max(1e-9, tseq["attn_ms"] + tseq["fold_ms"] + tseq["other_ms"])
+    kernels = {
+        "attention": dict(ms_per_launch=s_attn, tflops=aw["flops"] / (s_attn / 1e3) / 1e12,
+                          flops_per_launch=aw["flops"], share=tseq["attn_ms"] / s_tot),
+        "fold_chain": dict(ms_per_launch=s_fold, tflops=ffl / (s_fold / 1e3) / 1e12,
+                           flops_per_launch=ffl, share=tseq["fold_ms"] / s_tot),
+        "key_rotation_and_ring": dict(ms_per_launch=s_other, share=tseq["other_ms"] / s_tot),
+        "pass": "sequential prefill (fold chain, key rotation + window ring fill, attention), timed "
+                "separately",
+    }
+    # dominant kernel of the timed step.  Overlapped: the fold chain is its critical
+    # path (the attention runs beside it); its duration is the chain's span per step
+    # (first segment start to last segment end, events on the chain's stream).
+    # Sequential: the kernel with the larger share of the step.
+    if t["segments"] > 0:
+        dom = "fold_chain"
+        dom_ms = tm["fold_ms"] / max(1, tm["fold_launches"])
+    else:
+        dom = "attention" if tm["attn_ms"] >= tm["fold_ms"] else "fold_chain"
+        dom_ms = (tm["attn_ms"] / max(1, tm["attn_launches"]) if dom == "attention"
+                  else tm["fold_ms"] / max(1, tm["fold_launches"]))
+    dom_flops = aw["flops"] if dom == "attention" else ffl
+    big = w.max_slots > 256 or w.chunk > 128
+    dom_src = os.path.join(ROOT, "compressed_kv_state_gb300", "csrc",
+                           "kvm_attn_tc.cu" if dom == "attention" else
+                           ("kvm_fold.cu" if big else "kvm_fold_tc.cu"))
+    ach = dom_flops / (dom_ms / 1e3) / 1e12
+    roofline = dict(kernel=dom, bound="tensor", achieved=ach, peak=peaks["bf16"], unit="TFLOP/s",
+                    frac=ach / peaks["bf16"], peak_source=f"{peaks['src']} bf16 burst",
+                    ms_per_step=dom_ms, traffic=_ncu_traffic(dom_src))
+    ms_step = t["ms_step"]
+    step_roof = {"flops": aw["flops"] + ffl, "ms_per_step": ms_step,
+                 "achieved": (aw["flops"] + ffl) / (ms_step / 1e3) / 1e12,
+                 "peak": peaks["bf16"], "unit": "TFLOP/s",
+                 "frac": (aw["flops"] + ffl) / (ms_step / 1e3) / 1e12 / peaks["bf16"],
+                 "peak_source": f"{peaks['src']} bf16 burst",
+                 "flops_4d_count": aw["flops_4d"] + ffl,
+                 "frac_4d_count": (aw["flops_4d"] + ffl) / (ms_step / 1e3) / 1e12 / peaks["bf16"]}
+    flops = {"attention": aw["flops"], "attention_4d_count": aw["flops_4d"], "fold_similarity": ffl}
+    return kernels, roofline, step_roof, flops
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from compressed_kv_state_gb300 import kvm
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    clocks = Clocks(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    t = time_prefill(W, dev, stream, args.steps, args.warmup, args.segments, world)
+    layer = t["layer"]
+    q, k, v, g = t["host"]
+    dq, dk, dv, dg = t["dev"]
+    out = t["out"]
+    segments = t["segments"]
+    ms_step = t["ms_step"]
     value = job_throughput(W.B * W.N, world, ms_step)
 
     # end to end through the C ABI: pinned host inputs in, output back to host, every
@@ -307,7 +444,7 @@ def run_ours(args, rank, world, local_rank):
     hv = torch.from_numpy(v).bfloat16().pin_memory()
     hg = torch.from_numpy(g).pin_memory()
     houts = [torch.empty(out.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    dins = [(dq, dk, dv, dg), tuple(torch.empty_like(t) for t in (dq, dk, dv, dg))]
+    dins = [(dq, dk, dv, dg), tuple(torch.empty_like(x) for x in (dq, dk, dv, dg))]
     douts = [out, torch.empty_like(out)]
     s_in = [torch.cuda.Stream(dev) for _ in range(3)]
     s_out = torch.cuda.Stream(dev)
@@ -358,51 +495,39 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms_e2e = e0.elapsed_time(e1) / ke2e
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hg))
     d2h = houts[0].numel() * houts[0].element_size()
     # the pipelined outputs equal the device-resident step's output
     e2e_same = bool(torch.equal(houts[(ke2e - 1) & 1], out.cpu())) if ke2e > 0 else None
-    del dins, douts
+    launches = t["tm"]["kernels"]  # every kernel the library launched in the timed region
+    timing_main = dict(ms_step=ms_step, tm=t["tm"], tseq=t["tseq"], segments=segments)
+    del dins, douts, t
+    layer.close()
+    torch.cuda.synchronize(dev)
 
+    peaks = _peaks()
+    # the other prefill workloads, each timed the same way in this run
+    others = {}
+    if not args.no_other_workloads:
+        for key, w2 in PREFILL.items():
+            if w2.name == W.name:
+                continue
+            t2 = time_prefill(w2, dev, stream, max(3, args.steps // 4), args.warmup, args.segments, world)
+            kern2, roof2, step2, fl2 = prefill_report(w2, t2, peaks)
+            others[w2.name] = {"value": job_throughput(w2.B * w2.N, world, t2["ms_step"]), "unit": UNIT,
+                               "ms_per_step": t2["ms_step"], "steps": max(3, args.steps // 4),
+                               "roofline": roof2, "step_tensor_roofline": step2, "kernels": kern2,
+                               "algorithmic_flops_per_step": fl2,
+                               "overlap": {"fold_segments": t2["segments"]},
+                               "config": workload_config(w2, world)}
+            t2["layer"].close()
+            del t2
+            torch.cuda.synchronize(dev)
     decode = None if args.no_decode else run_decode(dev, stream)
     layer_fwd = None if args.no_layer else run_layer(dev, stream, max(3, args.steps // 2), args.segments)
     clk = clocks.stop()
 
-    peaks = _peaks()
-    aw = attention_work(W)
-    ffl = fold_work(W)
-    # sequential pass: each kernel's own duration and share of the step
-    s_attn = tseq["attn_ms"] / max(1, tseq["attn_launches"])
-    s_fold = tseq["fold_ms"] / max(1, tseq["fold_launches"])
-    s_other = tseq["other_ms"] / max(1, tseq["other_launches"])
-    s_tot = max(1e-9, tseq["attn_ms"] + tseq["fold_ms"] + tseq["other_ms"])
-    kernels = {
-        "attention": dict(ms_per_launch=s_attn, tflops=aw["flops"] / (s_attn / 1e3) / 1e12,
-                          flops_per_launch=aw["flops"], share=tseq["attn_ms"] / s_tot),
-        "fold_chain": dict(ms_per_launch=s_fold, tflops=ffl / (s_fold / 1e3) / 1e12,
-                           flops_per_launch=ffl, share=tseq["fold_ms"] / s_tot),
-        "key_rotation_and_ring": dict(ms_per_launch=s_other, share=tseq["other_ms"] / s_tot),
-        "pass": "sequential prefill (fold chain, key rotation + window ring fill, attention), timed "
-                "separately",
-    }
-    # dominant kernel of the timed (overlapped) step: the fold chain is its critical
-    # path (the attention runs beside it); its duration is the chain's span per step
-    # (first segment start to last segment end, events on the chain's stream)
-    if segments > 0:
-        dom = "fold_chain"
-        dom_ms = tm["fold_ms"] / max(1, tm["fold_launches"])
-    else:
-        dom = "attention" if tm["attn_ms"] >= tm["fold_ms"] else "fold_chain"
-        dom_ms = (tm["attn_ms"] / max(1, tm["attn_launches"]) if dom == "attention"
-                  else tm["fold_ms"] / max(1, tm["fold_launches"]))
-    dom_flops = aw["flops"] if dom == "attention" else ffl
-    dom_src = os.path.join(ROOT, "compressed_kv_state_gb300", "csrc",
-                           "kvm_attn_tc.cu" if dom == "attention" else "kvm_fold_tc.cu")
-    ach = dom_flops / (dom_ms / 1e3) / 1e12
-    roofline = dict(kernel=dom, bound="tensor", achieved=ach, peak=peaks["bf16"], unit="TFLOP/s",
-                    frac=ach / peaks["bf16"], peak_source=f"{peaks['src']} bf16 burst",
-                    ms_per_step=dom_ms, traffic=_ncu_traffic(dom_src))
-    launches = tm["kernels"]  # every kernel the library launched in the timed region
+    kernels, roofline, step_roof, flops = prefill_report(W, timing_main, peaks)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -410,14 +535,9 @@ def run_ours(args, rank, world, local_rank):
         "config": bench_config(world),
         "roofline": roofline,
         "kernels": kernels,
-        "algorithmic_flops_per_step": {"attention": aw["flops"], "attention_4d_count": aw["flops_4d"],
-                                       "fold_similarity": ffl},
+        "algorithmic_flops_per_step": flops,
         # the whole step against the tensor roofline: attention + similarity FLOPs per step time
-        "step_tensor_roofline": {"flops": aw["flops"] + ffl, "ms_per_step": ms_step,
-                                 "achieved": (aw["flops"] + ffl) / (ms_step / 1e3) / 1e12,
-                                 "peak": peaks["bf16"], "unit": "TFLOP/s",
-                                 "frac": (aw["flops"] + ffl) / (ms_step / 1e3) / 1e12 / peaks["bf16"],
-                                 "peak_source": f"{peaks['src']} bf16 burst"},
+        "step_tensor_roofline": step_roof,
         "e2e": {"value": W.B * W.N / (ms_e2e / 1e3), "unit": UNIT, "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "step i+1's host-to-device copies and step i-1's read-back overlap "
@@ -428,6 +548,7 @@ def run_ours(args, rank, world, local_rank):
                     "note": "fold segments on one SM partition (green context), attention of "
                             "folded chunks on the other, the rest on all SMs"},
         "clocks": clk,
+        "workloads": others,
         "decode": decode,
         "layer_forward": layer_fwd,
     }
@@ -537,15 +658,25 @@ def run_decode(dev, stream):
 
 # ------------------------------------------------------------- reference
 
+KEYS = {"plain": "N(0,1) keys", "repeat5": "5% repeated keys", "needles10": "10 planted needle keys",
+        "neardup20": "20% near-duplicate keys"}
+
+
+def workload_config(w, world):
+    in_bytes = w.B * w.H * w.N * (3 * w.d * 2 + 4)  # bf16 q, k, v and the fp32 gate
+    cfg = {"workload": w.name, "batch": w.B, "heads": w.H, "seq_len": w.N,
+           "head_dim": w.d, "chunk": w.chunk, "window": w.window,
+           "slots": w.max_slots, "sinks": w.n_sinks, "rope_dims": w.rope_dims,
+           "growth": "fixed" if w.sched == 0 else f"power law: {w.n_sinks} + ceil({w.coef:g} t^{w.expo:g})",
+           "keys": KEYS.get(w.keys, w.keys),
+           "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB), no flush",
+           "parallelism": f"rows (batch x head) independent, {world} replica(s)"}
+    return cfg
+
+
 def bench_config(world):
     """The workload both arms report (the reference arm times a sample of it)."""
-    in_bytes = W.B * W.H * W.N * (3 * W.d * 2 + 4)  # bf16 q, k, v and the fp32 gate
-    return {"workload": W.name, "batch": W.B, "heads": W.H, "seq_len": W.N,
-            "head_dim": W.d, "chunk": W.chunk, "window": W.window,
-            "slots": W.max_slots, "sinks": W.n_sinks, "rope_dims": W.rope_dims,
-            "keys": "5% repeated keys",
-            "l2": f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB), no flush",
-            "parallelism": f"rows (batch x head) independent, {world} replica(s)"}
+    return workload_config(W, world)
 
 
 def run_reference(args):
@@ -555,7 +686,7 @@ def run_reference(args):
         cpu_oracle_sample(W, one_thread=False)
     secs = []
     for _ in range(args.steps):  # timed: the oracle call of each step (not its input generation)
-        r = cpu_oracle_sample(W, one_thread=False)
+        r, _ = cpu_oracle_sample(W, one_thread=False)
         secs.append(r.pop("seconds"))
     wall = sum(secs)
     tokens_per_step = W.N * r["cores"] / W.H
@@ -582,8 +713,13 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="run the same workload with another batch size (profiling a smaller case)")
+    ap.add_argument("--workload", choices=sorted(PREFILL), default="fixed8k",
+                    help="headline prefill workload (the others are reported under 'workloads')")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="time only the headline prefill workload")
     args = ap.parse_args()
     global W
+    W = PREFILL[args.workload]
     if args.batch is not None:
         W = W.with_(B=args.batch, name=W.name.replace(f"B{W.B}", f"B{args.batch}"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -601,8 +737,20 @@ def main():
     line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         if world == 1 and not args.no_cpu:
-            line["cpu_baseline"] = cpu_oracle_sample(W)
-            line["cpu_baseline"].pop("seconds")
+            import torch
+            dev = torch.device("cuda", local_rank)
+            cb, (sub, odbg) = cpu_oracle_sample(W)
+            cb.pop("seconds")
+            line["cpu_baseline"] = cb
+            line["near_ties"] = near_tie_counts(sub, odbg, dev)
+            for w2 in PREFILL.values():
+                rec = line["workloads"].get(w2.name)
+                if rec is None:
+                    continue
+                cb2, (sub2, odbg2) = cpu_oracle_sample(w2, one_thread=False)
+                cb2.pop("seconds")
+                rec["cpu_baseline"] = cb2
+                rec["near_ties"] = near_tie_counts(sub2, odbg2, dev)
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
