@@ -69,7 +69,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
                 print(out)
     if force or jobs or not os.path.exists(LIB):
         tmp = LIB + f".tmp{os.getpid()}"
-        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+        r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)

@@ -7,11 +7,23 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/kvm.h"
 #include "kvm_host.h"
 #include "kvm_internal.cuh"
 
 using kvm::D;
+
+namespace {
+// NVTX range over an entry point (a no-op unless a profiler is attached)
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace
 using kvm::Sched;
 
 namespace kvm {
@@ -251,6 +263,7 @@ size_t kvm_workspace_bytes(const kvm_config* cfg) {
 }
 
 kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t bytes, kvm_layer** out) {
+    NvtxRange nvtx_range("kvm_layer_create");
     std::string why;
     if (!out) { g_err = "out is NULL"; return KVM_ERR_INVALID_ARG; }
     *out = nullptr;
@@ -308,6 +321,7 @@ kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t b
 
 kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* v, const float* gate,
                        int64_t n_tokens, void* out, void* cuda_stream, const kvm_debug* dbg) {
+    NvtxRange nvtx_range("kvm_prefill");
     if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
     const kvm_config& c = ly->cfg;
     if (n_tokens < 0 || n_tokens > c.max_tokens)
@@ -469,7 +483,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         }
         // attention launches on the second partition may claim only ready ranges
         const int all_ranges = aa.n_ranges;
-        aa.grid = 2 * P.sm_attn;
+        aa.grid = P.sm_attn;  // one attention CTA per SM of the partition
         aa.n_ranges = 1;
         e = timed(ly, PH_ATTN, P.s_attn, [&] { return kvm::launch_attn(aa, bf16, P.s_attn); });
         if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
@@ -496,7 +510,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         // what is left of the attention on every SM, once the chain is done
         e = cudaStreamWaitEvent(s, P.ev_seg[segs - 1], 0);
         aa.n_ranges = all_ranges;
-        aa.grid = 2 * P.sm_all;
+        aa.grid = P.sm_all;
         if (e == cudaSuccess) e = timed(ly, PH_ATTN, s, [&] { return kvm::launch_attn(aa, bf16, s); });
         if (e != cudaSuccess) return ly->cuda_fail(e, "attention launch");
         ly->kernels += 1;
@@ -534,6 +548,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
 
 kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const void* v, const float* gate,
                            void* out, void* cuda_stream) {
+    NvtxRange nvtx_range("kvm_decode_step");
     if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
     const kvm_config& c = ly->cfg;
     if (!q || !k || !v || !gate || !out)
@@ -641,6 +656,7 @@ static kvm_status copy_state(kvm_layer* ly, kvm_state_bufs* ext, bool to_ext, cu
 }
 
 kvm_status kvm_state_export(const kvm_layer* cly, kvm_state_bufs* dst, void* cuda_stream) {
+    NvtxRange nvtx_range("kvm_state_export");
     kvm_layer* ly = const_cast<kvm_layer*>(cly);
     if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
     if (!dst) return ly->fail(KVM_ERR_INVALID_ARG, "dst is NULL");
@@ -656,6 +672,7 @@ kvm_status kvm_state_export(const kvm_layer* cly, kvm_state_bufs* dst, void* cud
 }
 
 kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda_stream) {
+    NvtxRange nvtx_range("kvm_state_import");
     if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
     if (!src) return ly->fail(KVM_ERR_INVALID_ARG, "src is NULL");
     const kvm_config& c = ly->cfg;
@@ -797,6 +814,7 @@ size_t kvm_forward_scratch_bytes(const kvm_config* cfg, int32_t d_model, int64_t
 
 kvm_status kvm_layer_forward(kvm_layer* ly, int32_t d_model, const void* x, const void* w_in, const void* w_out,
                              int64_t n_tokens, void* y, void* scratch, size_t scratch_bytes, void* cuda_stream) {
+    NvtxRange nvtx_range("kvm_layer_forward");
     if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
     const kvm_config& c = ly->cfg;
     if (c.dtype != KVM_BF16) return ly->fail(KVM_ERR_UNSUPPORTED, "kvm_layer_forward needs a bf16 layer");

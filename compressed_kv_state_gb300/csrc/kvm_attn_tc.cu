@@ -8,29 +8,30 @@
 //
 // Work unit: a tile of 128 consecutive queries of one (b, h) row (chunks are
 // multiples of 128, so a tile never spans two chunks).  The tile's keys come
-// in blocks of 64: first ceil(n/64) blocks of the state snapshot, then the
+// in blocks of 128: first ceil(n/128) blocks of the state snapshot, then the
 // window from (c - W/C)*C up to the tile's end (the last block is causal).
 //
-// Persistent CTAs (two per SM, 256 threads, 97 KB shared memory and 256 TMEM
-// columns each, so the tensor core alternates between two tiles) take tiles in
-// turns, either statically strided or claimed from a counter shared by several
-// launches; warp roles:
-//   warp 0     TMA producer: claims the tile, loads Q and the K/V blocks
-//              (3 stages)
-//   warp 1     tensor-memory owner and MMA issuer (one thread):
-//              S = Q K^T into one of two 64-column TMEM S buffers, issued for
-//              block j+1 before O += P V of block j (O: 64 columns)
-//   warps 2-3  RoPE: rotate the Q tile in shared memory (128-byte swizzled
-//              rows) and hand it to the MMA; window keys normally arrive
-//              already rotated (k_rot, rotated once per key by
-//              rope_keys_kernel), and only without that copy do these warps
-//              rotate each window K block as well
-//   warps 4-7  softmax: thread i owns query row i (= TMEM lane i); one pass
-//              over the 64-column S row, lazy rescaling of O (only when the
-//              running maximum grows by more than 2^8), P written to shared
-//              memory as bf16 in the swizzled K-major layout the MMA reads.
+// Persistent CTAs (one per SM, 384 threads, 225 KB shared memory, all 512
+// tensor-memory columns) hold two tile slots.  Each slot has its own roles, so
+// the tensor core runs one slot's QK^T and PV while the other slot's softmax
+// works; tiles are taken statically strided or claimed from counters shared by
+// several launches.  Per slot:
+//   producer warp (0, 1)   claims the slot's tiles, loads Q and the K/V blocks
+//                          by TMA (3 stages of 128 keys)
+//   MMA warp (2, 3)        one thread issues S = Q K^T (N = 128) into the slot's
+//                          128-column S, then O += P V with P read from tensor
+//                          memory (the A-from-tensor-memory form); the next
+//                          block's QK^T follows that PV in issue order
+//   softmax warps (4-7,    thread i owns query row i (= TMEM lane i): rotates
+//   8-11)                  its row of the Q tile, then per block a max pass
+//                          and an exponent pass over the S row (packed fp32,
+//                          three-input max), lazy rescaling of O (only when the
+//                          running maximum grows by more than 2^8), P written
+//                          back as bf16 pairs over the first 64 S columns;
+//                          finally O / l to the output.
 // All mbarrier waits are bounded (about two seconds); on expiry the CTA
-// raises the device status word, drains and exits.
+// raises the device status word, lets its issued copies and MMAs land, and
+// exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,21 +44,6 @@
 namespace kvm {
 namespace tc {
 
-constexpr int NS = 3;                 // K/V pipeline stages
-constexpr int KB = 64;                // keys per block
-constexpr int Q_BYTES = 128 * 128;    // Q tile [128 x 64] bf16
-constexpr int KV_BYTES = KB * 128;    // K or V block [64 x 64] bf16
-constexpr int P_BYTES = 128 * 128;    // P block [128 x 64] bf16
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
-constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-constexpr int OFF_P = OFF_V + NS * KV_BYTES;    // 2 P buffers
-constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;  // 97.25 KB with alignment slack: two CTAs per SM
-constexpr int TMEM_COLS = 256;
-constexpr int TM_S = 0, TM_O = 128;             // S buffers at columns 0 and 64
-constexpr float TAU = 8.0f;  // lazy-rescale threshold (log2 units)
-
 #ifdef KVM_PROBE
 static __device__ unsigned long long g_probe_attn[64];
 #endif
@@ -66,7 +52,6 @@ struct TcArgs {
     int64_t N;
     int BH, C, W, M, r;
     int tiles_per_head, ntiles;
-    int k_rotated;   // window keys arrive rotated (no RoPE on K in the kernel)
     int* tile_ctr;   // dynamic claiming: one counter per range (nullptr: static striding)
     int n_ranges;
     int range_end[AttnArgs::MAX_RANGES];
@@ -82,42 +67,6 @@ struct Tile {
     int bh, e, n, nst, nwin, nblk;
     int64_t q0, ws;
 };
-
-// Tiles are numbered query-tile-major: number id is query tile id / BH of row
-// id % BH, so every prefix of the numbering is a set of whole chunks of all rows
-// (the order in which the fold chain makes their state snapshots available).
-__device__ __forceinline__ Tile tile_of(const TcArgs& a, int id) {
-    Tile t;
-    t.bh = id % a.BH;
-    t.q0 = (int64_t)(id / a.BH) * 128;
-    const int64_t c = t.q0 / a.C, Wc = a.W / a.C;
-    t.e = (int)(c - Wc - 1);
-    t.n = t.e >= 0 ? a.sched[t.e].n_after : 0;
-    t.ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
-    t.nst = (t.n + KB - 1) / KB;
-    t.nwin = (int)((t.q0 + 128 - t.ws) / KB);
-    t.nblk = t.nst + t.nwin;
-    return t;
-}
-
-// The tile a CTA processes in its tt-th turn, or -1 when it is done.  Dynamic
-// claiming: the next tile of the first range (from the CTA's cursor *range on)
-// that is not exhausted, one atomicAdd per claim (a compare-and-swap loop on a
-// shared counter collapses under contention from hundreds of CTAs).  Static:
-// blockIdx.x + tt * gridDim.x.
-__device__ __forceinline__ int next_tile(const TcArgs& a, int tt, int* range) {
-    if (a.tile_ctr) {
-        for (; *range < a.n_ranges; ++*range) {
-            const int r = *range;
-            const int lo = r > 0 ? a.range_end[r - 1] : 0;
-            const int id = lo + atomicAdd(a.tile_ctr + r, 1);
-            if (id < a.range_end[r]) return id;
-        }
-        return -1;
-    }
-    const int64_t id = blockIdx.x + (int64_t)tt * gridDim.x;
-    return id < a.ntiles ? (int)id : -1;
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -173,270 +122,264 @@ __device__ __forceinline__ void rope_row_vec(uint8_t* row, int row_idx, int64_t 
     }
 }
 
-__global__ void __launch_bounds__(256, 2)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
-                   const __grid_constant__ CUtensorMap tm_sv, const TcArgs a) {
+// Two query tiles in flight per CTA (one CTA per SM), each with its own
+// producer, MMA issuer and softmax warpgroup; while one tile's softmax runs,
+// the tensor core works on the other tile's QK^T and PV.
+constexpr int NSLOT = 2;              // query tiles in flight per CTA
+constexpr int NS = 3;                 // K/V stages per tile slot
+constexpr int KB = 128;               // keys per block
+constexpr int Q_BYTES = 128 * 128;    // Q tile [128 x 64] bf16
+constexpr int KV_BYTES = KB * 128;    // K or V block [128 x 64] bf16
+constexpr int OFF_Q = 0;                               // [NSLOT] Q tiles
+constexpr int OFF_K = OFF_Q + NSLOT * Q_BYTES;         // [NSLOT][NS] K blocks
+constexpr int OFF_V = OFF_K + NSLOT * NS * KV_BYTES;   // [NSLOT][NS] V blocks
+constexpr int OFF_BAR = OFF_V + NSLOT * NS * KV_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;       // 225.5 KB with alignment slack
+constexpr int TMEM_COLS = 512;                         // per slot: S (128 columns, P aliased on
+                                                       // its first 64) then O (64 columns)
+constexpr int NTHREADS = 384;
+// Register split (the block is launched with 168 registers a thread, 64512 in
+// all): the producer / MMA warpgroup drops to 64, the two softmax warpgroups rise
+// to 216, which keeps a whole 128-column S row in registers: 4 * 32 * 64 +
+// 8 * 32 * 216 = 63488 <= 64512.
+constexpr int REGS_LOW = 64, REGS_HIGH = 216;
+constexpr float TAU = 8.0f;  // lazy-rescale threshold (log2 units)
+
+// per-slot barrier indices
+enum {
+    B_QFULL = 0,                 // TMA Q landed
+    B_QREADY = 1,                // Q rotated (128 arrivals)
+    B_QEMPTY = 2,                // last QK of the tile done
+    B_KFULL = 3,                 // [NS] TMA K landed
+    B_VFULL = B_KFULL + NS,      // [NS] TMA V landed
+    B_KVEMPTY = B_VFULL + NS,    // [NS] PV of the stage done
+    B_SFULL = B_KVEMPTY + NS,    // QK done
+    B_PFULL = B_SFULL + 1,       // P written to tensor memory, O rescaled (128 arrivals)
+    B_PVDONE = B_PFULL + 1,      // PV done
+    B_FINAL = B_PVDONE + 1,      // MMA drain
+    B_TILE = B_FINAL + 1,        // [4] tile number of turn k published (ring of 4)
+    NBAR_SLOT = B_TILE + 4
+};
+
+__device__ __forceinline__ Tile tile_of2(const TcArgs& a, int id) {
+    Tile t;
+    t.bh = id % a.BH;
+    t.q0 = (int64_t)(id / a.BH) * 128;
+    const int64_t c = t.q0 / a.C, Wc = a.W / a.C;
+    t.e = (int)(c - Wc - 1);
+    t.n = t.e >= 0 ? a.sched[t.e].n_after : 0;
+    t.ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
+    t.nst = (t.n + KB - 1) / KB;
+    t.nwin = (int)((t.q0 + 128 - t.ws + KB - 1) / KB);
+    t.nblk = t.nst + t.nwin;
+    return t;
+}
+
+// The tile a slot processes in its k-th turn, or -1 when it is done.  Dynamic:
+// one atomicAdd per claim on the first range (from *range on) not exhausted.
+// Static: turn k of slot s is the CTA's turn 2k + s.
+__device__ __forceinline__ int next_tile2(const TcArgs& a, int slot, int k, int* range) {
+    if (a.tile_ctr) {
+        for (; *range < a.n_ranges; ++*range) {
+            const int r = *range;
+            const int lo = r > 0 ? a.range_end[r - 1] : 0;
+            const int id = lo + atomicAdd(a.tile_ctr + r, 1);
+            if (id < a.range_end[r]) return id;
+        }
+        return -1;
+    }
+    const int64_t id = blockIdx.x + (int64_t)(2 * k + slot) * gridDim.x;
+    return id < a.ntiles ? (int)id : -1;
+}
+
+// wait for a phase without the abort shortcut (drains after an abort), bounded
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity) && clock64() - t0 < (1ll << 28)) {
+    }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
+                    const __grid_constant__ CUtensorMap tm_sv, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte aligned tiles for the 128-byte swizzle (the slack is part of the request)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
-    enum {
-        B_QFULL = 0,               // TMA Q landed
-        B_QREADY = 1,              // Q rotated (64 arrivals)
-        B_QEMPTY = 2,              // last QK of the tile done
-        B_KFULL = 3,               // [NS] TMA K landed
-        B_VFULL = B_KFULL + NS,    // [NS] TMA V landed
-        B_KREADY = B_VFULL + NS,   // [NS] K rotated (64 arrivals)
-        B_KVEMPTY = B_KREADY + NS, // [NS] PV of the stage done
-        B_SFULL = B_KVEMPTY + NS,  // [2] QK done
-        B_PFULL = B_SFULL + 2,     // [2] S consumed, P written, O rescaled (128 arrivals)
-        B_PVDONE = B_PFULL + 2,    // [2] PV done
-        B_FINAL = B_PVDONE + 2,    // MMA drain
-        B_TILE = B_FINAL + 1,      // [4] tile number of turn tt published (ring of 4)
-        NBARS = B_TILE + 4
-    };
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NSLOT * NBAR_SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* tile_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);
-    auto bar = [&](int i) { return smem_u32(bars + i); };
-    // The producer publishes the tile of turn tt in ring slot tt % 4; the other roles
-    // read it after the slot's barrier.  A slot is rewritten four turns later, when
-    // every role has moved past that turn: the producer claims turn tt only after the
-    // last QK MMA of turn tt - 1, which follows the rotation of its Q (RoPE warps in
-    // turn tt - 1) and the softmax of a block of turn tt - 2 or later.
-    auto tile_wait = [&](int tt) -> int {
-        if (!mbar_wait(bar(B_TILE + (tt & 3)), (tt >> 2) & 1, abort_flag, a.status)) return -1;
-        return tile_ring[tt & 3];
+    volatile int* tile_ring = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [NSLOT][4]
+    auto bar = [&](int slot, int i) { return smem_u32(bars + slot * NBAR_SLOT + i); };
+    // The producer of a slot publishes the tile of its turn k in ring entry k % 4; the
+    // other roles read it after that entry's barrier.  An entry is rewritten four turns
+    // later: the producer claims turn k only after the last QK MMA of turn k - 1, which
+    // follows the Q rotation of turn k - 1 and the softmax of turn k - 2's last block.
+    auto tile_wait = [&](int slot, int k) -> int {
+        if (!mbar_wait(bar(slot, B_TILE + (k & 3)), (k >> 2) & 1, abort_flag, a.status)) return -1;
+        return tile_ring[slot * 4 + (k & 3)];
     };
 
     if (tid == 0) {
-        mbar_init(bar(B_QFULL), 1);
-        mbar_init(bar(B_QREADY), 64);
-        mbar_init(bar(B_QEMPTY), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_SFULL + i), 1);
-            mbar_init(bar(B_PFULL + i), 128);
-            mbar_init(bar(B_PVDONE + i), 1);
+        for (int s = 0; s < NSLOT; ++s) {
+            mbar_init(bar(s, B_QFULL), 1);
+            mbar_init(bar(s, B_QREADY), 128);
+            mbar_init(bar(s, B_QEMPTY), 1);
+            for (int i = 0; i < NS; ++i) {
+                mbar_init(bar(s, B_KFULL + i), 1);
+                mbar_init(bar(s, B_VFULL + i), 1);
+                mbar_init(bar(s, B_KVEMPTY + i), 1);
+            }
+            mbar_init(bar(s, B_SFULL), 1);
+            mbar_init(bar(s, B_PFULL), 128);
+            mbar_init(bar(s, B_PVDONE), 1);
+            mbar_init(bar(s, B_FINAL), 1);
+            for (int i = 0; i < 4; ++i) mbar_init(bar(s, B_TILE + i), 1);
         }
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(bar(B_KFULL + s), 1);
-            mbar_init(bar(B_VFULL + s), 1);
-            mbar_init(bar(B_KREADY + s), 64);
-            mbar_init(bar(B_KVEMPTY + s), 1);
-        }
-        mbar_init(bar(B_FINAL), 1);
-        for (int i = 0; i < 4; ++i) mbar_init(bar(B_TILE + i), 1);
         *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async();
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    if (warp == 2) tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-#ifdef KVM_PROBE
-    unsigned probe_sm = 0;
-    if (tid == 0) {
-        if (blockIdx.x == 0) g_probe_attn[31] = gridDim.x;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(probe_sm));
-        const unsigned long long now = atomicAdd(&g_probe_attn[32 + (probe_sm & 31)], 1ull) + 1;
-        atomicMax(&g_probe_attn[29], now);
-    }
-#endif
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sQ = smem_u32(smem + OFF_Q), sK = smem_u32(smem + OFF_K);
-    const uint32_t sV = smem_u32(smem + OFF_V), sP = smem_u32(smem + OFF_P);
+    const uint32_t sbase = smem_u32(smem);
     const int half = a.r / 2;
+    if (warp < 4)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
+    else
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
 
-    if (warp == 0) {
+    if (warp < 2) {
         // ------------------------------------------------------------ producer
+        const int slot = warp;
+        int last_g = -1;  // last block whose K/V copies were issued
         if (lane == 0) {
-            KVM_PROBE_DECL(3)
-            KVM_PROBE_START()
             int g = 0, range = 0;
-            for (int tt = 0;; ++tt) {
-                KVM_PROBE_LAP(2)
-                if (tt >= 1 && !mbar_wait(bar(B_QEMPTY), (tt - 1) & 1, abort_flag, a.status)) break;
-                KVM_PROBE_LAP(0)
-                const int id = next_tile(a, tt, &range);
-                tile_ring[tt & 3] = id;
-                mbar_arrive(bar(B_TILE + (tt & 3)));
+            for (int k = 0;; ++k) {
+                if (k >= 1 && !mbar_wait(bar(slot, B_QEMPTY), (k - 1) & 1, abort_flag, a.status)) break;
+                const int id = next_tile2(a, slot, k, &range);
+                tile_ring[slot * 4 + (k & 3)] = id;
+                mbar_arrive(bar(slot, B_TILE + (k & 3)));
                 if (id < 0) break;
-                const Tile T = tile_of(a, id);
-                mbar_expect_tx(bar(B_QFULL), Q_BYTES);
-                tma_load_3d(sQ, &tm_q, 0, (int)T.q0, T.bh, bar(B_QFULL));
+                const Tile T = tile_of2(a, id);
+                mbar_expect_tx(bar(slot, B_QFULL), Q_BYTES);
+                tma_load_3d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, 0, (int)T.q0, T.bh, bar(slot, B_QFULL));
                 bool ok = true;
                 for (int j = 0; j < T.nblk; ++j, ++g) {
-                    const int s = g % NS;
-                    KVM_PROBE_LAP(2)
-                    if (g >= NS && !mbar_wait(bar(B_KVEMPTY + s), ((g / NS) - 1) & 1, abort_flag, a.status)) {
+                    const int st = g % NS;
+                    if (g >= NS && !mbar_wait(bar(slot, B_KVEMPTY + st), ((g / NS) - 1) & 1, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
-                    KVM_PROBE_LAP(1)
-                    mbar_expect_tx(bar(B_KFULL + s), KV_BYTES);
-                    mbar_expect_tx(bar(B_VFULL + s), KV_BYTES);
+                    const uint32_t dk = sbase + OFF_K + (slot * NS + st) * KV_BYTES;
+                    const uint32_t dv = sbase + OFF_V + (slot * NS + st) * KV_BYTES;
+                    mbar_expect_tx(bar(slot, B_KFULL + st), KV_BYTES);
+                    mbar_expect_tx(bar(slot, B_VFULL + st), KV_BYTES);
                     if (j < T.nst) {
                         const int plane = T.bh * a.snap_events + T.e;
-                        tma_load_3d(sK + s * KV_BYTES, &tm_sk, 0, KB * j, plane, bar(B_KFULL + s));
-                        tma_load_3d(sV + s * KV_BYTES, &tm_sv, 0, KB * j, plane, bar(B_VFULL + s));
+                        tma_load_3d(dk, &tm_sk, 0, KB * j, plane, bar(slot, B_KFULL + st));
+                        tma_load_3d(dv, &tm_sv, 0, KB * j, plane, bar(slot, B_VFULL + st));
                     } else {
                         const int key0 = (int)(T.ws + KB * (j - T.nst));
-                        tma_load_3d(sK + s * KV_BYTES, &tm_k, 0, key0, T.bh, bar(B_KFULL + s));
-                        tma_load_3d(sV + s * KV_BYTES, &tm_v, 0, key0, T.bh, bar(B_VFULL + s));
+                        tma_load_3d(dk, &tm_k, 0, key0, T.bh, bar(slot, B_KFULL + st));
+                        tma_load_3d(dv, &tm_v, 0, key0, T.bh, bar(slot, B_VFULL + st));
                     }
+                    last_g = g;
                 }
                 if (!ok) break;
             }
-            KVM_PROBE_LAP(2)
-            KVM_PROBE_FLUSH(g_probe_attn, 0, 3)
+            // after an abort: the copies issued last on every stage land before exit
+            if (*abort_flag)
+                for (int gg = last_g; gg >= 0 && gg > last_g - NS; --gg) {
+                    drain_wait(bar(slot, B_KFULL + gg % NS), (gg / NS) & 1);
+                    drain_wait(bar(slot, B_VFULL + gg % NS), (gg / NS) & 1);
+                }
         }
-    } else if (warp == 1) {
+    } else if (warp < 4) {
         // ---------------------------------------------------------- MMA issuer
+        const int slot = warp - 2;
         if (lane == 0) {
             const uint32_t idesc_qk = idesc_bf16(128, KB, 0, 0);
             const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
             const int ks_state = min(a.r / 16, 3);
-            KVM_PROBE_DECL(5)
-            KVM_PROBE_START()
+            const uint32_t tS = tmem + 256 * slot, tO = tS + 128;
+            const uint32_t sQ = sbase + OFF_Q + slot * Q_BYTES;
             int g = 0;
             bool ok = true;
-            for (int tt = 0; ok; ++tt) {
-                const int id = tile_wait(tt);
+            for (int k = 0; ok; ++k) {
+                const int id = tile_wait(slot, k);
                 if (id < 0) break;
-                const Tile T = tile_of(a, id);
-                KVM_PROBE_LAP(4)
-                if (!mbar_wait(bar(B_QREADY), tt & 1, abort_flag, a.status)) break;
-                KVM_PROBE_LAP(0)
+                const Tile T = tile_of2(a, id);
+                if (!mbar_wait(bar(slot, B_QREADY), k & 1, abort_flag, a.status)) break;
                 tc_fence_after();
-                auto issue_qk = [&](int j, int gq) -> bool {
-                    const int s = gq % NS, sb = gq & 1;
-                    KVM_PROBE_LAP(4)
-                    if (!mbar_wait(bar(B_KREADY + s), (gq / NS) & 1, abort_flag, a.status)) return false;
-                    KVM_PROBE_LAP(1)
+                for (int j = 0; j < T.nblk; ++j) {
+                    const int gj = g + j, st = gj % NS;
+                    const uint32_t sK = sbase + OFF_K + (slot * NS + st) * KV_BYTES;
+                    const uint32_t sV = sbase + OFF_V + (slot * NS + st) * KV_BYTES;
+                    if (!mbar_wait(bar(slot, B_KFULL + st), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
+                    // S = Q K^T (state blocks: the non-rotary dims only; the state keys are
+                    // zero on the rotary dims).  It overwrites the P of block gj - 1, whose PV
+                    // was issued before it (tensor-core operations of a thread run in order).
                     const int ks0 = j < T.nst ? ks_state : 0;
                     for (int ks = ks0; ks < 4; ++ks) {
                         const uint64_t ad = sdesc_sw128(sQ + ks * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(sK + s * KV_BYTES + ks * 32, 16, 1024);
-                        mma_bf16_ss(tmem + TM_S + sb * KB, ad, bd, idesc_qk, ks > ks0);
+                        const uint64_t bd = sdesc_sw128(sK + ks * 32, 16, 1024);
+                        mma_bf16_ss(tS, ad, bd, idesc_qk, ks > ks0);
                     }
-                    mma_commit(bar(B_SFULL + sb));
-                    return true;
-                };
-                if (!issue_qk(0, g)) { ok = false; break; }
-                for (int j = 0; j < T.nblk; ++j) {
-                    const int gj = g + j, s = gj % NS, pb = gj & 1;
-                    // S buffer of block gj + 1 last held block gj - 1, consumed before its P was published
-                    if (j + 1 < T.nblk) {
-                        if (!issue_qk(j + 1, gj + 1)) { ok = false; break; }
-                    } else {
-                        mma_commit(bar(B_QEMPTY));
-                    }
-                    KVM_PROBE_LAP(4)
-                    if (!mbar_wait(bar(B_PFULL + pb), (gj >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-                    KVM_PROBE_LAP(2)
-                    if (!mbar_wait(bar(B_VFULL + s), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
-                    KVM_PROBE_LAP(3)
+                    mma_commit(bar(slot, B_SFULL));
+                    if (j + 1 == T.nblk) mma_commit(bar(slot, B_QEMPTY));
+                    if (!mbar_wait(bar(slot, B_PFULL), gj & 1, abort_flag, a.status)) { ok = false; break; }
+                    if (!mbar_wait(bar(slot, B_VFULL + st), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
+                    // O += P V: P (bf16, two keys per column) from tensor memory, V from shared
                     for (int ks = 0; ks < KB / 16; ++ks) {
-                        const uint64_t ad = sdesc_sw128(sP + pb * P_BYTES + ks * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(sV + s * KV_BYTES + ks * 2048, KV_BYTES, 1024);
-                        mma_bf16_ss(tmem + TM_O, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+                        const uint64_t bd = sdesc_sw128(sV + ks * 2048, KV_BYTES, 1024);
+                        mma_bf16_ts(tO, tS + 8 * ks, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                     }
-                    mma_commit(bar(B_PVDONE + pb));
-                    mma_commit(bar(B_KVEMPTY + s));
+                    mma_commit(bar(slot, B_PVDONE));
+                    mma_commit(bar(slot, B_KVEMPTY + st));
                 }
                 g += T.nblk;
             }
-            KVM_PROBE_LAP(4)
-            KVM_PROBE_FLUSH(g_probe_attn, 3, 5)
-            mma_commit(bar(B_FINAL));
-            mbar_wait(bar(B_FINAL), 0, abort_flag, nullptr);
+            // every MMA this thread issued completes before the tensor memory is released
+            mma_commit(bar(slot, B_FINAL));
+            drain_wait(bar(slot, B_FINAL), 0);
         }
-    } else if (warp < 4) {
-        // --------------------------------------------------------------- RoPE
-        const int rt = tid - 64;
-        KVM_PROBE_DECL(4)
-        KVM_PROBE_START()
-        int g = 0;
-        for (int tt = 0;; ++tt) {
-            const int id = tile_wait(tt);
-            if (id < 0) break;
-            const Tile T = tile_of(a, id);
-            KVM_PROBE_LAP(3)
-            if (!mbar_wait(bar(B_QFULL), tt & 1, abort_flag, a.status)) break;
-            KVM_PROBE_LAP(0)
-            if (half > 0) {
-                for (int row = rt; row < 128; row += 64) {
-                    const int64_t pos = T.q0 + row;
-                    if (pos < a.N) {
-                        if ((half & 7) == 0)
-                            rope_row_vec(smem + OFF_Q + row * 128, row, pos, a.rope, half);
-                        else
-                            rope_row(smem + OFF_Q + row * 128, row, pos, a.rope, half);
-                    }
-                }
-            }
-            fence_proxy_async();
-            mbar_arrive(bar(B_QREADY));
-            bool ok = true;
-            for (int j = 0; j < T.nblk; ++j, ++g) {
-                const int s = g % NS;
-                KVM_PROBE_LAP(2)
-                if (!mbar_wait(bar(B_KFULL + s), (g / NS) & 1, abort_flag, a.status)) {
-                    ok = false;
-                    break;
-                }
-                KVM_PROBE_LAP(1)
-                if (j >= T.nst && half > 0 && !a.k_rotated) {
-                    const int64_t pos = T.ws + KB * (j - T.nst) + rt;
-                    if (pos < a.N) {
-                        if ((half & 7) == 0)
-                            rope_row_vec(smem + OFF_K + s * KV_BYTES + rt * 128, rt, pos, a.rope, half);
-                        else
-                            rope_row(smem + OFF_K + s * KV_BYTES + rt * 128, rt, pos, a.rope, half);
-                    }
-                }
-                fence_proxy_async();
-                mbar_arrive(bar(B_KREADY + s));
-            }
-            if (!ok) break;
-        }
-        KVM_PROBE_LAP(2)
-        if (rt == 0) KVM_PROBE_FLUSH(g_probe_attn, 8, 4)
     } else {
         // ------------------------------------------------------------ softmax
-        const int row = tid - 128;                 // query row = TMEM lane
+        const int slot = (warp - 4) >> 2;
+        const int row = tid - 128 - 128 * slot;                // query row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tO = tmem + lane_base + TM_O;
+        const uint32_t tS = tmem + lane_base + 256 * slot, tO = tS + 128;
+        uint8_t* qrow = smem + OFF_Q + slot * Q_BYTES + row * 128;
         const float sc = a.scale_log2;
-        KVM_PROBE_DECL(10)
-        KVM_PROBE_START()
+        const float2 sc2 = make_float2(sc, sc);
         int g = 0;
         bool ok = true;
-        for (int tt = 0; ok; ++tt) {
-            const int id = tile_wait(tt);
+        for (int k = 0; ok; ++k) {
+            const int id = tile_wait(slot, k);
             if (id < 0) break;
-            const Tile T = tile_of(a, id);
+            const Tile T = tile_of2(a, id);
             const int64_t p = T.q0 + row;
+            // RoPE of this thread's query row, then hand the tile to the MMA
+            if (!mbar_wait(bar(slot, B_QFULL), k & 1, abort_flag, a.status)) break;
+            if (half > 0 && p < a.N) {
+                if ((half & 7) == 0)
+                    rope_row_vec(qrow, row, p, a.rope, half);
+                else
+                    rope_row(qrow, row, p, a.rope, half);
+            }
+            fence_proxy_async();
+            mbar_arrive(bar(slot, B_QREADY));
             float m_used = -INFINITY, l = 0.0f;
             for (int j = 0; j < T.nblk; ++j) {
-                const int gj = g + j, sb = gj & 1;
-                KVM_PROBE_LAP(9)
-                if (!mbar_wait(bar(B_SFULL + sb), (gj >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-                KVM_PROBE_LAP(0)
-#ifdef KVM_PROBE
-                probe_acc[8] += 1;
-#endif
+                const int gj = g + j;
+                if (!mbar_wait(bar(slot, B_SFULL), gj & 1, abort_flag, a.status)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t v[2][32];
-                tmem_ld32(tmem + lane_base + TM_S + sb * KB, v[0]);
-                tmem_ld32(tmem + lane_base + TM_S + sb * KB + 32, v[1]);
-                tmem_wait_ld();
                 const bool is_state = j < T.nst;
                 const int64_t key0 = is_state ? 0 : T.ws + KB * (j - T.nst);
                 // columns < lim are valid keys for this query (a causal block may have none)
@@ -447,24 +390,28 @@ __global__ void __launch_bounds__(256, 2)
                     const int64_t d = p - key0 + 1;
                     lim = d < 0 ? 0 : (d < KB ? (int)d : KB);
                 }
-                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (lim == KB) {
-                    // a full block: every column is a valid key
+                // the whole S row of this block in registers (one tensor-memory round trip)
+                uint32_t v[KB / 32][32];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < KB / 32; ++h) tmem_ld32(tS + 32 * h, v[h]);
+                tmem_wait_ld();
+                if (lim < KB) {
 #pragma unroll
-                        for (int x = 0; x < 32; ++x) mx[x & 3] = fmaxf(mx[x & 3], __uint_as_float(v[h][x]));
-                } else {
+                    for (int h = 0; h < KB / 32; ++h)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) {
-                            const float val = h * 32 + x < lim ? __uint_as_float(v[h][x]) : -INFINITY;
-                            v[h][x] = __float_as_uint(val);
-                            mx[x & 3] = fmaxf(mx[x & 3], val);
-                        }
+                        for (int x = 0; x < 32; ++x)
+                            if (32 * h + x >= lim) v[h][x] = __float_as_uint(-INFINITY);
                 }
-                const float mblk = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sc;
+                // the block's row maximum
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < KB / 32; ++h)
+#pragma unroll
+                    for (int x = 0; x < 32; x += 4) {
+                        mx0 = fmax3(mx0, __uint_as_float(v[h][x]), __uint_as_float(v[h][x + 1]));
+                        mx1 = fmax3(mx1, __uint_as_float(v[h][x + 2]), __uint_as_float(v[h][x + 3]));
+                    }
+                const float mblk = fmaxf(mx0, mx1) * sc;
                 bool rescale = false;
                 float alpha = 1.0f;
                 if (mblk > m_used) {
@@ -477,26 +424,32 @@ __global__ void __launch_bounds__(256, 2)
                     }
                 }
                 l *= alpha;
-                KVM_PROBE_LAP(1)
-                const float mneg = -m_used;
-                uint32_t pk[32];
-                float rs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                // p = 2^(s * scale - m), row sum, P as bf16 pairs over S's first 64 columns
+                // (column 16h + i takes keys 32h + 2i, 32h + 2i + 1, whose S values are in
+                // registers already)
+                const float2 mneg = make_float2(-m_used, -m_used);
+                float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < KB / 32; ++h) {
+                    uint32_t pk[16];
 #pragma unroll
                     for (int x = 0; x < 32; x += 2) {
-                        const float p0 = ex2(fmaf(__uint_as_float(v[h][x]), sc, mneg));
-                        const float p1 = ex2(fmaf(__uint_as_float(v[h][x + 1]), sc, mneg));
-                        rs[(x >> 1) & 3] += p0 + p1;
-                        pk[(h * 32 + x) >> 1] = pack_bf16(p0, p1);
+                        const float2 s2 = make_float2(__uint_as_float(v[h][x]), __uint_as_float(v[h][x + 1]));
+                        const float2 t2 = __ffma2_rn(s2, sc2, mneg);
+                        const float2 e2 = make_float2(ex2(t2.x), ex2(t2.y));
+                        rs[(x >> 1) & 3] = __fadd2_rn(rs[(x >> 1) & 3], e2);
+                        pk[x >> 1] = pack_bf16(e2.x, e2.y);
                     }
-                l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-                KVM_PROBE_LAP(4)
+                    tmem_st16(tS + 16 * h, pk);
+                }
+                tmem_wait_st();
+                l += ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
                 // tensor-memory loads and stores are warp-wide (.sync.aligned): the whole
                 // warp rescales when any of its rows must (the others scale by alpha = 1)
                 if (__any_sync(0xffffffffu, rescale)) {
                     // O holds blocks < j: wait for their last PV, then scale it in place
-                    if (!mbar_wait(bar(B_PVDONE + ((gj - 1) & 1)), ((gj - 1) >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                    if (!mbar_wait(bar(slot, B_PVDONE), (gj - 1) & 1, abort_flag, a.status)) { ok = false; break; }
                     tc_fence_after();
                     uint32_t o[32];
 #pragma unroll
@@ -509,26 +462,13 @@ __global__ void __launch_bounds__(256, 2)
                     }
                     tmem_wait_st();
                 }
-                KVM_PROBE_LAP(3)
-                // the P buffer was last read by the PV of block gj - 2
-                if (gj >= 2 && !mbar_wait(bar(B_PVDONE + sb), ((gj - 2) >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-                KVM_PROBE_LAP(2)
-                uint8_t* prow = smem + OFF_P + sb * P_BYTES + row * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    *reinterpret_cast<uint4*>(prow + ((ch ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-                fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive(bar(B_PFULL + sb));
-                KVM_PROBE_LAP(4)
+                mbar_arrive(bar(slot, B_PFULL));
             }
             if (!ok) break;
             // epilogue: O / l for this tile
             const int gl = g + T.nblk - 1;
-            KVM_PROBE_LAP(9)
-            if (!mbar_wait(bar(B_PVDONE + (gl & 1)), (gl >> 1) & 1, abort_flag, a.status)) { ok = false; break; }
-            KVM_PROBE_LAP(5)
+            if (!mbar_wait(bar(slot, B_PVDONE), gl & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
             const float il = 1.0f / l;
 #pragma unroll
@@ -548,23 +488,12 @@ __global__ void __launch_bounds__(256, 2)
             }
             tc_fence_before();
             g += T.nblk;
-            KVM_PROBE_LAP(6)
         }
-        if (row == 0) KVM_PROBE_FLUSH(g_probe_attn, 12, 10)
     }
 
     tc_fence_before();
     __syncthreads();
-#ifdef KVM_PROBE
-    if (tid == 0) atomicAdd(&g_probe_attn[32 + (probe_sm & 31)], ~0ull);
-#endif
-    if (*abort_flag) {
-        // let copies still in flight land before the shared memory is released
-        const long long t0 = clock64();
-        while (clock64() - t0 < (1ll << 22)) {
-        }
-    }
-    if (warp == 1) {
+    if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -645,6 +574,8 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     CUtensorMap mq, mk, mv, msk, msv;
     const uint64_t BH = (uint64_t)a.BH;
     const uint64_t planes_snap = BH * (uint64_t)(a.snap_events > 0 ? a.snap_events : 1);
+    // window keys must come rotated at their own positions when the layer has rotary dims
+    if (a.r > 0 && !a.k_rot) return cudaErrorInvalidValue;
     if (!make_tmap_bf16_3d(&mq, a.q, (uint64_t)a.N, BH, 128) || !make_tmap_bf16_3d(&mk, a.k_rot ? a.k_rot : a.k, (uint64_t)a.N, BH, KB) ||
         !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH, KB) ||
         !make_tmap_bf16_3d(&msk, a.snap_k, (uint64_t)a.M, planes_snap, KB) ||
@@ -659,7 +590,6 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     t.r = a.r;
     t.tiles_per_head = (int)((a.N + 127) / 128);
     t.ntiles = t.tiles_per_head * a.BH;
-    t.k_rotated = a.k_rot != nullptr;
     t.tile_ctr = a.tile_ctr;
     t.n_ranges = a.n_ranges < AttnArgs::MAX_RANGES ? a.n_ranges : AttnArgs::MAX_RANGES;
     for (int r = 0; r < AttnArgs::MAX_RANGES; ++r) {
@@ -677,43 +607,13 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        cudaFuncSetAttribute(attn_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     }
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared);
-        // Two CTAs per SM fit (2 x 97 KB shared memory, 2 x 256 x 128 registers, 2 x 256
-        // TMEM columns), but the occupancy calculator reports one for this kernel.  CTAs
-        // of the persistent grid never wait on each other, so a grid of two per SM is
-        // correct whether or not both are resident.
-        per_sm = 2;
-#ifdef KVM_PROBE
-        {
-            int dev = 0, smem_sm = 0, resv = 0, regs_sm = 0, occ = -1;
-            cudaGetDevice(&dev);
-            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-            cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev);
-            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
-            cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, attn_tc_kernel, 256, SMEM_BYTES);
-            cudaFuncAttributes fa;
-            cudaFuncGetAttributes(&fa, attn_tc_kernel);
-            for (int sz : {0, 16384, 49152, 65536, 81920, 99584}) {
-                int o2 = -1;
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o2, attn_tc_kernel, 256, sz);
-                int o3 = -1;
-                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o3, attn_tc_kernel, 128, sz);
-                fprintf(stderr, "[probe] dyn smem %d -> occupancy %d (256 thr) %d (128 thr)\n", sz, o2, o3);
-            }
-            fprintf(stderr, "[probe] attn occupancy %d (err %d %s) smem/SM %d reserved/block %d regs/SM %d "
-                    "kernel regs %d static smem %zu dyn %d maxdyn %d\n", occ, (int)oe, cudaGetErrorString(oe),
-                    smem_sm, resv, regs_sm, fa.numRegs, fa.sharedSizeBytes, SMEM_BYTES, fa.maxDynamicSharedSizeBytes);
-        }
-#endif
-    }
-    int grid = a.grid > 0 ? a.grid : per_sm * nsm;
-    if (!a.tile_ctr && grid > t.ntiles) grid = t.ntiles;
-    attn_tc_kernel<<<grid, 256, SMEM_BYTES, s>>>(mq, mk, mv, msk, msv, t);
+    // persistent: one CTA per SM (two query tiles in flight in each); a.grid, when
+    // given, is the number of CTAs for the SM partition the launch runs on
+    int grid = a.grid > 0 ? a.grid : nsm;
+    if (!a.tile_ctr && grid > (t.ntiles + 1) / 2) grid = (t.ntiles + 1) / 2;
+    attn_tc2_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, msk, msv, t);
     return cudaGetLastError();
 }
 

@@ -370,6 +370,7 @@ static size_t fold_smem_bytes(int C) {
 
 cudaError_t launch_fold(const FoldArgs& a, bool bf16, cudaStream_t s) {
     if (fold_tc_supported(a, bf16)) return launch_fold_tc(a, s);
+    if (fold_big_supported(a, bf16)) return launch_fold_big(a, s);
     const size_t smem = fold_smem_bytes(a.C);
     if (bf16) {
         cudaFuncSetAttribute(fold_chain_kernel<__nv_bfloat16>,

@@ -1,0 +1,632 @@
+// Fold chain on the tensor cores for large states (bf16 I/O, any max_slots up
+// to 4096, chunks up to 256 tokens): the case the on-chip chain (state in
+// tensor memory, at most 256 slots and 128 tokens) does not cover.
+//
+// "Key-Value Means" (gist.science technical summary), Core mechanisms 1-3
+// and 5 (the growable "KVM sqrt" state of Core mechanism 3 reaches hundreds to
+// thousands of slots); lay part "smart merge".  Same rule as the other fold
+// chains.  One CTA of 512 threads runs one (b, h) row's events back to back;
+// the state stays in the workspace (it fits in L2), and per event:
+//   - the winner-take-all directions u_j = unit(sum_k_j - mean) live in the
+//     workspace as bf16 hi + lo rows; TMA streams them through shared memory
+//     in blocks of NB slots (double-buffered), and the similarity of the
+//     chunk's keys to each block is a tcgen05 MMA chain into one of two
+//     tensor-memory buffers, so block b + 1 multiplies while block b is
+//     scanned (four threads per token, 64 slot columns each, running best /
+//     second / argmax in registers);
+//   - chunks of up to 256 tokens are two 128-row MMA tiles (NB = 128 then,
+//     else NB = 256: each S buffer is 256 tensor-memory columns);
+//   - the slots the event touches are compacted (a slot bitmap, prefix counts
+//     and per-slot 256-bit token masks), and one warp per touched slot adds
+//     its tokens in position order (dims across lanes), then writes the new
+//     direction, the read view and the sums back;
+//   - the read view of every slot is copied to the event's snapshot.
+// The merge is deterministic: no atomics on data (token masks are OR-ed).
+#include <cstddef>
+
+#include "kvm_internal.cuh"
+#include "tc_primitives.cuh"
+
+namespace kvm {
+namespace foldbig {
+
+using namespace tc;
+
+constexpr int NT = 512;       // threads
+constexpr int NW = NT / 32;   // warps
+constexpr int MAXC = 256;     // tokens per event
+constexpr int MAXM = 4096;    // slots
+constexpr int ROWB = 128;     // bytes of a 64-dim bf16 row
+constexpr int TILE_BYTES = 128 * ROWB;  // 128 token rows
+
+struct Misc {
+    // 8-byte barriers first, then the 16-byte-accessed masks (the struct starts
+    // 1024-byte aligned)
+    unsigned long long bar_k[2], bar_u[2], bar_s[2];
+    uint32_t tmem_slot;
+    int abort_flag;
+    alignas(16) uint32_t tmask[MAXC][MAXC / 32];  // merged tokens of a touched slot
+    float g[MAXC], kn[MAXC], m[MAXC];
+    float pb[4][MAXC], ps[4][MAXC];  // per-thread partial best / second best
+    int pa[4][MAXC];                 // and argmax
+    int kind[MAXC], slot[MAXC];
+    uint32_t slotbits[MAXM / 32];    // slots the event touches
+    int wbase[MAXM / 32 + 4];        // prefix counts of slotbits (compact index of a slot)
+    int tslot[MAXC];                 // touched slot of each compact index
+    int kfound[MAXC];                // founding token of a touched slot (-1: merges only)
+    int wapp[NW];                    // appended tokens per warp (selection order)
+};
+static_assert(offsetof(Misc, tmask) % 16 == 0, "token masks are read as 16-byte vectors");
+constexpr int BODY_BYTES = 192 * 1024;  // U blocks + chunk buffers (either tiling)
+constexpr int SMEM_BYTES = BODY_BYTES + (int)sizeof(Misc) + 1024;
+
+__device__ __forceinline__ int swz(int row, int ch) { return row * ROWB + (((ch ^ (row & 7)) & 7) << 4); }
+// dims (2l, 2l + 1) of a 128-byte swizzled bf16 row, as a float2
+__device__ __forceinline__ float2 row_pair(const uint8_t* base, int row, int l) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(base + swz(row, l >> 2) + ((l & 3) << 2));
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// (b, s, arg) <- best / second best / argmax of two partial results over
+// disjoint slot sets (ties go to the lower slot index)
+__device__ __forceinline__ void combine(float& b, float& s, int& arg, float b2, float s2, int a2) {
+    if (a2 < 0) return;
+    if (arg < 0) {
+        b = b2;
+        s = s2;
+        arg = a2;
+        return;
+    }
+    if (b2 > b || (b2 == b && a2 < arg)) {
+        s = fmaxf(fmaxf(s, s2), b);
+        b = b2;
+        arg = a2;
+    } else {
+        s = fmaxf(fmaxf(s, s2), b2);
+    }
+}
+
+// Running best / argmax (and, with GAP, second best) over 32 columns of slots
+// base .. base + 31 restricted to [lo, hi); slots increase along the scan, so a
+// strictly larger value takes the lead and ties keep the lower index.
+template <bool GAP>
+__device__ __forceinline__ void scan32(const uint32_t (&v)[32], int base, int lo, int hi, float& b, float& s,
+                                       int& arg) {
+    if (base >= lo && base + 32 <= hi) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+            const float val = __uint_as_float(v[x]);
+            arg = val > b ? base + x : arg;
+            if (GAP) s = fmaxf(s, fminf(val, b));
+            b = fmaxf(b, val);
+        }
+    } else if (base + 32 > lo && base < hi) {
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+            const int j = base + x;
+            const float val = (j >= lo && j < hi) ? __uint_as_float(v[x]) : -INFINITY;
+            arg = val > b ? j : arg;
+            if (GAP) s = fmaxf(s, fminf(val, b));
+            b = fmaxf(b, val);
+        }
+    }
+}
+
+// One warp renormalises slot j from its key sums x (dims 2l, 2l + 1 on lane l):
+// writes the direction u = unit(x - mean) as bf16 hi + lo into the workspace row
+// (hi at elements [0, 64), lo at [64, 128)) and returns the centred pair and |c|^2.
+__device__ __forceinline__ float warp_dir(float2 x, int l, __nv_bfloat16* urow, float2& c, uint32_t& hi_out,
+                                         uint32_t& lo_out) {
+    const float mean = warp_sum(x.x + x.y) * (1.0f / 64.0f);
+    c = make_float2(x.x - mean, x.y - mean);
+    const float ss = warp_sum(c.x * c.x + c.y * c.y);
+    const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
+    const float ux = c.x * inv, uy = c.y * inv;
+    const uint32_t hi = pack2(ux, uy);
+    const float2 hf = unpack2(hi);
+    const uint32_t lo = pack2(ux - hf.x, uy - hf.y);
+    reinterpret_cast<uint32_t*>(urow)[l] = hi;
+    reinterpret_cast<uint32_t*>(urow)[32 + l] = lo;
+    hi_out = hi;
+    lo_out = lo;
+    return ss;
+}
+
+template <bool GAP>
+__global__ void __launch_bounds__(NT, 1)
+    fold_big_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_u, const FoldArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Misc& X = *reinterpret_cast<Misc*>(sm + BODY_BYTES);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int bh = blockIdx.x;
+    const int C = a.C, S = a.S, M = a.M;
+    const int T = C > 128 ? 2 : 1;       // 128-token MMA tiles per chunk
+    const int NB = 256 / T;              // slots per similarity block
+    const int UBUF = NB * ROWB * 2;      // one U block: hi rows then lo rows
+    const int OFF_K = 2 * UBUF;
+    const int CHB = T * TILE_BYTES;      // one chunk buffer (keys or values)
+    const int OFF_V = OFF_K + 2 * CHB;
+
+    float* g_sk = a.sum_k + (int64_t)bh * M * D;
+    float* g_sv = a.sum_v + (int64_t)bh * M * D;
+    int* g_cnt = a.counts + (int64_t)bh * M;
+    float* g_rho = a.rho + (int64_t)bh * M;
+    __nv_bfloat16* g_u = reinterpret_cast<__nv_bfloat16*>(a.simdir) + (int64_t)bh * M * 128;
+    __nv_bfloat16* g_vk = reinterpret_cast<__nv_bfloat16*>(a.view_k) + (int64_t)bh * M * D;
+    __nv_bfloat16* g_vv = reinterpret_cast<__nv_bfloat16*>(a.view_v) + (int64_t)bh * M * D;
+
+    const Sched sc_first = a.sched ? a.sched[a.e_begin] : a.sched0;
+    int n = sc_first.n_before;
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&X.bar_k[i]), 1);
+            mbar_init(smem_u32(&X.bar_u[i]), 1);
+            mbar_init(smem_u32(&X.bar_s[i]), 1);
+        }
+        X.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(smem_u32(&X.tmem_slot), 512);
+    // directions of the slots the state already holds (a decode-boundary fold, a
+    // later segment or an imported state): one warp per slot, from the key sums
+    for (int j = warp; j < n; j += NW) {
+        const float2 x = reinterpret_cast<const float2*>(g_sk + (int64_t)j * D)[lane];
+        float2 c;
+        uint32_t hw, lw;
+        warp_dir(x, lane, g_u + (int64_t)j * 128, c, hw, lw);
+    }
+    fence_proxy_async_all();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = X.tmem_slot;
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t idesc = idesc_bf16(128, NB, 0, 0);
+    const int q = warp & 3, G = warp >> 2;  // TMEM lane quarter, column group
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    // this thread's token row and the 64 slot columns it scans in a block
+    const int tok = (T == 1 ? 0 : (G >> 1) * 128) + q * 32 + lane;
+    const int colslot = T == 1 ? 64 * G : 64 * (G & 1);
+    const int part = T == 1 ? G : (G & 1);
+    const int nparts = T == 1 ? 4 : 2;
+
+    // thread 0's record of asynchronous work not yet seen complete (parity or -1)
+    int pend_k[2] = {-1, -1}, pend_u[2] = {-1, -1}, pend_s[2] = {-1, -1};
+    int ph_k[2] = {0, 0}, ph_u[2] = {0, 0}, ph_s[2] = {0, 0};  // uses of each barrier so far
+
+    auto load_chunk = [&](int e, int cb) {
+        const int64_t off = ((int64_t)e * C) % a.src_len;
+        const uint32_t bar = smem_u32(&X.bar_k[cb]);
+        pend_k[cb] = ph_k[cb] & 1;
+        mbar_expect_tx(bar, 2 * T * TILE_BYTES);
+        for (int t = 0; t < T; ++t) {
+            tma_load_3d(sbase + OFF_K + cb * CHB + t * TILE_BYTES, &tm_k, 0, (int)(off + 128 * t), bh, bar);
+            tma_load_3d(sbase + OFF_V + cb * CHB + t * TILE_BYTES, &tm_v, 0, (int)(off + 128 * t), bh, bar);
+        }
+    };
+    auto load_u = [&](int blk, int ub) {
+        const uint32_t bar = smem_u32(&X.bar_u[ub]);
+        pend_u[ub] = ph_u[ub] & 1;
+        mbar_expect_tx(bar, UBUF);
+        tma_load_3d(sbase + ub * UBUF, &tm_u, 0, blk * NB, bh, bar);
+        tma_load_3d(sbase + ub * UBUF + NB * ROWB, &tm_u, 64, blk * NB, bh, bar);
+    };
+    // S buffer sb = chunk keys (T tiles) x (u_hi + u_lo) of U buffer ub
+    auto issue_mma = [&](int cb, int ub, int sb) {
+        tc_fence_after();
+        for (int t = 0; t < T; ++t)
+            for (int ks = 0; ks < 4; ++ks)
+                for (int pt = 0; pt < 2; ++pt) {
+                    const uint64_t ad = sdesc_sw128(sbase + OFF_K + cb * CHB + t * TILE_BYTES + ks * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sbase + ub * UBUF + pt * NB * ROWB + ks * 32, 16, 1024);
+                    mma_bf16_ss(tmem + 256 * sb + t * NB, ad, bd, idesc, (ks | pt) ? 1u : 0u);
+                }
+        mma_commit(smem_u32(&X.bar_s[sb]));
+        pend_s[sb] = ph_s[sb] & 1;
+    };
+    auto wait_bar = [&](unsigned long long* bar, int& ph, int* pend) -> bool {
+        const bool ok = mbar_wait(smem_u32(bar), ph & 1, &X.abort_flag, a.status);
+        if (ok && pend) *pend = -1;
+        ++ph;
+        return ok;
+    };
+
+    if (tid == 0 && a.e_begin < a.e_end && !a.test_stall) load_chunk(a.e_begin, 0);
+    bool fail = false;
+    // gates are loaded one event ahead (off the chain): thread 2t holds token t's
+    auto gate_of = [&](int e) -> float {
+        const int t = tid >> 1;
+        return ((tid & 1) == 0 && t < C && e < a.e_end)
+                   ? a.g_src[(int64_t)bh * a.src_row + ((int64_t)e * C) % a.src_len + t]
+                   : 0.0f;
+    };
+    float g_nx = gate_of(a.e_begin);
+    for (int e = a.e_begin, it = 0; e < a.e_end; ++e, ++it) {
+        const int cb = it & 1;
+        const Sched sc = a.sched ? a.sched[e] : a.sched0;
+        const int64_t first_pos = (int64_t)e * C;
+        const int n0 = sc.n0, na = sc.a;
+        const int nb = n0 > S ? (n0 + NB - 1) / NB : 0;
+        const uint8_t* kch = sm + OFF_K + cb * CHB;
+        const uint8_t* vch = sm + OFF_V + cb * CHB;
+        const float g_here = g_nx;
+        if (!wait_bar(&X.bar_k[cb], ph_k[cb], tid == 0 ? &pend_k[cb] : nullptr)) fail = true;
+        g_nx = gate_of(e + 1);
+        if (tid == 0) {
+            // the next chunk loads into the buffer the previous event finished with
+            if (!fail && e + 1 < a.e_end) load_chunk(e + 1, cb ^ 1);
+            if (!fail && nb > 0) {
+                load_u(0, 0);
+                if (nb > 1) load_u(1, 1);
+                if (!wait_bar(&X.bar_u[0], ph_u[0], &pend_u[0])) fail = true;
+                else issue_mma(cb, 0, 0);
+            }
+        }
+        // per-token set-up: gates, key norms (two threads per token), kinds
+        {
+            const int t = tid >> 1, h = tid & 1;
+            if (tid < 2 * C) {
+                float ss = 0.0f;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int row = t & 127;
+                    const uint4 w = *reinterpret_cast<const uint4*>(kch + (t >> 7) * TILE_BYTES + swz(row, 4 * h + ch));
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 f = unpack2(wv[u]);
+                        ss = fmaf(f.x, f.x, ss);
+                        ss = fmaf(f.y, f.y, ss);
+                    }
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (h == 0) {
+                    X.g[t] = g_here;
+                    X.kn[t] = sqrtf(ss);
+                    const bool sink = first_pos + t < S;
+                    X.kind[t] = sink ? 2 : -1;
+                    X.slot[t] = sink ? (int)(first_pos + t) : -1;
+                }
+            }
+            for (int i = tid; i < (M + 31) / 32; i += NT) X.slotbits[i] = 0u;
+            for (int i = tid; i < MAXC * (MAXC / 32) / 4; i += NT)
+                reinterpret_cast<uint4*>(&X.tmask[0][0])[i] = make_uint4(0, 0, 0, 0);
+            if (tid < MAXC) X.kfound[tid] = -1;
+        }
+        if (__syncthreads_or(fail)) break;
+
+        // similarity blocks: MMA of block b + 1 runs while block b is scanned
+        float best = -INFINITY, sec = -INFINITY;
+        int barg = -1;
+        for (int b = 0; b < nb; ++b) {
+            const int sb = b & 1;
+            if (tid == 0 && b + 1 < nb) {
+                if (!wait_bar(&X.bar_u[(b + 1) & 1], ph_u[(b + 1) & 1], &pend_u[(b + 1) & 1])) fail = true;
+                else issue_mma(cb, (b + 1) & 1, (b + 1) & 1);
+            }
+            const bool ok = wait_bar(&X.bar_s[sb], ph_s[sb], tid == 0 ? &pend_s[sb] : nullptr);
+            fail = fail || !ok;
+            tc_fence_after();
+            // U buffer sb is free once this block's MMA completed
+            if (tid == 0 && !fail && b + 2 < nb) load_u(b + 2, sb);
+            if (!__any_sync(0xffffffffu, fail)) {
+                uint32_t va[32], vb[32];
+                const uint32_t ta = tmem + lane_base + 256 * sb + 64 * G;
+                tmem_ld32(ta, va);
+                tmem_ld32(ta + 32, vb);
+                tmem_wait_ld();
+                if (tok < C) {
+                    const int base = b * NB + colslot;
+                    scan32<GAP>(va, base, S, n0, best, sec, barg);
+                    scan32<GAP>(vb, base + 32, S, n0, best, sec, barg);
+                }
+            }
+            tc_fence_before();
+            if (__syncthreads_or(fail)) {
+                fail = true;
+                break;
+            }
+        }
+        if (fail) break;
+        if (tok < C) {
+            X.pb[part][tok] = best;
+            X.ps[part][tok] = sec;
+            X.pa[part][tok] = barg;
+        }
+        __syncthreads();
+        // combine the partials of each token; surprise score m_t
+        best = -INFINITY;
+        sec = -INFINITY;
+        barg = -1;
+        const bool cand = tid < C && X.kind[tid] != 2;
+        if (cand && nb > 0)
+            for (int p = 0; p < nparts; ++p) combine(best, sec, barg, X.pb[p][tid], X.ps[p][tid], X.pa[p][tid]);
+        const float kn = tid < C ? X.kn[tid] : 0.0f;
+        if (cand) X.m[tid] = barg < 0 ? -INFINITY : (kn > 0.0f ? best / kn : 0.0f);
+        else if (tid < C) X.m[tid] = INFINITY;  // sinks are never append candidates
+        __syncthreads();
+
+        // surprise selection: the a lowest scores (ties to the lower position) are appended
+        if (na > 0) {
+            // rank = candidates with a smaller score (ties: lower position); only whether
+            // it is below a matters, so the count stops there
+            int rank = 0;
+            if (cand) {
+                const float mt = X.m[tid];
+                for (int u = 0; u < C && rank < na; ++u) {
+                    const float mu = X.m[u];
+                    rank += (mu < mt) || (mu == mt && u < tid);
+                }
+            }
+            const bool app = cand && rank < na;
+            // appended slots in position order: warp ballots and their prefix
+            unsigned bal = 0;
+            if (warp < (C + 31) / 32) {
+                bal = __ballot_sync(0xffffffffu, app);
+                if (lane == 0) X.wapp[warp] = __popc(bal);
+            }
+            __syncthreads();
+            if (cand) X.kind[tid] = app ? 1 : 0;
+            if (app) {
+                int before = __popc(bal & ((1u << lane) - 1u));
+                for (int w = 0; w < warp; ++w) before += X.wapp[w];
+                X.slot[tid] = n0 + before;
+            }
+            __syncthreads();
+            // directions of the new slots (one warp each, from g * k of the founding
+            // token), staged as fp32 hi + lo in the U area and written to the workspace
+            float* ustage = reinterpret_cast<float*>(sm);
+            for (int t = warp; t < C; t += NW) {
+                if (X.kind[t] != 1) continue;
+                const int jn = X.slot[t];
+                const float g = X.g[t];
+                const float2 kk = row_pair(kch + (t >> 7) * TILE_BYTES, t & 127, lane);
+                float2 c;
+                uint32_t hw, lw;
+                warp_dir(make_float2(g * kk.x, g * kk.y), lane, g_u + (int64_t)jn * 128, c, hw, lw);
+                const float2 hf = unpack2(hw), lf = unpack2(lw);
+                reinterpret_cast<float2*>(ustage + (jn - n0) * D)[lane] = make_float2(hf.x + lf.x, hf.y + lf.y);
+            }
+            __syncthreads();
+            // the remaining tokens also compare against the new slots
+            if (tid < C && X.kind[tid] == 0) {
+                float kx[64];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(kch + (tid >> 7) * TILE_BYTES + swz(tid & 127, ch));
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 f = unpack2(wv[u]);
+                        kx[ch * 8 + 2 * u] = f.x;
+                        kx[ch * 8 + 2 * u + 1] = f.y;
+                    }
+                }
+                for (int jj = 0; jj < na; ++jj) {
+                    const float4* ur = reinterpret_cast<const float4*>(ustage + jj * D);
+                    float p[8];
+#pragma unroll
+                    for (int x4 = 0; x4 < 16; ++x4) {
+                        const float4 u4 = ur[x4];
+                        if (x4 < 2) {
+                            p[4 * x4] = kx[4 * x4] * u4.x;
+                            p[4 * x4 + 1] = kx[4 * x4 + 1] * u4.y;
+                            p[4 * x4 + 2] = kx[4 * x4 + 2] * u4.z;
+                            p[4 * x4 + 3] = kx[4 * x4 + 3] * u4.w;
+                        } else {
+                            const int o = (4 * x4) & 7;
+                            p[o] = fmaf(kx[4 * x4], u4.x, p[o]);
+                            p[o + 1] = fmaf(kx[4 * x4 + 1], u4.y, p[o + 1]);
+                            p[o + 2] = fmaf(kx[4 * x4 + 2], u4.z, p[o + 2]);
+                            p[o + 3] = fmaf(kx[4 * x4 + 3], u4.w, p[o + 3]);
+                        }
+                    }
+                    const float s = ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
+                    const int jn = n0 + jj;
+                    if (s > best) {
+                        sec = best;
+                        best = s;
+                        barg = jn;
+                    } else if (s > sec) {
+                        sec = s;
+                    }
+                }
+            }
+        } else if (cand) {
+            X.kind[tid] = 0;
+        }
+        if (tid < C && X.kind[tid] == 0) {
+            X.slot[tid] = barg;
+            if (barg < 0 && a.status) atomicOr(a.status, STATUS_DEVICE);
+        }
+        if (tid < C && e < a.dbg_events) {
+            const int64_t o = ((int64_t)bh * a.dbg_events + e) * C + tid;
+            const int kd = X.kind[tid];
+            if (a.dbg_assign) a.dbg_assign[o] = X.slot[tid];
+            if (a.dbg_kind) a.dbg_kind[o] = kd;
+            if (a.dbg_m) a.dbg_m[o] = kd == 2 ? __int_as_float(0x7fc00000) : X.m[tid];
+            if (GAP && a.dbg_gap) {
+                float gp = __int_as_float(0x7fc00000);
+                if (kd == 0) gp = sec == -INFINITY ? INFINITY : (kn > 0.0f ? (best - sec) / kn : 0.0f);
+                a.dbg_gap[o] = gp;
+            }
+        }
+        // touched slots: bitmap, then compact indices in slot order
+        if (tid < C && X.slot[tid] >= 0) atomicOr(&X.slotbits[X.slot[tid] >> 5], 1u << (X.slot[tid] & 31));
+        __syncthreads();
+        const int nwords = (sc.n_after + 31) / 32;
+        if (warp == 0) {
+            int cnts[4], tot = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int w = lane * 4 + i;
+                cnts[i] = w < nwords ? __popc(X.slotbits[w]) : 0;
+                tot += cnts[i];
+            }
+            int incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            int run = incl - tot;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                X.wbase[lane * 4 + i] = run;
+                run += cnts[i];
+            }
+            if (lane == 31) X.wbase[MAXM / 32] = run;
+        }
+        __syncthreads();
+        if (tid < C && X.slot[tid] >= 0) {
+            const int s = X.slot[tid];
+            const int k = X.wbase[s >> 5] + __popc(X.slotbits[s >> 5] & ((1u << (s & 31)) - 1u));
+            X.tslot[k] = s;
+            if (X.kind[tid] == 0) atomicOr(&X.tmask[k][tid >> 5], 1u << (tid & 31));
+            else X.kfound[k] = tid;
+        }
+        __syncthreads();
+        const int ntouched = X.wbase[MAXM / 32];
+
+        // owners: one warp per touched slot, dims (2l, 2l + 1) on lane l; a warp takes
+        // its slots four at a time and issues the state loads of the four together
+        for (int k0 = warp; k0 < ntouched; k0 += 4 * NW) {
+            float2 xk[4], xv[4];
+            int cnt[4];
+            float rho[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int k = k0 + i * NW;
+                if (k < ntouched && X.kfound[k] < 0) {
+                    const int j = X.tslot[k];
+                    xk[i] = reinterpret_cast<const float2*>(g_sk + (int64_t)j * D)[lane];
+                    xv[i] = reinterpret_cast<const float2*>(g_sv + (int64_t)j * D)[lane];
+                    cnt[i] = g_cnt[j];
+                    rho[i] = g_rho[j];
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int k = k0 + i * NW;
+                if (k >= ntouched) continue;
+                const int j = X.tslot[k];
+                const int ft = X.kfound[k];
+                if (ft >= 0) {
+                    const float gf = X.g[ft];
+                    const float2 kk = row_pair(kch + (ft >> 7) * TILE_BYTES, ft & 127, lane);
+                    const float2 vv = row_pair(vch + (ft >> 7) * TILE_BYTES, ft & 127, lane);
+                    xk[i] = make_float2(gf * kk.x, gf * kk.y);
+                    xv[i] = make_float2(gf * vv.x, gf * vv.y);
+                    cnt[i] = 1;
+                    rho[i] = sqrtf(warp_sum(vv.x * vv.x + vv.y * vv.y));
+                }
+                // merged tokens in position order
+#pragma unroll 1
+                for (int w8 = 0; w8 < (C + 31) / 32; ++w8) {
+                    uint32_t m = X.tmask[k][w8];
+                    while (m) {
+                        const int t = (w8 << 5) + __ffs(m) - 1;
+                        m &= m - 1;
+                        const float gt = X.g[t];
+                        const float2 kk = row_pair(kch + (t >> 7) * TILE_BYTES, t & 127, lane);
+                        const float2 vv = row_pair(vch + (t >> 7) * TILE_BYTES, t & 127, lane);
+                        xk[i] = make_float2(fmaf(gt, kk.x, xk[i].x), fmaf(gt, kk.y, xk[i].y));
+                        xv[i] = make_float2(fmaf(gt, vv.x, xv[i].x), fmaf(gt, vv.y, xv[i].y));
+                        ++cnt[i];
+                    }
+                }
+                reinterpret_cast<float2*>(g_sk + (int64_t)j * D)[lane] = xk[i];
+                reinterpret_cast<float2*>(g_sv + (int64_t)j * D)[lane] = xv[i];
+                if (lane == 0) {
+                    g_cnt[j] = cnt[i];
+                    g_rho[j] = rho[i];
+                }
+                // direction, read key LayerNorm(sum / count) = c / sqrt(|c|^2 / 64 + eps count^2)
+                // with the rotary dims zeroed, read value rho * unit(sum_v) (or sum_v / count)
+                float2 c;
+                uint32_t hw, lw;
+                const float ss = warp_dir(xk[i], lane, g_u + (int64_t)j * 128, c, hw, lw);
+                const float fc = (float)cnt[i];
+                const float rs = 1.0f / sqrtf(ss * (1.0f / 64.0f) + a.ln_eps * fc * fc);
+                const int d0 = 2 * lane;
+                reinterpret_cast<uint32_t*>(g_vk + (int64_t)j * D)[lane] =
+                    pack2(d0 < a.r ? 0.0f : c.x * rs, d0 + 1 < a.r ? 0.0f : c.y * rs);
+                const float nv = sqrtf(warp_sum(xv[i].x * xv[i].x + xv[i].y * xv[i].y));
+                const float f = a.no_vnorm ? 1.0f / fc : (nv > 0.0f ? rho[i] / nv : 0.0f);
+                reinterpret_cast<uint32_t*>(g_vv + (int64_t)j * D)[lane] = pack2(xv[i].x * f, xv[i].y * f);
+            }
+        }
+        // the next event's TMA reads the directions written above
+        fence_proxy_async_all();
+        __syncthreads();
+        n = sc.n_after;
+        // snapshot of the read view after this event
+        if (a.snap_k && e < a.snap_events) {
+            const int64_t base = ((int64_t)bh * a.snap_events + e) * M * ROWB;
+            const int nchunks = n * ROWB / 16;
+            const uint4* sk4 = reinterpret_cast<const uint4*>(g_vk);
+            const uint4* sv4 = reinterpret_cast<const uint4*>(g_vv);
+            uint4* dk4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_k) + base);
+            uint4* dv4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_v) + base);
+            for (int i = tid; i < nchunks; i += NT) {
+                const uint4 wk = sk4[i], wv = sv4[i];
+                dk4[i] = wk;
+                dv4[i] = wv;
+            }
+        }
+    }
+
+    // after an abort: let the copies and MMAs this CTA issued land before its shared
+    // and tensor memory are released (each wait bounded; they depend on nothing else)
+    if (tid == 0 && X.abort_flag) {
+        auto drain = [&](unsigned long long* bar, int parity) {
+            if (parity < 0) return;
+            const long long t0 = clock64();
+            while (!mbar_try(smem_u32(bar), (uint32_t)parity) && clock64() - t0 < (1ll << 28)) {
+            }
+        };
+        for (int i = 0; i < 2; ++i) {
+            drain(&X.bar_k[i], pend_k[i]);
+            drain(&X.bar_u[i], pend_u[i]);
+            drain(&X.bar_s[i], pend_s[i]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace foldbig
+
+bool fold_big_supported(const FoldArgs& a, bool bf16) {
+    return bf16 && a.C >= 16 && a.C <= foldbig::MAXC && a.M <= foldbig::MAXM;
+}
+
+cudaError_t launch_fold_big(const FoldArgs& a, cudaStream_t s) {
+    using namespace foldbig;
+    const int T = a.C > 128 ? 2 : 1;
+    const int NB = 256 / T;
+    CUtensorMap mk, mv, mu;
+    if (!make_tmap_bf16_3d(&mk, a.k_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
+        !make_tmap_bf16_3d(&mv, a.v_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
+        !make_tmap_bf16_rows(&mu, a.simdir, 128, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)NB))
+        return cudaErrorInvalidValue;
+    auto kern = a.dbg_gap ? fold_big_kernel<true> : fold_big_kernel<false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    kern<<<a.BH, NT, SMEM_BYTES, s>>>(mk, mv, mu, a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvm

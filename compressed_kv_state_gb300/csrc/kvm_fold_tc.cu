@@ -39,21 +39,19 @@ constexpr int OFF_UHI = 0;                      // [256][128 B] swizzled (MMA B 
 constexpr int OFF_ULO = OFF_UHI + MAXS * ROWB;  // [256][128 B] swizzled
 constexpr int OFF_K = OFF_ULO + MAXS * ROWB;    // 2 x [128][128 B] swizzled chunk keys
 constexpr int OFF_V = OFF_K + 2 * TOK * ROWB;   // 2 x [128][128 B] swizzled chunk values
-constexpr int OFF_VK = OFF_V + 2 * TOK * ROWB;  // [256][128 B] read-view keys (plain rows)
-constexpr int OFF_VV = OFF_VK + MAXS * ROWB;    // [256][128 B] read-view values (plain rows)
+constexpr int OFF_VK = OFF_V + 2 * TOK * ROWB;  // [256][128 B] swizzled read-view keys
+constexpr int OFF_VV = OFF_VK + MAXS * ROWB;    // [256][128 B] swizzled read-view values
 constexpr int OFF_MISC = OFF_VV + MAXS * ROWB;
 
 struct Misc {
     float g[TOK], kn[TOK], m[TOK];
     float pb[4][TOK], ps[4][TOK];  // best / second best of each 64-slot quarter
     int pa[4][TOK];                // argmax of each quarter
-    int kind[TOK], slot[TOK], list[TOK];
-    int hist[4][MAXS];  // merged tokens per slot, per token warp
+    int kind[TOK], slot[TOK];
+    uint32_t tmask[MAXS][4];  // merged tokens of each slot: bit t of the 128-bit mask = token t
     int cnt[MAXS];      // written by key owners
     float rho[MAXS];    // written by value owners
     int cntv[MAXS];     // value owners' copy of the counts (read value of the no-norm ablation)
-    int cnt_new[MAXS];
-    int seg[MAXS + 1];
     int slot_tok[MAXS];
     unsigned long long bar_k[2];
     unsigned long long bar_s;
@@ -64,7 +62,8 @@ struct Misc {
 constexpr int SMEM_BYTES = OFF_MISC + (int)sizeof(Misc) + 1024;
 
 #ifdef KVM_PROBE
-static __device__ unsigned long long g_probe_fold[16];
+// per-phase cycles of four sample threads (0, 255, 256, 511), 20 counters each
+static __device__ unsigned long long g_probe_fold[80];
 #endif
 
 __device__ __forceinline__ int swz(int row, int ch) { return row * ROWB + (((ch ^ (row & 7)) & 7) << 4); }
@@ -159,54 +158,6 @@ __device__ __forceinline__ float dot64(const float (&x)[64], const float (&y)[64
     return ((p[0] + p[1]) + (p[2] + p[3])) + ((p[4] + p[5]) + (p[6] + p[7]));
 }
 
-// Key owner's renormalisation of slot j from its key sums (centred in place):
-// the winner-take-all direction u = c / |c| (as bf16 hi + lo terms) and the
-// read-view key LayerNorm(sum / count) = c / sqrt(|c|^2 / 64 + eps * count^2),
-// both from the centred sums c = sum - mean(sum); rotary dims of the key are 0.
-__device__ __forceinline__ void key_view_inplace(int j, float (&c)[64], int cnt, int r, float eps, uint8_t* sm) {
-    const float mean = sum64(c) * (1.0f / 64.0f);
-#pragma unroll
-    for (int x = 0; x < 64; ++x) c[x] -= mean;
-    const float ss = dot64(c, c);
-    const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
-    const float fc = (float)cnt;
-    const float rs = 1.0f / sqrtf(ss * (1.0f / 64.0f) + eps * fc * fc);
-    uint4* vk = reinterpret_cast<uint4*>(sm + OFF_VK + j * ROWB);
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint32_t hi[4], lo[4], wk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int x0 = ch * 8 + 2 * u;
-            const float a0 = c[x0] * inv, a1 = c[x0 + 1] * inv;
-            const __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-            const float2 hf = __bfloat1622float2(h);
-            const __nv_bfloat162 lw = __floats2bfloat162_rn(a0 - hf.x, a1 - hf.y);
-            hi[u] = *reinterpret_cast<const uint32_t*>(&h);
-            lo[u] = *reinterpret_cast<const uint32_t*>(&lw);
-            wk[u] = (x0 + 1 < r) ? 0u : pack2(x0 < r ? 0.0f : c[x0] * rs, c[x0 + 1] * rs);
-        }
-        *reinterpret_cast<uint4*>(sm + OFF_UHI + swz(j, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sm + OFF_ULO + swz(j, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        vk[ch] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-    }
-}
-
-// Value owner's read view of slot j: rho * unit(sum_v) (with the no-norm
-// ablation, the member mean sum_v / count: rho < 0 carries -1 / count).
-__device__ __forceinline__ void value_view(int j, const float (&sv)[64], float rho, uint8_t* sm) {
-    const float nv = sqrtf(dot64(sv, sv));
-    const float f = rho < 0.0f ? -rho : (nv > 0.0f ? rho / nv : 0.0f);
-    uint4* vv = reinterpret_cast<uint4*>(sm + OFF_VV + j * ROWB);
-#pragma unroll
-    for (int ch = 0; ch < 8; ++ch) {
-        uint32_t wv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) wv[u] = pack2(sv[ch * 8 + 2 * u] * f, sv[ch * 8 + 2 * u + 1] * f);
-        vv[ch] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-    }
-}
-
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&x)[64]) {
     uint32_t a[32], b[32];
     tmem_ld32(taddr, a);
@@ -224,6 +175,135 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const float (&x)[64]) 
     for (int i = 0; i < 32; ++i) {
         a[i] = __float_as_uint(x[i]);
         b[i] = __float_as_uint(x[32 + i]);
+    }
+    tmem_st32(taddr, a);
+    tmem_st32(taddr + 32, b);
+}
+
+// ---- packed fp32 (two lanes per instruction, sm_100 family) versions of the
+// owner-phase arithmetic.  Pair i holds dims (2i, 2i + 1); every reduction keeps
+// the order of the scalar helpers above (partial sums by dim mod 8, combined
+// pairwise), and a packed fused multiply-add rounds each lane once exactly like
+// fmaf, so the results are the scalar ones bit for bit.
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 bf2u(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// x = g * row
+__device__ __forceinline__ void set_row_sw2(const uint8_t* base, int row, float g, float2 (&x)[32]) {
+    const float2 g2 = f2(g);
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(base + swz(row, ch));
+        x[4 * ch + 0] = __fmul2_rn(g2, bf2u(w.x));
+        x[4 * ch + 1] = __fmul2_rn(g2, bf2u(w.y));
+        x[4 * ch + 2] = __fmul2_rn(g2, bf2u(w.z));
+        x[4 * ch + 3] = __fmul2_rn(g2, bf2u(w.w));
+    }
+}
+// x += g * row
+__device__ __forceinline__ void add_row_sw2(const uint8_t* base, int row, float g, float2 (&x)[32]) {
+    const float2 g2 = f2(g);
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        const uint4 w = *reinterpret_cast<const uint4*>(base + swz(row, ch));
+        x[4 * ch + 0] = __ffma2_rn(g2, bf2u(w.x), x[4 * ch + 0]);
+        x[4 * ch + 1] = __ffma2_rn(g2, bf2u(w.y), x[4 * ch + 1]);
+        x[4 * ch + 2] = __ffma2_rn(g2, bf2u(w.z), x[4 * ch + 2]);
+        x[4 * ch + 3] = __ffma2_rn(g2, bf2u(w.w), x[4 * ch + 3]);
+    }
+}
+__device__ __forceinline__ float fold8(const float2 (&p)[4]) {
+    return ((p[0].x + p[0].y) + (p[1].x + p[1].y)) + ((p[2].x + p[2].y) + (p[3].x + p[3].y));
+}
+__device__ __forceinline__ float sum64_2(const float2 (&x)[32]) {
+    float2 p[4] = {x[0], x[1], x[2], x[3]};
+#pragma unroll
+    for (int i = 4; i < 32; ++i) p[i & 3] = __fadd2_rn(p[i & 3], x[i]);
+    return fold8(p);
+}
+__device__ __forceinline__ float dot64_2(const float2 (&x)[32], const float2 (&y)[32]) {
+    float2 p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __fmul2_rn(x[i], y[i]);
+#pragma unroll
+    for (int i = 4; i < 32; ++i) p[i & 3] = __ffma2_rn(x[i], y[i], p[i & 3]);
+    return fold8(p);
+}
+__device__ __forceinline__ uint32_t pack2f(float2 v) { return pack2(v.x, v.y); }
+
+// Key owner, part 1 (on the chain's critical path): centre the key sums in place
+// and write the winner-take-all direction u = c / |c| as bf16 hi + lo terms.
+// Returns |c|^2.
+__device__ __forceinline__ float key_dir2(int j, float2 (&c)[32], uint8_t* sm) {
+    const float2 m2 = f2(-(sum64_2(c) * (1.0f / 64.0f)));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) c[i] = __fadd2_rn(c[i], m2);
+    const float ss = dot64_2(c, c);
+    const float2 inv = f2(ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f);
+    const float2 neg1 = f2(-1.0f);
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 a = __fmul2_rn(c[4 * ch + u], inv);
+            hi[u] = pack2f(a);
+            lo[u] = pack2f(__ffma2_rn(bf2u(hi[u]), neg1, a));  // a - hi, exact
+        }
+        *reinterpret_cast<uint4*>(sm + OFF_UHI + swz(j, ch)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sm + OFF_ULO + swz(j, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+    return ss;
+}
+// Key owner, part 2: the read-view key LayerNorm(sum / count) =
+// c / sqrt(|c|^2 / 64 + eps * count^2) with the rotary dims [0, r) zeroed.
+__device__ __forceinline__ void key_view2(int j, const float2 (&c)[32], float ss, int cnt, int r, float eps,
+                                          uint8_t* sm) {
+    const float fc = (float)cnt;
+    const float2 rs = f2(1.0f / sqrtf(ss * (1.0f / 64.0f) + eps * fc * fc));
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        uint32_t wk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int x0 = ch * 8 + 2 * u;
+            const float2 y = __fmul2_rn(c[4 * ch + u], rs);
+            wk[u] = (x0 + 1 < r) ? 0u : pack2(x0 < r ? 0.0f : y.x, y.y);
+        }
+        *reinterpret_cast<uint4*>(sm + OFF_VK + swz(j, ch)) = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+    }
+}
+// Value owner's read view: rho * unit(sum_v) (with the no-norm ablation, the
+// member mean sum_v / count: rho < 0 carries -1 / count).
+__device__ __forceinline__ void value_view2(int j, const float2 (&sv)[32], float rho, uint8_t* sm) {
+    const float nv = sqrtf(dot64_2(sv, sv));
+    const float2 f = f2(rho < 0.0f ? -rho : (nv > 0.0f ? rho / nv : 0.0f));
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(sm + OFF_VV + swz(j, ch)) =
+            make_uint4(pack2f(__fmul2_rn(sv[4 * ch], f)), pack2f(__fmul2_rn(sv[4 * ch + 1], f)),
+                       pack2f(__fmul2_rn(sv[4 * ch + 2], f)), pack2f(__fmul2_rn(sv[4 * ch + 3], f)));
+}
+__device__ __forceinline__ void tmem_ld64_2(uint32_t taddr, float2 (&x)[32]) {
+    uint32_t a[32], b[32];
+    tmem_ld32(taddr, a);
+    tmem_ld32(taddr + 32, b);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        x[i] = make_float2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+        x[16 + i] = make_float2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+    }
+}
+__device__ __forceinline__ void tmem_st64_2(uint32_t taddr, const float2 (&x)[32]) {
+    uint32_t a[32], b[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[2 * i] = __float_as_uint(x[i].x);
+        a[2 * i + 1] = __float_as_uint(x[i].y);
+        b[2 * i] = __float_as_uint(x[16 + i].x);
+        b[2 * i + 1] = __float_as_uint(x[16 + i].y);
     }
     tmem_st32(taddr, a);
     tmem_st32(taddr + 32, b);
@@ -273,6 +353,8 @@ template <bool GAP>
 __global__ void __launch_bounds__(NT, 1)
     fold_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_sk, const __grid_constant__ CUtensorMap tm_sv,
+                   const __grid_constant__ CUtensorMap tm_snk, const __grid_constant__ CUtensorMap tm_snv,
+                   const __grid_constant__ CUtensorMap tm_vk, const __grid_constant__ CUtensorMap tm_vv,
                    const FoldArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -285,8 +367,6 @@ __global__ void __launch_bounds__(NT, 1)
 
     int* g_counts = a.counts + (int64_t)bh * M;
     float* g_rho = a.rho + (int64_t)bh * M;
-    uint8_t* g_view_k = reinterpret_cast<uint8_t*>(a.view_k) + (int64_t)bh * M * ROWB;
-    uint8_t* g_view_v = reinterpret_cast<uint8_t*>(a.view_v) + (int64_t)bh * M * ROWB;
 
     // state before the first event (non-empty for a decode-boundary fold or a later segment)
     const Sched sc_first = a.sched ? a.sched[a.e_begin] : a.sched0;
@@ -335,7 +415,7 @@ __global__ void __launch_bounds__(NT, 1)
     int pend_st = -1, pend_ld[2] = {-1, -1}, pend_mma = -1;
 
     {
-        float x[64];
+        float2 x[32];
         if (nblk_st > 0) {
             if (tid == 0 && !mbar_wait(smem_u32(&X.bar_st), 0, &X.abort_flag, a.status)) {
                 X.abort_flag = 1;
@@ -348,25 +428,24 @@ __global__ void __launch_bounds__(NT, 1)
         for (int q = 0; q < 16; ++q) {
             const float4 f = (j < n && !X.abort_flag) ? *reinterpret_cast<const float4*>(stage + stage_off(j, q))
                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-            x[4 * q] = f.x;
-            x[4 * q + 1] = f.y;
-            x[4 * q + 2] = f.z;
-            x[4 * q + 3] = f.w;
+            x[2 * q] = make_float2(f.x, f.y);
+            x[2 * q + 1] = make_float2(f.z, f.w);
         }
         __syncthreads();  // the staging areas are free again
-        tmem_st64(t_own, x);
+        tmem_st64_2(t_own, x);
         tmem_wait_st();
         if (j < n) {
             if (!vside) {
                 const int cnt = g_counts[j];
                 X.cnt[j] = cnt;
-                key_view_inplace(j, x, cnt, a.r, a.ln_eps, sm);
+                const float ss = key_dir2(j, x, sm);
+                key_view2(j, x, ss, cnt, a.r, a.ln_eps, sm);
             } else {
                 const float rho = g_rho[j];
                 const int cnt = g_counts[j];
                 X.rho[j] = rho;
                 X.cntv[j] = cnt;
-                value_view(j, x, a.no_vnorm ? -1.0f / (float)cnt : rho, sm);
+                value_view2(j, x, a.no_vnorm ? -1.0f / (float)cnt : rho, sm);
             }
         } else {
             // slots not founded yet: zero direction (S = 0) and zero read view
@@ -376,9 +455,9 @@ __global__ void __launch_bounds__(NT, 1)
                 if (!vside) {
                     *reinterpret_cast<uint4*>(sm + OFF_UHI + swz(j, ch)) = z;
                     *reinterpret_cast<uint4*>(sm + OFF_ULO + swz(j, ch)) = z;
-                    *reinterpret_cast<uint4*>(sm + OFF_VK + j * ROWB + ch * 16) = z;
+                    *reinterpret_cast<uint4*>(sm + OFF_VK + swz(j, ch)) = z;
                 } else {
-                    *reinterpret_cast<uint4*>(sm + OFF_VV + j * ROWB + ch * 16) = z;
+                    *reinterpret_cast<uint4*>(sm + OFF_VV + swz(j, ch)) = z;
                 }
             }
         }
@@ -395,10 +474,27 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_3d(sK + buf * TOK * ROWB, &tm_k, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
         tma_load_3d(sV + buf * TOK * ROWB, &tm_v, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
     };
-    if (tid == 0 && a.e_begin < a.e_end && !a.test_stall) load_chunk(a.e_begin, 0);
+    // the first two chunks load now; chunk e + 2 is issued at the end of event e
+    if (tid == 0 && a.e_begin < a.e_end && !a.test_stall) {
+        load_chunk(a.e_begin, 0);
+        if (a.e_begin + 1 < a.e_end) load_chunk(a.e_begin + 1, 1);
+    }
     const uint32_t idesc = idesc_bf16(128, 256, 0, 0);
     int mma_count = 0;
-    KVM_PROBE_DECL(13)
+    bool mma_early = false;  // thread 0: this event's similarity MMA was issued by the previous event
+    // S = k (u_hi + u_lo)^T for the 128 chunk keys in buffer b against all 256 slot directions
+    auto issue_mma = [&](int b) {
+        tc_fence_after();
+        for (int ks = 0; ks < 4; ++ks)
+            for (int part = 0; part < 2; ++part) {
+                const uint64_t ad = sdesc_sw128(sK + b * TOK * ROWB + ks * 32, 16, 1024);
+                const uint64_t bd = sdesc_sw128((part ? sUL : sUH) + ks * 32, 16, 1024);
+                mma_bf16_ss(tmem + 256, ad, bd, idesc, (ks | part) ? 1u : 0u);
+            }
+        mma_commit(bar_s);
+        pend_mma = mma_count & 1;
+    };
+    KVM_PROBE_DECL(20)
     KVM_PROBE_START()
 
     // the next event's schedule entry and gates are loaded one event ahead, off the chain
@@ -430,21 +526,8 @@ __global__ void __launch_bounds__(NT, 1)
         const bool do_mma = n0 > S;
 
         // similarity of the chunk's keys to every slot direction
-        if (tid == 0 && !fail) {
-            if (do_mma) {
-                tc_fence_after();
-                for (int ks = 0; ks < 4; ++ks)
-                    for (int part = 0; part < 2; ++part) {
-                        const uint64_t ad = sdesc_sw128(sK + buf * TOK * ROWB + ks * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128((part ? sUL : sUH) + ks * 32, 16, 1024);
-                        mma_bf16_ss(tmem + 256, ad, bd, idesc, (ks | part) ? 1u : 0u);
-                    }
-                mma_commit(bar_s);
-                pend_mma = mma_count & 1;
-            }
-            // the next chunk's keys and values load while this event runs
-            if (e + 1 < a.e_end) load_chunk(e + 1, buf ^ 1);
-        }
+        if (tid == 0 && !fail && do_mma && !mma_early) issue_mma(buf);
+        mma_early = false;
         if (tid < C) X.g[tid] = g_here;
         // per-token set-up: two threads per token (warps 8-15), 32 dims each
         if (vside) {
@@ -459,9 +542,8 @@ __global__ void __launch_bounds__(NT, 1)
             }
         } else {
             X.slot_tok[j] = -1;
+            *reinterpret_cast<uint4*>(&X.tmask[j][0]) = make_uint4(0, 0, 0, 0);
         }
-        X.hist[tid >> 8][j] = 0;
-        X.hist[2 + (tid >> 8)][j] = 0;
         KVM_PROBE_LAP(1)
 
         // best / second / argmax over the mergeable slots [S, n0): each quarter of
@@ -620,50 +702,13 @@ __global__ void __launch_bounds__(NT, 1)
         }
 
         KVM_PROBE_LAP(4)
-        // merge lists: merged tokens grouped by slot, position order inside a slot.
-        // A token's rank among earlier tokens of its slot = earlier lanes of its
-        // warp with the same slot (match_any) + the same slot's count in earlier warps.
-        int rank_in_slot = 0, sj = -1;
-        const bool merged = tid < C && X.kind[tid] == 0 && X.slot[tid] >= 0;
-        if (warp < 4) {
-            sj = merged ? X.slot[tid] : -1;
-            const unsigned same = __match_any_sync(0xffffffffu, merged ? sj : MAXS + (tid & 31));
-            const int lane = tid & 31;
-            rank_in_slot = __popc(same & ((1u << lane) - 1u));
-            if (merged && rank_in_slot == 0) X.hist[warp][sj] = __popc(same);
-        }
-        __syncthreads();
-        if (merged)
-            for (int w = 0; w < warp; ++w) rank_in_slot += X.hist[w][sj];
-        if (warp == 0) {
-            // merged tokens per slot, then their exclusive scan (list offsets)
-            const int lane = tid & 31;
-            int v8[8], sacc = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int jj = lane * 8 + i;
-                v8[i] = X.hist[0][jj] + X.hist[1][jj] + X.hist[2][jj] + X.hist[3][jj];
-                X.cnt_new[jj] = v8[i];
-                sacc += v8[i];
-            }
-            int incl = sacc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            int run = incl - sacc;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                X.seg[lane * 8 + i] = run;
-                run += v8[i];
-            }
-            if (lane == 31) X.seg[MAXS] = run;
-            // the previous snapshot store must have finished reading the view
-            if (lane == 0) bulk_wait_read();
-        }
-        __syncthreads();
-        if (merged) X.list[X.seg[sj] + rank_in_slot] = tid;
+        // merge lists: each merged token sets its bit in its slot's 128-bit token mask
+        // (OR commutes, so the masks do not depend on timing); an owner then visits
+        // its tokens in position order, lowest bit first
+        if (tid < C && X.kind[tid] == 0 && X.slot[tid] >= 0)
+            atomicOr(&X.tmask[X.slot[tid]][tid >> 5], 1u << (tid & 31));
+        // the previous snapshot store must have finished reading the view
+        if (tid == 0) bulk_wait_read();
         __syncthreads();
         KVM_PROBE_LAP(5)
 
@@ -671,14 +716,16 @@ __global__ void __launch_bounds__(NT, 1)
         // count; value owner: value sums and read radius), then the new read view
         {
             const int ft = X.slot_tok[j];
-            const int nm = X.cnt_new[j];
+            const uint4 mk = *reinterpret_cast<const uint4*>(&X.tmask[j][0]);
+            const int nm = __popc(mk.x) + __popc(mk.y) + __popc(mk.z) + __popc(mk.w);
             const bool touched = ft >= 0 || nm > 0;
-            if (__any_sync(0xffffffffu, touched)) {
-                const int b0 = X.seg[j];
+            const bool wtouched = __any_sync(0xffffffffu, touched);
+            float2 x[32];
+            int cnt = 0;
+            float ss = 0.0f;
+            if (wtouched) {
                 const uint8_t* rows = vside ? vch : kch;
-                float x[64];
-                tmem_ld64(t_own, x);
-                int cnt = 0;
+                tmem_ld64_2(t_own, x);
                 float rho = 0.0f;
                 if (touched) {
                     if (!vside) cnt = X.cnt[j];
@@ -687,27 +734,52 @@ __global__ void __launch_bounds__(NT, 1)
                         cnt = X.cntv[j];
                     }
                     if (ft >= 0) {
-                        set_row_sw(rows, ft, X.g[ft], x);
+                        set_row_sw2(rows, ft, X.g[ft], x);
                         cnt = 0;
                         if (vside) rho = sqrtf(sq_row_sw<8>(vch, ft, 0));
                     }
                     // merged tokens in position order
-                    for (int i = b0; i < b0 + nm; ++i) {
-                        const int t = X.list[i];
-                        add_row_sw(rows, t, X.g[t], x);
+                    const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
+#pragma unroll
+                    for (int w4 = 0; w4 < 4; ++w4) {
+                        uint32_t m = mw[w4];
+                        while (m) {
+                            const int t = (w4 << 5) + __ffs(m) - 1;
+                            m &= m - 1;
+                            add_row_sw2(rows, t, X.g[t], x);
+                        }
                     }
                     cnt += nm + (ft >= 0 ? 1 : 0);
                 }
-                tmem_st64(t_own, x);
+                KVM_PROBE_LAP(13)
+                tmem_st64_2(t_own, x);
                 tmem_wait_st();
+                KVM_PROBE_LAP(14)
                 if (touched) {
                     if (!vside) {
                         X.cnt[j] = cnt;
-                        key_view_inplace(j, x, cnt, a.r, a.ln_eps, sm);
+                        ss = key_dir2(j, x, sm);
+                        KVM_PROBE_LAP(15)
+                        key_view2(j, x, ss, cnt, a.r, a.ln_eps, sm);
                     } else {
                         X.rho[j] = rho;
                         X.cntv[j] = cnt;
-                        value_view(j, x, a.no_vnorm ? -1.0f / (float)cnt : rho, sm);
+                        value_view2(j, x, a.no_vnorm ? -1.0f / (float)cnt : rho, sm);
+                    }
+                }
+            }
+            if (!vside) {
+                // every direction of this event is written: thread 0 issues the next
+                // event's similarity MMA now, while the value owners finish
+                fence_proxy_async();
+                KVM_PROBE_LAP(16)
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                KVM_PROBE_LAP(17)
+                if (tid == 0 && e + 1 < a.e_end && !X.abort_flag && sc_nx.n0 > S) {
+                    if (mbar_wait(smem_u32(&X.bar_k[buf ^ 1]), ((it + 1) >> 1) & 1, &X.abort_flag, a.status)) {
+                        pend_ld[buf ^ 1] = -1;
+                        issue_mma(buf ^ 1);
+                        mma_early = true;
                     }
                 }
             }
@@ -718,12 +790,15 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         tc_fence_after();
 
+        // chunk e + 2 loads into this event's buffer (its readers passed the barrier
+        // above), ahead of the snapshot copies in the copy engine's queue
+        if (tid == 0 && e + 2 < a.e_end) load_chunk(e + 2, buf);
         // snapshot of the read view after this event (async bulk copy)
         if (tid == 0 && a.snap_k && e < a.snap_events) {
-            const int64_t base = ((int64_t)bh * a.snap_events + e) * M * ROWB;
-            const uint32_t bytes = (uint32_t)sc.n_after * ROWB;
-            bulk_store(reinterpret_cast<uint8_t*>(a.snap_k) + base, smem_u32(sm + OFF_VK), bytes);
-            bulk_store(reinterpret_cast<uint8_t*>(a.snap_v) + base, smem_u32(sm + OFF_VV), bytes);
+            // the swizzled view rows leave by TMA tensor stores (the copy engine unswizzles)
+            const int plane = bh * a.snap_events + e;
+            tma_store_3d(&tm_snk, smem_u32(sm + OFF_VK), 0, 0, plane);
+            tma_store_3d(&tm_snv, smem_u32(sm + OFF_VV), 0, 0, plane);
             bulk_commit();
         }
         n = sc.n_after;
@@ -757,13 +832,14 @@ __global__ void __launch_bounds__(NT, 1)
                 tma_store_3d(&tm_sk, smem_u32(sm + OFF_UHI) + o, 32 * h, b * srows, bh);
                 tma_store_3d(&tm_sv, smem_u32(sm + OFF_K) + o, 32 * h, b * srows, bh);
             }
-        bulk_store(g_view_k, smem_u32(sm + OFF_VK), (uint32_t)n * ROWB);
-        bulk_store(g_view_v, smem_u32(sm + OFF_VV), (uint32_t)n * ROWB);
+        tma_store_3d(&tm_vk, smem_u32(sm + OFF_VK), 0, 0, bh);
+        tma_store_3d(&tm_vv, smem_u32(sm + OFF_VV), 0, 0, bh);
         bulk_commit();
         bulk_wait_all();
     }
     KVM_PROBE_LAP(10)
-    if (tid == 0) KVM_PROBE_FLUSH(g_probe_fold, 0, 13)
+    if (tid == 0 || tid == 255 || tid == 256 || tid == 511)
+        KVM_PROBE_FLUSH(g_probe_fold, 20 * (tid == 0 ? 0 : tid == 255 ? 1 : tid == 256 ? 2 : 3), 20)
     // after an abort: let the copies and MMAs this CTA issued land before its shared
     // and tensor memory are released (each wait bounded; they depend on nothing else)
     if (tid == 0 && X.abort_flag) {
@@ -795,16 +871,24 @@ bool fold_tc_supported(const FoldArgs& a, bool bf16) { return bf16 && a.C <= 128
 cudaError_t launch_fold_tc(const FoldArgs& args, cudaStream_t s) {
     FoldArgs a = args;
     a.stage_rows = a.M < foldtc::STAGE_ROWS ? a.M : foldtc::STAGE_ROWS;
-    CUtensorMap mk, mv, msk, msv;
+    CUtensorMap mk, mv, msk, msv, msnk, msnv, mvk, mvv;
+    // read view: [BH][M][64] bf16 stored a whole state (M <= 256 rows) per box;
+    // snapshots [BH * events][M][64] (the view maps again when there are none)
+    const bool snaps = a.snap_k && a.snap_events > 0;
+    const uint64_t snap_planes = snaps ? (uint64_t)a.BH * a.snap_events : (uint64_t)a.BH;
     if (!make_tmap_bf16_3d(&mk, a.k_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
         !make_tmap_bf16_3d(&mv, a.v_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
         !make_tmap_f32_3d(&msk, a.sum_k, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows) ||
-        !make_tmap_f32_3d(&msv, a.sum_v, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows))
+        !make_tmap_f32_3d(&msv, a.sum_v, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows) ||
+        !make_tmap_bf16_3d(&mvk, a.view_k, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.M) ||
+        !make_tmap_bf16_3d(&mvv, a.view_v, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.M) ||
+        !make_tmap_bf16_3d(&msnk, snaps ? a.snap_k : a.view_k, (uint64_t)a.M, snap_planes, (uint32_t)a.M) ||
+        !make_tmap_bf16_3d(&msnv, snaps ? a.snap_v : a.view_v, (uint64_t)a.M, snap_planes, (uint32_t)a.M))
         return cudaErrorInvalidValue;
     // the second-best similarity is tracked only when the debug record wants the top-2 gap
     auto kern = a.dbg_gap ? foldtc::fold_tc_kernel<true> : foldtc::fold_tc_kernel<false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, foldtc::SMEM_BYTES);
-    kern<<<a.BH, foldtc::NT, foldtc::SMEM_BYTES, s>>>(mk, mv, msk, msv, a);
+    kern<<<a.BH, foldtc::NT, foldtc::SMEM_BYTES, s>>>(mk, mv, msk, msv, msnk, msnv, mvk, mvv, a);
     return cudaGetLastError();
 }
 

@@ -220,6 +220,8 @@ struct GemmSpec {
 cudaError_t launch_fold(const FoldArgs& a, bool bf16, cudaStream_t s);
 bool fold_tc_supported(const FoldArgs& a, bool bf16);
 cudaError_t launch_fold_tc(const FoldArgs& a, cudaStream_t s);
+bool fold_big_supported(const FoldArgs& a, bool bf16);
+cudaError_t launch_fold_big(const FoldArgs& a, cudaStream_t s);
 cudaError_t launch_attn(const AttnArgs& a, bool bf16, cudaStream_t s);
 bool attn_tc_supported(const AttnArgs& a, bool bf16);
 cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s);

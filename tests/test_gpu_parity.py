@@ -62,6 +62,18 @@ SMALL = [
     # queries that spike on one key: a few rows of a warp rescale their output
     wl.Workload("qspike_B2H2N3000_C128W512", B=2, H=2, N=3000, chunk=128, window=512,
                 n_sinks=16, max_slots=128, keys="qspike5"),
+    # states beyond 256 slots and chunks of 256 tokens (bf16): the streamed tensor-core
+    # fold (slot blocks of 256, or 128 with two 128-token tiles), fixed and power-law
+    wl.Workload("big_fixed300_B1H2N6000_C128W256", B=1, H=2, N=6000, chunk=128, window=256,
+                n_sinks=16, max_slots=300, keys="repeat5"),
+    wl.Workload("big_fixed400_C64_B1H2N8000_W128", B=1, H=2, N=8000, chunk=64, window=128,
+                n_sinks=8, max_slots=400, keys="repeat5"),
+    _sized(wl.Workload("big_sqrt_C256_B1H2N6000_W256", B=1, H=2, N=6000, chunk=256, window=256,
+                       n_sinks=16, sched=1, keys="neardup20")),
+    wl.Workload("big_fixed600_C256_B2H1N9000_W512", B=2, H=1, N=9000, chunk=256, window=512,
+                n_sinks=16, max_slots=600, keys="repeat5"),
+    wl.Workload("ablate_novnorm_big_B1H2N6000_C128W256", B=1, H=2, N=6000, chunk=128,
+                window=256, n_sinks=16, max_slots=300, keys="repeat5", flags=1),
 ]
 
 
