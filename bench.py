@@ -133,15 +133,26 @@ class Clocks:
         self.path = None
 
     def start(self):
+        # The sampler is a child process: it must not outlive this program on any
+        # exit path (a profiler waits for the whole process tree), so it is stopped
+        # at interpreter exit too, and it ends by itself after max_s seconds.
+        import atexit
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                ["timeout", str(self.max_s), "nvidia-smi", f"--id={self.index}",
+                 f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            atexit.register(self._kill)
         except Exception:
             self.proc = None
+
+    max_s = 900
+
+    def _kill(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
 
     def stop(self):
         if self.proc is None:

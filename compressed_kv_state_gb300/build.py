@@ -41,17 +41,27 @@ def _stale(obj: str, src: str, deps) -> bool:
     return any(os.path.getmtime(p) > t for p in [src, *deps])
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every .cu under csrc/ and link libkvm.so; returns its path."""
+DEBUG_LIB = os.path.join(LIBDIR, "libkvm_debug.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile every .cu under csrc/ and link libkvm.so; returns its path.
+
+    debug=True builds the KVM_DEBUG variant (device-side checks that latch a
+    status word instead of accessing out of range) as lib/libkvm_debug.so, from
+    objects of its own."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir, lib = (os.path.join(BUILD, "debug"), DEBUG_LIB) if debug else (BUILD, LIB)
+    if debug:
+        extra_flags = (*extra_flags, "-DKVM_DEBUG")
+    os.makedirs(build_dir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     deps = (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) +
             glob.glob(os.path.join(INCLUDE, "*.h")))
     jobs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         objs.append(obj)
         if force or _stale(obj, src, deps):
             cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
@@ -67,13 +77,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for out in ex.map(run, jobs):
             if verbose and out:
                 print(out)
-    if force or jobs or not os.path.exists(LIB):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or not os.path.exists(lib):
+        tmp = lib + f".tmp{os.getpid()}"
         r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"], capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -700,6 +700,7 @@ kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda
     ra.ln_eps = c.ln_eps;
     ra.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) != 0;
     ra.BH = c.batch * c.heads;
+    ra.status = ly->at<int>(L.status);
     cudaError_t e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_renorm(ra, c.dtype == KVM_BF16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "renormalise launch");
     if (ra.n > 0) ly->kernels += 1;

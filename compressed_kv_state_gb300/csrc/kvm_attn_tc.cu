@@ -168,6 +168,7 @@ __device__ __forceinline__ Tile tile_of2(const TcArgs& a, int id) {
     const int64_t c = t.q0 / a.C, Wc = a.W / a.C;
     t.e = (int)(c - Wc - 1);
     t.n = t.e >= 0 ? a.sched[t.e].n_after : 0;
+    if (t.n > 0 && !kvm_check(t.e < a.snap_events && t.n <= a.M, a.status)) t.n = 0;
     t.ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
     t.nst = (t.n + KB - 1) / KB;
     t.nwin = (int)((t.q0 + 128 - t.ws + KB - 1) / KB);
@@ -258,8 +259,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int last_g = -1;  // last block whose K/V copies were issued
         if (lane == 0) {
             int g = 0, range = 0;
+            KVM_PROBE_DECL(4)
+            KVM_PROBE_START()
             for (int k = 0;; ++k) {
                 if (k >= 1 && !mbar_wait(bar(slot, B_QEMPTY), (k - 1) & 1, abort_flag, a.status)) break;
+                KVM_PROBE_LAP(2)
                 const int id = next_tile2(a, slot, k, &range);
                 tile_ring[slot * 4 + (k & 3)] = id;
                 mbar_arrive(bar(slot, B_TILE + (k & 3)));
@@ -270,10 +274,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 bool ok = true;
                 for (int j = 0; j < T.nblk; ++j, ++g) {
                     const int st = g % NS;
+                    KVM_PROBE_LAP(1)
                     if (g >= NS && !mbar_wait(bar(slot, B_KVEMPTY + st), ((g / NS) - 1) & 1, abort_flag, a.status)) {
                         ok = false;
                         break;
                     }
+                    KVM_PROBE_LAP(0)
                     const uint32_t dk = sbase + OFF_K + (slot * NS + st) * KV_BYTES;
                     const uint32_t dv = sbase + OFF_V + (slot * NS + st) * KV_BYTES;
                     mbar_expect_tx(bar(slot, B_KFULL + st), KV_BYTES);
@@ -291,6 +297,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 if (!ok) break;
             }
+            KVM_PROBE_LAP(1)
+            if (slot == 0) KVM_PROBE_FLUSH(g_probe_attn, 0, 3)
             // after an abort: the copies issued last on every stage land before exit
             if (*abort_flag)
                 for (int gg = last_g; gg >= 0 && gg > last_g - NS; --gg) {
@@ -309,17 +317,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t sQ = sbase + OFF_Q + slot * Q_BYTES;
             int g = 0;
             bool ok = true;
+            KVM_PROBE_DECL(8)
+            KVM_PROBE_START()
             for (int k = 0; ok; ++k) {
                 const int id = tile_wait(slot, k);
                 if (id < 0) break;
                 const Tile T = tile_of2(a, id);
+                KVM_PROBE_LAP(6)
                 if (!mbar_wait(bar(slot, B_QREADY), k & 1, abort_flag, a.status)) break;
+                KVM_PROBE_LAP(0)
                 tc_fence_after();
                 for (int j = 0; j < T.nblk; ++j) {
                     const int gj = g + j, st = gj % NS;
                     const uint32_t sK = sbase + OFF_K + (slot * NS + st) * KV_BYTES;
                     const uint32_t sV = sbase + OFF_V + (slot * NS + st) * KV_BYTES;
                     if (!mbar_wait(bar(slot, B_KFULL + st), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
+                    KVM_PROBE_LAP(1)
                     tc_fence_after();
                     // S = Q K^T (state blocks: the non-rotary dims only; the state keys are
                     // zero on the rotary dims).  It overwrites the P of block gj - 1, whose PV
@@ -332,8 +345,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     mma_commit(bar(slot, B_SFULL));
                     if (j + 1 == T.nblk) mma_commit(bar(slot, B_QEMPTY));
+                    KVM_PROBE_LAP(2)
                     if (!mbar_wait(bar(slot, B_PFULL), gj & 1, abort_flag, a.status)) { ok = false; break; }
+                    KVM_PROBE_LAP(3)
                     if (!mbar_wait(bar(slot, B_VFULL + st), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
+                    KVM_PROBE_LAP(4)
                     tc_fence_after();
                     // O += P V: P (bf16, two keys per column) from tensor memory, V from shared
                     for (int ks = 0; ks < KB / 16; ++ks) {
@@ -342,9 +358,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     mma_commit(bar(slot, B_PVDONE));
                     mma_commit(bar(slot, B_KVEMPTY + st));
+                    KVM_PROBE_LAP(5)
+#ifdef KVM_PROBE
+                    probe_acc[7] += 1;
+#endif
                 }
                 g += T.nblk;
             }
+            if (slot == 0) KVM_PROBE_FLUSH(g_probe_attn, 8, 8)
             // every MMA this thread issued completes before the tensor memory is released
             mma_commit(bar(slot, B_FINAL));
             drain_wait(bar(slot, B_FINAL), 0);
@@ -360,6 +381,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float2 sc2 = make_float2(sc, sc);
         int g = 0;
         bool ok = true;
+        KVM_PROBE_DECL(10)
+        KVM_PROBE_START()
         for (int k = 0; ok; ++k) {
             const int id = tile_wait(slot, k);
             if (id < 0) break;
@@ -367,6 +390,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int64_t p = T.q0 + row;
             // RoPE of this thread's query row, then hand the tile to the MMA
             if (!mbar_wait(bar(slot, B_QFULL), k & 1, abort_flag, a.status)) break;
+            KVM_PROBE_LAP(0)
             if (half > 0 && p < a.N) {
                 if ((half & 7) == 0)
                     rope_row_vec(qrow, row, p, a.rope, half);
@@ -375,10 +399,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             fence_proxy_async();
             mbar_arrive(bar(slot, B_QREADY));
+            KVM_PROBE_LAP(1)
             float m_used = -INFINITY, l = 0.0f;
             for (int j = 0; j < T.nblk; ++j) {
                 const int gj = g + j;
                 if (!mbar_wait(bar(slot, B_SFULL), gj & 1, abort_flag, a.status)) { ok = false; break; }
+                KVM_PROBE_LAP(2)
+#ifdef KVM_PROBE
+                probe_acc[9] += 1;
+#endif
                 tc_fence_after();
                 const bool is_state = j < T.nst;
                 const int64_t key0 = is_state ? 0 : T.ws + KB * (j - T.nst);
@@ -412,6 +441,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         mx1 = fmax3(mx1, __uint_as_float(v[h][x + 2]), __uint_as_float(v[h][x + 3]));
                     }
                 const float mblk = fmaxf(mx0, mx1) * sc;
+                KVM_PROBE_LAP(3)
                 bool rescale = false;
                 float alpha = 1.0f;
                 if (mblk > m_used) {
@@ -444,6 +474,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tmem_st16(tS + 16 * h, pk);
                 }
                 tmem_wait_st();
+                KVM_PROBE_LAP(4)
                 l += ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
                 // tensor-memory loads and stores are warp-wide (.sync.aligned): the whole
                 // warp rescales when any of its rows must (the others scale by alpha = 1)
@@ -464,11 +495,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tc_fence_before();
                 mbar_arrive(bar(slot, B_PFULL));
+                KVM_PROBE_LAP(5)
             }
             if (!ok) break;
             // epilogue: O / l for this tile
             const int gl = g + T.nblk - 1;
             if (!mbar_wait(bar(slot, B_PVDONE), gl & 1, abort_flag, a.status)) { ok = false; break; }
+            KVM_PROBE_LAP(6)
             tc_fence_after();
             const float il = 1.0f / l;
 #pragma unroll
@@ -488,7 +521,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             tc_fence_before();
             g += T.nblk;
+            KVM_PROBE_LAP(7)
         }
+        if (slot == 0 && row == 0) KVM_PROBE_FLUSH(g_probe_attn, 16, 10)
     }
 
     tc_fence_before();

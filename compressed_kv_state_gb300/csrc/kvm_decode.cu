@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
     const int64_t c = p / a.C, Wc = a.W / a.C;
     const int64_t ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
     const int ws_slot = (int)(ws % L);
-    const int n = a.n_slots;
+    const int n = kvm_check(a.n_slots <= a.M, a.status) ? a.n_slots : 0;
     const int nkeys = n + (int)(p - ws + 1);
     const T* vk = reinterpret_cast<const T*>(a.view_k) + (int64_t)bh * a.M * D;
     const T* vv = reinterpret_cast<const T*>(a.view_v) + (int64_t)bh * a.M * D;

@@ -1,4 +1,5 @@
-// Fold chain of the KVM layer: the sequential per-(batch, head) state update.
+// Fold chain of the KVM layer: the sequential per-(batch, head) state update
+// (the portable chain, for fp32 layers; bf16 layers use the tensor-core chains).
 //
 // "Key-Value Means" (gist.science technical summary):
 //   Core mechanism 1 - a chunk that overflows the window is folded into the
@@ -35,8 +36,20 @@ __device__ __forceinline__ void renorm_slot(const float* sk, const float* sv, in
     float c0 = s0 - mean, c1 = s1 - mean;
     float ss = warp_sum(c0 * c0 + c1 * c1);
     float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
-    sd[lane] = c0 * inv;
-    sd[lane + 32] = c1 * inv;
+    if (sizeof(T) == 2) {
+        // bf16 layers: the row holds the direction as bf16 hi + lo terms (elements
+        // [0, 64) and [64, 128)), the form the tensor-core fold chains stream
+        __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(sd);
+        const float a0 = c0 * inv, a1 = c1 * inv;
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(a0), h1 = __float2bfloat16_rn(a1);
+        u[lane] = h0;
+        u[lane + 32] = h1;
+        u[64 + lane] = __float2bfloat16_rn(a0 - __bfloat162float(h0));
+        u[64 + lane + 32] = __float2bfloat16_rn(a1 - __bfloat162float(h1));
+    } else {
+        sd[lane] = c0 * inv;
+        sd[lane + 32] = c1 * inv;
+    }
     // read key: LayerNorm(s / count), no affine, biased variance, rotary dims zeroed
     float ic = 1.0f / (float)cnt;
     float x0 = s0 * ic, x1 = s1 * ic;
@@ -359,6 +372,7 @@ __global__ void renorm_all_kernel(RenormArgs a) {
     if (gw >= total) return;
     const int64_t bh = gw / a.n, j = gw % a.n;
     const int64_t row = bh * a.M + j;
+    if (!kvm_check(a.counts[row] >= 1, a.status)) return;
     renorm_slot<T>(a.sum_k + row * D, a.sum_v + row * D, a.counts[row], a.rho[row],
                    a.simdir + row * D, reinterpret_cast<T*>(a.view_k) + row * D,
                    reinterpret_cast<T*>(a.view_v) + row * D, a.r, a.ln_eps, lane, a.no_vnorm);
@@ -369,18 +383,14 @@ static size_t fold_smem_bytes(int C) {
 }
 
 cudaError_t launch_fold(const FoldArgs& a, bool bf16, cudaStream_t s) {
+    // bf16 layers fold on the tensor cores (the state on chip up to 256 slots and
+    // 128 tokens a chunk, else streamed); this portable chain serves fp32 layers
     if (fold_tc_supported(a, bf16)) return launch_fold_tc(a, s);
     if (fold_big_supported(a, bf16)) return launch_fold_big(a, s);
+    if (bf16) return cudaErrorInvalidValue;
     const size_t smem = fold_smem_bytes(a.C);
-    if (bf16) {
-        cudaFuncSetAttribute(fold_chain_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        fold_chain_kernel<__nv_bfloat16><<<a.BH, FOLD_THREADS, smem, s>>>(a);
-    } else {
-        cudaFuncSetAttribute(fold_chain_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        fold_chain_kernel<float><<<a.BH, FOLD_THREADS, smem, s>>>(a);
-    }
+    cudaFuncSetAttribute(fold_chain_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    fold_chain_kernel<float><<<a.BH, FOLD_THREADS, smem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -17,9 +17,9 @@
 //   - chunks of up to 256 tokens are two 128-row MMA tiles (NB = 128 then,
 //     else NB = 256: each S buffer is 256 tensor-memory columns);
 //   - the slots the event touches are compacted (a slot bitmap, prefix counts
-//     and per-slot 256-bit token masks), and one warp per touched slot adds
-//     its tokens in position order (dims across lanes), then writes the new
-//     direction, the read view and the sums back;
+//     and per-slot 256-bit token masks); eight lanes per touched slot (eight
+//     dims each, four slots per warp at a time) add its tokens in position
+//     order, then write the new direction, the read view and the sums back;
 //   - the read view of every slot is copied to the event's snapshot.
 // The merge is deterministic: no atomics on data (token masks are OR-ed).
 #include <cstddef>
@@ -57,6 +57,9 @@ struct Misc {
     int wapp[NW];                    // appended tokens per warp (selection order)
 };
 static_assert(offsetof(Misc, tmask) % 16 == 0, "token masks are read as 16-byte vectors");
+#ifdef KVM_PROBE
+static __device__ unsigned long long g_probe_big[32];
+#endif
 constexpr int BODY_BYTES = 192 * 1024;  // U blocks + chunk buffers (either tiling)
 constexpr int SMEM_BYTES = BODY_BYTES + (int)sizeof(Misc) + 1024;
 
@@ -176,14 +179,8 @@ __global__ void __launch_bounds__(NT, 1)
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(smem_u32(&X.tmem_slot), 512);
-    // directions of the slots the state already holds (a decode-boundary fold, a
-    // later segment or an imported state): one warp per slot, from the key sums
-    for (int j = warp; j < n; j += NW) {
-        const float2 x = reinterpret_cast<const float2*>(g_sk + (int64_t)j * D)[lane];
-        float2 c;
-        uint32_t hw, lw;
-        warp_dir(x, lane, g_u + (int64_t)j * 128, c, hw, lw);
-    }
+    // the directions of the slots the state already holds are in the workspace: written
+    // by the events that touched them, or by the state import's renormalisation
     fence_proxy_async_all();
     tc_fence_before();
     __syncthreads();
@@ -250,6 +247,8 @@ __global__ void __launch_bounds__(NT, 1)
                    : 0.0f;
     };
     float g_nx = gate_of(a.e_begin);
+    KVM_PROBE_DECL(16)
+    KVM_PROBE_START()
     for (int e = a.e_begin, it = 0; e < a.e_end; ++e, ++it) {
         const int cb = it & 1;
         const Sched sc = a.sched ? a.sched[e] : a.sched0;
@@ -261,14 +260,16 @@ __global__ void __launch_bounds__(NT, 1)
         const float g_here = g_nx;
         if (!wait_bar(&X.bar_k[cb], ph_k[cb], tid == 0 ? &pend_k[cb] : nullptr)) fail = true;
         g_nx = gate_of(e + 1);
+        KVM_PROBE_LAP(0)
+#ifdef KVM_PROBE
+        probe_acc[15] += 1;
+#endif
         if (tid == 0) {
             // the next chunk loads into the buffer the previous event finished with
             if (!fail && e + 1 < a.e_end) load_chunk(e + 1, cb ^ 1);
             if (!fail && nb > 0) {
                 load_u(0, 0);
                 if (nb > 1) load_u(1, 1);
-                if (!wait_bar(&X.bar_u[0], ph_u[0], &pend_u[0])) fail = true;
-                else issue_mma(cb, 0, 0);
             }
         }
         // per-token set-up: gates, key norms (two threads per token), kinds
@@ -302,7 +303,13 @@ __global__ void __launch_bounds__(NT, 1)
                 reinterpret_cast<uint4*>(&X.tmask[0][0])[i] = make_uint4(0, 0, 0, 0);
             if (tid < MAXC) X.kfound[tid] = -1;
         }
+        // the first block's directions have been loading during the set-up
+        if (tid == 0 && !fail && nb > 0) {
+            if (!wait_bar(&X.bar_u[0], ph_u[0], &pend_u[0])) fail = true;
+            else issue_mma(cb, 0, 0);
+        }
         if (__syncthreads_or(fail)) break;
+        KVM_PROBE_LAP(1)
 
         // similarity blocks: MMA of block b + 1 runs while block b is scanned
         float best = -INFINITY, sec = -INFINITY;
@@ -337,6 +344,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         if (fail) break;
+        KVM_PROBE_LAP(2)
         if (tok < C) {
             X.pb[part][tok] = best;
             X.ps[part][tok] = sec;
@@ -354,6 +362,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (cand) X.m[tid] = barg < 0 ? -INFINITY : (kn > 0.0f ? best / kn : 0.0f);
         else if (tid < C) X.m[tid] = INFINITY;  // sinks are never append candidates
         __syncthreads();
+        KVM_PROBE_LAP(3)
 
         // surprise selection: the a lowest scores (ties to the lower position) are appended
         if (na > 0) {
@@ -362,9 +371,12 @@ __global__ void __launch_bounds__(NT, 1)
             int rank = 0;
             if (cand) {
                 const float mt = X.m[tid];
-                for (int u = 0; u < C && rank < na; ++u) {
-                    const float mu = X.m[u];
-                    rank += (mu < mt) || (mu == mt && u < tid);
+                for (int u0 = 0; u0 < C && rank < na; u0 += 8) {  // C is a multiple of 16
+                    const float4 m0 = *reinterpret_cast<const float4*>(&X.m[u0]);
+                    const float4 m1 = *reinterpret_cast<const float4*>(&X.m[u0 + 4]);
+                    const float mu[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) rank += (mu[i] < mt) || (mu[i] == mt && u0 + i < tid);
                 }
             }
             const bool app = cand && rank < na;
@@ -444,6 +456,7 @@ __global__ void __launch_bounds__(NT, 1)
         } else if (cand) {
             X.kind[tid] = 0;
         }
+        KVM_PROBE_LAP(4)
         if (tid < C && X.kind[tid] == 0) {
             X.slot[tid] = barg;
             if (barg < 0 && a.status) atomicOr(a.status, STATUS_DEVICE);
@@ -461,6 +474,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         // touched slots: bitmap, then compact indices in slot order
+        if (tid < C && X.slot[tid] >= 0 && !kvm_check(X.slot[tid] < sc.n_after, a.status)) X.slot[tid] = -1;
         if (tid < C && X.slot[tid] >= 0) atomicOr(&X.slotbits[X.slot[tid] >> 5], 1u << (X.slot[tid] & 31));
         __syncthreads();
         const int nwords = (sc.n_after + 31) / 32;
@@ -496,78 +510,145 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
         const int ntouched = X.wbase[MAXM / 32];
+        KVM_PROBE_LAP(5)
 
-        // owners: one warp per touched slot, dims (2l, 2l + 1) on lane l; a warp takes
-        // its slots four at a time and issues the state loads of the four together
-        for (int k0 = warp; k0 < ntouched; k0 += 4 * NW) {
-            float2 xk[4], xv[4];
-            int cnt[4];
-            float rho[4];
+        // owners: eight lanes per touched slot (dims 8 sl .. 8 sl + 7 on sub-lane sl), so
+        // a warp works on four slots at a time; reductions over the eight lanes
+        {
+            const int grp = lane >> 3, sl = lane & 7;
+            for (int k = 4 * warp + grp; k - grp < ntouched; k += 4 * NW) {
+                const bool act = k < ntouched;
+                const int j = act ? X.tslot[k] : 0;
+                const int ft = act ? X.kfound[k] : -1;
+                float xk[8], xv[8];
+                int cnt = 0;
+                float rho = 0.0f;
+                if (act && ft < 0) {
+                    const float4* pk = reinterpret_cast<const float4*>(g_sk + (int64_t)j * D + 8 * sl);
+                    const float4* pv = reinterpret_cast<const float4*>(g_sv + (int64_t)j * D + 8 * sl);
+                    const float4 k0 = pk[0], k1 = pk[1], v0 = pv[0], v1 = pv[1];
+                    xk[0] = k0.x; xk[1] = k0.y; xk[2] = k0.z; xk[3] = k0.w;
+                    xk[4] = k1.x; xk[5] = k1.y; xk[6] = k1.z; xk[7] = k1.w;
+                    xv[0] = v0.x; xv[1] = v0.y; xv[2] = v0.z; xv[3] = v0.w;
+                    xv[4] = v1.x; xv[5] = v1.y; xv[6] = v1.z; xv[7] = v1.w;
+                    cnt = g_cnt[j];
+                    rho = g_rho[j];
+                } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int k = k0 + i * NW;
-                if (k < ntouched && X.kfound[k] < 0) {
-                    const int j = X.tslot[k];
-                    xk[i] = reinterpret_cast<const float2*>(g_sk + (int64_t)j * D)[lane];
-                    xv[i] = reinterpret_cast<const float2*>(g_sv + (int64_t)j * D)[lane];
-                    cnt[i] = g_cnt[j];
-                    rho[i] = g_rho[j];
+                    for (int i = 0; i < 8; ++i) xk[i] = xv[i] = 0.0f;
                 }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int k = k0 + i * NW;
-                if (k >= ntouched) continue;
-                const int j = X.tslot[k];
-                const int ft = X.kfound[k];
-                if (ft >= 0) {
+                // a token's eight dims of this sub-lane: one 16-byte swizzled chunk
+                auto chunk8 = [&](const uint8_t* base, int t, float (&y)[8]) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(base + (t >> 7) * TILE_BYTES + swz(t & 127, sl));
+                    const float2 a0 = unpack2(w.x), a1 = unpack2(w.y), a2 = unpack2(w.z), a3 = unpack2(w.w);
+                    y[0] = a0.x; y[1] = a0.y; y[2] = a1.x; y[3] = a1.y;
+                    y[4] = a2.x; y[5] = a2.y; y[6] = a3.x; y[7] = a3.y;
+                };
+                float vsq = 0.0f;
+                if (act && ft >= 0) {
                     const float gf = X.g[ft];
-                    const float2 kk = row_pair(kch + (ft >> 7) * TILE_BYTES, ft & 127, lane);
-                    const float2 vv = row_pair(vch + (ft >> 7) * TILE_BYTES, ft & 127, lane);
-                    xk[i] = make_float2(gf * kk.x, gf * kk.y);
-                    xv[i] = make_float2(gf * vv.x, gf * vv.y);
-                    cnt[i] = 1;
-                    rho[i] = sqrtf(warp_sum(vv.x * vv.x + vv.y * vv.y));
+                    float kk[8], vv[8];
+                    chunk8(kch, ft, kk);
+                    chunk8(vch, ft, vv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        xk[i] = gf * kk[i];
+                        xv[i] = gf * vv[i];
+                        vsq = fmaf(vv[i], vv[i], vsq);
+                    }
+                    cnt = 1;
                 }
+                // |v| of a founding token (read radius), over the group's eight lanes
+                vsq += __shfl_xor_sync(0xffffffffu, vsq, 1);
+                vsq += __shfl_xor_sync(0xffffffffu, vsq, 2);
+                vsq += __shfl_xor_sync(0xffffffffu, vsq, 4);
+                if (act && ft >= 0) rho = sqrtf(vsq);
                 // merged tokens in position order
+                if (act) {
 #pragma unroll 1
-                for (int w8 = 0; w8 < (C + 31) / 32; ++w8) {
-                    uint32_t m = X.tmask[k][w8];
-                    while (m) {
-                        const int t = (w8 << 5) + __ffs(m) - 1;
-                        m &= m - 1;
-                        const float gt = X.g[t];
-                        const float2 kk = row_pair(kch + (t >> 7) * TILE_BYTES, t & 127, lane);
-                        const float2 vv = row_pair(vch + (t >> 7) * TILE_BYTES, t & 127, lane);
-                        xk[i] = make_float2(fmaf(gt, kk.x, xk[i].x), fmaf(gt, kk.y, xk[i].y));
-                        xv[i] = make_float2(fmaf(gt, vv.x, xv[i].x), fmaf(gt, vv.y, xv[i].y));
-                        ++cnt[i];
+                    for (int w8 = 0; w8 < (C + 31) / 32; ++w8) {
+                        uint32_t m = X.tmask[k][w8];
+                        while (m) {
+                            const int t = (w8 << 5) + __ffs(m) - 1;
+                            m &= m - 1;
+                            const float gt = X.g[t];
+                            float kk[8], vv[8];
+                            chunk8(kch, t, kk);
+                            chunk8(vch, t, vv);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                xk[i] = fmaf(gt, kk[i], xk[i]);
+                                xv[i] = fmaf(gt, vv[i], xv[i]);
+                            }
+                            ++cnt;
+                        }
                     }
                 }
-                reinterpret_cast<float2*>(g_sk + (int64_t)j * D)[lane] = xk[i];
-                reinterpret_cast<float2*>(g_sv + (int64_t)j * D)[lane] = xv[i];
-                if (lane == 0) {
-                    g_cnt[j] = cnt[i];
-                    g_rho[j] = rho[i];
+                __syncwarp();
+                // centred key, its norm, and the value norm: sums over the group's lanes
+                float s1 = 0.0f, sv = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    s1 += xk[i];
+                    sv = fmaf(xv[i], xv[i], sv);
                 }
-                // direction, read key LayerNorm(sum / count) = c / sqrt(|c|^2 / 64 + eps count^2)
-                // with the rotary dims zeroed, read value rho * unit(sum_v) (or sum_v / count)
-                float2 c;
-                uint32_t hw, lw;
-                const float ss = warp_dir(xk[i], lane, g_u + (int64_t)j * 128, c, hw, lw);
-                const float fc = (float)cnt[i];
-                const float rs = 1.0f / sqrtf(ss * (1.0f / 64.0f) + a.ln_eps * fc * fc);
-                const int d0 = 2 * lane;
-                reinterpret_cast<uint32_t*>(g_vk + (int64_t)j * D)[lane] =
-                    pack2(d0 < a.r ? 0.0f : c.x * rs, d0 + 1 < a.r ? 0.0f : c.y * rs);
-                const float nv = sqrtf(warp_sum(xv[i].x * xv[i].x + xv[i].y * xv[i].y));
-                const float f = a.no_vnorm ? 1.0f / fc : (nv > 0.0f ? rho[i] / nv : 0.0f);
-                reinterpret_cast<uint32_t*>(g_vv + (int64_t)j * D)[lane] = pack2(xv[i].x * f, xv[i].y * f);
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+                    sv += __shfl_xor_sync(0xffffffffu, sv, o);
+                }
+                const float mean = s1 * (1.0f / 64.0f);
+                float c[8], ss = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    c[i] = xk[i] - mean;
+                    ss = fmaf(c[i], c[i], ss);
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                if (act) {
+                    float4* qk = reinterpret_cast<float4*>(g_sk + (int64_t)j * D + 8 * sl);
+                    float4* qv = reinterpret_cast<float4*>(g_sv + (int64_t)j * D + 8 * sl);
+                    qk[0] = make_float4(xk[0], xk[1], xk[2], xk[3]);
+                    qk[1] = make_float4(xk[4], xk[5], xk[6], xk[7]);
+                    qv[0] = make_float4(xv[0], xv[1], xv[2], xv[3]);
+                    qv[1] = make_float4(xv[4], xv[5], xv[6], xv[7]);
+                    if (sl == 0) {
+                        g_cnt[j] = cnt;
+                        g_rho[j] = rho;
+                    }
+                    // direction u = c / |c| as bf16 hi + lo; read key LayerNorm(sum / count) =
+                    // c / sqrt(|c|^2 / 64 + eps count^2) with the rotary dims zeroed; read value
+                    // rho * unit(sum_v) (or sum_v / count)
+                    const float inv = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
+                    const float fc = (float)cnt;
+                    const float rs = 1.0f / sqrtf(ss * (1.0f / 64.0f) + a.ln_eps * fc * fc);
+                    const float nv = sqrtf(sv);
+                    const float f = a.no_vnorm ? 1.0f / fc : (nv > 0.0f ? rho / nv : 0.0f);
+                    uint32_t hi[4], lo[4], wk[4], wv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float u0 = c[2 * i] * inv, u1 = c[2 * i + 1] * inv;
+                        hi[i] = pack2(u0, u1);
+                        const float2 hf = unpack2(hi[i]);
+                        lo[i] = pack2(u0 - hf.x, u1 - hf.y);
+                        const int d0 = 8 * sl + 2 * i;
+                        wk[i] = pack2(d0 < a.r ? 0.0f : c[2 * i] * rs, d0 + 1 < a.r ? 0.0f : c[2 * i + 1] * rs);
+                        wv[i] = pack2(xv[2 * i] * f, xv[2 * i + 1] * f);
+                    }
+                    uint4* urow = reinterpret_cast<uint4*>(g_u + (int64_t)j * 128);
+                    urow[sl] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    urow[8 + sl] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    reinterpret_cast<uint4*>(g_vk + (int64_t)j * D)[sl] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                    reinterpret_cast<uint4*>(g_vv + (int64_t)j * D)[sl] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                }
             }
         }
+        KVM_PROBE_LAP(6)
         // the next event's TMA reads the directions written above
         fence_proxy_async_all();
         __syncthreads();
+        KVM_PROBE_LAP(7)
         n = sc.n_after;
         // snapshot of the read view after this event
         if (a.snap_k && e < a.snap_events) {
@@ -583,8 +664,10 @@ __global__ void __launch_bounds__(NT, 1)
                 dv4[i] = wv;
             }
         }
+        KVM_PROBE_LAP(8)
     }
 
+    if (tid == 0) KVM_PROBE_FLUSH(g_probe_big, 0, 16)
     // after an abort: let the copies and MMAs this CTA issued land before its shared
     // and tensor memory are released (each wait bounded; they depend on nothing else)
     if (tid == 0 && X.abort_flag) {
@@ -609,6 +692,8 @@ __global__ void __launch_bounds__(NT, 1)
 }
 
 }  // namespace foldbig
+
+KVM_PROBE_READOUT(kvm_probe_read_big, foldbig::g_probe_big)
 
 bool fold_big_supported(const FoldArgs& a, bool bf16) {
     return bf16 && a.C >= 16 && a.C <= foldbig::MAXC && a.M <= foldbig::MAXM;

@@ -705,7 +705,8 @@ __global__ void __launch_bounds__(NT, 1)
         // merge lists: each merged token sets its bit in its slot's 128-bit token mask
         // (OR commutes, so the masks do not depend on timing); an owner then visits
         // its tokens in position order, lowest bit first
-        if (tid < C && X.kind[tid] == 0 && X.slot[tid] >= 0)
+        if (tid < C && X.kind[tid] == 0 && X.slot[tid] >= 0 &&
+            kvm_check(X.slot[tid] >= S && X.slot[tid] < sc.n_after, a.status))
             atomicOr(&X.tmask[X.slot[tid]][tid >> 5], 1u << (tid & 31));
         // the previous snapshot store must have finished reading the view
         if (tid == 0) bulk_wait_read();

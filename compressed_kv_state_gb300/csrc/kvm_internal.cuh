@@ -13,6 +13,19 @@ constexpr int D = 64;  // head_dim supported by every kernel
 // Device status word bits (latched, read and cleared by kvm_layer_sync).
 enum : int { STATUS_TIMEOUT = 1, STATUS_DEVICE = 2 };
 
+// Device-side checks of the KVM_DEBUG build (-DKVM_DEBUG): a failed check latches
+// STATUS_DEVICE in the layer's status word (kvm_layer_sync then reports
+// KVM_ERR_DEVICE) and the caller skips the access it guards.  In normal builds the
+// check is compiled out and the access is unconditional.
+#ifdef KVM_DEBUG
+__device__ __forceinline__ bool kvm_check(bool ok, int* status) {
+    if (!ok && status) atomicOr(status, STATUS_DEVICE);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool kvm_check(bool, int*) { return true; }
+#endif
+
 // Per-event schedule entry, computed on the host in double precision (the
 // schedule depends only on counts of tokens, never on data).
 struct Sched {
@@ -195,6 +208,7 @@ struct RenormArgs {
     float ln_eps;
     int no_vnorm;  // ablation: read value = sum_v / count
     int BH;
+    int* status;   // device status word (device-side checks of the debug build)
 };
 
 // Projection GEMM of the whole layer: C = A * W^T, A [rows, K] bf16 (or the

@@ -11,7 +11,9 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "lib", "libkvm.so")
+# KVM_LIBRARY selects another build of the same library (the KVM_DEBUG variant,
+# lib/libkvm_debug.so, with device-side checks); default: lib/libkvm.so
+LIB_PATH = os.environ.get("KVM_LIBRARY") or os.path.join(_HERE, "lib", "libkvm.so")
 
 KVM_OK, KVM_ERR_INVALID_ARG, KVM_ERR_UNSUPPORTED, KVM_ERR_CAPACITY = 0, 1, 2, 3
 KVM_ERR_WORKSPACE, KVM_ERR_CUDA, KVM_ERR_TIMEOUT, KVM_ERR_DEVICE = 4, 5, 6, 7
