@@ -135,8 +135,8 @@ constexpr int OFF_K = OFF_Q + NSLOT * Q_BYTES;         // [NSLOT][NS] K blocks
 constexpr int OFF_V = OFF_K + NSLOT * NS * KV_BYTES;   // [NSLOT][NS] V blocks
 constexpr int OFF_BAR = OFF_V + NSLOT * NS * KV_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;       // 225.5 KB with alignment slack
-constexpr int TMEM_COLS = 512;                         // per slot: S (128 columns, P aliased on
-                                                       // its first 64) then O (64 columns)
+constexpr int TMEM_COLS = 512;                         // per slot (256 columns): S (128),
+                                                       // O (64), P (64: bf16 key pairs)
 constexpr int NTHREADS = 384;
 // Register split (the block is launched with 168 registers a thread, 64512 in
 // all): the producer / MMA warpgroup drops to 64, the two softmax warpgroups rise
@@ -154,7 +154,8 @@ enum {
     B_VFULL = B_KFULL + NS,      // [NS] TMA V landed
     B_KVEMPTY = B_VFULL + NS,    // [NS] PV of the stage done
     B_SFULL = B_KVEMPTY + NS,    // QK done
-    B_PFULL = B_SFULL + 1,       // P written to tensor memory, O rescaled (128 arrivals)
+    B_SFREE = B_SFULL + 1,       // S read into registers by the softmax (128 arrivals)
+    B_PFULL = B_SFREE + 1,       // P written to tensor memory, O rescaled (128 arrivals)
     B_PVDONE = B_PFULL + 1,      // PV done
     B_FINAL = B_PVDONE + 1,      // MMA drain
     B_TILE = B_FINAL + 1,        // [4] tile number of turn k published (ring of 4)
@@ -232,6 +233,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mbar_init(bar(s, B_KVEMPTY + i), 1);
             }
             mbar_init(bar(s, B_SFULL), 1);
+            mbar_init(bar(s, B_SFREE), 128);
             mbar_init(bar(s, B_PFULL), 128);
             mbar_init(bar(s, B_PVDONE), 1);
             mbar_init(bar(s, B_FINAL), 1);
@@ -313,12 +315,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t idesc_qk = idesc_bf16(128, KB, 0, 0);
             const uint32_t idesc_pv = idesc_bf16(128, 64, 0, 1);
             const int ks_state = min(a.r / 16, 3);
-            const uint32_t tS = tmem + 256 * slot, tO = tS + 128;
+            const uint32_t tS = tmem + 256 * slot, tO = tS + 128, tP = tS + 192;
             const uint32_t sQ = sbase + OFF_Q + slot * Q_BYTES;
             int g = 0;
             bool ok = true;
             KVM_PROBE_DECL(8)
             KVM_PROBE_START()
+            // S = Q K^T of block gb (state blocks: the non-rotary dims only; the state keys
+            // are zero on the rotary dims), once the softmax has read block gb - 1's S
+            auto issue_qk = [&](int gb, bool state) -> bool {
+                const int st = gb % NS;
+                if (gb > 0 && !mbar_wait(bar(slot, B_SFREE), (gb - 1) & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(bar(slot, B_KFULL + st), (gb / NS) & 1, abort_flag, a.status)) return false;
+                KVM_PROBE_LAP(1)
+                tc_fence_after();
+                const uint32_t sK = sbase + OFF_K + (slot * NS + st) * KV_BYTES;
+                const int ks0 = state ? ks_state : 0;
+                for (int ks = ks0; ks < 4; ++ks) {
+                    const uint64_t ad = sdesc_sw128(sQ + ks * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(sK + ks * 32, 16, 1024);
+                    mma_bf16_ss(tS, ad, bd, idesc_qk, ks > ks0);
+                }
+                mma_commit(bar(slot, B_SFULL));
+                KVM_PROBE_LAP(2)
+                return true;
+            };
             for (int k = 0; ok; ++k) {
                 const int id = tile_wait(slot, k);
                 if (id < 0) break;
@@ -327,34 +348,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!mbar_wait(bar(slot, B_QREADY), k & 1, abort_flag, a.status)) break;
                 KVM_PROBE_LAP(0)
                 tc_fence_after();
+                if (!issue_qk(g, T.nst > 0)) break;
                 for (int j = 0; j < T.nblk; ++j) {
                     const int gj = g + j, st = gj % NS;
-                    const uint32_t sK = sbase + OFF_K + (slot * NS + st) * KV_BYTES;
-                    const uint32_t sV = sbase + OFF_V + (slot * NS + st) * KV_BYTES;
-                    if (!mbar_wait(bar(slot, B_KFULL + st), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
-                    KVM_PROBE_LAP(1)
-                    tc_fence_after();
-                    // S = Q K^T (state blocks: the non-rotary dims only; the state keys are
-                    // zero on the rotary dims).  It overwrites the P of block gj - 1, whose PV
-                    // was issued before it (tensor-core operations of a thread run in order).
-                    const int ks0 = j < T.nst ? ks_state : 0;
-                    for (int ks = ks0; ks < 4; ++ks) {
-                        const uint64_t ad = sdesc_sw128(sQ + ks * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(sK + ks * 32, 16, 1024);
-                        mma_bf16_ss(tS, ad, bd, idesc_qk, ks > ks0);
+                    // the next block's QK^T overlaps this block's softmax
+                    if (j + 1 < T.nblk) {
+                        if (!issue_qk(gj + 1, j + 1 < T.nst)) { ok = false; break; }
                     }
-                    mma_commit(bar(slot, B_SFULL));
-                    if (j + 1 == T.nblk) mma_commit(bar(slot, B_QEMPTY));
-                    KVM_PROBE_LAP(2)
+                    if (j + 1 == T.nblk) mma_commit(bar(slot, B_QEMPTY));  // all QK^T of the tile issued
                     if (!mbar_wait(bar(slot, B_PFULL), gj & 1, abort_flag, a.status)) { ok = false; break; }
                     KVM_PROBE_LAP(3)
                     if (!mbar_wait(bar(slot, B_VFULL + st), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
                     KVM_PROBE_LAP(4)
                     tc_fence_after();
                     // O += P V: P (bf16, two keys per column) from tensor memory, V from shared
+                    const uint32_t sV = sbase + OFF_V + (slot * NS + st) * KV_BYTES;
                     for (int ks = 0; ks < KB / 16; ++ks) {
                         const uint64_t bd = sdesc_sw128(sV + ks * 2048, KV_BYTES, 1024);
-                        mma_bf16_ts(tO, tS + 8 * ks, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+                        mma_bf16_ts(tO, tP + 8 * ks, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(bar(slot, B_PVDONE));
                     mma_commit(bar(slot, B_KVEMPTY + st));
@@ -375,7 +386,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int slot = (warp - 4) >> 2;
         const int row = tid - 128 - 128 * slot;                // query row = TMEM lane
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base + 256 * slot, tO = tS + 128;
+        const uint32_t tS = tmem + lane_base + 256 * slot, tO = tS + 128, tP = tS + 192;
         uint8_t* qrow = smem + OFF_Q + slot * Q_BYTES + row * 128;
         const float sc = a.scale_log2;
         const float2 sc2 = make_float2(sc, sc);
@@ -424,6 +435,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int h = 0; h < KB / 32; ++h) tmem_ld32(tS + 32 * h, v[h]);
                 tmem_wait_ld();
+                // S is in registers: the next block's QK^T may overwrite it
+                tc_fence_before();
+                mbar_arrive(bar(slot, B_SFREE));
                 if (lim < KB) {
 #pragma unroll
                     for (int h = 0; h < KB / 32; ++h)
@@ -454,9 +468,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                 }
                 l *= alpha;
-                // p = 2^(s * scale - m), row sum, P as bf16 pairs over S's first 64 columns
-                // (column 16h + i takes keys 32h + 2i, 32h + 2i + 1, whose S values are in
-                // registers already)
+                // the previous block's PV has read P and updated O (it ran while this
+                // block's S was loaded and reduced)
+                if (gj > 0 && !mbar_wait(bar(slot, B_PVDONE), (gj - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                // tensor-memory loads and stores are warp-wide (.sync.aligned): the whole
+                // warp rescales when any of its rows must (the others scale by alpha = 1)
+                if (__any_sync(0xffffffffu, rescale)) {
+                    uint32_t o[32];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(tO + h * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
+                        tmem_st32(tO + h * 32, o);
+                    }
+                }
+                // p = 2^(s * scale - m), row sum, P as bf16 key pairs into the P columns
                 const float2 mneg = make_float2(-m_used, -m_used);
                 float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                 make_float2(0.f, 0.f)};
@@ -471,28 +500,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         rs[(x >> 1) & 3] = __fadd2_rn(rs[(x >> 1) & 3], e2);
                         pk[x >> 1] = pack_bf16(e2.x, e2.y);
                     }
-                    tmem_st16(tS + 16 * h, pk);
+                    tmem_st16(tP + 16 * h, pk);
                 }
                 tmem_wait_st();
                 KVM_PROBE_LAP(4)
                 l += ((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y));
-                // tensor-memory loads and stores are warp-wide (.sync.aligned): the whole
-                // warp rescales when any of its rows must (the others scale by alpha = 1)
-                if (__any_sync(0xffffffffu, rescale)) {
-                    // O holds blocks < j: wait for their last PV, then scale it in place
-                    if (!mbar_wait(bar(slot, B_PVDONE), (gj - 1) & 1, abort_flag, a.status)) { ok = false; break; }
-                    tc_fence_after();
-                    uint32_t o[32];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        tmem_ld32(tO + h * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * alpha);
-                        tmem_st32(tO + h * 32, o);
-                    }
-                    tmem_wait_st();
-                }
                 tc_fence_before();
                 mbar_arrive(bar(slot, B_PFULL));
                 KVM_PROBE_LAP(5)

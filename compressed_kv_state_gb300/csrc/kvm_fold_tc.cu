@@ -34,6 +34,8 @@ using namespace tc;
 constexpr int MAXS = 256;  // slots held on chip
 constexpr int TOK = 128;   // token rows of the MMA tile
 constexpr int NT = 512;    // threads: key owner j and value owner 256 + j of every slot j
+constexpr int TMA_T = NT - 1;  // issues the chunk loads and the view stores (a value-side
+                               // thread: its warp has slack, thread 0 is on the chain)
 constexpr int ROWB = 128;  // bytes of one 64-dim bf16 row
 constexpr int OFF_UHI = 0;                      // [256][128 B] swizzled (MMA B operand)
 constexpr int OFF_ULO = OFF_UHI + MAXS * ROWB;  // [256][128 B] swizzled
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_3d(sV + buf * TOK * ROWB, &tm_v, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
     };
     // the first two chunks load now; chunk e + 2 is issued at the end of event e
-    if (tid == 0 && a.e_begin < a.e_end && !a.test_stall) {
+    if (tid == TMA_T && a.e_begin < a.e_end && !a.test_stall) {
         load_chunk(a.e_begin, 0);
         if (a.e_begin + 1 < a.e_end) load_chunk(a.e_begin + 1, 1);
     }
@@ -709,7 +711,7 @@ __global__ void __launch_bounds__(NT, 1)
             kvm_check(X.slot[tid] >= S && X.slot[tid] < sc.n_after, a.status))
             atomicOr(&X.tmask[X.slot[tid]][tid >> 5], 1u << (tid & 31));
         // the previous snapshot store must have finished reading the view
-        if (tid == 0) bulk_wait_read();
+        if (tid == TMA_T) bulk_wait_read();
         __syncthreads();
         KVM_PROBE_LAP(5)
 
@@ -724,9 +726,11 @@ __global__ void __launch_bounds__(NT, 1)
             float2 x[32];
             int cnt = 0;
             float ss = 0.0f;
+
             if (wtouched) {
                 const uint8_t* rows = vside ? vch : kch;
                 tmem_ld64_2(t_own, x);
+                KVM_PROBE_LAP(18)
                 float rho = 0.0f;
                 if (touched) {
                     if (!vside) cnt = X.cnt[j];
@@ -760,8 +764,11 @@ __global__ void __launch_bounds__(NT, 1)
                     if (!vside) {
                         X.cnt[j] = cnt;
                         ss = key_dir2(j, x, sm);
+                        // the next event's MMA reads these directions (async proxy)
+                        fence_proxy_async();
                         KVM_PROBE_LAP(15)
                         key_view2(j, x, ss, cnt, a.r, a.ln_eps, sm);
+                        KVM_PROBE_LAP(19)
                     } else {
                         X.rho[j] = rho;
                         X.cntv[j] = cnt;
@@ -770,9 +777,9 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
             if (!vside) {
-                // every direction of this event is written: thread 0 issues the next
-                // event's similarity MMA now, while the value owners finish
-                fence_proxy_async();
+                // every direction of this event is written (and fenced by its writer):
+                // thread 0 issues the next event's similarity MMA now, while the value
+                // owners finish
                 KVM_PROBE_LAP(16)
                 asm volatile("bar.sync 1, 256;" ::: "memory");
                 KVM_PROBE_LAP(17)
@@ -793,9 +800,9 @@ __global__ void __launch_bounds__(NT, 1)
 
         // chunk e + 2 loads into this event's buffer (its readers passed the barrier
         // above), ahead of the snapshot copies in the copy engine's queue
-        if (tid == 0 && e + 2 < a.e_end) load_chunk(e + 2, buf);
+        if (tid == TMA_T && e + 2 < a.e_end) load_chunk(e + 2, buf);
         // snapshot of the read view after this event (async bulk copy)
-        if (tid == 0 && a.snap_k && e < a.snap_events) {
+        if (tid == TMA_T && a.snap_k && e < a.snap_events) {
             // the swizzled view rows leave by TMA tensor stores (the copy engine unswizzles)
             const int plane = bh * a.snap_events + e;
             tma_store_3d(&tm_snk, smem_u32(sm + OFF_VK), 0, 0, plane);
@@ -809,7 +816,7 @@ __global__ void __launch_bounds__(NT, 1)
     // write the state back for decode, export and later segments: the sums go
     // through swizzled staging tiles (key sums in the direction area, value sums
     // in the chunk area) and leave by TMA; the read view leaves by bulk copy
-    if (tid == 0) bulk_wait_all();
+    if (tid == TMA_T) bulk_wait_all();
     {
         float x[64];
         tmem_ld64(t_own, x);
@@ -825,7 +832,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     fence_proxy_async();
     __syncthreads();
-    if (tid == 0 && n > 0 && !X.abort_flag) {
+    if (tid == TMA_T && n > 0 && !X.abort_flag) {
         const int nb = (n + srows - 1) / srows;
         for (int h = 0; h < 2; ++h)
             for (int b = 0; b < nb; ++b) {
@@ -843,17 +850,20 @@ __global__ void __launch_bounds__(NT, 1)
         KVM_PROBE_FLUSH(g_probe_fold, 20 * (tid == 0 ? 0 : tid == 255 ? 1 : tid == 256 ? 2 : 3), 20)
     // after an abort: let the copies and MMAs this CTA issued land before its shared
     // and tensor memory are released (each wait bounded; they depend on nothing else)
-    if (tid == 0 && X.abort_flag) {
+    if (X.abort_flag && (tid == 0 || tid == TMA_T)) {
         auto drain = [&](uint32_t bar, int parity) {
             if (parity < 0) return;
             const long long t0 = clock64();
             while (!mbar_try(bar, (uint32_t)parity) && clock64() - t0 < (1ll << 28)) {
             }
         };
-        drain(smem_u32(&X.bar_st), pend_st);
-        drain(smem_u32(&X.bar_k[0]), pend_ld[0]);
-        drain(smem_u32(&X.bar_k[1]), pend_ld[1]);
-        drain(bar_s, pend_mma);
+        if (tid == 0) {
+            drain(smem_u32(&X.bar_st), pend_st);
+            drain(bar_s, pend_mma);
+        } else {
+            drain(smem_u32(&X.bar_k[0]), pend_ld[0]);
+            drain(smem_u32(&X.bar_k[1]), pend_ld[1]);
+        }
     }
     tc_fence_before();
     __syncthreads();

@@ -93,3 +93,4 @@ def test_decode_butterfly_leaves_key_i_on_lane_i():
         v = nv
         off, w = off >> 1, w >> 1
     np.testing.assert_array_equal(v[:, 0], part.sum(axis=0))
+
