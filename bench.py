@@ -190,13 +190,16 @@ class Clocks:
 
 # -------------------------------------------------------------- traffic
 
-def _ncu_traffic(kernel_file):
-    """DRAM bytes per launch from a committed ncu summary, only if it was taken on
-    the current source of the kernel (same sha256); else None."""
+def _ncu_traffic(kernel_file, workload):
+    """DRAM bytes per launch from a committed ncu summary (entry "<file>@<workload>",
+    else "<file>"), only if it was taken on the current source of the kernel (same
+    sha256); else None."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
-    d = json.load(open(p)).get(os.path.basename(kernel_file))
+    allv = json.load(open(p))
+    name = os.path.basename(kernel_file)
+    d = allv.get(f"{name}@{workload}") or allv.get(name)
     if not d:
         return None
     sha = hashlib.sha256(open(kernel_file, "rb").read()).hexdigest()
@@ -410,11 +413,11 @@ def prefill_report(w, t, peaks):
     big = w.max_slots > 256 or w.chunk > 128
     dom_src = os.path.join(ROOT, "compressed_kv_state_gb300", "csrc",
                            "kvm_attn_tc.cu" if dom == "attention" else
-                           ("kvm_fold.cu" if big else "kvm_fold_tc.cu"))
+                           ("kvm_fold_big.cu" if big else "kvm_fold_tc.cu"))
     ach = dom_flops / (dom_ms / 1e3) / 1e12
     roofline = dict(kernel=dom, bound="tensor", achieved=ach, peak=peaks["bf16"], unit="TFLOP/s",
                     frac=ach / peaks["bf16"], peak_source=f"{peaks['src']} bf16 burst",
-                    ms_per_step=dom_ms, traffic=_ncu_traffic(dom_src))
+                    ms_per_step=dom_ms, traffic=_ncu_traffic(dom_src, w.name))
     ms_step = t["ms_step"]
     step_roof = {"flops": aw["flops"] + ffl, "ms_per_step": ms_step,
                  "achieved": (aw["flops"] + ffl) / (ms_step / 1e3) / 1e12,

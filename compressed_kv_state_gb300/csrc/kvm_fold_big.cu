@@ -247,6 +247,25 @@ __global__ void __launch_bounds__(NT, 1)
                    : 0.0f;
     };
     float g_nx = gate_of(a.e_begin);
+    // snapshot of the read view after event snap_e (n rows); the copy is made before the
+    // next event's owners rewrite the view, at the barrier that ends its set-up
+    int snap_e = -1, snap_n = 0;
+    auto snapshot = [&]() {
+        if (a.snap_k && snap_e >= 0 && snap_e < a.snap_events) {
+            const int64_t base = ((int64_t)bh * a.snap_events + snap_e) * M * ROWB;
+            const int nchunks = snap_n * ROWB / 16;
+            const uint4* sk4 = reinterpret_cast<const uint4*>(g_vk);
+            const uint4* sv4 = reinterpret_cast<const uint4*>(g_vv);
+            uint4* dk4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_k) + base);
+            uint4* dv4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_v) + base);
+            for (int i = tid; i < nchunks; i += NT) {
+                const uint4 wk = sk4[i], wv = sv4[i];
+                dk4[i] = wk;
+                dv4[i] = wv;
+            }
+        }
+        snap_e = -1;
+    };
     KVM_PROBE_DECL(16)
     KVM_PROBE_START()
     for (int e = a.e_begin, it = 0; e < a.e_end; ++e, ++it) {
@@ -303,6 +322,7 @@ __global__ void __launch_bounds__(NT, 1)
                 reinterpret_cast<uint4*>(&X.tmask[0][0])[i] = make_uint4(0, 0, 0, 0);
             if (tid < MAXC) X.kfound[tid] = -1;
         }
+        snapshot();
         // the first block's directions have been loading during the set-up
         if (tid == 0 && !fail && nb > 0) {
             if (!wait_bar(&X.bar_u[0], ph_u[0], &pend_u[0])) fail = true;
@@ -379,6 +399,7 @@ __global__ void __launch_bounds__(NT, 1)
                     for (int i = 0; i < 8; ++i) rank += (mu[i] < mt) || (mu[i] == mt && u0 + i < tid);
                 }
             }
+            KVM_PROBE_LAP(9)
             const bool app = cand && rank < na;
             // appended slots in position order: warp ballots and their prefix
             unsigned bal = 0;
@@ -394,6 +415,7 @@ __global__ void __launch_bounds__(NT, 1)
                 X.slot[tid] = n0 + before;
             }
             __syncthreads();
+            KVM_PROBE_LAP(10)
             // directions of the new slots (one warp each, from g * k of the founding
             // token), staged as fp32 hi + lo in the U area and written to the workspace
             float* ustage = reinterpret_cast<float*>(sm);
@@ -409,6 +431,7 @@ __global__ void __launch_bounds__(NT, 1)
                 reinterpret_cast<float2*>(ustage + (jn - n0) * D)[lane] = make_float2(hf.x + lf.x, hf.y + lf.y);
             }
             __syncthreads();
+            KVM_PROBE_LAP(11)
             // the remaining tokens also compare against the new slots
             if (tid < C && X.kind[tid] == 0) {
                 float kx[64];
@@ -516,27 +539,33 @@ __global__ void __launch_bounds__(NT, 1)
         // a warp works on four slots at a time; reductions over the eight lanes
         {
             const int grp = lane >> 3, sl = lane & 7;
+            // the state of a round's slots is loaded one round ahead (global-memory latency)
+            float4 nk0 = make_float4(0.f, 0.f, 0.f, 0.f), nk1 = nk0, nv0 = nk0, nv1 = nk0;
+            int ncnt = 0;
+            float nrho = 0.0f;
+            auto load_round = [&](int kk) {
+                if (kk < ntouched && X.kfound[kk] < 0) {
+                    const int jj = X.tslot[kk];
+                    const float4* pk = reinterpret_cast<const float4*>(g_sk + (int64_t)jj * D + 8 * sl);
+                    const float4* pv = reinterpret_cast<const float4*>(g_sv + (int64_t)jj * D + 8 * sl);
+                    nk0 = pk[0];
+                    nk1 = pk[1];
+                    nv0 = pv[0];
+                    nv1 = pv[1];
+                    ncnt = g_cnt[jj];
+                    nrho = g_rho[jj];
+                }
+            };
+            load_round(4 * warp + grp);
             for (int k = 4 * warp + grp; k - grp < ntouched; k += 4 * NW) {
                 const bool act = k < ntouched;
                 const int j = act ? X.tslot[k] : 0;
                 const int ft = act ? X.kfound[k] : -1;
-                float xk[8], xv[8];
-                int cnt = 0;
-                float rho = 0.0f;
-                if (act && ft < 0) {
-                    const float4* pk = reinterpret_cast<const float4*>(g_sk + (int64_t)j * D + 8 * sl);
-                    const float4* pv = reinterpret_cast<const float4*>(g_sv + (int64_t)j * D + 8 * sl);
-                    const float4 k0 = pk[0], k1 = pk[1], v0 = pv[0], v1 = pv[1];
-                    xk[0] = k0.x; xk[1] = k0.y; xk[2] = k0.z; xk[3] = k0.w;
-                    xk[4] = k1.x; xk[5] = k1.y; xk[6] = k1.z; xk[7] = k1.w;
-                    xv[0] = v0.x; xv[1] = v0.y; xv[2] = v0.z; xv[3] = v0.w;
-                    xv[4] = v1.x; xv[5] = v1.y; xv[6] = v1.z; xv[7] = v1.w;
-                    cnt = g_cnt[j];
-                    rho = g_rho[j];
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) xk[i] = xv[i] = 0.0f;
-                }
+                float xk[8] = {nk0.x, nk0.y, nk0.z, nk0.w, nk1.x, nk1.y, nk1.z, nk1.w};
+                float xv[8] = {nv0.x, nv0.y, nv0.z, nv0.w, nv1.x, nv1.y, nv1.z, nv1.w};
+                int cnt = ncnt;
+                float rho = nrho;
+                load_round(k + 4 * NW);
                 // a token's eight dims of this sub-lane: one 16-byte swizzled chunk
                 auto chunk8 = [&](const uint8_t* base, int t, float (&y)[8]) {
                     const uint4 w = *reinterpret_cast<const uint4*>(base + (t >> 7) * TILE_BYTES + swz(t & 127, sl));
@@ -650,22 +679,12 @@ __global__ void __launch_bounds__(NT, 1)
         __syncthreads();
         KVM_PROBE_LAP(7)
         n = sc.n_after;
-        // snapshot of the read view after this event
-        if (a.snap_k && e < a.snap_events) {
-            const int64_t base = ((int64_t)bh * a.snap_events + e) * M * ROWB;
-            const int nchunks = n * ROWB / 16;
-            const uint4* sk4 = reinterpret_cast<const uint4*>(g_vk);
-            const uint4* sv4 = reinterpret_cast<const uint4*>(g_vv);
-            uint4* dk4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_k) + base);
-            uint4* dv4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_v) + base);
-            for (int i = tid; i < nchunks; i += NT) {
-                const uint4 wk = sk4[i], wv = sv4[i];
-                dk4[i] = wk;
-                dv4[i] = wv;
-            }
-        }
+        // this event's snapshot is copied while the next event sets up
+        snap_e = e;
+        snap_n = n;
         KVM_PROBE_LAP(8)
     }
+    if (!fail) snapshot();
 
     if (tid == 0) KVM_PROBE_FLUSH(g_probe_big, 0, 16)
     // after an abort: let the copies and MMAs this CTA issued land before its shared
