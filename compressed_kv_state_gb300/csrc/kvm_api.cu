@@ -438,8 +438,9 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     // overlapped prefill: fold segments on one SM partition, the attention of
     // the chunks each segment has made ready on the other
     int segs = 0;
-    if (ly->overlap_segs != 0 && !dbg && E >= 2 && kvm::fold_tc_supported(fa, bf16) &&
-        kvm::attn_tc_supported(aa, bf16) && c.chunk == 128) {
+    if (ly->overlap_segs != 0 && !dbg && E >= 2 &&
+        (kvm::fold_tc_supported(fa, bf16) || kvm::fold_big_supported(fa, bf16)) &&
+        kvm::attn_tc_supported(aa, bf16)) {
         if (!ly->part_tried) {
             ly->part_tried = true;
             kvm::host::partition_make(ly->device, BH, &ly->part, ly->part_why);

@@ -594,10 +594,15 @@ __global__ void __launch_bounds__(NT, 1)
                 if (act && ft >= 0) rho = sqrtf(vsq);
                 // merged tokens in position order
                 if (act) {
-#pragma unroll 1
-                    for (int w8 = 0; w8 < (C + 31) / 32; ++w8) {
-                        uint32_t m = X.tmask[k][w8];
-                        while (m) {
+                    // one loop over the set bits of all mask words (a warp runs as many
+                    // rounds as its busiest slot has tokens)
+                    const int nw = (C + 31) / 32;
+                    int w8 = 0;
+                    uint32_t m = X.tmask[k][0];
+                    while (true) {
+                        while (m == 0u && ++w8 < nw) m = X.tmask[k][w8];
+                        if (w8 >= nw) break;
+                        {
                             const int t = (w8 << 5) + __ffs(m) - 1;
                             m &= m - 1;
                             const float gt = X.g[t];

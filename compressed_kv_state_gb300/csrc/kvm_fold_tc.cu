@@ -743,16 +743,16 @@ __global__ void __launch_bounds__(NT, 1)
                         cnt = 0;
                         if (vside) rho = sqrtf(sq_row_sw<8>(vch, ft, 0));
                     }
-                    // merged tokens in position order
-                    const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
-#pragma unroll
-                    for (int w4 = 0; w4 < 4; ++w4) {
-                        uint32_t m = mw[w4];
-                        while (m) {
-                            const int t = (w4 << 5) + __ffs(m) - 1;
-                            m &= m - 1;
-                            add_row_sw2(rows, t, X.g[t], x);
-                        }
+                    // merged tokens in position order, one loop over the whole 128-bit mask
+                    // (a warp runs as many rounds as its busiest slot has tokens)
+                    unsigned long long m_lo = ((unsigned long long)mk.y << 32) | mk.x;
+                    unsigned long long m_hi = ((unsigned long long)mk.w << 32) | mk.z;
+                    while (m_lo | m_hi) {
+                        const bool low = m_lo != 0ull;
+                        const unsigned long long m = low ? m_lo : m_hi;
+                        const int t = (low ? 0 : 64) + __ffsll((long long)m) - 1;
+                        if (low) m_lo &= m_lo - 1; else m_hi &= m_hi - 1;
+                        add_row_sw2(rows, t, X.g[t], x);
                     }
                     cnt += nm + (ft >= 0 ? 1 : 0);
                 }

@@ -23,6 +23,11 @@ MID = wl.Workload("fixed_B2H3N4096_C128W512", B=2, H=3, N=4096, chunk=128, windo
                   n_sinks=16, max_slots=256, keys="repeat5")
 RAGGED = wl.Workload("fixed_B1H4N3000_C128W256_ragged", B=1, H=4, N=3000, chunk=128, window=256,
                      n_sinks=16, max_slots=96, keys="repeat5")
+# the streamed-state fold (more than 256 slots; chunks of 256 tokens) in the overlapped prefill
+BIG = wl.Workload("big_fixed300_B1H2N6000_C128W256", B=1, H=2, N=6000, chunk=128, window=256,
+                  n_sinks=16, max_slots=300, keys="repeat5")
+BIG256 = wl.Workload("big_fixed600_C256_B2H1N9000_W512", B=2, H=1, N=9000, chunk=256, window=512,
+                     n_sinks=16, max_slots=600, keys="repeat5")
 
 
 # Under a CUDA injection library (a profiler or tracer) the library makes no SM
@@ -56,7 +61,8 @@ def _same_state(a, b):
         assert a[key] == b[key], key
 
 
-@pytest.mark.parametrize("w", [MID, RAGGED, wl.FIXED_8K], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [MID, RAGGED, wl.FIXED_8K, BIG, BIG256, wl.SQRT_8K, wl.LONG_64K],
+                         ids=lambda w: w.name)
 def test_overlapped_equals_sequential(w):
     inputs = wl.prefill_inputs(w)
     E = oracle.n_events(oracle_cfg(w), w.N)
@@ -73,7 +79,7 @@ def test_overlapped_equals_sequential(w):
         _same_state(st_o, st_s)
 
 
-@pytest.mark.parametrize("w", [MID, wl.FIXED_8K], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [MID, wl.FIXED_8K, BIG256], ids=lambda w: w.name)
 def test_overlapped_outputs_match_oracle(w):
     """Sampled heads of the overlapped prefill (the benchmark's launch
     configuration at full size) against the oracle."""
