@@ -112,7 +112,7 @@ Layout layout_of(const kvm_config& c) {
     L.counts = take(BH * M * 4);
     L.rho = take(BH * M * 4);
     L.simdir = take(BH * M * d * 4);
-    L.view_k = take(BH * M * d * es);
+    L.view_k = take(BH * M * (size_t)kvm::view_k_dims(c.rope_dims) * es);  // non-rotary dims only
     L.view_v = take(BH * M * d * es);
     L.ring_k = take(BH * ring * d * es);
     L.ring_v = take(BH * ring * d * es);
@@ -243,12 +243,15 @@ static cudaError_t timed(kvm_layer* ly, int phase, cudaStream_t s, F&& f) {
         if (e != cudaSuccess) return e;
         ly->pool.push_back(t);
     }
+    // copies of the handles: f() may launch through timed() again, and the pool's
+    // storage moves when it grows
     kvm_layer::Timed& t = ly->pool[ly->used++];
     t.phase = phase;
-    cudaEventRecord(t.a, s);
-    cudaError_t e = f();
-    cudaEventRecord(t.b, s);
-    return e;
+    const cudaEvent_t ta = t.a, tb = t.b;
+    cudaError_t e = cudaEventRecord(ta, s);
+    if (e == cudaSuccess) e = f();
+    const cudaError_t e2 = cudaEventRecord(tb, s);
+    return e != cudaSuccess ? e : e2;
 }
 
 extern "C" {
@@ -446,7 +449,9 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             kvm::host::partition_make(ly->device, BH, &ly->part, ly->part_why);
         }
         if (ly->part.ok) {
-            segs = ly->overlap_segs > 0 ? ly->overlap_segs : 3;
+            // automatic: restarts of the on-chip chain reload its state (2 segments measured
+            // best); the streamed chain restarts for free (8)
+            segs = ly->overlap_segs > 0 ? ly->overlap_segs : (kvm::fold_tc_supported(fa, bf16) ? 2 : 8);
             if (segs > kvm::host::Partition::MAX_SEGS) segs = kvm::host::Partition::MAX_SEGS;
             if (segs > E) segs = (int)E;
         }

@@ -33,8 +33,9 @@ template <> __device__ __forceinline__ float2 ld2s<float>(const float* p) { retu
 // 1024 rows of the decode sweep take two waves).  Keys (state rows, then the window in
 // position order) are split into one contiguous range per warp; each warp
 // streams its range in tiles of 32 keys through two shared-memory stages of
-// its own, filled by bulk copies (a tile is at most three contiguous row runs:
-// state view, window up to the ring's end, window from the ring's start).
+// its own, filled by bulk copies (a tile holds state rows only, or window rows
+// only: the state's compact key rows (the non-rotary dims), or at most two
+// contiguous runs of the window ring).
 // Scores are dim-parallel (lane = 2 dims) with a butterfly transpose-reduce
 // that leaves key i's score on lane i; P V is dim-parallel from shared memory;
 // online softmax per warp, warps combined at the end.
@@ -94,24 +95,33 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
     const int ws_slot = (int)(ws % L);
     const int n = kvm_check(a.n_slots <= a.M, a.status) ? a.n_slots : 0;
     const int nkeys = n + (int)(p - ws + 1);
-    const T* vk = reinterpret_cast<const T*>(a.view_k) + (int64_t)bh * a.M * D;
+    // compact read-key rows: dims [D - DK, D) (the state keys are zero on the rotary dims)
+    const int DK = view_k_dims(a.r), k0d = D - DK;
+    const uint32_t RBK = (uint32_t)(DK * (int)sizeof(T));
+    const T* vk = reinterpret_cast<const T*>(a.view_k) + (int64_t)bh * a.M * DK;
     const T* vv = reinterpret_cast<const T*>(a.view_v) + (int64_t)bh * a.M * D;
     const int per = ((nkeys + DEC_WARPS * TK - 1) / (DEC_WARPS * TK)) * TK;
     const int beg = warp * per, end = min(nkeys, beg + per);
     uint8_t* stage = dsm + warp * 2 * 2 * TILE;  // [2 stages][K tile, V tile]
 
+    // a tile ends after TK keys, at the range's end, or where the state rows end
+    auto tile_end = [&](int k0) {
+        const int k1 = min(end, k0 + TK);
+        return (k0 < n && k1 > n) ? n : k1;
+    };
     // issue the copies of keys [k0, k1) into stage b (lane 0 only)
     auto issue = [&](int k0, int k1, int b) {
         const uint32_t bar = dsmem_u32(&bars[warp][b]);
         const uint32_t sk = dsmem_u32(stage + b * 2 * TILE), sv = sk + TILE;
+        const bool st = k0 < n;
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"((uint32_t)((k1 - k0) * RB * 2)) : "memory");
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar),
+                     "r"((uint32_t)(k1 - k0) * ((st ? RBK : (uint32_t)RB) + (uint32_t)RB)) : "memory");
         int kk = k0;
-        if (kk < n) {  // state rows
-            const int e = min(k1, n);
-            bulk_g2s(sk, vk + (int64_t)kk * D, (uint32_t)((e - kk) * RB), bar);
-            bulk_g2s(sv, vv + (int64_t)kk * D, (uint32_t)((e - kk) * RB), bar);
-            kk = e;
+        if (st) {  // state rows (compact keys)
+            bulk_g2s(sk, vk + (int64_t)kk * DK, (uint32_t)(k1 - kk) * RBK, bar);
+            bulk_g2s(sv, vv + (int64_t)kk * D, (uint32_t)((k1 - kk) * RB), bar);
+            kk = k1;
         }
         while (kk < k1) {  // window rows, contiguous up to the ring's end
             int slot = ws_slot + (kk - n);
@@ -127,12 +137,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
     float m = -INFINITY, l = 0.0f, acc0 = 0.0f, acc1 = 0.0f;
     const float2 qv = make_float2(qs[2 * lane], qs[2 * lane + 1]);
     int it = 0;
-    if (lane == 0 && beg < end) issue(beg, min(end, beg + TK), 0);
+    if (lane == 0 && beg < end) issue(beg, tile_end(beg), 0);
     __syncwarp();
-    for (int k0 = beg; k0 < end; k0 += TK, ++it) {
+    for (int k0 = beg, k1; k0 < end; k0 = k1, ++it) {
         const int b = it & 1;
-        const int cnt = min(TK, end - k0);
-        if (lane == 0 && k0 + TK < end) issue(k0 + TK, min(end, k0 + 2 * TK), b ^ 1);
+        k1 = tile_end(k0);
+        const int cnt = k1 - k0;
+        if (lane == 0 && k1 < end) issue(k1, tile_end(k1), b ^ 1);
         // wait for this tile: every lane waits on the stage's barrier (try_wait suspends
         // the warp in hardware; bounded: a copy that never lands latches a timeout)
         {
@@ -155,11 +166,23 @@ __global__ void __launch_bounds__(DEC_THREADS, 4) decode_kernel(DecodeArgs a) {
         const T* kt = reinterpret_cast<const T*>(stage + b * 2 * TILE);
         const T* vt = reinterpret_cast<const T*>(stage + b * 2 * TILE + TILE);
         // partial dot products of this lane's two dims with every key of the tile
+        // (state rows: compact, nothing stored below dim D - DK; rows past cnt are
+        // stale and masked after the reduction)
         float v[TK];
+        if (k0 < n) {
+            const bool has = 2 * lane >= k0d;
+            const T* kl = kt + (has ? 2 * lane - k0d : 0);
 #pragma unroll
-        for (int j = 0; j < TK; ++j) {
-            const float2 kx = ld2s<T>(kt + j * D + 2 * lane);
-            v[j] = qv.x * kx.x + qv.y * kx.y;
+            for (int j = 0; j < TK; ++j) {
+                const float2 kx = has ? ld2s<T>(kl + j * DK) : make_float2(0.0f, 0.0f);
+                v[j] = qv.x * kx.x + qv.y * kx.y;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < TK; ++j) {
+                const float2 kx = ld2s<T>(kt + j * D + 2 * lane);
+                v[j] = qv.x * kx.x + qv.y * kx.y;
+            }
         }
         // butterfly transpose-reduce: afterwards lane i holds key i's score
 #pragma unroll

@@ -57,8 +57,10 @@ __device__ __forceinline__ void renorm_slot(const float* sk, const float* sv, in
     float d0 = x0 - mx, d1 = x1 - mx;
     float var = warp_sum(d0 * d0 + d1 * d1) * (1.0f / D);
     float rs = 1.0f / sqrtf(var + eps);
-    vk[lane] = from_f<T>(lane < r ? 0.0f : d0 * rs);
-    vk[lane + 32] = from_f<T>(lane + 32 < r ? 0.0f : d1 * rs);
+    // vk holds dims [D - view_k_dims(r), D) of the read key (the compact view)
+    const int k0 = D - view_k_dims(r);
+    if (lane >= k0) vk[lane - k0] = from_f<T>(lane < r ? 0.0f : d0 * rs);
+    if (lane + 32 >= k0) vk[lane + 32 - k0] = from_f<T>(lane + 32 < r ? 0.0f : d1 * rs);
     // read value: rho * unit(sum_v) (ablation: the member mean sum_v / count)
     float v0 = sv[lane], v1 = sv[lane + 32];
     float nv = sqrtf(warp_sum(v0 * v0 + v1 * v1));
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(FOLD_THREADS, 2) fold_chain_kernel(FoldArgs a)
     int* counts = a.counts + (int64_t)bh * M;
     float* rho = a.rho + (int64_t)bh * M;
     float* simdir = a.simdir + (int64_t)bh * M * D;
-    T* view_k = reinterpret_cast<T*>(a.view_k) + (int64_t)bh * M * D;
+    const int DK = view_k_dims(a.r);  // dims of a compact read-key row
+    T* view_k = reinterpret_cast<T*>(a.view_k) + (int64_t)bh * M * DK;
     T* view_v = reinterpret_cast<T*>(a.view_v) + (int64_t)bh * M * D;
     const T* ksrc = reinterpret_cast<const T*>(a.k_src) + (int64_t)bh * a.src_row * D;
     const T* vsrc = reinterpret_cast<const T*>(a.v_src) + (int64_t)bh * a.src_row * D;
@@ -341,21 +344,26 @@ __global__ void __launch_bounds__(FOLD_THREADS, 2) fold_chain_kernel(FoldArgs a)
         for (int i = warp; i < ntouch; i += nwarps) {
             const int j = touched[i];
             renorm_slot<T>(sum_k + (int64_t)j * D, sum_v + (int64_t)j * D, counts[j], rho[j],
-                           simdir + (int64_t)j * D, view_k + (int64_t)j * D,
+                           simdir + (int64_t)j * D, view_k + (int64_t)j * DK,
                            view_v + (int64_t)j * D, a.r, a.ln_eps, lane, a.no_vnorm);
         }
         __syncthreads();
 
         // 9. snapshot of the view after this event, for the attention of chunk e + W/C + 1
         if (a.snap_k && e < a.snap_events) {
+            // full snapshot rows: the compact key view's rows behind zeros on the
+            // leading dims it does not store
             const int64_t base = ((int64_t)bh * a.snap_events + e) * M * D;
-            const int nbytes = sc.n_after * D * (int)sizeof(T);
+            constexpr int CPR = D * (int)sizeof(T) / 16;     // 16-byte pieces of a full row
+            const int zc = (D - DK) * (int)sizeof(T) / 16;   // pieces before the compact part
+            const int n_pc = sc.n_after * CPR;
             const uint4* sk4 = reinterpret_cast<const uint4*>(view_k);
             const uint4* sv4 = reinterpret_cast<const uint4*>(view_v);
             uint4* dk4 = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.snap_k) + base);
             uint4* dv4 = reinterpret_cast<uint4*>(reinterpret_cast<T*>(a.snap_v) + base);
-            for (int i = tid; i < nbytes / 16; i += FOLD_THREADS) {
-                dk4[i] = sk4[i];
+            for (int i = tid; i < n_pc; i += FOLD_THREADS) {
+                const int row = i / CPR, pc = i - row * CPR;
+                dk4[i] = pc < zc ? make_uint4(0u, 0u, 0u, 0u) : sk4[row * (CPR - zc) + pc - zc];
                 dv4[i] = sv4[i];
             }
         }
@@ -374,7 +382,7 @@ __global__ void renorm_all_kernel(RenormArgs a) {
     const int64_t row = bh * a.M + j;
     if (!kvm_check(a.counts[row] >= 1, a.status)) return;
     renorm_slot<T>(a.sum_k + row * D, a.sum_v + row * D, a.counts[row], a.rho[row],
-                   a.simdir + row * D, reinterpret_cast<T*>(a.view_k) + row * D,
+                   a.simdir + row * D, reinterpret_cast<T*>(a.view_k) + row * view_k_dims(a.r),
                    reinterpret_cast<T*>(a.view_v) + row * D, a.r, a.ln_eps, lane, a.no_vnorm);
 }
 

@@ -164,7 +164,8 @@ __global__ void __launch_bounds__(NT, 1)
     int* g_cnt = a.counts + (int64_t)bh * M;
     float* g_rho = a.rho + (int64_t)bh * M;
     __nv_bfloat16* g_u = reinterpret_cast<__nv_bfloat16*>(a.simdir) + (int64_t)bh * M * 128;
-    __nv_bfloat16* g_vk = reinterpret_cast<__nv_bfloat16*>(a.view_k) + (int64_t)bh * M * D;
+    const int DK = view_k_dims(a.r), zc = (D - DK) / 8;  // compact read-key rows: 16-byte pieces zc..7
+    __nv_bfloat16* g_vk = reinterpret_cast<__nv_bfloat16*>(a.view_k) + (int64_t)bh * M * DK;
     __nv_bfloat16* g_vv = reinterpret_cast<__nv_bfloat16*>(a.view_v) + (int64_t)bh * M * D;
 
     const Sched sc_first = a.sched ? a.sched[a.e_begin] : a.sched0;
@@ -252,14 +253,17 @@ __global__ void __launch_bounds__(NT, 1)
     int snap_e = -1, snap_n = 0;
     auto snapshot = [&]() {
         if (a.snap_k && snap_e >= 0 && snap_e < a.snap_events) {
+            // full snapshot rows: the compact key rows behind zeros on the leading pieces
             const int64_t base = ((int64_t)bh * a.snap_events + snap_e) * M * ROWB;
-            const int nchunks = snap_n * ROWB / 16;
+            const int nchunks = snap_n * 8;
             const uint4* sk4 = reinterpret_cast<const uint4*>(g_vk);
             const uint4* sv4 = reinterpret_cast<const uint4*>(g_vv);
             uint4* dk4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_k) + base);
             uint4* dv4 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(a.snap_v) + base);
             for (int i = tid; i < nchunks; i += NT) {
-                const uint4 wk = sk4[i], wv = sv4[i];
+                const int row = i >> 3, pc = i & 7;
+                const uint4 wk = pc < zc ? make_uint4(0u, 0u, 0u, 0u) : sk4[row * (8 - zc) + pc - zc];
+                const uint4 wv = sv4[i];
                 dk4[i] = wk;
                 dv4[i] = wv;
             }
@@ -673,7 +677,8 @@ __global__ void __launch_bounds__(NT, 1)
                     uint4* urow = reinterpret_cast<uint4*>(g_u + (int64_t)j * 128);
                     urow[sl] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
                     urow[8 + sl] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                    reinterpret_cast<uint4*>(g_vk + (int64_t)j * D)[sl] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                    if (sl >= zc)
+                        reinterpret_cast<uint4*>(g_vk + (int64_t)j * DK)[sl - zc] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
                     reinterpret_cast<uint4*>(g_vv + (int64_t)j * D)[sl] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }

@@ -356,8 +356,7 @@ __global__ void __launch_bounds__(NT, 1)
     fold_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                    const __grid_constant__ CUtensorMap tm_sk, const __grid_constant__ CUtensorMap tm_sv,
                    const __grid_constant__ CUtensorMap tm_snk, const __grid_constant__ CUtensorMap tm_snv,
-                   const __grid_constant__ CUtensorMap tm_vk, const __grid_constant__ CUtensorMap tm_vv,
-                   const FoldArgs a) {
+                   const __grid_constant__ CUtensorMap tm_vv, const FoldArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     Misc& X = *reinterpret_cast<Misc*>(sm + OFF_MISC);
@@ -832,6 +831,16 @@ __global__ void __launch_bounds__(NT, 1)
     }
     fence_proxy_async();
     __syncthreads();
+    // the compact read-key view (the non-rotary 16-byte pieces of every row) leaves by
+    // plain stores; the read-value view and the sums by TMA
+    if (n > 0 && !X.abort_flag) {
+        const int DK = view_k_dims(a.r), zc = (D - DK) / 8, pr = DK / 8;
+        uint4* gvk = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.view_k) + (int64_t)bh * M * DK);
+        for (int i = tid; i < n * pr; i += NT) {
+            const int row = i / pr, pc = zc + (i - row * pr);
+            gvk[i] = *reinterpret_cast<const uint4*>(sm + OFF_VK + swz(row, pc));
+        }
+    }
     if (tid == TMA_T && n > 0 && !X.abort_flag) {
         const int nb = (n + srows - 1) / srows;
         for (int h = 0; h < 2; ++h)
@@ -840,7 +849,6 @@ __global__ void __launch_bounds__(NT, 1)
                 tma_store_3d(&tm_sk, smem_u32(sm + OFF_UHI) + o, 32 * h, b * srows, bh);
                 tma_store_3d(&tm_sv, smem_u32(sm + OFF_K) + o, 32 * h, b * srows, bh);
             }
-        tma_store_3d(&tm_vk, smem_u32(sm + OFF_VK), 0, 0, bh);
         tma_store_3d(&tm_vv, smem_u32(sm + OFF_VV), 0, 0, bh);
         bulk_commit();
         bulk_wait_all();
@@ -882,24 +890,24 @@ bool fold_tc_supported(const FoldArgs& a, bool bf16) { return bf16 && a.C <= 128
 cudaError_t launch_fold_tc(const FoldArgs& args, cudaStream_t s) {
     FoldArgs a = args;
     a.stage_rows = a.M < foldtc::STAGE_ROWS ? a.M : foldtc::STAGE_ROWS;
-    CUtensorMap mk, mv, msk, msv, msnk, msnv, mvk, mvv;
-    // read view: [BH][M][64] bf16 stored a whole state (M <= 256 rows) per box;
-    // snapshots [BH * events][M][64] (the view maps again when there are none)
+    CUtensorMap mk, mv, msk, msv, msnk, msnv, mvv;
+    // read-value view: [BH][M][64] bf16 stored a whole state (M <= 256 rows) per box;
+    // snapshots [BH * events][M][64] (maps of the read-value view when there are none:
+    // nothing is stored through them then)
     const bool snaps = a.snap_k && a.snap_events > 0;
     const uint64_t snap_planes = snaps ? (uint64_t)a.BH * a.snap_events : (uint64_t)a.BH;
     if (!make_tmap_bf16_3d(&mk, a.k_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
         !make_tmap_bf16_3d(&mv, a.v_src, (uint64_t)a.src_row, (uint64_t)a.BH, 128) ||
         !make_tmap_f32_3d(&msk, a.sum_k, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows) ||
         !make_tmap_f32_3d(&msv, a.sum_v, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.stage_rows) ||
-        !make_tmap_bf16_3d(&mvk, a.view_k, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.M) ||
         !make_tmap_bf16_3d(&mvv, a.view_v, (uint64_t)a.M, (uint64_t)a.BH, (uint32_t)a.M) ||
-        !make_tmap_bf16_3d(&msnk, snaps ? a.snap_k : a.view_k, (uint64_t)a.M, snap_planes, (uint32_t)a.M) ||
+        !make_tmap_bf16_3d(&msnk, snaps ? a.snap_k : a.view_v, (uint64_t)a.M, snap_planes, (uint32_t)a.M) ||
         !make_tmap_bf16_3d(&msnv, snaps ? a.snap_v : a.view_v, (uint64_t)a.M, snap_planes, (uint32_t)a.M))
         return cudaErrorInvalidValue;
     // the second-best similarity is tracked only when the debug record wants the top-2 gap
     auto kern = a.dbg_gap ? foldtc::fold_tc_kernel<true> : foldtc::fold_tc_kernel<false>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, foldtc::SMEM_BYTES);
-    kern<<<a.BH, foldtc::NT, foldtc::SMEM_BYTES, s>>>(mk, mv, msk, msv, msnk, msnv, mvk, mvv, a);
+    kern<<<a.BH, foldtc::NT, foldtc::SMEM_BYTES, s>>>(mk, mv, msk, msv, msnk, msnv, mvv, a);
     return cudaGetLastError();
 }
 

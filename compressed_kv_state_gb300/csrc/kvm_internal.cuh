@@ -26,6 +26,13 @@ __device__ __forceinline__ bool kvm_check(bool ok, int* status) {
 __device__ __forceinline__ bool kvm_check(bool, int*) { return true; }
 #endif
 
+// Dims kept per row of the state's read-key view: the non-rotary dims [r, D), rounded
+// up to a multiple of 8 (16 bytes of bf16) and at least 8; the row holds dims
+// [D - view_k_dims(r), D) of the read key.
+__host__ __device__ constexpr int view_k_dims(int r) {
+    return ((D - r + 7) / 8) * 8 < 8 ? 8 : ((D - r + 7) / 8) * 8;
+}
+
 // Per-event schedule entry, computed on the host in double precision (the
 // schedule depends only on counts of tokens, never on data).
 struct Sched {
@@ -64,7 +71,10 @@ __device__ __forceinline__ float warp_max(float v) {
 //   simdir [BH, M, D] fp32 = unit(sum_k - mean(sum_k)), the direction the
 //   winner-take-all cosine compares against (cosine against LayerNorm(x) is
 //   cosine against x - mean(x));
-//   view_k / view_v [BH, M, D] in the I/O dtype = the just-in-time read view.
+//   view_k [BH, M, view_k_dims(r)] and view_v [BH, M, D] in the I/O dtype = the
+//   just-in-time read view.  The read key is zero on the rotary dims [0, r), so
+//   view_k stores only its last view_k_dims(r) dims (rounded up to whole 16-byte
+//   pieces of bf16); the per-event snapshots keep full rows.
 struct FoldArgs {
     float* sum_k;
     float* sum_v;

@@ -229,13 +229,15 @@ kvm_status kvm_layer_get_timing(kvm_layer* layer, kvm_timing* out);
  * sequential prefill (same kernels, same per-tile arithmetic).
  *
  * segments: 0 = never overlap; n > 0 = n fold segments (at most 16, at most
- * the number of fold events); < 0 = automatic (the default).  Overlap applies
- * only to the tensor-core paths (bf16, chunk a multiple of 128 and <= 128,
- * max_slots <= 256), without a debug record, with at least 2 fold events, and
- * when the device leaves at least one SM partition beside B*H SMs, and not
- * while a CUDA injection library (a profiler) is attached; otherwise the
- * prefill runs sequentially.  The partition is made on first use and
- * released by kvm_layer_destroy. */
+ * the number of fold events); < 0 = automatic (the default: 2 segments when
+ * the state fits on chip (max_slots <= 256, chunk 128), where each segment
+ * restart reloads the state; 8 with the streamed state, which restarts for
+ * free).  Overlap applies only to the tensor-core paths (bf16, chunk 128 or
+ * 256, max_slots <= 4096), without a debug record, with at least 2 fold
+ * events, and when the device leaves at least one SM partition beside B*H
+ * SMs, and not while a CUDA injection library (a profiler) is attached;
+ * otherwise the prefill runs sequentially.  The partition is made on first
+ * use and released by kvm_layer_destroy. */
 kvm_status kvm_layer_set_overlap(kvm_layer* layer, int32_t segments);
 
 /* Fold segments the layer's last kvm_prefill ran with (0: sequential). */
