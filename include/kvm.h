@@ -104,7 +104,8 @@ typedef struct kvm_layer kvm_layer;
  *   ring_g       : fp32 [B, H, W + C]        their merge gates
  * Host scalars (identical for every (batch, head): the schedule is data
  * independent): n_slots, n_overflow (tokens folded so far), pos (next
- * position).  Rows >= n_slots of the slot arrays are unspecified on export
+ * position).  Rows >= n_slots of the slot arrays, and ring rows that hold no
+ * token (positions outside n_overflow .. pos-1), are unspecified on export
  * and ignored on import. */
 typedef struct {
     float* sum_k;
