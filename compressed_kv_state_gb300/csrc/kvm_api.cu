@@ -124,6 +124,7 @@ Layout layout_of(const kvm_config& c) {
     L.sched = take((E + 1) * sizeof(Sched));
     L.status = take(256);  // status word at 0, attention tile-range counters at TILE_CTR_OFF
     L.k_rot = take(c.dtype == KVM_BF16 && c.rope_dims > 0 ? BH * (size_t)c.max_tokens * d * es : 0);
+    L.q_rot = take(c.dtype == KVM_BF16 && c.rope_dims > 0 ? BH * (size_t)c.max_tokens * d * es : 0);
     L.total = o;
     return L;
 }
@@ -425,6 +426,10 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     const bool pre_rotate = bf16 && c.rope_dims > 0 && n_tokens > 0 && kvm::attn_tc_supported(aa, bf16);
     if (pre_rotate) {
         aa.k_rot = ka.k_rot;
+        // the queries are rotated in the same pass
+        ka.q = q;
+        ka.q_rot = ly->ws + L.q_rot;
+        aa.q_rot = ka.q_rot;
         // the window ring is filled in the same pass
         if (ring_work) {
             ka.v = v;
@@ -875,6 +880,119 @@ kvm_status kvm_layer_forward(kvm_layer* ly, int32_t d_model, const void* x, cons
     e = timed(ly, PH_PROJ, s, [&] { return kvm::launch_gemm_tc(outp, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "output projection launch");
     ly->kernels += 1;
+    return KVM_OK;
+}
+
+namespace {
+struct BwdScratch {
+    size_t qr, kr, lse, dd, dks, dvs, drho, sk, sv, gk, gv, cnt, rho, grho, total;
+};
+BwdScratch bwd_scratch_of(const kvm_config& c, int64_t n_tokens) {
+    BwdScratch b;
+    const size_t BH = (size_t)c.batch * c.heads, M = c.max_slots;
+    const size_t rows = BH * (size_t)n_tokens, es = c.dtype == KVM_BF16 ? 2 : 4;
+    const size_t E = (size_t)kvm::host::n_events_for(c, n_tokens);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = kvm::host::align_up(o + bytes); return at; };
+    b.qr = take(rows * D * es);
+    b.kr = take(rows * D * es);
+    b.lse = take(rows * 4);
+    b.dd = take(rows * 4);
+    b.dks = take(BH * E * M * D * 4);
+    b.dvs = take(BH * E * M * D * 4);
+    b.drho = take(BH * E * M * 4);
+    b.sk = take(BH * M * D * 4);
+    b.sv = take(BH * M * D * 4);
+    b.gk = take(BH * M * D * 4);
+    b.gv = take(BH * M * D * 4);
+    b.cnt = take(BH * M * 4);
+    b.rho = take(BH * M * 4);
+    b.grho = take(BH * M * 4);
+    b.total = o;
+    return b;
+}
+}  // namespace
+
+size_t kvm_backward_scratch_bytes(const kvm_config* cfg, int64_t n_tokens) {
+    std::string why;
+    if (!validate(cfg, why)) { g_err = why; return 0; }
+    if (n_tokens < 0 || n_tokens > cfg->max_tokens) { g_err = "n_tokens must be in [0, max_tokens]"; return 0; }
+    return bwd_scratch_of(*cfg, n_tokens).total;
+}
+
+kvm_status kvm_prefill_backward(kvm_layer* ly, const void* q, const void* k, const void* v, const float* gate,
+                                const void* out, const void* dout, const kvm_debug* rec, int64_t n_tokens,
+                                float* dq, float* dk, float* dv, float* dgate, void* scratch,
+                                size_t scratch_bytes, void* cuda_stream) {
+    NvtxRange nvtx_range("kvm_prefill_backward");
+    if (!ly) { g_err = "layer is NULL"; return KVM_ERR_INVALID_ARG; }
+    const kvm_config& c = ly->cfg;
+    if (!q || !k || !v || !gate || !out || !dout || !dq || !dk || !dv || !dgate || !scratch)
+        return ly->fail(KVM_ERR_INVALID_ARG, "q, k, v, gate, out, dout, dq, dk, dv, dgate and scratch must be non-NULL");
+    if (c.chunk > kvm::MAX_BW_C) return ly->fail(KVM_ERR_UNSUPPORTED, "the backward supports chunks of at most 256 tokens");
+    if (c.rope_dims % 4) return ly->fail(KVM_ERR_UNSUPPORTED, "the backward needs rope_dims a multiple of 4");
+    if (n_tokens < 0 || n_tokens > c.max_tokens) return ly->fail(KVM_ERR_INVALID_ARG, "n_tokens must be in [0, max_tokens]");
+    const int64_t E = kvm::host::n_events_for(c, n_tokens);
+    if (ly->pos != n_tokens || ly->n_overflow != E * c.chunk)
+        return ly->fail(KVM_ERR_INVALID_ARG, "the layer's last prefill was not of n_tokens tokens");
+    if (E > 0 && (!rec || !rec->assign || !rec->kind || rec->max_events < E))
+        return ly->fail(KVM_ERR_INVALID_ARG, "the forward's record (assign and kind of every fold event) is needed");
+    const BwdScratch B = bwd_scratch_of(c, n_tokens);
+    if (reinterpret_cast<uintptr_t>(scratch) % ALIGN || scratch_bytes < B.total)
+        return ly->fail(KVM_ERR_WORKSPACE, "scratch missing, misaligned or smaller than kvm_backward_scratch_bytes");
+    DeviceGuard g(ly->device);
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    ly->last_stream = s;
+    const Layout& L = ly->L;
+    char* sc = static_cast<char*>(scratch);
+    kvm::BackwardArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = gate;
+    a.out = out;
+    a.dout = dout;
+    a.assign = rec ? rec->assign : nullptr;
+    a.kind = rec ? rec->kind : nullptr;
+    a.rec_events = rec ? (int)rec->max_events : 0;
+    a.snap_k = ly->ws + L.snap_k;
+    a.snap_v = ly->ws + L.snap_v;
+    a.snap_events = (int)ly->E_max;
+    a.sched = ly->at<kvm::Sched>(L.sched);
+    a.rope = ly->at<float2>(L.rope);
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dg = dgate;
+    a.qr = sc + B.qr;
+    a.kr = sc + B.kr;
+    a.lse = reinterpret_cast<float*>(sc + B.lse);
+    a.dd = reinterpret_cast<float*>(sc + B.dd);
+    a.dks = reinterpret_cast<float*>(sc + B.dks);
+    a.dvs = reinterpret_cast<float*>(sc + B.dvs);
+    a.drho = reinterpret_cast<float*>(sc + B.drho);
+    a.sk = reinterpret_cast<float*>(sc + B.sk);
+    a.sv = reinterpret_cast<float*>(sc + B.sv);
+    a.gk = reinterpret_cast<float*>(sc + B.gk);
+    a.gv = reinterpret_cast<float*>(sc + B.gv);
+    a.cnt = reinterpret_cast<int*>(sc + B.cnt);
+    a.rho = reinterpret_cast<float*>(sc + B.rho);
+    a.grho = reinterpret_cast<float*>(sc + B.grho);
+    a.N = n_tokens;
+    a.BH = c.batch * c.heads;
+    a.C = c.chunk;
+    a.W = c.window;
+    a.M = c.max_slots;
+    a.r = c.rope_dims;
+    a.E = (int)E;
+    a.ln_eps = c.ln_eps;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    a.inv_sqrt_d = (float)(1.0 / std::sqrt((double)D));
+    a.no_vnorm = (c.flags & KVM_FLAG_NO_VALUE_NORM) ? 1 : 0;
+    a.status = ly->at<int>(L.status);
+    cudaError_t e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_backward(a, c.dtype == KVM_BF16, s); });
+    if (e != cudaSuccess) return ly->cuda_fail(e, "backward launch");
+    ly->kernels += a.E > 0 ? 6 : 4;
     return KVM_OK;
 }
 

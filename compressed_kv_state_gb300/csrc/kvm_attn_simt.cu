@@ -180,12 +180,53 @@ __global__ void ring_fill_kernel(RingFillArgs a) {
 // is a multiple of 8, one dim at a time otherwise); the rest are copied.  Rows
 // (b, h) are strided over gridDim.y and chunks of a row over gridDim.x, so the
 // position of a chunk needs no division.
+// Rotate the 16-byte chunk c (dims 8c .. 8c+7) of row p of src (row-major [N][8] chunks)
+// in place in w: rotate-half pairs (x, x + half) on the rotary dims [0, r).
+__device__ __forceinline__ void rope_chunk(const uint4* src, int64_t p, int c, int r, const float2* rope, uint4& w) {
+    const int half = r / 2;
+    if (8 * c >= r) return;
+    if ((half & 7) == 0) {
+        const int hc = half >> 3;
+        const bool low = c < hc;  // dims [0, half) pair with [half, r)
+        const uint4 o = src[p * 8 + (low ? c + hc : c - hc)];
+        const float4* tab = reinterpret_cast<const float4*>(rope + p * half + (low ? c : c - hc) * 8);
+        const float4 t[4] = {tab[0], tab[1], tab[2], tab[3]};
+        const float ce[8] = {t[0].x, t[0].z, t[1].x, t[1].z, t[2].x, t[2].z, t[3].x, t[3].z};
+        const float se[8] = {t[0].y, t[0].w, t[1].y, t[1].w, t[2].y, t[2].w, t[3].y, t[3].w};
+        __nv_bfloat162* m2 = reinterpret_cast<__nv_bfloat162*>(&w);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 mv = __bfloat1622float2(m2[u]), ov = __bfloat1622float2(o2[u]);
+            const float c0 = ce[2 * u], c1 = ce[2 * u + 1], s0 = se[2 * u], s1 = se[2 * u + 1];
+            m2[u] = low ? __floats2bfloat162_rn(mv.x * c0 - ov.x * s0, mv.y * c1 - ov.y * s1)
+                        : __floats2bfloat162_rn(mv.x * c0 + ov.x * s0, mv.y * c1 + ov.y * s1);
+        }
+    } else {
+        const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(src + p * 8);
+        __nv_bfloat16* m = reinterpret_cast<__nv_bfloat16*>(&w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int x = 8 * c + e;
+            if (x < 2 * half) {
+                const int i2 = x < half ? x : x - half;
+                const float2 cs = rope[p * half + i2];
+                const float kv = __bfloat162float(krow[x]);
+                const float r2 = x < half ? kv * cs.x - __bfloat162float(krow[x + half]) * cs.y
+                                          : kv * cs.x + __bfloat162float(krow[x - half]) * cs.y;
+                m[e] = __float2bfloat16_rn(r2);
+            }
+        }
+    }
+}
+
 __global__ void rope_keys_kernel(RopeKeysArgs a) {
-    const int half = a.r / 2;
     const int64_t per_row = a.N * 8;
     for (int bh = blockIdx.y; bh < a.BH; bh += gridDim.y) {
         const uint4* src = reinterpret_cast<const uint4*>(a.k) + (int64_t)bh * per_row;
         uint4* dst = reinterpret_cast<uint4*>(a.k_rot) + (int64_t)bh * per_row;
+        const uint4* qsrc = a.q ? reinterpret_cast<const uint4*>(a.q) + (int64_t)bh * per_row : nullptr;
+        uint4* qdst = a.q ? reinterpret_cast<uint4*>(a.q_rot) + (int64_t)bh * per_row : nullptr;
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per_row;
              i += (int64_t)gridDim.x * blockDim.x) {
             const int64_t p = i >> 3;
@@ -201,43 +242,14 @@ __global__ void rope_keys_kernel(RopeKeysArgs a) {
                     reinterpret_cast<const uint4*>(a.v)[(int64_t)bh * per_row + i];
                 if (c == 0) a.ring_g[rrow] = a.g[(int64_t)bh * a.N + p];
             }
-            if (8 * c < a.r) {
-                if ((half & 7) == 0) {
-                    const int hc = half >> 3;
-                    const bool low = c < hc;  // dims [0, half) pair with [half, r)
-                    const uint4 o = src[p * 8 + (low ? c + hc : c - hc)];
-                    const float4* tab = reinterpret_cast<const float4*>(a.rope + p * half + (low ? c : c - hc) * 8);
-                    const float4 t[4] = {tab[0], tab[1], tab[2], tab[3]};
-                    const float ce[8] = {t[0].x, t[0].z, t[1].x, t[1].z, t[2].x, t[2].z, t[3].x, t[3].z};
-                    const float se[8] = {t[0].y, t[0].w, t[1].y, t[1].w, t[2].y, t[2].w, t[3].y, t[3].w};
-                    __nv_bfloat162* m2 = reinterpret_cast<__nv_bfloat162*>(&w);
-                    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float2 mv = __bfloat1622float2(m2[u]), ov = __bfloat1622float2(o2[u]);
-                        const float c0 = ce[2 * u], c1 = ce[2 * u + 1], s0 = se[2 * u], s1 = se[2 * u + 1];
-                        m2[u] = low ? __floats2bfloat162_rn(mv.x * c0 - ov.x * s0, mv.y * c1 - ov.y * s1)
-                                    : __floats2bfloat162_rn(mv.x * c0 + ov.x * s0, mv.y * c1 + ov.y * s1);
-                    }
-                } else {
-                    const __nv_bfloat16* krow = reinterpret_cast<const __nv_bfloat16*>(src + p * 8);
-                    __nv_bfloat16* m = reinterpret_cast<__nv_bfloat16*>(&w);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int x = 8 * c + e;
-                        if (x < 2 * half) {
-                            const int i2 = x < half ? x : x - half;
-                            const float2 cs = a.rope[p * half + i2];
-                            const float kv = __bfloat162float(krow[x]);
-                            const float r2 = x < half ? kv * cs.x - __bfloat162float(krow[x + half]) * cs.y
-                                                      : kv * cs.x + __bfloat162float(krow[x - half]) * cs.y;
-                            m[e] = __float2bfloat16_rn(r2);
-                        }
-                    }
-                }
-            }
+            rope_chunk(src, p, c, a.r, a.rope, w);
             dst[i] = w;
             if (ring) reinterpret_cast<uint4*>(a.ring_kr)[rrow * 8 + c] = w;
+            if (qsrc) {
+                uint4 wq = qsrc[i];
+                rope_chunk(qsrc, p, c, a.r, a.rope, wq);
+                qdst[i] = wq;
+            }
         }
     }
 }

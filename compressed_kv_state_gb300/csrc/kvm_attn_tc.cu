@@ -61,6 +61,7 @@ struct TcArgs {
     float scale_log2;
     __nv_bfloat16* out;
     int* status;
+    int q_prerot;    // queries come rotated: no RoPE in the kernel, the MMA waits for the copy
 };
 
 struct Tile {
@@ -264,13 +265,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             KVM_PROBE_DECL(4)
             KVM_PROBE_START()
             for (int k = 0;; ++k) {
-                if (k >= 1 && !mbar_wait(bar(slot, B_QEMPTY), (k - 1) & 1, abort_flag, a.status)) break;
-                KVM_PROBE_LAP(2)
+                // the next tile is picked and published before its query buffer is free
+                // (consumers are at most two tiles behind: the ring holds four)
                 const int id = next_tile2(a, slot, k, &range);
                 tile_ring[slot * 4 + (k & 3)] = id;
                 mbar_arrive(bar(slot, B_TILE + (k & 3)));
                 if (id < 0) break;
                 const Tile T = tile_of2(a, id);
+                if (k >= 1 && !mbar_wait(bar(slot, B_QEMPTY), (k - 1) & 1, abort_flag, a.status)) break;
+                KVM_PROBE_LAP(2)
                 mbar_expect_tx(bar(slot, B_QFULL), Q_BYTES);
                 tma_load_3d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, 0, (int)T.q0, T.bh, bar(slot, B_QFULL));
                 bool ok = true;
@@ -345,17 +348,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (id < 0) break;
                 const Tile T = tile_of2(a, id);
                 KVM_PROBE_LAP(6)
-                if (!mbar_wait(bar(slot, B_QREADY), k & 1, abort_flag, a.status)) break;
+                if (!mbar_wait(bar(slot, a.q_prerot ? B_QFULL : B_QREADY), k & 1, abort_flag, a.status)) break;
                 KVM_PROBE_LAP(0)
                 tc_fence_after();
                 if (!issue_qk(g, T.nst > 0)) break;
+                // the query tile is free once the tile's last QK^T completes: the next
+                // tile's query loads while this tile's last blocks run
+                if (T.nblk == 1) mma_commit(bar(slot, B_QEMPTY));
                 for (int j = 0; j < T.nblk; ++j) {
                     const int gj = g + j, st = gj % NS;
                     // the next block's QK^T overlaps this block's softmax
                     if (j + 1 < T.nblk) {
                         if (!issue_qk(gj + 1, j + 1 < T.nst)) { ok = false; break; }
+                        if (j + 2 == T.nblk) mma_commit(bar(slot, B_QEMPTY));
                     }
-                    if (j + 1 == T.nblk) mma_commit(bar(slot, B_QEMPTY));  // all QK^T of the tile issued
                     if (!mbar_wait(bar(slot, B_PFULL), gj & 1, abort_flag, a.status)) { ok = false; break; }
                     KVM_PROBE_LAP(3)
                     if (!mbar_wait(bar(slot, B_VFULL + st), (gj / NS) & 1, abort_flag, a.status)) { ok = false; break; }
@@ -399,17 +405,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (id < 0) break;
             const Tile T = tile_of2(a, id);
             const int64_t p = T.q0 + row;
-            // RoPE of this thread's query row, then hand the tile to the MMA
-            if (!mbar_wait(bar(slot, B_QFULL), k & 1, abort_flag, a.status)) break;
-            KVM_PROBE_LAP(0)
-            if (half > 0 && p < a.N) {
-                if ((half & 7) == 0)
-                    rope_row_vec(qrow, row, p, a.rope, half);
-                else
-                    rope_row(qrow, row, p, a.rope, half);
+            // RoPE of this thread's query row, then hand the tile to the MMA (nothing to
+            // do when the queries come rotated: the MMA waits for their copy itself)
+            if (!a.q_prerot) {
+                if (!mbar_wait(bar(slot, B_QFULL), k & 1, abort_flag, a.status)) break;
+                KVM_PROBE_LAP(0)
+                if (half > 0 && p < a.N) {
+                    if ((half & 7) == 0)
+                        rope_row_vec(qrow, row, p, a.rope, half);
+                    else
+                        rope_row(qrow, row, p, a.rope, half);
+                }
+                fence_proxy_async();
+                mbar_arrive(bar(slot, B_QREADY));
             }
-            fence_proxy_async();
-            mbar_arrive(bar(slot, B_QREADY));
             KVM_PROBE_LAP(1)
             float m_used = -INFINITY, l = 0.0f;
             for (int j = 0; j < T.nblk; ++j) {
@@ -623,7 +632,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     const uint64_t planes_snap = BH * (uint64_t)(a.snap_events > 0 ? a.snap_events : 1);
     // window keys must come rotated at their own positions when the layer has rotary dims
     if (a.r > 0 && !a.k_rot) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_3d(&mq, a.q, (uint64_t)a.N, BH, 128) || !make_tmap_bf16_3d(&mk, a.k_rot ? a.k_rot : a.k, (uint64_t)a.N, BH, KB) ||
+    if (!make_tmap_bf16_3d(&mq, a.q_rot ? a.q_rot : a.q, (uint64_t)a.N, BH, 128) || !make_tmap_bf16_3d(&mk, a.k_rot ? a.k_rot : a.k, (uint64_t)a.N, BH, KB) ||
         !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH, KB) ||
         !make_tmap_bf16_3d(&msk, a.snap_k, (uint64_t)a.M, planes_snap, KB) ||
         !make_tmap_bf16_3d(&msv, a.snap_v, (uint64_t)a.M, planes_snap, KB))
@@ -649,6 +658,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     t.scale_log2 = a.scale_log2;
     t.out = reinterpret_cast<__nv_bfloat16*>(a.out);
     t.status = status;
+    t.q_prerot = a.q_rot != nullptr || a.r == 0;
     static int nsm = 0;
     if (nsm == 0) {
         int dev = 0;

@@ -21,6 +21,7 @@ struct Layout {
     size_t sum_k, sum_v, counts, rho, simdir, view_k, view_v;
     size_t ring_k, ring_v, ring_g, ring_kr, snap_k, snap_v, rope, sched, status;
     size_t k_rot;  // keys rotated at their own positions (bf16 layers with rope_dims > 0; else empty)
+    size_t q_rot;  // queries rotated at their own positions (same condition)
     size_t total;
 };
 

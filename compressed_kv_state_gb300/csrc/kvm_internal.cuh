@@ -143,6 +143,9 @@ struct AttnArgs {
     // Tensor-core path: keys already rotated at their own positions (launch_rope_keys),
     // read instead of k for the window; nullptr = rotate window keys in the kernel.
     const void* k_rot;
+    // Tensor-core path: queries already rotated at their own positions (the same pass),
+    // loaded instead of q; nullptr = each tile rotates its queries in the kernel.
+    const void* q_rot;
 };
 
 // Keys rotated once at their own positions (rotate-half RoPE on dims [0, r)),
@@ -151,6 +154,8 @@ struct AttnArgs {
 struct RopeKeysArgs {
     const void* k;
     void* k_rot;
+    const void* q;   // optional (nullptr: none): queries rotated into q_rot in the same pass
+    void* q_rot;
     const float2* rope;  // [max_tokens, r/2] (cos, sin)
     int r;
     int64_t N;
@@ -168,6 +173,51 @@ struct RopeKeysArgs {
     int64_t first;
     int L;
 };
+
+// Backward of a prefill at the forward's fold decisions (kvm_backward.cu).  All
+// arrays are device memory; [BH, N, D] rows in the layer's dtype unless noted.
+constexpr int MAX_BW_C = 256;  // chunk sizes the backward supports
+struct BackwardArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;       // [BH, N]
+    const void* out;      // the forward's output
+    const void* dout;     // gradient of the loss with respect to out
+    const int32_t* assign;  // the forward's debug record [BH, rec_events, C]
+    const int32_t* kind;
+    int rec_events;
+    const void* snap_k;   // the forward's read rows after every event [BH, snap_events, M, D]
+    const void* snap_v;
+    int snap_events;
+    const Sched* sched;
+    const float2* rope;
+    float* dq;            // fp32 [BH, N, D]
+    float* dk;
+    float* dv;
+    float* dg;            // fp32 [BH, N]
+    // scratch
+    void* qr;             // rotated q and k [BH, N, D]
+    void* kr;
+    float* lse;           // [BH, N] log2-sum-exp of each query's scores
+    float* dd;            // [BH, N] dout . out
+    float* dks;           // [BH, E, M, D] read-row gradients, then sum gradients
+    float* dvs;
+    float* drho;          // [BH, E, M]
+    float* sk;            // [BH, M, D] replayed sums
+    float* sv;
+    int* cnt;             // [BH, M]
+    float* rho;
+    float* gk;            // [BH, M, D] accumulated sum gradients
+    float* gv;
+    float* grho;          // [BH, M]
+    int64_t N;
+    int BH, C, W, M, r, E;
+    float ln_eps, scale_log2, inv_sqrt_d;
+    int no_vnorm;
+    int* status;          // a record entry outside [0, M) or of no known kind latches STATUS_DEVICE
+};
+cudaError_t launch_backward(const BackwardArgs& a, bool bf16, cudaStream_t s);
 
 struct DecodeArgs {
     const void* q;

@@ -208,6 +208,8 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         kvm::RopeKeysArgs ka{};
         ka.k = k;
         ka.k_rot = ws + L.k_rot;
+        ka.q = q;
+        ka.q_rot = ws + L.q_rot;
         ka.rope = aa.rope;
         ka.r = c.rope_dims;
         ka.N = n_tokens;
@@ -215,6 +217,7 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         ka.grid = 8 * (nsm > 0 ? nsm : 1);
         e = kvm::launch_rope_keys(ka, s);
         aa.k_rot = ka.k_rot;
+        aa.q_rot = ka.q_rot;
     }
     if (e == cudaSuccess) e = kvm::launch_attn(aa, bf16, s);
     if (e != cudaSuccess) {

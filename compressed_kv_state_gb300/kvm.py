@@ -100,6 +100,10 @@ def _load():
     lib.kvm_layer_get_overlap.argtypes = [P, P]
     lib.kvm_prefill_noalloc.restype = ctypes.c_int
     lib.kvm_prefill_noalloc.argtypes = [P, P, P, P, P, I64, P, P]
+    lib.kvm_backward_scratch_bytes.restype = ctypes.c_size_t
+    lib.kvm_backward_scratch_bytes.argtypes = [P, I64]
+    lib.kvm_prefill_backward.restype = ctypes.c_int
+    lib.kvm_prefill_backward.argtypes = [P, P, P, P, P, P, P, P, I64, P, P, P, P, P, ctypes.c_size_t, P]
     lib.kvm_layer_destroy.restype = None
     lib.kvm_layer_destroy.argtypes = [P]
     return lib
@@ -237,6 +241,23 @@ def kvm_prefill_noalloc(cfg: kvm_config, q, k, v, gate, n_tokens: int, out, stre
     _check(st, None)
 
 
+def kvm_backward_scratch_bytes(cfg: kvm_config, n_tokens: int) -> int:
+    n = lib.kvm_backward_scratch_bytes(ctypes.byref(cfg), int(n_tokens))
+    if n == 0:
+        raise KvmError(KVM_ERR_INVALID_ARG, kvm_last_error(None))
+    return n
+
+
+def kvm_prefill_backward(layer, q, k, v, gate, out, dout, record: kvm_debug | None, n_tokens: int,
+                         dq, dk, dv, dgate, scratch, stream=None):
+    """Backward of the layer's last prefill at its fold decisions (fp32 gradients)."""
+    st = lib.kvm_prefill_backward(layer, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), _ptr(dout),
+                                  ctypes.byref(record) if record is not None else None, int(n_tokens),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgate), _ptr(scratch),
+                                  int(scratch.numel() * scratch.element_size()), _stream(stream))
+    _check(st, layer)
+
+
 def kvm_last_error(layer) -> str:
     return lib.kvm_last_error(layer).decode()
 
@@ -310,6 +331,23 @@ class KvmLayer:
         self._io(out, shp)
         kvm_prefill(self.handle, q, k, v, gate, N, out, stream, dbg)
         return out
+
+    def prefill_backward(self, q, k, v, gate, out, dout, record: kvm_debug | None, stream=None):
+        """Gradients (dq, dk, dv, dgate; fp32) of the last prefill of these inputs, at its
+        fold decisions (record: the kvm_debug that prefill filled)."""
+        import torch
+        c = self.cfg
+        N = q.shape[2]
+        shp = (c.batch, c.heads, N, c.head_dim)
+        for t in (q, k, v, out, dout):
+            self._io(t, shp)
+        self._io(gate, shp[:3], torch.float32)
+        dev = q.device
+        dq, dk, dv = (torch.empty(shp, dtype=torch.float32, device=dev) for _ in range(3))
+        dg = torch.empty(shp[:3], dtype=torch.float32, device=dev)
+        scratch = torch.empty(kvm_backward_scratch_bytes(c, N), dtype=torch.uint8, device=dev)
+        kvm_prefill_backward(self.handle, q, k, v, gate, out, dout, record, N, dq, dk, dv, dg, scratch, stream)
+        return dq, dk, dv, dg
 
     def decode_step(self, q, k, v, gate, out=None, stream=None):
         import torch

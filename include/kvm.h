@@ -301,6 +301,36 @@ kvm_status kvm_layer_forward(kvm_layer* layer, int32_t d_model, const void* x, c
 kvm_status kvm_prefill_noalloc(const kvm_config* cfg, const void* q, const void* k, const void* v,
                                const float* gate, int64_t n_tokens, void* out, void* cuda_stream);
 
+/* Backward of kvm_prefill for chunk-parallel training ("Key-Value Means",
+ * technical summary, Contributions: the layer trains chunk-parallel).  The
+ * pages do not say how the gradient passes the winner-take-all assignment;
+ * here the fold's discrete decisions (the slot of every merged token, the
+ * surprise-selected appends, the sinks) are constants from the forward, and
+ * the gradient flows through the attention, RoPE, the just-in-time read of
+ * the state (LayerNorm(sum_k / count) with the rotary dims zeroed,
+ * rho * unit(sum_v)), the gate-weighted member sums and the founders' read
+ * radius rho = |v|.  Counts carry no gradient.
+ *
+ * Call it after the layer's kvm_prefill of the same q, k, v, gate and
+ * n_tokens, with no other prefill on the layer in between (it reads the
+ * forward's per-event read rows from the workspace): out is that prefill's
+ * output, record its debug record (assign and kind of every fold event; NULL
+ * allowed when no event folded), dout the loss gradient with respect to out
+ * (dtype [B, H, n_tokens, d]).  Outputs fp32: dq, dk, dv [B, H, n_tokens, d],
+ * dgate [B, H, n_tokens]; every element is written.  scratch: device memory of
+ * kvm_backward_scratch_bytes(cfg, n_tokens) bytes, 256-byte aligned.  Chunks of
+ * at most 256 tokens and rope_dims a multiple of 4 (else KVM_ERR_UNSUPPORTED).
+ * KVM_ERR_INVALID_ARG when the layer's last prefill was not of n_tokens tokens
+ * or the record is missing or shorter than the fold events; a record entry
+ * that names no slot of its event's state is skipped and makes kvm_layer_sync
+ * report KVM_ERR_DEVICE. */
+size_t kvm_backward_scratch_bytes(const kvm_config* cfg, int64_t n_tokens);
+kvm_status kvm_prefill_backward(kvm_layer* layer, const void* q, const void* k, const void* v,
+                                const float* gate, const void* out, const void* dout,
+                                const kvm_debug* record, int64_t n_tokens, float* dq, float* dk,
+                                float* dv, float* dgate, void* scratch, size_t scratch_bytes,
+                                void* cuda_stream);
+
 /* Free the layer's host metadata.  The workspace stays the caller's. */
 void kvm_layer_destroy(kvm_layer* layer);
 
