@@ -539,6 +539,7 @@ def run_ours(args, rank, world, local_rank):
             torch.cuda.synchronize(dev)
     decode = None if args.no_decode else run_decode(dev, stream)
     layer_fwd = None if args.no_layer else run_layer(dev, stream, max(3, args.steps // 2), args.segments)
+    bwd = None if args.no_backward else run_backward(dev, stream, max(3, args.steps // 4))
     clk = clocks.stop()
 
     kernels, roofline, step_roof, flops = prefill_report(W, timing_main, peaks)
@@ -565,8 +566,75 @@ def run_ours(args, rank, world, local_rank):
         "workloads": others,
         "decode": decode,
         "layer_forward": layer_fwd,
+        "backward": bwd,
     }
     return line
+
+
+def run_backward(dev, stream, steps):
+    """Backward of the headline prefill at its fold decisions (kvm_prefill_backward):
+    one sequential prefill with a decision record, then the backward timed alone
+    with CUDA events; fp32 gradients of q, k, v and the gate."""
+    import torch
+    from compressed_kv_state_gb300 import kvm
+    q, k, v, g = wl.prefill_inputs(W)
+    rng = np.random.default_rng(11)
+    dout = rng.standard_normal(q.shape).astype(np.float32)
+    tq, tk, tv, tdo = (torch.from_numpy(x).to(dev).bfloat16() for x in (q, k, v, dout))
+    tg = torch.from_numpy(g).to(dev)
+    cfg = kvm.make_config(batch=W.B, heads=W.H, rope_dims=W.rope_dims, chunk=W.chunk, window=W.window,
+                          n_sinks=W.n_sinks, sched=W.sched, max_slots=W.max_slots, max_tokens=W.N)
+    layer = kvm.KvmLayer(cfg, device=dev)
+    E = _n_events(W)
+    shp = (W.B, W.H, E, W.chunk)
+    assign = torch.empty(shp, dtype=torch.int32, device=dev)
+    kind = torch.empty(shp, dtype=torch.int32, device=dev)
+    rec = kvm.kvm_debug(assign.data_ptr(), kind.data_ptr(), None, None, E)
+    out = layer.prefill(tq, tk, tv, tg, stream=stream, dbg=rec)
+    nq = (W.B, W.H, W.N, W.d)
+    dq, dk, dv = (torch.empty(nq, dtype=torch.float32, device=dev) for _ in range(3))
+    dg = torch.empty(nq[:3], dtype=torch.float32, device=dev)
+    scratch = torch.empty(kvm.kvm_backward_scratch_bytes(cfg, W.N), dtype=torch.uint8, device=dev)
+
+    def step():
+        kvm.kvm_prefill_backward(layer.handle, tq, tk, tv, tg, out, tdo, rec, W.N, dq, dk, dv, dg, scratch,
+                                 stream)
+
+    for _ in range(2):
+        step()
+    layer.sync()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    layer.sync()
+    ms = e0.elapsed_time(e1) / steps
+    aw = attention_work(W)
+    flops = 2.5 * aw["flops_4d"]  # five products of 2d per (query, key) pair against two forward
+    peak = fp32_simt_peak_tflops()
+    tf = flops / (ms / 1e3) / 1e12
+    layer.close()
+    return {"ms_per_call": ms, "steps": steps, "value": W.B * W.N / (ms / 1e3), "unit": "tokens/s",
+            "algorithmic_flops": flops,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_source": "fp32 FMA lanes x 2 x max SM clock (152 SMs x 128 lanes x 2 x 2070 MHz)"},
+            "finite": bool(torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+                           and torch.isfinite(dg).all()),
+            "note": "fold decisions from the forward's record are constants (no gradient through the "
+                    "winner-take-all assignment); SIMT kernels, fp32 arithmetic"}
+
+
+def fp32_simt_peak_tflops():
+    """Nominal fp32 FMA rate: 152 SMs x 128 fp32 lanes x 2 FLOP x 2070 MHz."""
+    return 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def _n_events(w):
+    nchunks = -(-w.N // w.chunk)
+    return max(0, nchunks - w.window // w.chunk - 1)
 
 
 def run_layer(dev, stream, steps, segments=-1, d_model=768):
@@ -722,6 +790,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-layer", action="store_true", help="skip the whole-layer forward line")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward line")
     ap.add_argument("--segments", type=int, default=-1,
                     help="fold segments of the overlapped prefill (0: sequential, <0: automatic)")
     ap.add_argument("--no-cpu", action="store_true")
