@@ -125,6 +125,17 @@ Layout layout_of(const kvm_config& c) {
     L.status = take(256);  // status word at 0, attention tile-range counters at TILE_CTR_OFF
     L.k_rot = take(c.dtype == KVM_BF16 && c.rope_dims > 0 ? BH * (size_t)c.max_tokens * d * es : 0);
     L.q_rot = take(c.dtype == KVM_BF16 && c.rope_dims > 0 ? BH * (size_t)c.max_tokens * d * es : 0);
+    // the streamed-state chain's per-event log of touched rows (snapshots are rebuilt from it)
+    kvm::FoldArgs probe{};
+    probe.C = c.chunk;
+    probe.M = c.max_slots;
+    const bool logs = kvm::fold_logs_rows(probe, c.dtype == KVM_BF16);
+    const size_t lrows = logs ? BH * E * (size_t)c.chunk : 0;
+    L.log_k = take(lrows * d * es);
+    L.log_v = take(lrows * d * es);
+    L.log_idx = take(lrows * 4);
+    L.log_cnt = take(logs ? BH * E * 4 : 0);
+    L.logs = logs;
     L.total = o;
     return L;
 }
@@ -369,6 +380,24 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     fa.snap_k = ly->ws + L.snap_k;
     fa.snap_v = ly->ws + L.snap_v;
     fa.snap_events = (int)ly->E_max;
+    if (L.logs) {
+        fa.log_k = ly->ws + L.log_k;
+        fa.log_v = ly->ws + L.log_v;
+        fa.log_idx = ly->at<int>(L.log_idx);
+        fa.log_cnt = ly->at<int>(L.log_cnt);
+    }
+    kvm::SnapRebuildArgs rb{};
+    rb.log_k = fa.log_k;
+    rb.log_v = fa.log_v;
+    rb.log_idx = fa.log_idx;
+    rb.log_cnt = fa.log_cnt;
+    rb.snap_k = fa.snap_k;
+    rb.snap_v = fa.snap_v;
+    rb.snap_events = fa.snap_events;
+    rb.C = c.chunk;
+    rb.M = c.max_slots;
+    rb.BH = (int)BH;
+    rb.sched = fa.sched;
     if (dbg) {
         fa.dbg_assign = dbg->assign;
         fa.dbg_kind = dbg->kind;
@@ -507,6 +536,17 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
                 if (r == cudaSuccess) r = cudaEventRecord(P.ev_seg[sg], P.s_fold);
                 if (r != cudaSuccess) return r;
                 ly->kernels += 1;
+                if (L.logs && sg + 1 < segs) {
+                    // the segment's snapshots, from its row log, on the attention's SMs (the
+                    // last segment's run on every SM, before the last attention launch)
+                    rb.e_begin = fa.e_begin;
+                    rb.e_end = fa.e_end;
+                    r = cudaStreamWaitEvent(P.s_attn, P.ev_seg[sg], 0);
+                    if (r == cudaSuccess) r = timed(ly, PH_OTHER, P.s_attn, [&] { return kvm::launch_snap_rebuild(rb, P.s_attn); });
+                    if (r == cudaSuccess) r = cudaEventRecord(P.ev_rebuilt, P.s_attn);
+                    if (r != cudaSuccess) return r;
+                    ly->kernels += 1;
+                }
                 if (sg + 1 < segs) {
                     r = cudaStreamWaitEvent(P.s_attn, P.ev_seg[sg], 0);
                     aa.n_ranges = sg + 2;
@@ -518,8 +558,17 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             return cudaSuccess;
         });
         if (e != cudaSuccess) return ly->cuda_fail(e, "overlapped fold / attention launch");
-        // what is left of the attention on every SM, once the chain is done
+        // what is left of the attention on every SM, once the chain is done (and, with
+        // the row log, once the last snapshots are rebuilt)
         e = cudaStreamWaitEvent(s, P.ev_seg[segs - 1], 0);
+        if (e == cudaSuccess && L.logs) {
+            rb.e_begin = (int)(E * (segs - 1) / segs);
+            rb.e_end = (int)E;
+            // it reads the previous segment's last snapshot, rebuilt on the attention's SMs
+            if (segs > 1) e = cudaStreamWaitEvent(s, P.ev_rebuilt, 0);
+            if (e == cudaSuccess) e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_snap_rebuild(rb, s); });
+            if (e == cudaSuccess) ly->kernels += 1;
+        }
         aa.n_ranges = all_ranges;
         aa.grid = P.sm_all;
         if (e == cudaSuccess) e = timed(ly, PH_ATTN, s, [&] { return kvm::launch_attn(aa, bf16, s); });
@@ -533,6 +582,13 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             e = timed(ly, PH_FOLD, s, [&] { return kvm::launch_fold(fa, bf16, s); });
             if (e != cudaSuccess) return ly->cuda_fail(e, "fold chain launch");
             ly->kernels += 1;
+            if (L.logs) {
+                rb.e_begin = 0;
+                rb.e_end = (int)E;
+                e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_snap_rebuild(rb, s); });
+                if (e != cudaSuccess) return ly->cuda_fail(e, "snapshot rebuild launch");
+                ly->kernels += 1;
+            }
         }
         if (pre_rotate) {
             ka.grid = 8 * ly->nsm;

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(NT, 1)
     // next event's owners rewrite the view, at the barrier that ends its set-up
     int snap_e = -1, snap_n = 0;
     auto snapshot = [&]() {
-        if (a.snap_k && snap_e >= 0 && snap_e < a.snap_events) {
+        if (a.snap_k && !a.log_k && snap_e >= 0 && snap_e < a.snap_events) {
             // full snapshot rows: the compact key rows behind zeros on the leading pieces
             const int64_t base = ((int64_t)bh * a.snap_events + snap_e) * M * ROWB;
             const int nchunks = snap_n * 8;
@@ -537,6 +537,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
         const int ntouched = X.wbase[MAXM / 32];
+        if (tid == 0 && a.log_k && e < a.snap_events) a.log_cnt[(int64_t)bh * a.snap_events + e] = ntouched;
         KVM_PROBE_LAP(5)
 
         // owners: eight lanes per touched slot (dims 8 sl .. 8 sl + 7 on sub-lane sl), so
@@ -680,6 +681,13 @@ __global__ void __launch_bounds__(NT, 1)
                     if (sl >= zc)
                         reinterpret_cast<uint4*>(g_vk + (int64_t)j * DK)[sl - zc] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
                     reinterpret_cast<uint4*>(g_vv + (int64_t)j * D)[sl] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                    if (a.log_k && e < a.snap_events) {
+                        // the touched row, full width (zeros on the rotary dims), into the event's log
+                        const int64_t lrow = ((int64_t)bh * a.snap_events + e) * C + k;
+                        reinterpret_cast<uint4*>(a.log_k)[lrow * 8 + sl] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+                        reinterpret_cast<uint4*>(a.log_v)[lrow * 8 + sl] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                        if (sl == 0) a.log_idx[lrow] = j;
+                    }
                 }
             }
         }
@@ -726,6 +734,74 @@ KVM_PROBE_READOUT(kvm_probe_read_big, foldbig::g_probe_big)
 
 bool fold_big_supported(const FoldArgs& a, bool bf16) {
     return bf16 && a.C >= 16 && a.C <= foldbig::MAXC && a.M <= foldbig::MAXM;
+}
+
+namespace foldbig {
+// One CTA per (row, slot range) walks the events in order: snapshot e takes, for each
+// slot of its range below n_after(e), the row event e logged for it, else the row of
+// snapshot e - 1 (a slot new at e is always logged: founding touches it).
+constexpr int RB_T = 256;        // threads
+constexpr int RB_SLOTS = 256;    // slots per CTA
+__global__ void __launch_bounds__(RB_T) snap_rebuild_kernel(const SnapRebuildArgs a) {
+    __shared__ int inv[RB_SLOTS];
+    const int tid = threadIdx.x;
+    const int splits = (a.M + RB_SLOTS - 1) / RB_SLOTS;
+    const int bh = blockIdx.x / splits;
+    const int j0 = (blockIdx.x % splits) * RB_SLOTS;
+    if (bh >= a.BH) return;
+    for (int i = tid; i < RB_SLOTS; i += RB_T) inv[i] = -1;
+    const uint4* lk = reinterpret_cast<const uint4*>(a.log_k);
+    const uint4* lv = reinterpret_cast<const uint4*>(a.log_v);
+    uint4* sk = reinterpret_cast<uint4*>(a.snap_k);
+    uint4* sv = reinterpret_cast<uint4*>(a.snap_v);
+    __syncthreads();
+    for (int e = a.e_begin; e < a.e_end; ++e) {
+        const int64_t ev = (int64_t)bh * a.snap_events + e;
+        int cnt = a.log_cnt[ev];
+        cnt = cnt < 0 ? 0 : (cnt > a.C ? a.C : cnt);
+        const int* idx = a.log_idx + ev * a.C;
+        for (int i = tid; i < cnt; i += RB_T) {
+            const int j = idx[i];
+            if (j >= j0 && j < j0 + RB_SLOTS) inv[j - j0] = i;
+        }
+        __syncthreads();
+        const int n = a.sched[e].n_after;
+        const int j1 = n < j0 + RB_SLOTS ? n : j0 + RB_SLOTS;
+        const int64_t dst = ev * a.M * 8, prev = (ev - 1) * a.M * 8, lrow = ev * a.C * 8;
+        for (int q = tid; q < (j1 - j0) * 8; q += RB_T) {
+            const int j = j0 + (q >> 3), pc = q & 7;
+            const int i = inv[j - j0];
+            uint4 wk = make_uint4(0u, 0u, 0u, 0u), wv = wk;
+            if (i >= 0) {
+                wk = lk[lrow + (int64_t)i * 8 + pc];
+                wv = lv[lrow + (int64_t)i * 8 + pc];
+            } else if (e > 0) {
+                wk = sk[prev + (int64_t)j * 8 + pc];
+                wv = sv[prev + (int64_t)j * 8 + pc];
+            }
+            sk[dst + (int64_t)j * 8 + pc] = wk;
+            sv[dst + (int64_t)j * 8 + pc] = wv;
+        }
+        __syncthreads();
+        for (int i = tid; i < cnt; i += RB_T) {
+            const int j = idx[i];
+            if (j >= j0 && j < j0 + RB_SLOTS) inv[j - j0] = -1;
+        }
+        __syncthreads();
+    }
+}
+}  // namespace foldbig
+
+cudaError_t launch_snap_rebuild(const SnapRebuildArgs& a, cudaStream_t s) {
+    using namespace foldbig;
+    if (a.e_begin >= a.e_end || a.BH == 0) return cudaSuccess;
+    const int splits = (a.M + RB_SLOTS - 1) / RB_SLOTS;
+    snap_rebuild_kernel<<<a.BH * splits, RB_T, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+bool fold_logs_rows(const FoldArgs& a, bool bf16) {
+    return !fold_tc_supported(a, bf16) && fold_big_supported(a, bf16);
 }
 
 cudaError_t launch_fold_big(const FoldArgs& a, cudaStream_t s) {

@@ -22,6 +22,8 @@ struct Layout {
     size_t ring_k, ring_v, ring_g, ring_kr, snap_k, snap_v, rope, sched, status;
     size_t k_rot;  // keys rotated at their own positions (bf16 layers with rope_dims > 0; else empty)
     size_t q_rot;  // queries rotated at their own positions (same condition)
+    size_t log_k, log_v, log_idx, log_cnt;  // the streamed chain's row log (empty otherwise)
+    bool logs;
     size_t total;
 };
 
@@ -49,6 +51,7 @@ struct Partition {
     cudaEvent_t ev_fork = nullptr;              // primary context
     cudaEvent_t ev_seg[MAX_SEGS] = {};          // fold partition: end of segment k
     cudaEvent_t ev_attn = nullptr;              // attention partition: end of its work
+    cudaEvent_t ev_rebuilt = nullptr;           // attention partition: snapshots of a segment rebuilt
 };
 // fold_rows SMs (rounded up to the split granularity) for the fold chain, the
 // rest for attention.  False (with the reason) when the device or driver

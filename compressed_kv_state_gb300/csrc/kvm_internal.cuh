@@ -99,6 +99,14 @@ struct FoldArgs {
     void* snap_k;
     void* snap_v;
     int snap_events;  // events per (b,h) row in the snapshot arrays
+    // streamed-state chain only: instead of copying every row to the snapshot, each
+    // event logs the rows it touched (full bf16 rows [BH, snap_events, C, D], their
+    // slots [BH, snap_events, C] and count [BH, snap_events]); launch_snap_rebuild
+    // turns the log into the snapshots on other SMs (nullptr: copy as before)
+    void* log_k;
+    void* log_v;
+    int* log_idx;
+    int* log_cnt;
     // optional debug record [BH, dbg_events, C]
     int* dbg_assign;
     int* dbg_kind;
@@ -173,6 +181,25 @@ struct RopeKeysArgs {
     int64_t first;
     int L;
 };
+
+// Snapshots of the read view from the streamed chain's per-event row log: snapshot e
+// = snapshot e - 1 (rows < n_after(e)) with the rows event e touched replaced by
+// their logged values.  Events [e_begin, e_end) of every row, in order; the
+// snapshot of e_begin - 1 must be complete (an earlier call).  bf16.
+struct SnapRebuildArgs {
+    const void* log_k;
+    const void* log_v;
+    const int* log_idx;
+    const int* log_cnt;
+    void* snap_k;
+    void* snap_v;
+    int snap_events, C, M, BH;
+    const Sched* sched;
+    int e_begin, e_end;
+    int grid;  // CTAs to launch (0: enough for the device)
+};
+cudaError_t launch_snap_rebuild(const SnapRebuildArgs& a, cudaStream_t s);
+bool fold_logs_rows(const FoldArgs& a, bool bf16);  // the streamed chain runs (and logs)
 
 // Backward of a prefill at the forward's fold decisions (kvm_backward.cu).  All
 // arrays are device memory; [BH, N, D] rows in the layer's dtype unless noted.

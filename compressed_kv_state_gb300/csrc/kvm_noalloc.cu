@@ -180,7 +180,31 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         fa.snap_events = (int)E;
         fa.status = reinterpret_cast<int*>(ws + L.status);
         fa.BH = BH;
+        if (L.logs) {
+            fa.log_k = ws + L.log_k;
+            fa.log_v = ws + L.log_v;
+            fa.log_idx = reinterpret_cast<int*>(ws + L.log_idx);
+            fa.log_cnt = reinterpret_cast<int*>(ws + L.log_cnt);
+        }
         e = kvm::launch_fold(fa, bf16, s);
+        if (e == cudaSuccess && L.logs) {
+            // the snapshots, from the chain's row log
+            kvm::SnapRebuildArgs rb{};
+            rb.log_k = fa.log_k;
+            rb.log_v = fa.log_v;
+            rb.log_idx = fa.log_idx;
+            rb.log_cnt = fa.log_cnt;
+            rb.snap_k = fa.snap_k;
+            rb.snap_v = fa.snap_v;
+            rb.snap_events = fa.snap_events;
+            rb.C = c.chunk;
+            rb.M = c.max_slots;
+            rb.BH = BH;
+            rb.sched = fa.sched;
+            rb.e_begin = 0;
+            rb.e_end = (int)E;
+            e = kvm::launch_snap_rebuild(rb, s);
+        }
     }
     kvm::AttnArgs aa{};
     aa.q = q;

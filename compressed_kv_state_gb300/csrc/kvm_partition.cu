@@ -131,6 +131,7 @@ bool partition_make(int device, int fold_rows, Partition* p, std::string& why) {
     p->s_fold = reinterpret_cast<cudaStream_t>(s1);
     p->s_attn = reinterpret_cast<cudaStream_t>(s2);
     if (!events_in(d, g1, p->ev_seg, Partition::MAX_SEGS) || !events_in(d, g2, &p->ev_attn, 1) ||
+        !events_in(d, g2, &p->ev_rebuilt, 1) ||
         cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess) {
         partition_free(p);
         why = "event creation failed";
@@ -150,6 +151,7 @@ void partition_free(Partition* p) {
     for (auto& e : p->ev_seg)
         if (e) cudaEventDestroy(e);
     if (p->ev_attn) cudaEventDestroy(p->ev_attn);
+    if (p->ev_rebuilt) cudaEventDestroy(p->ev_rebuilt);
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (d.ok) {
         if (p->s_fold) d.stream_destroy(reinterpret_cast<CUstream>(p->s_fold));
