@@ -11,8 +11,11 @@
 // gate-weighted member sums (Core mechanism 2) and the founders' read radius
 // rho = |v| (Core mechanism 3).
 //
-// Kernels (fp32 arithmetic, inputs in the layer's dtype; one warp per query,
-// key or state row, lanes over the 64 dims, two each):
+// Chunks a multiple of 64 take the tiled path (bwd_tile below: 64-query tiles, 64-key
+// blocks in shared memory, the five products as small fp32 multiplies); the kernels
+// listed here serve the other chunk sizes, and bwd_rotate and bwd_sweep serve both
+// (fp32 arithmetic, inputs in the layer's dtype; one warp per query, key or state row,
+// lanes over the 64 dims, two each):
 //   bwd_rotate   q and k rotated at their own positions (scratch)
 //   bwd_stats    per query: log2-sum-exp of its scores and D = dout . out
 //   bwd_dq       per query: dq (state part in plain coordinates, window part
@@ -419,6 +422,261 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
     }
 }
 
+// ---------------------------------------------------------------- tiled path
+// Chunks a multiple of 64: one CTA per (row, 64-query tile), 256 threads.  The tile's
+// queries and dout stay in shared memory (row-major and transposed); its keys come in
+// blocks of 64 (the read rows of its chunk's state, then its window), and per block the
+// five products S = Q K^T, dP = dO V^T, dQ += dS K, dK = dS^T Q, dV = P^T dO run as
+// 64 x 64 x 64 fp32 multiplies, each thread owning a 4 x 4 piece of every output.  A first
+// pass over the blocks gives each query its log2-sum-exp.  dK and dV of a block are added
+// to global accumulators (a window key is seen by W/C + 1 chunks; a read row by its one
+// chunk's two tiles).
+constexpr int TQ = 64, TKB = 64, TPAD = 68;  // tile rows, key-block rows, padded row (floats)
+constexpr int TILE_SMEM = (10 * TQ * TPAD + 2 * TQ) * (int)sizeof(float);
+
+template <typename T>
+__device__ __forceinline__ void tile_load(float* rm, float* tr, const T* src, int nrows, int tid) {
+    // rows [0, nrows) of src (64 dims each) into rm[r][x] and tr[x][r]; the rest zero
+    for (int q = tid; q < TQ * (D / 4); q += 256) {
+        const int r = q >> 4, x0 = (q & 15) * 4;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < nrows) {
+            if (sizeof(T) == 2) {
+                const uint2 w = *reinterpret_cast<const uint2*>(src + (int64_t)r * D + x0);
+                v[0] = __uint_as_float(w.x << 16);
+                v[1] = __uint_as_float(w.x & 0xffff0000u);
+                v[2] = __uint_as_float(w.y << 16);
+                v[3] = __uint_as_float(w.y & 0xffff0000u);
+            } else {
+                const float4 f = *reinterpret_cast<const float4*>(src + (int64_t)r * D + x0);
+                v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+            }
+        }
+        if (rm) *reinterpret_cast<float4*>(rm + r * TPAD + x0) = make_float4(v[0], v[1], v[2], v[3]);
+        if (tr)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) tr[(x0 + u) * TPAD + r] = v[u];
+    }
+}
+
+// acc[4][4] += A^T-slab product: sum over k of a[k][i0..i0+3] * b[k][j0..j0+3]
+__device__ __forceinline__ void mm4x4(float (&acc)[4][4], const float* a, const float* b, int i0, int j0, int K) {
+#pragma unroll 8
+    for (int k = 0; k < K; ++k) {
+        const float4 x = *reinterpret_cast<const float4*>(a + k * TPAD + i0);
+        const float4 y = *reinterpret_cast<const float4*>(b + k * TPAD + j0);
+        const float xa[4] = {x.x, x.y, x.z, x.w}, ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], ya[j], acc[i][j]);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256, 1) bwd_tile(BackwardArgs a) {
+    extern __shared__ float tsm[];
+    float* Qs = tsm;                 // [64][TPAD] rotated queries, row-major
+    float* Qt = Qs + TQ * TPAD;      // transposed
+    float* Gs = Qt + TQ * TPAD;      // dout, row-major
+    float* Gt = Gs + TQ * TPAD;      // transposed
+    float* Ks = Gt + TQ * TPAD;      // key block, row-major
+    float* Kt = Ks + TQ * TPAD;      // transposed
+    float* Vt = Kt + TQ * TPAD;      // value block, transposed
+    float* Ps = Vt + TQ * TPAD;      // P, row-major [query][key]
+    float* Ds = Ps + TQ * TPAD;      // dS, row-major
+    float* Dt = Ds + TQ * TPAD;      // dS transposed [key][query]
+    float* Ls = Dt + TQ * TPAD;      // log2-sum-exp per query
+    float* Dd = Ls + TQ;             // dout . out per query
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int i0 = 4 * ty, j0 = 4 * tx;
+    const int tiles = (int)((a.N + TQ - 1) / TQ);
+    const int bh = blockIdx.x / tiles;
+    const int64_t q0 = (int64_t)(blockIdx.x % tiles) * TQ;
+    const int nq = (int)(a.N - q0 < TQ ? a.N - q0 : TQ);
+    const int Wc = a.W / a.C;
+    const int64_t c = q0 / a.C, e = c - Wc - 1, ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
+    const int n = e >= 0 ? a.sched[e].n_after : 0;
+    const int64_t row = (int64_t)bh * a.N;
+    const int64_t plane = ((int64_t)bh * a.snap_events + (e >= 0 ? e : 0)) * a.M * D;
+    const T* kh = reinterpret_cast<const T*>(a.snap_k) + plane;
+    const T* vh = reinterpret_cast<const T*>(a.snap_v) + plane;
+    const T* kr = reinterpret_cast<const T*>(a.kr) + row * D;
+    const T* vv = reinterpret_cast<const T*>(a.v) + row * D;
+    const int nbs = (n + TKB - 1) / TKB;
+    const int nbw = (int)((q0 + nq - ws + TKB - 1) / TKB);
+    const float sl = a.scale_log2;
+
+    tile_load<T>(Qs, Qt, reinterpret_cast<const T*>(a.qr) + (row + q0) * D, nq, tid);
+    tile_load<T>(Gs, Gt, reinterpret_cast<const T*>(a.dout) + (row + q0) * D, nq, tid);
+    // dout . out of every query (four threads a row)
+    {
+        const int r = tid >> 2, part = tid & 3;
+        float d = 0.0f;
+        if (r < nq) {
+            const T* o = reinterpret_cast<const T*>(a.out) + (row + q0 + r) * D + 16 * part;
+            const T* g = reinterpret_cast<const T*>(a.dout) + (row + q0 + r) * D + 16 * part;
+            for (int x = 0; x < 16; ++x) d = fmaf(to_f<T>(o[x]), to_f<T>(g[x]), d);
+        }
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        if (part == 0) Dd[r] = d;
+    }
+    // key block b: rows, values and the count of valid keys; window blocks mask causally
+    auto load_block = [&](int b, bool want_v) -> int {
+        int kv;
+        if (b < nbs) {
+            kv = n - TKB * b < TKB ? n - TKB * b : TKB;
+            tile_load<T>(Ks, Kt, kh + (int64_t)TKB * b * D, kv, tid);
+            if (want_v) tile_load<T>(nullptr, Vt, vh + (int64_t)TKB * b * D, kv, tid);
+        } else {
+            const int64_t t0 = ws + (int64_t)TKB * (b - nbs);
+            kv = (int)(q0 + nq - t0 < TKB ? q0 + nq - t0 : TKB);
+            tile_load<T>(Ks, Kt, kr + t0 * D, kv, tid);
+            if (want_v) tile_load<T>(nullptr, Vt, vv + t0 * D, kv, tid);
+        }
+        return kv;
+    };
+    auto scores = [&](int b, int kv, float (&sc)[4][4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sc[i][j] = 0.0f;
+        mm4x4(sc, Qt, Kt, i0, j0, D);
+        const bool win = b >= nbs;
+        const int64_t t0 = win ? ws + (int64_t)TKB * (b - nbs) : 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool ok = i0 + i < nq && j0 + j < kv && (!win || t0 + j0 + j <= q0 + i0 + i);
+                sc[i][j] = ok ? sc[i][j] * sl : -INFINITY;
+            }
+    };
+    // pass 1: log2-sum-exp of each query over all its keys
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}, l[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int b = 0; b < nbs + nbw; ++b) {
+        __syncthreads();
+        const int kv = load_block(b, false);
+        __syncthreads();
+        float sc[4][4];
+        scores(b, kv, sc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float mb = fmaxf(fmaxf(sc[i][0], sc[i][1]), fmaxf(sc[i][2], sc[i][3]));
+            const float mn = fmaxf(m[i], mb);
+            if (mn == -INFINITY) continue;
+            float add = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) add += exp2f(sc[i][j] - mn);
+            l[i] = l[i] * exp2f(m[i] - mn) + add;
+            m[i] = mn;
+        }
+    }
+    // combine the 16 threads of a row (a half-warp)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float M = m[i];
+        for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = m[i] == -INFINITY ? 0.0f : l[i] * exp2f(m[i] - M);
+        for (int o = 8; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (tx == 0) Ls[i0 + i] = M + log2f(L);
+    }
+    // pass 2: the gradients
+    float dq[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dq[i][j] = 0.0f;
+    for (int b = 0; b < nbs + nbw; ++b) {
+        __syncthreads();
+        const int kv = load_block(b, true);
+        __syncthreads();
+        float sc[4][4], dp[4][4];
+        scores(b, kv, sc);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dp[i][j] = 0.0f;
+        mm4x4(dp, Gt, Vt, i0, j0, D);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float L = Ls[i0 + i], Dv = Dd[i0 + i];
+            float pr[4], ds[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                pr[j] = sc[i][j] == -INFINITY ? 0.0f : exp2f(sc[i][j] - L);
+                ds[j] = pr[j] * (dp[i][j] - Dv);
+                Dt[(j0 + j) * TPAD + i0 + i] = ds[j];
+            }
+            *reinterpret_cast<float4*>(Ps + (i0 + i) * TPAD + j0) = make_float4(pr[0], pr[1], pr[2], pr[3]);
+            *reinterpret_cast<float4*>(Ds + (i0 + i) * TPAD + j0) = make_float4(ds[0], ds[1], ds[2], ds[3]);
+        }
+        __syncthreads();
+        // dQ += dS K (rows i0.., dims j0..)
+        mm4x4(dq, Dt, Ks, i0, j0, TKB);
+        // dK = dS^T Q and dV = P^T dO for keys 4ty.., dims 4tx.. (slabs over the queries)
+        float dk[4][4], dv[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dk[i][j] = dv[i][j] = 0.0f;
+        mm4x4(dk, Ds, Qs, i0, j0, TQ);
+        mm4x4(dv, Ps, Gs, i0, j0, TQ);
+        const bool win = b >= nbs;
+        const int64_t kbase = win ? ws + (int64_t)TKB * (b - nbs) : (int64_t)TKB * b;
+        float* gk = win ? a.dk + (row + kbase) * D
+                        : a.dks + (((int64_t)bh * a.E + e) * a.M + kbase) * D;
+        float* gv = win ? a.dv + (row + kbase) * D
+                        : a.dvs + (((int64_t)bh * a.E + e) * a.M + kbase) * D;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i0 + i >= kv) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                atomicAdd(gk + (int64_t)(i0 + i) * D + j0 + j, dk[i][j] * a.inv_sqrt_d);
+                atomicAdd(gv + (int64_t)(i0 + i) * D + j0 + j, dv[i][j]);
+            }
+        }
+    }
+    // dq: scaled, then rotated back (pairs across threads: through shared memory)
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(Ps + (i0 + i) * TPAD + j0) =
+            make_float4(dq[i][0] * a.inv_sqrt_d, dq[i][1] * a.inv_sqrt_d, dq[i][2] * a.inv_sqrt_d, dq[i][3] * a.inv_sqrt_d);
+    __syncthreads();
+    const int half = a.r / 2;
+    for (int q = tid; q < nq * D; q += 256) {
+        const int r = q >> 6, x = q & 63;
+        const int64_t pp = q0 + r;
+        float y = Ps[r * TPAD + x];
+        if (x < 2 * half) {
+            const int i2 = x < half ? x : x - half;
+            const float2 cs = a.rope[pp * half + i2];
+            y = x < half ? y * cs.x + Ps[r * TPAD + x + half] * cs.y : y * cs.x - Ps[r * TPAD + x - half] * cs.y;
+        }
+        a.dq[(row + pp) * D + x] = y;
+    }
+}
+
+// rotate the accumulated window-key gradients back (in place) and zero the gate gradient
+__global__ void bwd_unrotate_dk(BackwardArgs a) {
+    const int64_t rows = (int64_t)a.BH * a.N;
+    const int half = a.r / 2;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < rows * half;
+         w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t rr = w / half;
+        const int i = (int)(w - rr * half);
+        const int64_t p = rr % a.N;
+        float* k = a.dk + rr * D;
+        const float2 cs = a.rope[p * half + i];
+        const float y0 = k[i], y1 = k[i + half];
+        k[i] = y0 * cs.x + y1 * cs.y;
+        k[i + half] = y1 * cs.x - y0 * cs.y;
+    }
+}
+
 template <typename T>
 cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
     const int64_t rows = (int64_t)a.BH * a.N;
@@ -426,14 +684,33 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
     const int wpb = BW_WARPS;
     const unsigned gq = (unsigned)((rows + wpb - 1) / wpb);
     bwd_rotate<T><<<2048, 256, 0, s>>>(a);
-    bwd_stats<T><<<gq, BW_THREADS, 0, s>>>(a);
-    bwd_dq<T><<<gq, BW_THREADS, 0, s>>>(a);
-    bwd_dkv_win<T><<<gq, BW_THREADS, 0, s>>>(a);
-    if (a.E > 0) {
-        const int64_t ws = (int64_t)a.BH * a.E * a.M;
-        bwd_dstate<T><<<(unsigned)((ws + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
-        bwd_sweep<T><<<a.BH, BW_THREADS, 0, s>>>(a);
+    if (a.C % TQ == 0) {
+        // tiled path: gradients accumulate into zeroed outputs and read-row arrays
+        cudaError_t e = cudaMemsetAsync(a.dk, 0, (size_t)rows * D * sizeof(float), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a.dv, 0, (size_t)rows * D * sizeof(float), s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(a.dg, 0, (size_t)rows * sizeof(float), s);
+        const size_t rs = (size_t)a.BH * a.E * a.M * D * sizeof(float);
+        if (e == cudaSuccess && a.E > 0) e = cudaMemsetAsync(a.dks, 0, rs, s);
+        if (e == cudaSuccess && a.E > 0) e = cudaMemsetAsync(a.dvs, 0, rs, s);
+        if (e != cudaSuccess) return e;
+        static bool attr = false;
+        if (!attr) {
+            cudaFuncSetAttribute(bwd_tile<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, TILE_SMEM);
+            attr = true;
+        }
+        const int tiles = (int)((a.N + TQ - 1) / TQ);
+        bwd_tile<T><<<(unsigned)(a.BH * tiles), 256, TILE_SMEM, s>>>(a);
+        if (a.r > 0) bwd_unrotate_dk<<<2048, 256, 0, s>>>(a);
+    } else {
+        bwd_stats<T><<<gq, BW_THREADS, 0, s>>>(a);
+        bwd_dq<T><<<gq, BW_THREADS, 0, s>>>(a);
+        bwd_dkv_win<T><<<gq, BW_THREADS, 0, s>>>(a);
+        if (a.E > 0) {
+            const int64_t ws = (int64_t)a.BH * a.E * a.M;
+            bwd_dstate<T><<<(unsigned)((ws + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
+        }
     }
+    if (a.E > 0) bwd_sweep<T><<<a.BH, BW_THREADS, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -3,7 +3,8 @@
 Both sides take the fold decisions the GPU forward recorded (the backward's
 reading: decisions are constants), so near ties cannot make them differ.  The
 oracle (oracle/backward.py, pinned on the CPU) differentiates the restated
-prefill in fp64 on the exact bf16/fp32 input values.  Tolerance: the GPU reads
+prefill in fp64 on the exact bf16/fp32 input values.  Chunks that are multiples of
+64 run the tiled kernels, others the row-per-warp kernels; both are covered.  Tolerance: the GPU reads
 its state through bf16 read rows and rotates in bf16 for bf16 layers, so every
 gradient is compared against its own scale: max |gpu - oracle| <= TOL x
 max |oracle|, TOL 3e-2 (bf16) / 1e-4 (fp32); and the relative Frobenius error
@@ -32,6 +33,11 @@ CASES = [
                 n_sinks=8, max_slots=40, keys="repeat5", flags=1),
     wl.Workload("bwd_norope_fp32_B1H1N600_C64W128", B=1, H=1, N=600, chunk=64, window=128,
                 n_sinks=4, max_slots=24, keys="plain", dtype="fp32", rope_dims=0),
+    # chunks that are not a multiple of 64 take the row-per-warp kernels
+    wl.Workload("bwd_C32_B1H2N500_W64", B=1, H=2, N=500, chunk=32, window=64, n_sinks=4,
+                max_slots=32, keys="repeat5"),
+    wl.Workload("bwd_C32_fp32_B1H1N400_W96", B=1, H=1, N=400, chunk=32, window=96, n_sinks=4,
+                max_slots=24, keys="repeat5", dtype="fp32"),
 ]
 
 
