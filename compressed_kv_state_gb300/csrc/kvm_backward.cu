@@ -237,188 +237,143 @@ __global__ void bwd_dstate(BackwardArgs a) {
     reinterpret_cast<float2*>(a.dvs + o)[lane] = av;
 }
 
+// Per slot, one warp (lanes over the dims, two each): every slot's history is its own,
+// so the rows' slots run in parallel.  Pass 1 replays the slot through the events with
+// the recorded decisions (its founder first, then its merged tokens in position order:
+// the forward's fp32 sums) and turns each event's read-row gradients of the slot into
+// sum and radius gradients (LayerNorm and normalisation backward), in place.  Pass 2
+// runs the events backwards, summing those gradients, and each of the slot's tokens
+// reads the sum at its own event (the gradients of every state that holds it).
 template <typename T>
 __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
-    __shared__ int slot[MAX_BW_C], kd[MAX_BW_C], ord[MAX_BW_C], run_beg[MAX_BW_C + 1];
-    __shared__ int nruns_s;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int bh = blockIdx.x;
-    const int C = a.C, M = a.M;
+    const int lane = threadIdx.x & 31;
+    const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (w >= (int64_t)a.BH * a.M) return;
+    const int bh = (int)(w / a.M);
+    const int j = (int)(w % a.M);
+    const int C = a.C, M = a.M, r = a.r;
     const int64_t row = (int64_t)bh * a.N;
     const T* kk = reinterpret_cast<const T*>(a.k) + row * D;
     const T* vv = reinterpret_cast<const T*>(a.v) + row * D;
     const float* gg = a.g + row;
-    float* sk = a.sk + (int64_t)bh * M * D;
-    float* sv = a.sv + (int64_t)bh * M * D;
-    int* cnt = a.cnt + (int64_t)bh * M;
-    float* rho = a.rho + (int64_t)bh * M;
-    float* gk = a.gk + (int64_t)bh * M * D;
-    float* gv = a.gv + (int64_t)bh * M * D;
-    float* grho = a.grho + (int64_t)bh * M;
-    const int r = a.r;
-
-    // an entry of the record that names no slot of this state, or no kind, is
-    // reported and its token skipped (kind -1)
-    auto load_event = [&](int e) {
-        const int n = a.sched[e].n_after;
-        for (int i = tid; i < C; i += BW_THREADS) {
-            const int64_t o = ((int64_t)bh * a.rec_events + e) * C + i;
-            const int j = a.assign[o], kn = a.kind[o];
-            const bool ok = j >= 0 && j < n && kn >= 0 && kn <= 2;
-            if (!ok && a.status) atomicOr(a.status, STATUS_DEVICE);
-            slot[i] = ok ? j : 0;
-            kd[i] = ok ? kn : -1;
-        }
+    if (a.E == 0 || j >= a.sched[a.E - 1].n_after) return;  // slot never founded
+    // the record of event e: kind of token i if it went to slot j (founder 1/2, merged 0),
+    // else -1; the warp of slot 0 reports entries that name no slot of the event
+    auto kind_of = [&](int e, int i, int n) -> int {
+        const int64_t o = ((int64_t)bh * a.rec_events + e) * C + i;
+        const int sj = a.assign[o], kn = a.kind[o];
+        const bool ok = sj >= 0 && sj < n && kn >= 0 && kn <= 2;
+        if (!ok && j == 0 && a.status) atomicOr(a.status, STATUS_DEVICE);
+        return ok && sj == j ? kn : -1;
     };
-    for (int i = tid; i < M * D; i += BW_THREADS) {
-        sk[i] = 0.0f;
-        sv[i] = 0.0f;
-    }
-    for (int i = tid; i < M; i += BW_THREADS) {
-        cnt[i] = 1;  // a slot merged into before any founding (an invalid record) divides by 1
-        rho[i] = 0.0f;
-    }
-    __syncthreads();
-
-    // pass 1: replay the fold; each event's read-row gradients become sum / radius gradients
+    float2 sk = make_float2(0.f, 0.f), sv = sk;
+    int cnt = 0;
+    float rho = 0.0f;
+    // pass 1
     for (int e = 0; e < a.E; ++e) {
-        load_event(e);
-        __syncthreads();
-        // founders: the new slot's sums, count 1, radius |v|
-        for (int i = warp; i < C; i += BW_WARPS) {
-            if (kd[i] != 1 && kd[i] != 2) continue;
-            const int j = slot[i];
-            const int64_t t = (int64_t)e * C + i;
-            const float gt = gg[t];
-            const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
-            reinterpret_cast<float2*>(sk + (int64_t)j * D)[lane] = make_float2(gt * kx.x, gt * kx.y);
-            reinterpret_cast<float2*>(sv + (int64_t)j * D)[lane] = make_float2(gt * vx.x, gt * vx.y);
-            const float nv = sqrtf(warp_sum(dot2(vx, vx)));
-            if (lane == 0) {
-                cnt[j] = 1;
-                rho[j] = nv;
+        const int n = a.sched[e].n_after;
+        if (j >= n) continue;  // not founded yet (founding appends at the end)
+        // the founder first (the forward sets a new slot from it), then the merged
+        // tokens in position order, whatever their positions relative to the founder
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int base = 0; base < C; base += 32) {
+                const int i = base + lane;
+                const int kn = i < C ? kind_of(e, i, n) : -1;
+                unsigned sel = __ballot_sync(0xffffffffu, pass == 0 ? (kn == 1 || kn == 2) : kn == 0);
+                while (sel) {
+                    const int ii = base + __ffs(sel) - 1;
+                    sel &= sel - 1;
+                    const int64_t t = (int64_t)e * C + ii;
+                    const float gt = gg[t];
+                    const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
+                    if (pass == 0) {
+                        sk = make_float2(gt * kx.x, gt * kx.y);
+                        sv = make_float2(gt * vx.x, gt * vx.y);
+                        cnt = 1;
+                        rho = sqrtf(warp_sum(dot2(vx, vx)));
+                    } else {
+                        sk = make_float2(fmaf(gt, kx.x, sk.x), fmaf(gt, kx.y, sk.y));
+                        sv = make_float2(fmaf(gt, vx.x, sv.x), fmaf(gt, vx.y, sv.y));
+                        ++cnt;
+                    }
+                }
             }
         }
-        // merged tokens sorted by (slot, position): runs of one slot, in position order
-        if (tid < C) {
-            int rank = 0;
-            if (kd[tid] == 0) {
-                const int si = slot[tid];
-                for (int u = 0; u < C; ++u)
-                    rank += kd[u] == 0 && (slot[u] < si || (slot[u] == si && u < tid));
-                ord[rank] = tid;
-            }
+        // read-row gradients -> sum and radius gradients of the state after event e
+        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D;
+        const float cn = (float)(cnt > 0 ? cnt : 1);
+        const float2 x = make_float2(sk.x / cn, sk.y / cn);
+        const float mu = warp_sum(x.x + x.y) * (1.0f / D);
+        const float2 xc = make_float2(x.x - mu, x.y - mu);
+        const float var = warp_sum(dot2(xc, xc)) * (1.0f / D);
+        const float isd = 1.0f / sqrtf(var + a.ln_eps);
+        const float2 xh = make_float2(xc.x * isd, xc.y * isd);
+        float2 gkh = reinterpret_cast<const float2*>(a.dks + o)[lane];
+        if (2 * lane < r) gkh.x = 0.0f;  // the rotary dims of the read key are constant zeros
+        if (2 * lane + 1 < r) gkh.y = 0.0f;
+        const float mg = warp_sum(gkh.x + gkh.y) * (1.0f / D);
+        const float mgx = warp_sum(dot2(gkh, xh)) * (1.0f / D);
+        const float2 dsk = make_float2((gkh.x - mg - xh.x * mgx) * isd / cn, (gkh.y - mg - xh.y * mgx) * isd / cn);
+        const float2 gvh = reinterpret_cast<const float2*>(a.dvs + o)[lane];
+        float2 dsv;
+        float dr = 0.0f;
+        if (a.no_vnorm) {
+            dsv = make_float2(gvh.x / cn, gvh.y / cn);
+        } else {
+            const float nv = sqrtf(warp_sum(dot2(sv, sv)));
+            const float inv = nv > 0.0f ? 1.0f / nv : 0.0f;
+            const float2 u = make_float2(sv.x * inv, sv.y * inv);
+            dr = warp_sum(dot2(u, gvh));
+            const float f = rho * inv;
+            dsv = make_float2(f * (gvh.x - u.x * dr), f * (gvh.y - u.y * dr));
         }
-        const int nm = __syncthreads_count(tid < C && kd[tid] == 0);
-        if (tid == 0) {
-            int nr = 0;
-            for (int q = 0; q < nm; ++q)
-                if (q == 0 || slot[ord[q]] != slot[ord[q - 1]]) run_beg[nr++] = q;
-            run_beg[nr] = nm;
-            nruns_s = nr;
-        }
-        __syncthreads();
-        for (int ru = warp; ru < nruns_s; ru += BW_WARPS) {
-            const int j = slot[ord[run_beg[ru]]];
-            float2 xk = reinterpret_cast<const float2*>(sk + (int64_t)j * D)[lane];
-            float2 xv = reinterpret_cast<const float2*>(sv + (int64_t)j * D)[lane];
-            for (int q = run_beg[ru]; q < run_beg[ru + 1]; ++q) {
-                const int64_t t = (int64_t)e * C + ord[q];
+        reinterpret_cast<float2*>(a.dks + o)[lane] = dsk;
+        reinterpret_cast<float2*>(a.dvs + o)[lane] = dsv;
+        if (lane == 0) a.drho[((int64_t)bh * a.E + e) * M + j] = dr;
+    }
+    // pass 2
+    float2 Gk = make_float2(0.f, 0.f), Gv = Gk;
+    float Gr = 0.0f;
+    for (int e = a.E - 1; e >= 0; --e) {
+        const int n = a.sched[e].n_after;
+        if (j >= n) continue;
+        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D;
+        const float2 dk = reinterpret_cast<const float2*>(a.dks + o)[lane];
+        const float2 dv = reinterpret_cast<const float2*>(a.dvs + o)[lane];
+        Gk = make_float2(Gk.x + dk.x, Gk.y + dk.y);
+        Gv = make_float2(Gv.x + dv.x, Gv.y + dv.y);
+        Gr += a.drho[((int64_t)bh * a.E + e) * M + j];
+        for (int base = 0; base < C; base += 32) {
+            const int i = base + lane;
+            const int64_t oo = ((int64_t)bh * a.rec_events + e) * C + i;
+            const int kn = i < C && a.assign[oo] == j ? a.kind[oo] : -1;
+            unsigned mine = __ballot_sync(0xffffffffu, kn >= 0 && kn <= 2);
+            while (mine) {
+                const int ii = base + __ffs(mine) - 1;
+                mine &= mine - 1;
+                const int kd = __shfl_sync(0xffffffffu, kn, ii - base);
+                const int64_t t = (int64_t)e * C + ii;
                 const float gt = gg[t];
                 const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
-                xk = make_float2(fmaf(gt, kx.x, xk.x), fmaf(gt, kx.y, xk.y));
-                xv = make_float2(fmaf(gt, vx.x, xv.x), fmaf(gt, vx.y, xv.y));
+                float2* dkp = reinterpret_cast<float2*>(a.dk + (row + t) * D) + lane;
+                float2* dvp = reinterpret_cast<float2*>(a.dv + (row + t) * D) + lane;
+                float2 dkt = *dkp, dvt = *dvp;
+                dkt.x = fmaf(gt, Gk.x, dkt.x);
+                dkt.y = fmaf(gt, Gk.y, dkt.y);
+                dvt.x = fmaf(gt, Gv.x, dvt.x);
+                dvt.y = fmaf(gt, Gv.y, dvt.y);
+                if (kd == 1 || kd == 2) {  // founder: rho = |v|
+                    const float nv = sqrtf(warp_sum(dot2(vx, vx)));
+                    const float f = nv > 0.0f ? Gr / nv : 0.0f;
+                    dvt.x = fmaf(f, vx.x, dvt.x);
+                    dvt.y = fmaf(f, vx.y, dvt.y);
+                }
+                *dkp = dkt;
+                *dvp = dvt;
+                const float dgt = warp_sum(dot2(kx, Gk) + dot2(vx, Gv));
+                if (lane == 0) a.dg[row + t] += dgt;
             }
-            reinterpret_cast<float2*>(sk + (int64_t)j * D)[lane] = xk;
-            reinterpret_cast<float2*>(sv + (int64_t)j * D)[lane] = xv;
-            if (lane == 0) cnt[j] += run_beg[ru + 1] - run_beg[ru];
         }
-        __syncthreads();
-        // read-row gradients -> sum and radius gradients of the state after event e
-        const int n = a.sched[e].n_after;
-        for (int j = warp; j < n; j += BW_WARPS) {
-            const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D;
-            const float cn = (float)cnt[j];
-            const float2 s = reinterpret_cast<const float2*>(sk + (int64_t)j * D)[lane];
-            const float2 x = make_float2(s.x / cn, s.y / cn);
-            const float mu = warp_sum(x.x + x.y) * (1.0f / D);
-            const float2 xc = make_float2(x.x - mu, x.y - mu);
-            const float var = warp_sum(dot2(xc, xc)) * (1.0f / D);
-            const float isd = 1.0f / sqrtf(var + a.ln_eps);
-            const float2 xh = make_float2(xc.x * isd, xc.y * isd);
-            float2 gkh = reinterpret_cast<const float2*>(a.dks + o)[lane];
-            if (2 * lane < r) gkh.x = 0.0f;  // the rotary dims of the read key are constant zeros
-            if (2 * lane + 1 < r) gkh.y = 0.0f;
-            const float mg = warp_sum(gkh.x + gkh.y) * (1.0f / D);
-            const float mgx = warp_sum(dot2(gkh, xh)) * (1.0f / D);
-            const float2 dsk = make_float2((gkh.x - mg - xh.x * mgx) * isd / cn, (gkh.y - mg - xh.y * mgx) * isd / cn);
-            const float2 gvh = reinterpret_cast<const float2*>(a.dvs + o)[lane];
-            const float2 svv = reinterpret_cast<const float2*>(sv + (int64_t)j * D)[lane];
-            float2 dsv;
-            float dr = 0.0f;
-            if (a.no_vnorm) {
-                dsv = make_float2(gvh.x / cn, gvh.y / cn);
-            } else {
-                const float nv = sqrtf(warp_sum(dot2(svv, svv)));
-                const float inv = nv > 0.0f ? 1.0f / nv : 0.0f;
-                const float2 u = make_float2(svv.x * inv, svv.y * inv);
-                dr = warp_sum(dot2(u, gvh));
-                const float f = rho[j] * inv;
-                dsv = make_float2(f * (gvh.x - u.x * dr), f * (gvh.y - u.y * dr));
-            }
-            reinterpret_cast<float2*>(a.dks + o)[lane] = dsk;
-            reinterpret_cast<float2*>(a.dvs + o)[lane] = dsv;
-            if (lane == 0) a.drho[((int64_t)bh * a.E + e) * M + j] = dr;
-        }
-        __syncthreads();
-    }
-
-    // pass 2: from the last event back, G = sum of the gradients of every state that
-    // holds a token's contribution; each token reads G at its own event
-    for (int i = tid; i < M * D; i += BW_THREADS) {
-        gk[i] = 0.0f;
-        gv[i] = 0.0f;
-    }
-    for (int i = tid; i < M; i += BW_THREADS) grho[i] = 0.0f;
-    __syncthreads();
-    for (int e = a.E - 1; e >= 0; --e) {
-        load_event(e);
-        const int n = a.sched[e].n_after;
-        const int64_t base = ((int64_t)bh * a.E + e) * M;
-        for (int i = tid; i < n * D; i += BW_THREADS) {
-            gk[i] += a.dks[base * D + i];
-            gv[i] += a.dvs[base * D + i];
-        }
-        for (int i = tid; i < n; i += BW_THREADS) grho[i] += a.drho[base + i];
-        __syncthreads();
-        for (int i = warp; i < C; i += BW_WARPS) {
-            const int kdi = kd[i];
-            if (kdi < 0) continue;
-            const int j = slot[i];
-            const int64_t t = (int64_t)e * C + i;
-            const float gt = gg[t];
-            const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
-            const float2 Gk = reinterpret_cast<const float2*>(gk + (int64_t)j * D)[lane];
-            const float2 Gv = reinterpret_cast<const float2*>(gv + (int64_t)j * D)[lane];
-            float2* dkp = reinterpret_cast<float2*>(a.dk + (row + t) * D) + lane;
-            float2* dvp = reinterpret_cast<float2*>(a.dv + (row + t) * D) + lane;
-            float2 dk = *dkp, dv = *dvp;
-            dk.x = fmaf(gt, Gk.x, dk.x);
-            dk.y = fmaf(gt, Gk.y, dk.y);
-            dv.x = fmaf(gt, Gv.x, dv.x);
-            dv.y = fmaf(gt, Gv.y, dv.y);
-            if (kdi == 1 || kdi == 2) {  // founder: rho = |v|
-                const float nv = sqrtf(warp_sum(dot2(vx, vx)));
-                const float f = nv > 0.0f ? grho[j] / nv : 0.0f;
-                dv.x = fmaf(f, vx.x, dv.x);
-                dv.y = fmaf(f, vx.y, dv.y);
-            }
-            *dkp = dk;
-            *dvp = dv;
-            const float dgt = warp_sum(dot2(kx, Gk) + dot2(vx, Gv));
-            if (lane == 0) a.dg[row + t] += dgt;
-        }
-        __syncthreads();
     }
 }
 
@@ -710,7 +665,10 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
             bwd_dstate<T><<<(unsigned)((ws + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
         }
     }
-    if (a.E > 0) bwd_sweep<T><<<a.BH, BW_THREADS, 0, s>>>(a);
+    if (a.E > 0) {
+        const int64_t slots = (int64_t)a.BH * a.M;
+        bwd_sweep<T><<<(unsigned)((slots + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
+    }
     return cudaGetLastError();
 }
 
