@@ -624,7 +624,8 @@ def run_backward(dev, stream, steps):
             "finite": bool(torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
                            and torch.isfinite(dg).all()),
             "note": "fold decisions from the forward's record are constants (no gradient through the "
-                    "winner-take-all assignment); SIMT kernels, fp32 arithmetic"}
+                    "winner-take-all assignment); fp32 arithmetic: 64x64 query/key tiles in shared "
+                    "memory for the five products, one warp per slot for the state sweep"}
 
 
 def fp32_simt_peak_tflops():

@@ -220,8 +220,28 @@ __device__ __forceinline__ void rope_chunk(const uint4* src, int64_t p, int c, i
     }
 }
 
+// The loads a rotated 16-byte piece of a key and of a query needs (each piece, its
+// rotate-half partner, and their shared (cos, sin) entries) are issued before any
+// arithmetic (the vector path: r/2 a multiple of 8).
+__device__ __forceinline__ uint4 rope_apply(uint4 w, const uint4& o, const float4 (&t)[4], bool low) {
+    const float ce[8] = {t[0].x, t[0].z, t[1].x, t[1].z, t[2].x, t[2].z, t[3].x, t[3].z};
+    const float se[8] = {t[0].y, t[0].w, t[1].y, t[1].w, t[2].y, t[2].w, t[3].y, t[3].w};
+    __nv_bfloat162* m2 = reinterpret_cast<__nv_bfloat162*>(&w);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 mv = __bfloat1622float2(m2[u]), ov = __bfloat1622float2(o2[u]);
+        const float c0 = ce[2 * u], c1 = ce[2 * u + 1], s0 = se[2 * u], s1 = se[2 * u + 1];
+        m2[u] = low ? __floats2bfloat162_rn(mv.x * c0 - ov.x * s0, mv.y * c1 - ov.y * s1)
+                    : __floats2bfloat162_rn(mv.x * c0 + ov.x * s0, mv.y * c1 + ov.y * s1);
+    }
+    return w;
+}
+
 __global__ void rope_keys_kernel(RopeKeysArgs a) {
     const int64_t per_row = a.N * 8;
+    const int half = a.r / 2, hc = half >> 3;
+    const bool vec = (half & 7) == 0;
     for (int bh = blockIdx.y; bh < a.BH; bh += gridDim.y) {
         const uint4* src = reinterpret_cast<const uint4*>(a.k) + (int64_t)bh * per_row;
         uint4* dst = reinterpret_cast<uint4*>(a.k_rot) + (int64_t)bh * per_row;
@@ -231,7 +251,19 @@ __global__ void rope_keys_kernel(RopeKeysArgs a) {
              i += (int64_t)gridDim.x * blockDim.x) {
             const int64_t p = i >> 3;
             const int c = (int)(i & 7);
-            uint4 w = src[i];
+            const bool rot = 8 * c < a.r, low = c < hc;
+            const int64_t partner = p * 8 + (low ? c + hc : c - hc);
+            // every load of this piece first
+            uint4 w = src[i], wq = make_uint4(0u, 0u, 0u, 0u), o = w, oq = w;
+            float4 t[4];
+            if (qsrc) wq = qsrc[i];
+            if (vec && rot) {
+                o = src[partner];
+                if (qsrc) oq = qsrc[partner];
+                const float4* tab = reinterpret_cast<const float4*>(a.rope + p * half + (low ? c : c - hc) * 8);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) t[u] = tab[u];
+            }
             const bool ring = a.ring_k && p >= a.first;
             int64_t rrow = 0;
             if (ring) {
@@ -242,14 +274,18 @@ __global__ void rope_keys_kernel(RopeKeysArgs a) {
                     reinterpret_cast<const uint4*>(a.v)[(int64_t)bh * per_row + i];
                 if (c == 0) a.ring_g[rrow] = a.g[(int64_t)bh * a.N + p];
             }
-            rope_chunk(src, p, c, a.r, a.rope, w);
+            if (vec) {
+                if (rot) {
+                    w = rope_apply(w, o, t, low);
+                    if (qsrc) wq = rope_apply(wq, oq, t, low);
+                }
+            } else {
+                rope_chunk(src, p, c, a.r, a.rope, w);
+                if (qsrc) rope_chunk(qsrc, p, c, a.r, a.rope, wq);
+            }
             dst[i] = w;
             if (ring) reinterpret_cast<uint4*>(a.ring_kr)[rrow * 8 + c] = w;
-            if (qsrc) {
-                uint4 wq = qsrc[i];
-                rope_chunk(qsrc, p, c, a.r, a.rope, wq);
-                qdst[i] = wq;
-            }
+            if (qsrc) qdst[i] = wq;
         }
     }
 }
