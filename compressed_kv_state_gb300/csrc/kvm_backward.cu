@@ -615,6 +615,295 @@ __global__ void __launch_bounds__(256, 1) bwd_tile(BackwardArgs a) {
     }
 }
 
+// ------------------------------------------------------- tensor-core tiled path
+// bf16 layers, chunks a multiple of 64: the same tiles as bwd_tile, the five products on
+// the tensor cores (mma.sync m16n8k16, bf16 operands, fp32 accumulators; P and dS are
+// rounded to bf16 for the three products that take them, as attention backwards do).
+// Four warps; warp w owns query rows 16w .. 16w + 15 for S, dP and dQ, and keys
+// 16w .. 16w + 15 of the block for dK and dV.  Operands come from padded shared-memory
+// tiles by ldmatrix (transposed where a product needs the other major order).
+constexpr int MQ = 64, MPAD = 72;  // tile rows; padded row of bf16 (144 bytes: conflict-free ldmatrix)
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void ldm_x4(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(su32(p)));
+}
+__device__ __forceinline__ void ldm_x4_t(uint32_t (&r)[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(su32(p)));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t packbf(float x, float y) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// rows [0, nrows) of a [., 64] bf16 array into a padded tile (zeros beyond)
+__device__ __forceinline__ void mtile_load(__nv_bfloat16* t, const __nv_bfloat16* src, int nrows, int tid) {
+    for (int q = tid; q < MQ * 8; q += 128) {
+        const int r = q >> 3, c8 = (q & 7) * 8;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (r < nrows) w = *reinterpret_cast<const uint4*>(src + (int64_t)r * D + c8);
+        *reinterpret_cast<uint4*>(t + r * MPAD + c8) = w;
+    }
+}
+
+// acc[8 n-tiles] (16 rows x 64 cols) += A (16 x 64, rows a_row0.. of a row-major tile)
+// times B^T where B is a row-major [n][k] tile (n = the 64 output columns)
+__device__ __forceinline__ void mm_rows_nk(float (&acc)[8][4], const __nv_bfloat16* A, const __nv_bfloat16* B,
+                                           int lane) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        uint32_t a[4];
+        ldm_x4(a, A + (lane & 15) * MPAD + kk * 16 + (lane >> 4) * 8);
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            uint32_t b[4];  // n-tiles 2np, 2np + 1; k halves
+            ldm_x4(b, B + (np * 16 + (lane & 7) + ((lane >> 4) << 3)) * MPAD + kk * 16 + ((lane >> 3) & 1) * 8);
+            mma16816(acc[2 * np], a, b[0], b[1]);
+            mma16816(acc[2 * np + 1], a, b[2], b[3]);
+        }
+    }
+}
+// acc (16 x 64 dims) += A (16 x 64 along k, from registers) times B where B is a
+// row-major [k][n] tile
+__device__ __forceinline__ void mm_regs_kn(float (&acc)[8][4], const uint32_t (&a)[4][4], const __nv_bfloat16* B,
+                                           int lane) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            uint32_t b[4];
+            ldm_x4_t(b, B + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * MPAD + np * 16 + (lane >> 4) * 8);
+            mma16816(acc[2 * np], a[kk], b[0], b[1]);
+            mma16816(acc[2 * np + 1], a[kk], b[2], b[3]);
+        }
+    }
+}
+// acc (16 keys x 64 dims) += A^T (A a row-major [k = query][m = key] tile, keys m0..)
+// times B (a row-major [k = query][n = dim] tile)
+__device__ __forceinline__ void mm_tt(float (&acc)[8][4], const __nv_bfloat16* A, int m0, const __nv_bfloat16* B,
+                                      int lane) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+        uint32_t a[4];
+        ldm_x4_t(a, A + (kk * 16 + (lane & 7) + (lane >> 4) * 8) * MPAD + m0 + ((lane >> 3) & 1) * 8);
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+            uint32_t b[4];
+            ldm_x4_t(b, B + (kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * MPAD + np * 16 + (lane >> 4) * 8);
+            mma16816(acc[2 * np], a, b[0], b[1]);
+            mma16816(acc[2 * np + 1], a, b[2], b[3]);
+        }
+    }
+}
+
+constexpr int MTILE_SMEM = 6 * MQ * MPAD * 2 + 2 * MQ * 4;
+
+__global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
+    extern __shared__ __align__(16) uint8_t msm[];
+    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(msm);
+    __nv_bfloat16* Gs = Qs + MQ * MPAD;   // dout
+    __nv_bfloat16* Ks = Gs + MQ * MPAD;
+    __nv_bfloat16* Vs = Ks + MQ * MPAD;
+    __nv_bfloat16* Ps = Vs + MQ * MPAD;   // P [query][key]
+    __nv_bfloat16* Ss = Ps + MQ * MPAD;   // dS [query][key]
+    float* Ls = reinterpret_cast<float*>(Ss + MQ * MPAD);
+    float* Dd = Ls + MQ;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int tiles = (int)((a.N + MQ - 1) / MQ);
+    const int bh = blockIdx.x / tiles;
+    const int64_t q0 = (int64_t)(blockIdx.x % tiles) * MQ;
+    const int nq = (int)(a.N - q0 < MQ ? a.N - q0 : MQ);
+    const int Wc = a.W / a.C;
+    const int64_t c = q0 / a.C, e = c - Wc - 1, ws = c - Wc > 0 ? (c - Wc) * a.C : 0;
+    const int n = e >= 0 ? a.sched[e].n_after : 0;
+    const int64_t row = (int64_t)bh * a.N;
+    const int64_t plane = ((int64_t)bh * a.snap_events + (e >= 0 ? e : 0)) * a.M * D;
+    const __nv_bfloat16* kh = reinterpret_cast<const __nv_bfloat16*>(a.snap_k) + plane;
+    const __nv_bfloat16* vh = reinterpret_cast<const __nv_bfloat16*>(a.snap_v) + plane;
+    const __nv_bfloat16* kr = reinterpret_cast<const __nv_bfloat16*>(a.kr) + row * D;
+    const __nv_bfloat16* vv = reinterpret_cast<const __nv_bfloat16*>(a.v) + row * D;
+    const int nbs = (n + MQ - 1) / MQ;
+    const int nbw = (int)((q0 + nq - ws + MQ - 1) / MQ);
+    const float sl = a.scale_log2;
+    const int r0 = 16 * warp;  // this warp's query rows (and keys of a block for dK, dV)
+
+    mtile_load(Qs, reinterpret_cast<const __nv_bfloat16*>(a.qr) + (row + q0) * D, nq, tid);
+    mtile_load(Gs, reinterpret_cast<const __nv_bfloat16*>(a.dout) + (row + q0) * D, nq, tid);
+    {   // dout . out per query (two threads a row)
+        const int r = tid >> 1, part = tid & 1;
+        float d = 0.0f;
+        if (r < nq) {
+            const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(a.out) + (row + q0 + r) * D + 32 * part;
+            const __nv_bfloat16* gp = reinterpret_cast<const __nv_bfloat16*>(a.dout) + (row + q0 + r) * D + 32 * part;
+            for (int x = 0; x < 32; ++x) d = fmaf(__bfloat162float(o[x]), __bfloat162float(gp[x]), d);
+        }
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        if (part == 0) Dd[r] = d;
+    }
+    auto load_block = [&](int b, bool want_v) -> int {
+        int kv;
+        if (b < nbs) {
+            kv = n - MQ * b < MQ ? n - MQ * b : MQ;
+            mtile_load(Ks, kh + (int64_t)MQ * b * D, kv, tid);
+            if (want_v) mtile_load(Vs, vh + (int64_t)MQ * b * D, kv, tid);
+        } else {
+            const int64_t t0 = ws + (int64_t)MQ * (b - nbs);
+            kv = (int)(q0 + nq - t0 < MQ ? q0 + nq - t0 : MQ);
+            mtile_load(Ks, kr + t0 * D, kv, tid);
+            if (want_v) mtile_load(Vs, vv + t0 * D, kv, tid);
+        }
+        return kv;
+    };
+    // scores of this warp's rows (fragment rows g, g + 8; columns 8 nt + 2 t4, + 1), log2 units
+    auto scores = [&](int b, int kv, float (&sc)[8][4]) {
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) sc[nt][u] = 0.0f;
+        mm_rows_nk(sc, Qs + r0 * MPAD, Ks, lane);
+        const bool win = b >= nbs;
+        const int64_t t0 = win ? ws + (int64_t)MQ * (b - nbs) : 0;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int qi = r0 + g + (u >> 1) * 8, kj = nt * 8 + 2 * t4 + (u & 1);
+                const bool ok = qi < nq && kj < kv && (!win || t0 + kj <= q0 + qi);
+                sc[nt][u] = ok ? sc[nt][u] * sl : -INFINITY;
+            }
+    };
+    // pass 1: log2-sum-exp per query
+    float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
+    for (int b = 0; b < nbs + nbw; ++b) {
+        __syncthreads();
+        const int kv = load_block(b, false);
+        __syncthreads();
+        float sc[8][4];
+        scores(b, kv, sc);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float mb = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) mb = fmaxf(mb, fmaxf(sc[nt][2 * h], sc[nt][2 * h + 1]));
+            const float mn = fmaxf(m2[h], mb);
+            if (mn == -INFINITY) continue;
+            float add = 0.0f;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) add += exp2f(sc[nt][2 * h] - mn) + exp2f(sc[nt][2 * h + 1] - mn);
+            l2[h] = l2[h] * exp2f(m2[h] - mn) + add;
+            m2[h] = mn;
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // the four threads of a row
+        float M = m2[h];
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+        float L = m2[h] == -INFINITY ? 0.0f : l2[h] * exp2f(m2[h] - M);
+        L += __shfl_xor_sync(0xffffffffu, L, 1);
+        L += __shfl_xor_sync(0xffffffffu, L, 2);
+        if (t4 == 0) Ls[r0 + g + 8 * h] = M + log2f(L);
+    }
+    __syncwarp();
+    // pass 2
+    float dq[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dq[nt][u] = 0.0f;
+    for (int b = 0; b < nbs + nbw; ++b) {
+        __syncthreads();
+        const int kv = load_block(b, true);
+        __syncthreads();
+        float sc[8][4], dp[8][4];
+        scores(b, kv, sc);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dp[nt][u] = 0.0f;
+        mm_rows_nk(dp, Gs + r0 * MPAD, Vs, lane);
+        uint32_t afrag[4][4];  // dS as A fragments (keys along k) for dQ
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int qi = r0 + g + 8 * h;
+            const float L = Ls[qi], Dv = Dd[qi];
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const float p0 = sc[nt][2 * h] == -INFINITY ? 0.0f : exp2f(sc[nt][2 * h] - L);
+                const float p1 = sc[nt][2 * h + 1] == -INFINITY ? 0.0f : exp2f(sc[nt][2 * h + 1] - L);
+                const float d0 = p0 * (dp[nt][2 * h] - Dv), d1 = p1 * (dp[nt][2 * h + 1] - Dv);
+                const uint32_t pp = packbf(p0, p1), dd = packbf(d0, d1);
+                *reinterpret_cast<uint32_t*>(Ps + qi * MPAD + nt * 8 + 2 * t4) = pp;
+                *reinterpret_cast<uint32_t*>(Ss + qi * MPAD + nt * 8 + 2 * t4) = dd;
+                // A fragment of k-step nt/2: regs 0/1 (rows g / g+8) from the even n-tile,
+                // 2/3 from the odd one
+                afrag[nt >> 1][(nt & 1) * 2 + h] = dd;
+            }
+        }
+        // dQ += dS K
+        mm_regs_kn(dq, afrag, Ks, lane);
+        __syncthreads();  // P and dS of every warp are in shared memory
+        // dK = dS^T Q, dV = P^T dO for keys r0 .. r0 + 15 of the block
+        float dk[8][4], dv[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) dk[nt][u] = dv[nt][u] = 0.0f;
+        mm_tt(dk, Ss, r0, Qs, lane);
+        mm_tt(dv, Ps, r0, Gs, lane);
+        const bool win = b >= nbs;
+        const int64_t kbase = win ? ws + (int64_t)MQ * (b - nbs) : (int64_t)MQ * b;
+        float* gk = win ? a.dk + (row + kbase) * D : a.dks + (((int64_t)bh * a.E + e) * a.M + kbase) * D;
+        float* gv = win ? a.dv + (row + kbase) * D : a.dvs + (((int64_t)bh * a.E + e) * a.M + kbase) * D;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int kj = r0 + g + 8 * h;
+            if (kj >= kv) continue;
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int dd0 = nt * 8 + 2 * t4;
+                atomicAdd(gk + (int64_t)kj * D + dd0, dk[nt][2 * h] * a.inv_sqrt_d);
+                atomicAdd(gk + (int64_t)kj * D + dd0 + 1, dk[nt][2 * h + 1] * a.inv_sqrt_d);
+                atomicAdd(gv + (int64_t)kj * D + dd0, dv[nt][2 * h]);
+                atomicAdd(gv + (int64_t)kj * D + dd0 + 1, dv[nt][2 * h + 1]);
+            }
+        }
+    }
+    // dq: scaled and rotated back (pairs across threads: through shared memory as fp32)
+    __syncthreads();
+    float* Fq = reinterpret_cast<float*>(msm);  // [64][64] fp32 over the Q / dout tiles
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+            const int qi = r0 + g + 8 * h, x = nt * 8 + 2 * t4;
+            Fq[qi * D + x] = dq[nt][2 * h] * a.inv_sqrt_d;
+            Fq[qi * D + x + 1] = dq[nt][2 * h + 1] * a.inv_sqrt_d;
+        }
+    __syncthreads();
+    const int half = a.r / 2;
+    for (int q = tid; q < nq * D; q += 128) {
+        const int rr = q >> 6, x = q & 63;
+        const int64_t pp = q0 + rr;
+        float y = Fq[rr * D + x];
+        if (x < 2 * half) {
+            const int i2 = x < half ? x : x - half;
+            const float2 cs = a.rope[pp * half + i2];
+            y = x < half ? y * cs.x + Fq[rr * D + x + half] * cs.y : y * cs.x - Fq[rr * D + x - half] * cs.y;
+        }
+        a.dq[(row + pp) * D + x] = y;
+    }
+}
+
 // rotate the accumulated window-key gradients back (in place) and zero the gate gradient
 __global__ void bwd_unrotate_dk(BackwardArgs a) {
     const int64_t rows = (int64_t)a.BH * a.N;
@@ -651,10 +940,14 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
         static bool attr = false;
         if (!attr) {
             cudaFuncSetAttribute(bwd_tile<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, TILE_SMEM);
+            cudaFuncSetAttribute(bwd_tile_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, MTILE_SMEM);
             attr = true;
         }
         const int tiles = (int)((a.N + TQ - 1) / TQ);
-        bwd_tile<T><<<(unsigned)(a.BH * tiles), 256, TILE_SMEM, s>>>(a);
+        if (sizeof(T) == 2)
+            bwd_tile_tc<<<(unsigned)(a.BH * tiles), 128, MTILE_SMEM, s>>>(a);
+        else
+            bwd_tile<T><<<(unsigned)(a.BH * tiles), 256, TILE_SMEM, s>>>(a);
         if (a.r > 0) bwd_unrotate_dk<<<2048, 256, 0, s>>>(a);
     } else {
         bwd_stats<T><<<gq, BW_THREADS, 0, s>>>(a);
