@@ -320,6 +320,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int ks_state = min(a.r / 16, 3);
             const uint32_t tS = tmem + 256 * slot, tO = tS + 128, tP = tS + 192;
             const uint32_t sQ = sbase + OFF_Q + slot * Q_BYTES;
+            // shared-memory descriptors of the slot's Q tile and of its first K and V stage
+            const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(sbase + OFF_K + slot * NS * KV_BYTES, 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(sbase + OFF_V + slot * NS * KV_BYTES, KV_BYTES, 1024);
             int g = 0;
             bool ok = true;
             KVM_PROBE_DECL(8)
@@ -332,13 +336,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!mbar_wait(bar(slot, B_KFULL + st), (gb / NS) & 1, abort_flag, a.status)) return false;
                 KVM_PROBE_LAP(1)
                 tc_fence_after();
-                const uint32_t sK = sbase + OFF_K + (slot * NS + st) * KV_BYTES;
+                // descriptors: the address field is the byte address / 16, so a K-step of
+                // 32 bytes adds 2 and a stage adds KV_BYTES / 16
+                const uint64_t dk = dk0 + (uint64_t)(st * (KV_BYTES >> 4));
                 const int ks0 = state ? ks_state : 0;
-                for (int ks = ks0; ks < 4; ++ks) {
-                    const uint64_t ad = sdesc_sw128(sQ + ks * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sK + ks * 32, 16, 1024);
-                    mma_bf16_ss(tS, ad, bd, idesc_qk, ks > ks0);
-                }
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+                    if (ks >= ks0) mma_bf16_ss(tS, dq0 + 2 * ks, dk + 2 * ks, idesc_qk, ks > ks0);
                 mma_commit(bar(slot, B_SFULL));
                 KVM_PROBE_LAP(2)
                 return true;
@@ -368,11 +372,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     KVM_PROBE_LAP(4)
                     tc_fence_after();
                     // O += P V: P (bf16, two keys per column) from tensor memory, V from shared
-                    const uint32_t sV = sbase + OFF_V + (slot * NS + st) * KV_BYTES;
-                    for (int ks = 0; ks < KB / 16; ++ks) {
-                        const uint64_t bd = sdesc_sw128(sV + ks * 2048, KV_BYTES, 1024);
-                        mma_bf16_ts(tO, tP + 8 * ks, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-                    }
+                    const uint64_t dv = dv0 + (uint64_t)(st * (KV_BYTES >> 4));
+#pragma unroll
+                    for (int ks = 0; ks < KB / 16; ++ks)
+                        mma_bf16_ts(tO, tP + 8 * ks, dv + 128 * ks, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
                     mma_commit(bar(slot, B_PVDONE));
                     mma_commit(bar(slot, B_KVEMPTY + st));
                     KVM_PROBE_LAP(5)
