@@ -125,6 +125,8 @@ Layout layout_of(const kvm_config& c) {
     L.status = take(256);  // status word at 0, attention tile-range counters at TILE_CTR_OFF
     L.k_rot = take(c.dtype == KVM_BF16 && c.rope_dims > 0 ? BH * (size_t)c.max_tokens * d * es : 0);
     L.q_rot = take(c.dtype == KVM_BF16 && c.rope_dims > 0 ? BH * (size_t)c.max_tokens * d * es : 0);
+    L.has_lse = c.dtype == KVM_BF16 && c.chunk % 128 == 0;
+    L.lse = take(L.has_lse ? BH * (size_t)c.max_tokens * 4 : 0);
     // the streamed-state chain's per-event log of touched rows (snapshots are rebuilt from it)
     kvm::FoldArgs probe{};
     probe.C = c.chunk;
@@ -205,6 +207,7 @@ struct kvm_layer {
     int device;
     int64_t n_slots, n_overflow, pos;
     int64_t E_max;
+    bool lse_valid = false;    // the last prefill wrote every query's log2-sum-exp (L.lse)
     int nsm = 0;               // SMs of the device
     std::vector<Sched> sched;  // prefill-from-empty schedule (host copy)
     cudaStream_t last_stream;
@@ -300,6 +303,7 @@ kvm_status kvm_layer_create(const kvm_config* cfg, void* dev_workspace, size_t b
     ly->L = L;
     ly->device = attr.device;
     ly->n_slots = ly->n_overflow = ly->pos = 0;
+    ly->lse_valid = false;
     ly->E_max = n_events_for(*cfg, cfg->max_tokens);
     ly->last_stream = nullptr;
     DeviceGuard g(ly->device);
@@ -427,6 +431,9 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     aa.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     aa.BH = BH;
     aa.status = ly->at<int>(L.status);
+    // every query's log2-sum-exp, kept for the backward (the tensor-core attention only)
+    aa.lse = L.has_lse && n_tokens > 0 && kvm::attn_tc_supported(aa, bf16) ? ly->at<float>(L.lse) : nullptr;
+    ly->lse_valid = false;
 
     kvm::RingFillArgs ra{};
     ra.k = k;
@@ -610,6 +617,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
     ly->n_slots = E > 0 ? ly->sched[E - 1].n_after : 0;
     ly->n_overflow = E * c.chunk;
     ly->pos = n_tokens;
+    ly->lse_valid = aa.lse != nullptr;
     return KVM_OK;
 }
 
@@ -696,6 +704,7 @@ kvm_status kvm_decode_step(kvm_layer* ly, const void* q, const void* k, const vo
     ly->n_slots = n;
     ly->n_overflow = t;
     ly->pos = p + 1;
+    ly->lse_valid = false;
     return KVM_OK;
 }
 
@@ -791,6 +800,7 @@ kvm_status kvm_state_import(kvm_layer* ly, const kvm_state_bufs* src, void* cuda
     ly->n_slots = src->n_slots;
     ly->n_overflow = src->n_overflow;
     ly->pos = src->pos;
+    ly->lse_valid = false;
     return KVM_OK;
 }
 
@@ -941,7 +951,7 @@ kvm_status kvm_layer_forward(kvm_layer* ly, int32_t d_model, const void* x, cons
 
 namespace {
 struct BwdScratch {
-    size_t qr, kr, lse, dd, dks, dvs, drho, sk, sv, gk, gv, cnt, rho, grho, total;
+    size_t qr, kr, lse, dd, dks, dvs, drho, mem, moff, total;
 };
 BwdScratch bwd_scratch_of(const kvm_config& c, int64_t n_tokens) {
     BwdScratch b;
@@ -957,13 +967,8 @@ BwdScratch bwd_scratch_of(const kvm_config& c, int64_t n_tokens) {
     b.dks = take(BH * E * M * D * 4);
     b.dvs = take(BH * E * M * D * 4);
     b.drho = take(BH * E * M * 4);
-    b.sk = take(BH * M * D * 4);
-    b.sv = take(BH * M * D * 4);
-    b.gk = take(BH * M * D * 4);
-    b.gv = take(BH * M * D * 4);
-    b.cnt = take(BH * M * 4);
-    b.rho = take(BH * M * 4);
-    b.grho = take(BH * M * 4);
+    b.mem = take(BH * E * (size_t)c.chunk * 4);
+    b.moff = take(BH * (M + 1) * 4);
     b.total = o;
     return b;
 }
@@ -988,6 +993,7 @@ kvm_status kvm_prefill_backward(kvm_layer* ly, const void* q, const void* k, con
     if (c.chunk > kvm::MAX_BW_C) return ly->fail(KVM_ERR_UNSUPPORTED, "the backward supports chunks of at most 256 tokens");
     if (c.rope_dims % 4) return ly->fail(KVM_ERR_UNSUPPORTED, "the backward needs rope_dims a multiple of 4");
     if (n_tokens < 0 || n_tokens > c.max_tokens) return ly->fail(KVM_ERR_INVALID_ARG, "n_tokens must be in [0, max_tokens]");
+    if (n_tokens >= (int64_t(1) << 29)) return ly->fail(KVM_ERR_UNSUPPORTED, "the backward supports fewer than 2^29 tokens");
     const int64_t E = kvm::host::n_events_for(c, n_tokens);
     if (ly->pos != n_tokens || ly->n_overflow != E * c.chunk)
         return ly->fail(KVM_ERR_INVALID_ARG, "the layer's last prefill was not of n_tokens tokens");
@@ -1024,16 +1030,12 @@ kvm_status kvm_prefill_backward(kvm_layer* ly, const void* q, const void* k, con
     a.kr = sc + B.kr;
     a.lse = reinterpret_cast<float*>(sc + B.lse);
     a.dd = reinterpret_cast<float*>(sc + B.dd);
+    a.lse_fwd = ly->lse_valid ? ly->at<float>(L.lse) : nullptr;
     a.dks = reinterpret_cast<float*>(sc + B.dks);
     a.dvs = reinterpret_cast<float*>(sc + B.dvs);
     a.drho = reinterpret_cast<float*>(sc + B.drho);
-    a.sk = reinterpret_cast<float*>(sc + B.sk);
-    a.sv = reinterpret_cast<float*>(sc + B.sv);
-    a.gk = reinterpret_cast<float*>(sc + B.gk);
-    a.gv = reinterpret_cast<float*>(sc + B.gv);
-    a.cnt = reinterpret_cast<int*>(sc + B.cnt);
-    a.rho = reinterpret_cast<float*>(sc + B.rho);
-    a.grho = reinterpret_cast<float*>(sc + B.grho);
+    a.mem = reinterpret_cast<int*>(sc + B.mem);
+    a.moff = reinterpret_cast<int*>(sc + B.moff);
     a.N = n_tokens;
     a.BH = c.batch * c.heads;
     a.C = c.chunk;
@@ -1048,7 +1050,10 @@ kvm_status kvm_prefill_backward(kvm_layer* ly, const void* q, const void* k, con
     a.status = ly->at<int>(L.status);
     cudaError_t e = timed(ly, PH_OTHER, s, [&] { return kvm::launch_backward(a, c.dtype == KVM_BF16, s); });
     if (e != cudaSuccess) return ly->cuda_fail(e, "backward launch");
-    ly->kernels += a.E > 0 ? 6 : 4;
+    // rotation; the tiled products (+ the rotation back of dk) or the four row kernels;
+    // the member lists and the slot sweep
+    const bool tiled = c.chunk % 64 == 0;
+    ly->kernels += 1 + (tiled ? 1 + (c.rope_dims > 0) : 3 + (a.E > 0)) + (a.E > 0 ? 2 : 0);
     return KVM_OK;
 }
 

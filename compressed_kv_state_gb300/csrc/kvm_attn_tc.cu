@@ -62,6 +62,7 @@ struct TcArgs {
     __nv_bfloat16* out;
     int* status;
     int q_prerot;    // queries come rotated: no RoPE in the kernel, the MMA waits for the copy
+    float* lse;      // optional: log2-sum-exp per query
 };
 
 struct Tile {
@@ -528,6 +529,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             KVM_PROBE_LAP(6)
             tc_fence_after();
             const float il = 1.0f / l;
+            if (a.lse && p < a.N) a.lse[(int64_t)T.bh * a.N + p] = m_used + log2f(l);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t o[32];
@@ -662,6 +664,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     t.out = reinterpret_cast<__nv_bfloat16*>(a.out);
     t.status = status;
     t.q_prerot = a.q_rot != nullptr || a.r == 0;
+    t.lse = a.lse;
     static int nsm = 0;
     if (nsm == 0) {
         int dev = 0;

@@ -237,13 +237,100 @@ __global__ void bwd_dstate(BackwardArgs a) {
     reinterpret_cast<float2*>(a.dvs + o)[lane] = av;
 }
 
+// Per row, one CTA: every slot's members (the tokens the recorded decisions sent to it)
+// as one list in the replay's order: by event, the founder first, then the merged tokens
+// in position order.  Entry (t << 2) | kind; slot j's part is mem[moff[j] .. moff[j + 1]).
+// A record entry that names no slot of its event or no known kind latches the status
+// word and is left out.
+constexpr int MB_THREADS = 256;
+__global__ void __launch_bounds__(MB_THREADS) bwd_members(BackwardArgs a) {
+    extern __shared__ int cur[];  // [M + 1]: counts, then list cursors
+    __shared__ int part[MB_THREADS / 32];
+    const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int C = a.C, M = a.M, E = a.E;
+    const int64_t rec0 = (int64_t)bh * a.rec_events * C;
+    int* moff = a.moff + (int64_t)bh * (M + 1);
+    int* list = a.mem + (int64_t)bh * E * C;
+    // kind of entry (e, i) and its slot, or -1 for an invalid entry
+    auto entry = [&](int e, int i, int& sj) -> int {
+        const int64_t o = rec0 + (int64_t)e * C + i;
+        sj = a.assign[o];
+        const int kn = a.kind[o];
+        return sj >= 0 && sj < a.sched[e].n_after && kn >= 0 && kn <= 2 ? kn : -1;
+    };
+    for (int j = tid; j <= M; j += MB_THREADS) cur[j] = 0;
+    __syncthreads();
+    for (int q = tid; q < E * C; q += MB_THREADS) {
+        int sj;
+        if (entry(q / C, q % C, sj) >= 0)
+            atomicAdd(&cur[sj], 1);
+        else if (a.status)
+            atomicOr(a.status, STATUS_DEVICE);
+    }
+    __syncthreads();
+    // exclusive prefix sum of the counts: each thread a contiguous range of slots
+    const int per = (M + MB_THREADS - 1) / MB_THREADS;
+    const int j0 = min(M, tid * per), j1 = min(M, j0 + per);
+    int own = 0;
+    for (int j = j0; j < j1; ++j) own += cur[j];
+    int x = own;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, d);
+        if (lane >= d) x += y;
+    }
+    if (lane == 31) part[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int p = lane < MB_THREADS / 32 ? part[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < MB_THREADS / 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, p, d);
+            if (lane >= d) p += y;
+        }
+        if (lane < MB_THREADS / 32) part[lane] = p;
+    }
+    __syncthreads();
+    int run = x - own + (warp > 0 ? part[warp - 1] : 0);
+    for (int j = j0; j < j1; ++j) {
+        const int c = cur[j];
+        cur[j] = run;
+        moff[j] = run;
+        run += c;
+    }
+    if (j0 < j1 && j1 == M) moff[M] = run;
+    __syncthreads();
+    // one warp appends in order: per event the founders, then the merged tokens; lanes of a
+    // batch that go to the same slot take consecutive places in lane (= position) order
+    if (warp == 0) {
+        const unsigned below = (1u << lane) - 1u;
+        for (int e = 0; e < E; ++e)
+            for (int pass = 0; pass < 2; ++pass)
+                for (int base = 0; base < C; base += 32) {
+                    const int i = base + lane;
+                    int sj = -1, kn = -1;
+                    if (i < C) kn = entry(e, i, sj);
+                    const bool in = kn >= 0 && (pass == 0 ? kn >= 1 : kn == 0);
+                    const unsigned peers = __match_any_sync(0xffffffffu, in ? sj : -1 - lane);
+                    int at = 0;
+                    if (in) at = cur[sj] + __popc(peers & below);
+                    __syncwarp();
+                    if (in) {
+                        list[at] = (int)((((int64_t)e * C + i) << 2) | kn);
+                        if ((peers & below) == 0u) cur[sj] += __popc(peers);
+                    }
+                    __syncwarp();
+                }
+    }
+}
+
 // Per slot, one warp (lanes over the dims, two each): every slot's history is its own,
 // so the rows' slots run in parallel.  Pass 1 replays the slot through the events with
-// the recorded decisions (its founder first, then its merged tokens in position order:
-// the forward's fp32 sums) and turns each event's read-row gradients of the slot into
-// sum and radius gradients (LayerNorm and normalisation backward), in place.  Pass 2
-// runs the events backwards, summing those gradients, and each of the slot's tokens
-// reads the sum at its own event (the gradients of every state that holds it).
+// the recorded decisions (its member list: the founder first, then its merged tokens in
+// position order: the forward's fp32 sums) and turns each event's read-row gradients of
+// the slot into sum and radius gradients (LayerNorm and normalisation backward), in
+// place.  Pass 2 runs the events backwards, summing those gradients, and each of the
+// slot's tokens reads the sum at its own event (the gradients of every state that holds it).
 template <typename T>
 __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
     const int lane = threadIdx.x & 31;
@@ -257,46 +344,43 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
     const T* vv = reinterpret_cast<const T*>(a.v) + row * D;
     const float* gg = a.g + row;
     if (a.E == 0 || j >= a.sched[a.E - 1].n_after) return;  // slot never founded
-    // the record of event e: kind of token i if it went to slot j (founder 1/2, merged 0),
-    // else -1; the warp of slot 0 reports entries that name no slot of the event
-    auto kind_of = [&](int e, int i, int n) -> int {
-        const int64_t o = ((int64_t)bh * a.rec_events + e) * C + i;
-        const int sj = a.assign[o], kn = a.kind[o];
-        const bool ok = sj >= 0 && sj < n && kn >= 0 && kn <= 2;
-        if (!ok && j == 0 && a.status) atomicOr(a.status, STATUS_DEVICE);
-        return ok && sj == j ? kn : -1;
+    const int* lst = a.mem + (int64_t)bh * a.E * C;
+    const int m0 = a.moff[(int64_t)bh * (M + 1) + j], m1 = a.moff[(int64_t)bh * (M + 1) + j + 1];
+    // the member list through a window of 32 entries in the lanes' registers (p is the
+    // same in every lane): a window starts at p going forwards, ends at p going backwards
+    int wbase = -64, wbuf = 0;
+    auto member = [&](int p, bool fwd) -> int {
+        if (p < wbase || p >= wbase + 32) {
+            wbase = fwd ? p : max(m0, p - 31);
+            wbuf = wbase + lane < m1 ? lst[wbase + lane] : 0;
+        }
+        return __shfl_sync(0xffffffffu, wbuf, p - wbase);
     };
     float2 sk = make_float2(0.f, 0.f), sv = sk;
     int cnt = 0;
     float rho = 0.0f;
     // pass 1
+    int ptr = m0;
     for (int e = 0; e < a.E; ++e) {
         const int n = a.sched[e].n_after;
         if (j >= n) continue;  // not founded yet (founding appends at the end)
-        // the founder first (the forward sets a new slot from it), then the merged
-        // tokens in position order, whatever their positions relative to the founder
-        for (int pass = 0; pass < 2; ++pass) {
-            for (int base = 0; base < C; base += 32) {
-                const int i = base + lane;
-                const int kn = i < C ? kind_of(e, i, n) : -1;
-                unsigned sel = __ballot_sync(0xffffffffu, pass == 0 ? (kn == 1 || kn == 2) : kn == 0);
-                while (sel) {
-                    const int ii = base + __ffs(sel) - 1;
-                    sel &= sel - 1;
-                    const int64_t t = (int64_t)e * C + ii;
-                    const float gt = gg[t];
-                    const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
-                    if (pass == 0) {
-                        sk = make_float2(gt * kx.x, gt * kx.y);
-                        sv = make_float2(gt * vx.x, gt * vx.y);
-                        cnt = 1;
-                        rho = sqrtf(warp_sum(dot2(vx, vx)));
-                    } else {
-                        sk = make_float2(fmaf(gt, kx.x, sk.x), fmaf(gt, kx.y, sk.y));
-                        sv = make_float2(fmaf(gt, vx.x, sv.x), fmaf(gt, vx.y, sv.y));
-                        ++cnt;
-                    }
-                }
+        const int64_t tend = (int64_t)(e + 1) * C;
+        while (ptr < m1) {
+            const int ent = member(ptr, true);
+            const int64_t t = ent >> 2;
+            if (t >= tend) break;  // a member of a later event
+            ++ptr;
+            const float gt = gg[t];
+            const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
+            if ((ent & 3) != 0) {  // the founder sets the slot
+                sk = make_float2(gt * kx.x, gt * kx.y);
+                sv = make_float2(gt * vx.x, gt * vx.y);
+                cnt = 1;
+                rho = sqrtf(warp_sum(dot2(vx, vx)));
+            } else {
+                sk = make_float2(fmaf(gt, kx.x, sk.x), fmaf(gt, kx.y, sk.y));
+                sv = make_float2(fmaf(gt, vx.x, sv.x), fmaf(gt, vx.y, sv.y));
+                ++cnt;
             }
         }
         // read-row gradients -> sum and radius gradients of the state after event e
@@ -331,9 +415,10 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
         reinterpret_cast<float2*>(a.dvs + o)[lane] = dsv;
         if (lane == 0) a.drho[((int64_t)bh * a.E + e) * M + j] = dr;
     }
-    // pass 2
+    // pass 2: the members from the last backwards
     float2 Gk = make_float2(0.f, 0.f), Gv = Gk;
     float Gr = 0.0f;
+    ptr = m1 - 1;
     for (int e = a.E - 1; e >= 0; --e) {
         const int n = a.sched[e].n_after;
         if (j >= n) continue;
@@ -343,36 +428,31 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
         Gk = make_float2(Gk.x + dk.x, Gk.y + dk.y);
         Gv = make_float2(Gv.x + dv.x, Gv.y + dv.y);
         Gr += a.drho[((int64_t)bh * a.E + e) * M + j];
-        for (int base = 0; base < C; base += 32) {
-            const int i = base + lane;
-            const int64_t oo = ((int64_t)bh * a.rec_events + e) * C + i;
-            const int kn = i < C && a.assign[oo] == j ? a.kind[oo] : -1;
-            unsigned mine = __ballot_sync(0xffffffffu, kn >= 0 && kn <= 2);
-            while (mine) {
-                const int ii = base + __ffs(mine) - 1;
-                mine &= mine - 1;
-                const int kd = __shfl_sync(0xffffffffu, kn, ii - base);
-                const int64_t t = (int64_t)e * C + ii;
-                const float gt = gg[t];
-                const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
-                float2* dkp = reinterpret_cast<float2*>(a.dk + (row + t) * D) + lane;
-                float2* dvp = reinterpret_cast<float2*>(a.dv + (row + t) * D) + lane;
-                float2 dkt = *dkp, dvt = *dvp;
-                dkt.x = fmaf(gt, Gk.x, dkt.x);
-                dkt.y = fmaf(gt, Gk.y, dkt.y);
-                dvt.x = fmaf(gt, Gv.x, dvt.x);
-                dvt.y = fmaf(gt, Gv.y, dvt.y);
-                if (kd == 1 || kd == 2) {  // founder: rho = |v|
-                    const float nv = sqrtf(warp_sum(dot2(vx, vx)));
-                    const float f = nv > 0.0f ? Gr / nv : 0.0f;
-                    dvt.x = fmaf(f, vx.x, dvt.x);
-                    dvt.y = fmaf(f, vx.y, dvt.y);
-                }
-                *dkp = dkt;
-                *dvp = dvt;
-                const float dgt = warp_sum(dot2(kx, Gk) + dot2(vx, Gv));
-                if (lane == 0) a.dg[row + t] += dgt;
+        const int64_t tbeg = (int64_t)e * C;
+        while (ptr >= m0) {
+            const int ent = member(ptr, false);
+            const int64_t t = ent >> 2;
+            if (t < tbeg) break;  // a member of an earlier event
+            --ptr;
+            const float gt = gg[t];
+            const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
+            float2* dkp = reinterpret_cast<float2*>(a.dk + (row + t) * D) + lane;
+            float2* dvp = reinterpret_cast<float2*>(a.dv + (row + t) * D) + lane;
+            float2 dkt = *dkp, dvt = *dvp;
+            dkt.x = fmaf(gt, Gk.x, dkt.x);
+            dkt.y = fmaf(gt, Gk.y, dkt.y);
+            dvt.x = fmaf(gt, Gv.x, dvt.x);
+            dvt.y = fmaf(gt, Gv.y, dvt.y);
+            if ((ent & 3) != 0) {  // founder: rho = |v|
+                const float nv = sqrtf(warp_sum(dot2(vx, vx)));
+                const float f = nv > 0.0f ? Gr / nv : 0.0f;
+                dvt.x = fmaf(f, vx.x, dvt.x);
+                dvt.y = fmaf(f, vx.y, dvt.y);
             }
+            *dkp = dkt;
+            *dvp = dvt;
+            const float dgt = warp_sum(dot2(kx, Gk) + dot2(vx, Gv));
+            if (lane == 0) a.dg[row + t] += dgt;
         }
     }
 }
@@ -781,9 +861,13 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
                 sc[nt][u] = ok ? sc[nt][u] * sl : -INFINITY;
             }
     };
-    // pass 1: log2-sum-exp per query
+    // pass 1: log2-sum-exp per query (the forward's, when it kept them)
     float m2[2] = {-INFINITY, -INFINITY}, l2[2] = {0.f, 0.f};
-    for (int b = 0; b < nbs + nbw; ++b) {
+    if (a.lse_fwd) {
+        for (int rr = tid; rr < MQ; rr += 128) Ls[rr] = rr < nq ? a.lse_fwd[row + q0 + rr] : 0.0f;
+        __syncthreads();
+    }
+    for (int b = 0; a.lse_fwd == nullptr && b < nbs + nbw; ++b) {
         __syncthreads();
         const int kv = load_block(b, false);
         __syncthreads();
@@ -804,7 +888,7 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
         }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {  // the four threads of a row
+    for (int h = 0; h < 2 && a.lse_fwd == nullptr; ++h) {  // the four threads of a row
         float M = m2[h];
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
@@ -960,6 +1044,7 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
     }
     if (a.E > 0) {
         const int64_t slots = (int64_t)a.BH * a.M;
+        bwd_members<<<(unsigned)a.BH, MB_THREADS, (size_t)(a.M + 1) * sizeof(int), s>>>(a);
         bwd_sweep<T><<<(unsigned)((slots + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
     }
     return cudaGetLastError();

@@ -24,6 +24,8 @@ struct Layout {
     size_t q_rot;  // queries rotated at their own positions (same condition)
     size_t log_k, log_v, log_idx, log_cnt;  // the streamed chain's row log (empty otherwise)
     bool logs;
+    size_t lse;    // log2-sum-exp of every query's scores, written by the tensor-core attention
+    bool has_lse;  // (bf16 layers with chunks a multiple of 128; else empty)
     size_t total;
 };
 

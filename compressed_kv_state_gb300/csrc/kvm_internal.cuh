@@ -154,6 +154,9 @@ struct AttnArgs {
     // Tensor-core path: queries already rotated at their own positions (the same pass),
     // loaded instead of q; nullptr = each tile rotates its queries in the kernel.
     const void* q_rot;
+    // Tensor-core path, optional: fp32 [BH, N] log2-sum-exp of every query's scaled
+    // scores (max + log2 of the sum of 2^(s * scale_log2 - max)), for the backward.
+    float* lse;
 };
 
 // Keys rotated once at their own positions (rotate-half RoPE on dims [0, r)),
@@ -228,16 +231,12 @@ struct BackwardArgs {
     void* kr;
     float* lse;           // [BH, N] log2-sum-exp of each query's scores
     float* dd;            // [BH, N] dout . out
+    const float* lse_fwd; // [BH, N] the forward's log2-sum-exp per query, or nullptr (recomputed)
     float* dks;           // [BH, E, M, D] read-row gradients, then sum gradients
     float* dvs;
     float* drho;          // [BH, E, M]
-    float* sk;            // [BH, M, D] replayed sums
-    float* sv;
-    int* cnt;             // [BH, M]
-    float* rho;
-    float* gk;            // [BH, M, D] accumulated sum gradients
-    float* gv;
-    float* grho;          // [BH, M]
+    int* mem;             // [BH, E * C] every slot's member tokens in replay order: (t << 2) | kind
+    int* moff;            // [BH, M + 1] slot j's members are mem[moff[j] .. moff[j + 1])
     int64_t N;
     int BH, C, W, M, r, E;
     float ln_eps, scale_log2, inv_sqrt_d;
