@@ -734,6 +734,23 @@ __device__ __forceinline__ void mtile_load(__nv_bfloat16* t, const __nv_bfloat16
     }
 }
 
+// rows [0, nrows) of a [., 64] bf16 array into a padded tile by asynchronous copies
+// (rows past nrows are zero-filled: a copy of 0 source bytes)
+__device__ __forceinline__ void mtile_load_async(__nv_bfloat16* t, const __nv_bfloat16* src, int nrows, int tid) {
+    for (int q = tid; q < MQ * 8; q += 128) {
+        const int r = q >> 3, c8 = (q & 7) * 8;
+        const bool ok = r < nrows;
+        const __nv_bfloat16* g = ok ? src + (int64_t)r * D + c8 : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(su32(t + r * MPAD + c8)), "l"(g),
+                     "r"(ok ? 16 : 0)
+                     : "memory");
+    }
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // acc[8 n-tiles] (16 rows x 64 cols) += A (16 x 64, rows a_row0.. of a row-major tile)
 // times B^T where B is a row-major [n][k] tile (n = the 64 output columns)
 __device__ __forceinline__ void mm_rows_nk(float (&acc)[8][4], const __nv_bfloat16* A, const __nv_bfloat16* B,
@@ -784,7 +801,7 @@ __device__ __forceinline__ void mm_tt(float (&acc)[8][4], const __nv_bfloat16* A
     }
 }
 
-constexpr int MTILE_SMEM = 6 * MQ * MPAD * 2 + 2 * MQ * 4;
+constexpr int MTILE_SMEM = 8 * MQ * MPAD * 2 + 2 * MQ * 4;
 
 __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
     extern __shared__ __align__(16) uint8_t msm[];
@@ -794,7 +811,9 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
     __nv_bfloat16* Vs = Ks + MQ * MPAD;
     __nv_bfloat16* Ps = Vs + MQ * MPAD;   // P [query][key]
     __nv_bfloat16* Ss = Ps + MQ * MPAD;   // dS [query][key]
-    float* Ls = reinterpret_cast<float*>(Ss + MQ * MPAD);
+    __nv_bfloat16* K2 = Ss + MQ * MPAD;   // second K / V buffers (the next block's copies)
+    __nv_bfloat16* V2 = K2 + MQ * MPAD;
+    float* Ls = reinterpret_cast<float*>(V2 + MQ * MPAD);
     float* Dd = Ls + MQ;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = lane >> 2, t4 = lane & 3;
@@ -844,12 +863,12 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
         return kv;
     };
     // scores of this warp's rows (fragment rows g, g + 8; columns 8 nt + 2 t4, + 1), log2 units
-    auto scores = [&](int b, int kv, float (&sc)[8][4]) {
+    auto scores = [&](int b, int kv, const __nv_bfloat16* Kb, float (&sc)[8][4]) {
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int u = 0; u < 4; ++u) sc[nt][u] = 0.0f;
-        mm_rows_nk(sc, Qs + r0 * MPAD, Ks, lane);
+        mm_rows_nk(sc, Qs + r0 * MPAD, Kb, lane);
         const bool win = b >= nbs;
         const int64_t t0 = win ? ws + (int64_t)MQ * (b - nbs) : 0;
 #pragma unroll
@@ -872,7 +891,7 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
         const int kv = load_block(b, false);
         __syncthreads();
         float sc[8][4];
-        scores(b, kv, sc);
+        scores(b, kv, Ks, sc);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             float mb = -INFINITY;
@@ -904,17 +923,47 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
     for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int u = 0; u < 4; ++u) dq[nt][u] = 0.0f;
-    for (int b = 0; b < nbs + nbw; ++b) {
-        __syncthreads();
-        const int kv = load_block(b, true);
-        __syncthreads();
+    // K and V blocks double-buffered: block b + 1 is copied while block b is worked on
+    auto block_rows = [&](int b) -> int {
+        if (b < nbs) return n - MQ * b < MQ ? n - MQ * b : MQ;
+        const int64_t t0 = ws + (int64_t)MQ * (b - nbs);
+        return (int)(q0 + nq - t0 < MQ ? q0 + nq - t0 : MQ);
+    };
+    auto issue_block = [&](int b, __nv_bfloat16* kd, __nv_bfloat16* vd) {
+        const int kv = block_rows(b);
+        if (b < nbs) {
+            mtile_load_async(kd, kh + (int64_t)MQ * b * D, kv, tid);
+            mtile_load_async(vd, vh + (int64_t)MQ * b * D, kv, tid);
+        } else {
+            const int64_t t0 = ws + (int64_t)MQ * (b - nbs);
+            mtile_load_async(kd, kr + t0 * D, kv, tid);
+            mtile_load_async(vd, vv + t0 * D, kv, tid);
+        }
+        cp_async_commit();
+    };
+    const int nblocks = nbs + nbw;
+    __syncthreads();  // pass 1 is done with the K buffer
+    issue_block(0, Ks, Vs);
+    for (int b = 0; b < nblocks; ++b) {
+        __nv_bfloat16* Kc = (b & 1) ? K2 : Ks;
+        __nv_bfloat16* Vc = (b & 1) ? V2 : Vs;
+        // the other buffers were last read by block b - 1's S, dP and dQ products, which
+        // every thread finished before block b - 1's barrier ahead of its dK, dV products
+        if (b + 1 < nblocks) {
+            issue_block(b + 1, (b & 1) ? Ks : K2, (b & 1) ? Vs : V2);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();  // every thread's copies of block b have landed
+        const int kv = block_rows(b);
         float sc[8][4], dp[8][4];
-        scores(b, kv, sc);
+        scores(b, kv, Kc, sc);
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
             for (int u = 0; u < 4; ++u) dp[nt][u] = 0.0f;
-        mm_rows_nk(dp, Gs + r0 * MPAD, Vs, lane);
+        mm_rows_nk(dp, Gs + r0 * MPAD, Vc, lane);
         uint32_t afrag[4][4];  // dS as A fragments (keys along k) for dQ
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -934,7 +983,7 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
             }
         }
         // dQ += dS K
-        mm_regs_kn(dq, afrag, Ks, lane);
+        mm_regs_kn(dq, afrag, Kc, lane);
         __syncthreads();  // P and dS of every warp are in shared memory
         // dK = dS^T Q, dV = P^T dO for keys r0 .. r0 + 15 of the block
         float dk[8][4], dv[8][4];
