@@ -415,6 +415,20 @@ __global__ void __launch_bounds__(NT, 1)
     // tensor memory after an abort
     int pend_st = -1, pend_ld[2] = {-1, -1}, pend_mma = -1;
 
+    auto load_chunk = [&](int e, int buf) {
+        pend_ld[buf] = ((e - a.e_begin) >> 1) & 1;
+        const int64_t off = ((int64_t)e * C) % a.src_len;
+        mbar_expect_tx(smem_u32(&X.bar_k[buf]), 2 * TOK * ROWB);
+        tma_load_3d(sK + buf * TOK * ROWB, &tm_k, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
+        tma_load_3d(sV + buf * TOK * ROWB, &tm_v, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
+    };
+    // the first two chunks load now, while the state is restored (the chunk buffers are
+    // not staging areas); chunk e + 2 is issued at the end of event e
+    if (tid == TMA_T && a.e_begin < a.e_end && !a.test_stall) {
+        load_chunk(a.e_begin, 0);
+        if (a.e_begin + 1 < a.e_end) load_chunk(a.e_begin + 1, 1);
+    }
+
     {
         float2 x[32];
         if (nblk_st > 0) {
@@ -468,18 +482,6 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc_fence_after();
 
-    auto load_chunk = [&](int e, int buf) {
-        pend_ld[buf] = ((e - a.e_begin) >> 1) & 1;
-        const int64_t off = ((int64_t)e * C) % a.src_len;
-        mbar_expect_tx(smem_u32(&X.bar_k[buf]), 2 * TOK * ROWB);
-        tma_load_3d(sK + buf * TOK * ROWB, &tm_k, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
-        tma_load_3d(sV + buf * TOK * ROWB, &tm_v, 0, (int)off, bh, smem_u32(&X.bar_k[buf]));
-    };
-    // the first two chunks load now; chunk e + 2 is issued at the end of event e
-    if (tid == TMA_T && a.e_begin < a.e_end && !a.test_stall) {
-        load_chunk(a.e_begin, 0);
-        if (a.e_begin + 1 < a.e_end) load_chunk(a.e_begin + 1, 1);
-    }
     const uint32_t idesc = idesc_bf16(128, 256, 0, 0);
     int mma_count = 0;
     bool mma_early = false;  // thread 0: this event's similarity MMA was issued by the previous event
