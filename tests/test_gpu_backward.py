@@ -38,6 +38,11 @@ CASES = [
                 max_slots=32, keys="repeat5"),
     wl.Workload("bwd_C32_fp32_B1H1N400_W96", B=1, H=1, N=400, chunk=32, window=96, n_sinks=4,
                 max_slots=24, keys="repeat5", dtype="fp32"),
+    # no fold event yet (N <= W + C): window attention only, no member lists or sweep
+    wl.Workload("bwd_E0_B1H2N170_C64W128", B=1, H=2, N=170, chunk=64, window=128, n_sinks=4,
+                max_slots=16, keys="repeat5"),
+    wl.Workload("bwd_E0_B1H1N250_C128W128", B=1, H=1, N=250, chunk=128, window=128, n_sinks=4,
+                max_slots=16, keys="repeat5"),
 ]
 
 
