@@ -466,6 +466,10 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         ka.q = q;
         ka.q_rot = ly->ws + L.q_rot;
         aa.q_rot = ka.q_rot;
+        // 32 rotary dims: only they are rotated and stored (the attention reads the rest of
+        // each row from q and k)
+        ka.compact = c.rope_dims == 32;
+        aa.rot_compact = ka.compact;
         // the window ring is filled in the same pass
         if (ring_work) {
             ka.v = v;

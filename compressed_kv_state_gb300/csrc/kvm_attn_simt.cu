@@ -238,25 +238,101 @@ __device__ __forceinline__ uint4 rope_apply(uint4 w, const uint4& o, const float
     return w;
 }
 
+// One thread per 16-byte piece (8 dims) of a row.  Full rows: every piece of k and q is
+// written to k_rot / q_rot (the rotary pieces rotated).  Compact rows: only the r / 8
+// rotary pieces are (rows of r dims).  Ring tokens get their whole rows in the ring.
+// Compact rows: the ring tokens' pieces past the rotary dims (pieces RC .. 7), as they are.
+__device__ __forceinline__ void ring_rest_compact(const RopeKeysArgs& a, int bh, int RC) {
+    const int64_t row0 = (int64_t)bh * a.N * 8;
+    const uint4* src = reinterpret_cast<const uint4*>(a.k) + row0;
+    const int NR = 8 - RC;
+    const int64_t cnt = (a.N - a.first) * NR;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < cnt; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t p = a.first + i / NR;
+        const int c = RC + (int)(i % NR);
+        const int64_t fi = p * 8 + c;
+        const int64_t slot = p - (p / a.L) * a.L;
+        const int64_t rrow = (int64_t)bh * a.L + slot;
+        const uint4 w = src[fi];
+        reinterpret_cast<uint4*>(a.ring_k)[rrow * 8 + c] = w;
+        reinterpret_cast<uint4*>(a.ring_v)[rrow * 8 + c] = reinterpret_cast<const uint4*>(a.v)[row0 + fi];
+        reinterpret_cast<uint4*>(a.ring_kr)[rrow * 8 + c] = w;
+    }
+}
+
+// Compact rows, r = 32: one thread per rotate-half pair of pieces (u, u + 2) of a
+// position: the two pieces of k and q and their shared (cos, sin) entries are loaded
+// once for both outputs.
+__device__ __forceinline__ void rope_pairs_compact(const RopeKeysArgs& a) {
+    constexpr int RC = 4, HC = 2;  // pieces of a compact row; pairs per position
+    const int half = 16;
+    const int64_t items = a.N * HC;
+    for (int bh = blockIdx.y; bh < a.BH; bh += gridDim.y) {
+        const int64_t row0 = (int64_t)bh * a.N * 8;
+        const uint4* src = reinterpret_cast<const uint4*>(a.k) + row0;
+        const uint4* qsrc = reinterpret_cast<const uint4*>(a.q) + row0;
+        uint4* dst = reinterpret_cast<uint4*>(a.k_rot) + (int64_t)bh * a.N * RC;
+        uint4* qdst = reinterpret_cast<uint4*>(a.q_rot) + (int64_t)bh * a.N * RC;
+        for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items;
+             i += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t p = i >> 1;
+            const int u = (int)(i & 1);
+            const uint4 klo = src[p * 8 + u], khi = src[p * 8 + u + HC];
+            const uint4 qlo = qsrc[p * 8 + u], qhi = qsrc[p * 8 + u + HC];
+            const float4* tab = reinterpret_cast<const float4*>(a.rope + p * half + u * 8);
+            const float4 t[4] = {tab[0], tab[1], tab[2], tab[3]};
+            const uint4 rlo = rope_apply(klo, khi, t, true), rhi = rope_apply(khi, klo, t, false);
+            dst[p * RC + u] = rlo;
+            dst[p * RC + u + HC] = rhi;
+            qdst[p * RC + u] = rope_apply(qlo, qhi, t, true);
+            qdst[p * RC + u + HC] = rope_apply(qhi, qlo, t, false);
+            if (a.ring_k && p >= a.first) {  // the window ring: whole rows (the rest below)
+                const int64_t slot = p - (p / a.L) * a.L;
+                const int64_t rrow = (int64_t)bh * a.L + slot;
+                const uint4* vs = reinterpret_cast<const uint4*>(a.v) + row0;
+                uint4* rk = reinterpret_cast<uint4*>(a.ring_k) + rrow * 8;
+                uint4* rv = reinterpret_cast<uint4*>(a.ring_v) + rrow * 8;
+                uint4* rkr = reinterpret_cast<uint4*>(a.ring_kr) + rrow * 8;
+                rk[u] = klo;
+                rk[u + HC] = khi;
+                rv[u] = vs[p * 8 + u];
+                rv[u + HC] = vs[p * 8 + u + HC];
+                rkr[u] = rlo;
+                rkr[u + HC] = rhi;
+                if (u == 0) a.ring_g[rrow] = a.g[(int64_t)bh * a.N + p];
+            }
+        }
+        if (a.ring_k) ring_rest_compact(a, bh, RC);
+    }
+}
+
 __global__ void rope_keys_kernel(RopeKeysArgs a) {
-    const int64_t per_row = a.N * 8;
+    if (a.compact && a.q) {
+        rope_pairs_compact(a);
+        return;
+    }
+    const int RC = a.compact ? a.r / 8 : 8;  // pieces of a k_rot / q_rot row
+    const int lg = RC == 8 ? 3 : (RC == 4 ? 2 : (RC == 2 ? 1 : 0));
+    const int64_t per_row = a.N * RC;
     const int half = a.r / 2, hc = half >> 3;
     const bool vec = (half & 7) == 0;
     for (int bh = blockIdx.y; bh < a.BH; bh += gridDim.y) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.k) + (int64_t)bh * per_row;
+        const int64_t row0 = (int64_t)bh * a.N * 8;  // first piece of this row in k, q, v
+        const uint4* src = reinterpret_cast<const uint4*>(a.k) + row0;
         uint4* dst = reinterpret_cast<uint4*>(a.k_rot) + (int64_t)bh * per_row;
-        const uint4* qsrc = a.q ? reinterpret_cast<const uint4*>(a.q) + (int64_t)bh * per_row : nullptr;
+        const uint4* qsrc = a.q ? reinterpret_cast<const uint4*>(a.q) + row0 : nullptr;
         uint4* qdst = a.q ? reinterpret_cast<uint4*>(a.q_rot) + (int64_t)bh * per_row : nullptr;
         for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < per_row;
              i += (int64_t)gridDim.x * blockDim.x) {
-            const int64_t p = i >> 3;
-            const int c = (int)(i & 7);
+            const int64_t p = i >> lg;
+            const int c = (int)(i & (RC - 1));
+            const int64_t fi = p * 8 + c;  // the piece in a full row
             const bool rot = 8 * c < a.r, low = c < hc;
             const int64_t partner = p * 8 + (low ? c + hc : c - hc);
             // every load of this piece first
-            uint4 w = src[i], wq = make_uint4(0u, 0u, 0u, 0u), o = w, oq = w;
+            uint4 w = src[fi], wq = make_uint4(0u, 0u, 0u, 0u), o = w, oq = w;
             float4 t[4];
-            if (qsrc) wq = qsrc[i];
+            if (qsrc) wq = qsrc[fi];
             if (vec && rot) {
                 o = src[partner];
                 if (qsrc) oq = qsrc[partner];
@@ -270,8 +346,7 @@ __global__ void rope_keys_kernel(RopeKeysArgs a) {
                 const int64_t slot = p - (p / a.L) * a.L;
                 rrow = (int64_t)bh * a.L + slot;
                 reinterpret_cast<uint4*>(a.ring_k)[rrow * 8 + c] = w;
-                reinterpret_cast<uint4*>(a.ring_v)[rrow * 8 + c] =
-                    reinterpret_cast<const uint4*>(a.v)[(int64_t)bh * per_row + i];
+                reinterpret_cast<uint4*>(a.ring_v)[rrow * 8 + c] = reinterpret_cast<const uint4*>(a.v)[row0 + fi];
                 if (c == 0) a.ring_g[rrow] = a.g[(int64_t)bh * a.N + p];
             }
             if (vec) {
@@ -287,6 +362,8 @@ __global__ void rope_keys_kernel(RopeKeysArgs a) {
             if (ring) reinterpret_cast<uint4*>(a.ring_kr)[rrow * 8 + c] = w;
             if (qsrc) qdst[i] = wq;
         }
+        // compact rows: the ring tokens' pieces past the rotary dims, as they are
+        if (RC < 8 && a.ring_k) ring_rest_compact(a, bh, RC);
     }
 }
 
@@ -295,7 +372,8 @@ cudaError_t launch_rope_keys(const RopeKeysArgs& a, cudaStream_t s) {
     // a.grid CTAs in total, spread over rows (y) and the chunks of a row (x)
     const int gy = a.BH < 65535 ? a.BH : 65535;
     int gx = a.grid / gy;
-    const int64_t need = (a.N * 8 + 255) / 256;
+    if (a.compact && a.r != 32) return cudaErrorInvalidValue;
+    const int64_t need = (a.N * (a.compact ? (a.q ? 2 : a.r / 8) : 8) + 255) / 256;
     if (gx < 1) gx = 1;
     if (gx > need) gx = (int)need;
     rope_keys_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, s>>>(a);

@@ -63,6 +63,8 @@ struct TcArgs {
     int* status;
     int q_prerot;    // queries come rotated: no RoPE in the kernel, the MMA waits for the copy
     float* lse;      // optional: log2-sum-exp per query
+    int split;       // Q and window-K tiles as two 64-byte halves: rotated dims [0, 32) from
+                     // the compact q_rot / k_rot rows, dims [32, 64) from q / k
 };
 
 struct Tile {
@@ -206,7 +208,8 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
-                    const __grid_constant__ CUtensorMap tm_sv, const TcArgs a) {
+                    const __grid_constant__ CUtensorMap tm_sv, const __grid_constant__ CUtensorMap tm_qh,
+                    const __grid_constant__ CUtensorMap tm_kh, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -276,7 +279,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (k >= 1 && !mbar_wait(bar(slot, B_QEMPTY), (k - 1) & 1, abort_flag, a.status)) break;
                 KVM_PROBE_LAP(2)
                 mbar_expect_tx(bar(slot, B_QFULL), Q_BYTES);
-                tma_load_3d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, 0, (int)T.q0, T.bh, bar(slot, B_QFULL));
+                if (a.split) {  // rotated half, then dims [32, 64) of the unrotated row
+                    tma_load_3d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, 0, (int)T.q0, T.bh, bar(slot, B_QFULL));
+                    tma_load_3d(sbase + OFF_Q + slot * Q_BYTES + Q_BYTES / 2, &tm_qh, 32, (int)T.q0, T.bh,
+                                bar(slot, B_QFULL));
+                } else {
+                    tma_load_3d(sbase + OFF_Q + slot * Q_BYTES, &tm_q, 0, (int)T.q0, T.bh, bar(slot, B_QFULL));
+                }
                 bool ok = true;
                 for (int j = 0; j < T.nblk; ++j, ++g) {
                     const int st = g % NS;
@@ -297,6 +306,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     } else {
                         const int key0 = (int)(T.ws + KB * (j - T.nst));
                         tma_load_3d(dk, &tm_k, 0, key0, T.bh, bar(slot, B_KFULL + st));
+                        if (a.split) tma_load_3d(dk + KV_BYTES / 2, &tm_kh, 32, key0, T.bh, bar(slot, B_KFULL + st));
                         tma_load_3d(dv, &tm_v, 0, key0, T.bh, bar(slot, B_VFULL + st));
                     }
                     last_g = g;
@@ -325,6 +335,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
             const uint64_t dk0 = sdesc_sw128(sbase + OFF_K + slot * NS * KV_BYTES, 16, 1024);
             const uint64_t dv0 = sdesc_sw128(sbase + OFF_V + slot * NS * KV_BYTES, KV_BYTES, 1024);
+            // the same tiles as 64-byte-swizzled halves (split Q and window K)
+            const uint64_t dq64 = sdesc_sw64(sQ);
+            const uint64_t dk64 = sdesc_sw64(sbase + OFF_K + slot * NS * KV_BYTES);
             int g = 0;
             bool ok = true;
             KVM_PROBE_DECL(8)
@@ -341,9 +354,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // 32 bytes adds 2 and a stage adds KV_BYTES / 16
                 const uint64_t dk = dk0 + (uint64_t)(st * (KV_BYTES >> 4));
                 const int ks0 = state ? ks_state : 0;
+                if (a.split) {
+                    // 64-byte halves: K-steps 0, 1 in the rotated half, 2, 3 in the other
+                    // (state keys: the 128-byte-swizzled rows of the snapshot, K-steps 2, 3)
+                    const uint64_t dks64 = dk64 + (uint64_t)(st * (KV_BYTES >> 4));
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    if (ks >= ks0) mma_bf16_ss(tS, dq0 + 2 * ks, dk + 2 * ks, idesc_qk, ks > ks0);
+                    for (int ks = 0; ks < 4; ++ks) {
+                        if (ks < ks0) continue;
+                        const uint64_t ad = dq64 + (uint64_t)((ks >> 1) * (Q_BYTES / 2 >> 4) + 2 * (ks & 1));
+                        const uint64_t bd = state ? dk + 2 * ks
+                                                  : dks64 + (uint64_t)((ks >> 1) * (KV_BYTES / 2 >> 4) + 2 * (ks & 1));
+                        mma_bf16_ss(tS, ad, bd, idesc_qk, ks > ks0);
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        if (ks >= ks0) mma_bf16_ss(tS, dq0 + 2 * ks, dk + 2 * ks, idesc_qk, ks > ks0);
+                }
                 mma_commit(bar(slot, B_SFULL));
                 KVM_PROBE_LAP(2)
                 return true;
@@ -626,19 +653,51 @@ bool make_tmap_f32_3d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t 
     return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map over [planes][rows][row_elems] with a 32 x box_rows box, 64-byte swizzle
+// (row_elems 32 or 64; a box of dims [32, 64) starts at x = 32).
+static bool make_tmap_bf16_half(CUtensorMap* m, const void* base, uint64_t row_elems, uint64_t rows,
+                                uint64_t planes, uint32_t box_rows) {
+    using namespace tc;
+    auto enc = get_encode();
+    if (!enc || (row_elems != 32 && row_elems != 64)) return false;
+    cuuint64_t dims[3] = {row_elems, rows, planes};
+    cuuint64_t strides[2] = {row_elems * 2, rows * row_elems * 2};
+    cuuint32_t box[3] = {32, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool attn_tc_supported(const AttnArgs& a, bool bf16) {
     return bf16 && a.C % 128 == 0 && a.N > 0;
 }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     using namespace tc;
-    CUtensorMap mq, mk, mv, msk, msv;
+    CUtensorMap mq, mk, mv, msk, msv, mqh, mkh;
     const uint64_t BH = (uint64_t)a.BH;
     const uint64_t planes_snap = BH * (uint64_t)(a.snap_events > 0 ? a.snap_events : 1);
     // window keys must come rotated at their own positions when the layer has rotary dims
     if (a.r > 0 && !a.k_rot) return cudaErrorInvalidValue;
-    if (!make_tmap_bf16_3d(&mq, a.q_rot ? a.q_rot : a.q, (uint64_t)a.N, BH, 128) || !make_tmap_bf16_3d(&mk, a.k_rot ? a.k_rot : a.k, (uint64_t)a.N, BH, KB) ||
-        !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH, KB) ||
+    // compact rotated rows (r = 32): Q and window-K tiles in two 64-byte halves
+    const bool split = a.rot_compact != 0;
+    if (split && (a.r != 32 || !a.q_rot)) return cudaErrorInvalidValue;
+    bool maps_ok;
+    if (split)
+        maps_ok = make_tmap_bf16_half(&mq, a.q_rot, 32, (uint64_t)a.N, BH, 128) &&
+                  make_tmap_bf16_half(&mqh, a.q, 64, (uint64_t)a.N, BH, 128) &&
+                  make_tmap_bf16_half(&mk, a.k_rot, 32, (uint64_t)a.N, BH, KB) &&
+                  make_tmap_bf16_half(&mkh, a.k, 64, (uint64_t)a.N, BH, KB);
+    else
+        maps_ok = make_tmap_bf16_3d(&mq, a.q_rot ? a.q_rot : a.q, (uint64_t)a.N, BH, 128) &&
+                  make_tmap_bf16_3d(&mk, a.k_rot ? a.k_rot : a.k, (uint64_t)a.N, BH, KB);
+    if (!split) {  // unused by the kernel: any valid map
+        mqh = mq;
+        mkh = mk;
+    }
+    if (!maps_ok || !make_tmap_bf16_3d(&mv, a.v, (uint64_t)a.N, BH, KB) ||
         !make_tmap_bf16_3d(&msk, a.snap_k, (uint64_t)a.M, planes_snap, KB) ||
         !make_tmap_bf16_3d(&msv, a.snap_v, (uint64_t)a.M, planes_snap, KB))
         return cudaErrorInvalidValue;
@@ -665,6 +724,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     t.status = status;
     t.q_prerot = a.q_rot != nullptr || a.r == 0;
     t.lse = a.lse;
+    t.split = split ? 1 : 0;
     static int nsm = 0;
     if (nsm == 0) {
         int dev = 0;
@@ -676,7 +736,7 @@ cudaError_t launch_attn_tc(const AttnArgs& a, int* status, cudaStream_t s) {
     // given, is the number of CTAs for the SM partition the launch runs on
     int grid = a.grid > 0 ? a.grid : nsm;
     if (!a.tile_ctr && grid > (t.ntiles + 1) / 2) grid = (t.ntiles + 1) / 2;
-    attn_tc2_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, msk, msv, t);
+    attn_tc2_kernel<<<grid, NTHREADS, SMEM_BYTES, s>>>(mq, mk, mv, msk, msv, mqh, mkh, t);
     return cudaGetLastError();
 }
 

@@ -154,6 +154,8 @@ struct AttnArgs {
     // Tensor-core path: queries already rotated at their own positions (the same pass),
     // loaded instead of q; nullptr = each tile rotates its queries in the kernel.
     const void* q_rot;
+    // k_rot / q_rot hold only the r rotated dims of each row (RopeKeysArgs::compact)
+    int rot_compact;
     // Tensor-core path, optional: fp32 [BH, N] log2-sum-exp of every query's scaled
     // scores (max + log2 of the sum of 2^(s * scale_log2 - max)), for the backward.
     float* lse;
@@ -172,6 +174,9 @@ struct RopeKeysArgs {
     int64_t N;
     int BH;
     int grid;            // CTAs to launch (a multiple of the SM count of the launch's partition)
+    // compact rows (r == 32): k_rot / q_rot hold only the r rotated dims of each row
+    // ([BH, N, r]); the dims past r are read from k / q themselves
+    int compact;
     // optional window ring fill in the same pass (ring_k == nullptr: none): tokens
     // [first, N) enter the ring at row position mod L with their unrotated key,
     // value, gate and the rotated key (the same values as ring_fill_kernel writes)

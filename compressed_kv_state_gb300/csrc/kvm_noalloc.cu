@@ -239,9 +239,11 @@ extern "C" kvm_status kvm_prefill_noalloc(const kvm_config* cfg_in, const void* 
         ka.N = n_tokens;
         ka.BH = BH;
         ka.grid = 8 * (nsm > 0 ? nsm : 1);
+        ka.compact = c.rope_dims == 32;
         e = kvm::launch_rope_keys(ka, s);
         aa.k_rot = ka.k_rot;
         aa.q_rot = ka.q_rot;
+        aa.rot_compact = ka.compact;
     }
     if (e == cudaSuccess) e = kvm::launch_attn(aa, bf16, s);
     if (e != cudaSuccess) {

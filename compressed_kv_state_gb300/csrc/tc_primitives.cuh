@@ -141,6 +141,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Shared-memory matrix descriptor, 64-byte swizzle, K-major: rows of 64 bytes (32 bf16),
+// 8-row groups 512 bytes apart (tiles 512-byte aligned); swizzle mode 4 = 64B.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(512 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;
+    return d;
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, dense.
 // a_mn / b_mn: operand stored MN-major (1) or K-major (0).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
