@@ -36,6 +36,10 @@ constexpr int TOK = 128;   // token rows of the MMA tile
 constexpr int NT = 512;    // threads: key owner j and value owner 256 + j of every slot j
 constexpr int TMA_T = NT - 1;  // issues the chunk loads and the view stores (a value-side
                                // thread: its warp has slack, thread 0 is on the chain)
+// A value warp, idle once its own slots are done, issues the next event's similarity MMA
+// after the key side's barrier (lane 0), and skips the event's closing barrier: issuing
+// holds the thread while the tensor core takes the MMAs, off every other thread's path.
+constexpr int MMA_W = 14;
 constexpr int ROWB = 128;  // bytes of one 64-dim bf16 row
 constexpr int OFF_UHI = 0;                      // [256][128 B] swizzled (MMA B operand)
 constexpr int OFF_ULO = OFF_UHI + MAXS * ROWB;  // [256][128 B] swizzled
@@ -484,7 +488,6 @@ __global__ void __launch_bounds__(NT, 1)
 
     const uint32_t idesc = idesc_bf16(128, 256, 0, 0);
     int mma_count = 0;
-    bool mma_early = false;  // thread 0: this event's similarity MMA was issued by the previous event
     // S = k (u_hi + u_lo)^T for the 128 chunk keys in buffer b against all 256 slot directions
     auto issue_mma = [&](int b) {
         tc_fence_after();
@@ -529,8 +532,9 @@ __global__ void __launch_bounds__(NT, 1)
         const bool do_mma = n0 > S;
 
         // similarity of the chunk's keys to every slot direction
-        if (tid == 0 && !fail && do_mma && !mma_early) issue_mma(buf);
-        mma_early = false;
+        // the first event of a launch: thread 0 issues its MMA; every later one was issued
+        // at the end of the previous event by the issuer warp
+        if (tid == 0 && !fail && do_mma && it == 0) issue_mma(buf);
         if (tid < C) X.g[tid] = g_here;
         // per-token set-up: two threads per token (warps 8-15), 32 dims each
         if (vside) {
@@ -777,26 +781,26 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                 }
             }
-            if (!vside) {
-                // every direction of this event is written (and fenced by its writer):
-                // thread 0 issues the next event's similarity MMA now, while the value
-                // owners finish
+            if (!vside || warp == MMA_W) {
+                // every direction of this event is written (and fenced by its writer): the
+                // issuer warp (its own read views written and fenced first) issues the next
+                // event's similarity MMA now, while the value owners finish
+                if (warp == MMA_W) fence_proxy_async();
                 KVM_PROBE_LAP(16)
-                asm volatile("bar.sync 1, 256;" ::: "memory");
+                asm volatile("bar.sync 1, 288;" ::: "memory");
                 KVM_PROBE_LAP(17)
-                if (tid == 0 && e + 1 < a.e_end && !X.abort_flag && sc_nx.n0 > S) {
-                    if (mbar_wait(smem_u32(&X.bar_k[buf ^ 1]), ((it + 1) >> 1) & 1, &X.abort_flag, a.status)) {
-                        pend_ld[buf ^ 1] = -1;
+                if (tid == MMA_W * 32 && e + 1 < a.e_end && !X.abort_flag && sc_nx.n0 > S) {
+                    if (mbar_wait(smem_u32(&X.bar_k[buf ^ 1]), ((it + 1) >> 1) & 1, &X.abort_flag, a.status))
                         issue_mma(buf ^ 1);
-                        mma_early = true;
-                    }
                 }
             }
         }
         KVM_PROBE_LAP(6)
         tc_fence_before();
         fence_proxy_async();
-        __syncthreads();
+        // the event's closing barrier: every warp but the issuer (which met the key side
+        // above after its last access of this event's chunk and state rows)
+        if (warp != MMA_W) asm volatile("bar.sync 2, 480;" ::: "memory");
         tc_fence_after();
 
         // chunk e + 2 loads into this event's buffer (its readers passed the barrier
@@ -813,6 +817,9 @@ __global__ void __launch_bounds__(NT, 1)
         n = sc.n_after;
         KVM_PROBE_LAP(7)
     }
+    // the issuer warp left the last event without its closing barrier: every warp is done
+    // with the chunk area (the value sums' staging tiles below) before anyone writes there
+    __syncthreads();
 
     // write the state back for decode, export and later segments: the sums go
     // through swizzled staging tiles (key sums in the direction area, value sums
@@ -860,15 +867,15 @@ __global__ void __launch_bounds__(NT, 1)
         KVM_PROBE_FLUSH(g_probe_fold, 20 * (tid == 0 ? 0 : tid == 255 ? 1 : tid == 256 ? 2 : 3), 20)
     // after an abort: let the copies and MMAs this CTA issued land before its shared
     // and tensor memory are released (each wait bounded; they depend on nothing else)
-    if (X.abort_flag && (tid == 0 || tid == TMA_T)) {
+    if (X.abort_flag && (tid == 0 || tid == TMA_T || tid == MMA_W * 32)) {
         auto drain = [&](uint32_t bar, int parity) {
             if (parity < 0) return;
             const long long t0 = clock64();
             while (!mbar_try(bar, (uint32_t)parity) && clock64() - t0 < (1ll << 28)) {
             }
         };
-        if (tid == 0) {
-            drain(smem_u32(&X.bar_st), pend_st);
+        if (tid == 0 || tid == MMA_W * 32) {
+            if (tid == 0) drain(smem_u32(&X.bar_st), pend_st);
             drain(bar_s, pend_mma);
         } else {
             drain(smem_u32(&X.bar_k[0]), pend_ld[0]);
