@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(NT, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&X.bar_k[i]), 1);
             mbar_init(smem_u32(&X.bar_u[i]), 1);
-            mbar_init(smem_u32(&X.bar_s[i]), 1);
+            mbar_init(smem_u32(&X.bar_s[i]), 2);  // one commit from each issuer
         }
         X.abort_flag = 0;
         fence_barrier_init();
@@ -188,7 +188,13 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_after();
     const uint32_t tmem = X.tmem_slot;
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t idesc = idesc_bf16(128, NB, 0, 0);
+    const uint32_t idesc = idesc_bf16(128, 128, 0, 0);
+    // two threads in different warps issue a block's similarity MMAs, each half of them
+    // (issuing holds the thread about as long as the tensor core takes the MMAs, and the
+    // issuing warp scans only after it): thread 0 takes k = 0, thread ISS2 k = 1
+    constexpr int ISS2 = 256;
+    const bool issuer = tid == 0 || tid == ISS2;
+    const int ik = tid == 0 ? 0 : 1;
     const int q = warp & 3, G = warp >> 2;  // TMEM lane quarter, column group
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     // this thread's token row and the 64 slot columns it scans in a block
@@ -218,16 +224,19 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_3d(sbase + ub * UBUF, &tm_u, 0, blk * NB, bh, bar);
         tma_load_3d(sbase + ub * UBUF + NB * ROWB, &tm_u, 64, blk * NB, bh, bar);
     };
-    // S buffer sb = chunk keys (T tiles) x (u_hi + u_lo) of U buffer ub
-    auto issue_mma = [&](int cb, int ub, int sb) {
+    // S buffer sb = chunk keys (T tiles) x (u_hi + u_lo) of U buffer ub.  Issuer k takes
+    // eight N = 128 MMAs: with one token tile the slot columns [128k, 128k + 128), with two
+    // the token tile k; every accumulator element takes the same K-steps in the same order
+    auto issue_mma = [&](int cb, int ub, int sb, int k) {
         tc_fence_after();
-        for (int t = 0; t < T; ++t)
-            for (int ks = 0; ks < 4; ++ks)
-                for (int pt = 0; pt < 2; ++pt) {
-                    const uint64_t ad = sdesc_sw128(sbase + OFF_K + cb * CHB + t * TILE_BYTES + ks * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(sbase + ub * UBUF + pt * NB * ROWB + ks * 32, 16, 1024);
-                    mma_bf16_ss(tmem + 256 * sb + t * NB, ad, bd, idesc, (ks | pt) ? 1u : 0u);
-                }
+        const int t = T == 1 ? 0 : k, c0 = T == 1 ? 128 * k : 0;
+        for (int ks = 0; ks < 4; ++ks)
+            for (int pt = 0; pt < 2; ++pt) {
+                const uint64_t ad = sdesc_sw128(sbase + OFF_K + cb * CHB + t * TILE_BYTES + ks * 32, 16, 1024);
+                const uint64_t bd =
+                    sdesc_sw128(sbase + ub * UBUF + (pt * NB + c0) * ROWB + ks * 32, 16, 1024);
+                mma_bf16_ss(tmem + 256 * sb + t * NB + c0, ad, bd, idesc, (ks | pt) ? 1u : 0u);
+            }
         mma_commit(smem_u32(&X.bar_s[sb]));
         pend_s[sb] = ph_s[sb] & 1;
     };
@@ -328,9 +337,9 @@ __global__ void __launch_bounds__(NT, 1)
         }
         snapshot();
         // the first block's directions have been loading during the set-up
-        if (tid == 0 && !fail && nb > 0) {
-            if (!wait_bar(&X.bar_u[0], ph_u[0], &pend_u[0])) fail = true;
-            else issue_mma(cb, 0, 0);
+        if (issuer && !fail && nb > 0) {
+            if (!wait_bar(&X.bar_u[0], ph_u[0], tid == 0 ? &pend_u[0] : nullptr)) fail = true;
+            else issue_mma(cb, 0, 0, ik);
         }
         if (__syncthreads_or(fail)) break;
         KVM_PROBE_LAP(1)
@@ -340,11 +349,13 @@ __global__ void __launch_bounds__(NT, 1)
         int barg = -1;
         for (int b = 0; b < nb; ++b) {
             const int sb = b & 1;
-            if (tid == 0 && b + 1 < nb) {
-                if (!wait_bar(&X.bar_u[(b + 1) & 1], ph_u[(b + 1) & 1], &pend_u[(b + 1) & 1])) fail = true;
-                else issue_mma(cb, (b + 1) & 1, (b + 1) & 1);
+            if (issuer && b + 1 < nb) {
+                if (!wait_bar(&X.bar_u[(b + 1) & 1], ph_u[(b + 1) & 1], tid == 0 ? &pend_u[(b + 1) & 1] : nullptr))
+                    fail = true;
+                else
+                    issue_mma(cb, (b + 1) & 1, (b + 1) & 1, ik);
             }
-            const bool ok = wait_bar(&X.bar_s[sb], ph_s[sb], tid == 0 ? &pend_s[sb] : nullptr);
+            const bool ok = wait_bar(&X.bar_s[sb], ph_s[sb], issuer ? &pend_s[sb] : nullptr);
             fail = fail || !ok;
             tc_fence_after();
             // U buffer sb is free once this block's MMA completed
@@ -707,7 +718,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0) KVM_PROBE_FLUSH(g_probe_big, 0, 16)
     // after an abort: let the copies and MMAs this CTA issued land before its shared
     // and tensor memory are released (each wait bounded; they depend on nothing else)
-    if (tid == 0 && X.abort_flag) {
+    if (issuer && X.abort_flag) {
         auto drain = [&](unsigned long long* bar, int parity) {
             if (parity < 0) return;
             const long long t0 = clock64();
@@ -715,9 +726,11 @@ __global__ void __launch_bounds__(NT, 1)
             }
         };
         for (int i = 0; i < 2; ++i) {
-            drain(&X.bar_k[i], pend_k[i]);
-            drain(&X.bar_u[i], pend_u[i]);
-            drain(&X.bar_s[i], pend_s[i]);
+            if (tid == 0) {
+                drain(&X.bar_k[i], pend_k[i]);
+                drain(&X.bar_u[i], pend_u[i]);
+            }
+            drain(&X.bar_s[i], pend_s[i]);  // each issuer: the MMAs it issued
         }
     }
     tc_fence_before();
