@@ -634,7 +634,7 @@ def run_backward(dev, stream, steps):
 
     def step():
         kvm.kvm_prefill_backward(layer.handle, tq, tk, tv, tg, out, tdo, rec, W.N, dq, dk, dv, dg, scratch,
-                                 stream)
+                                 stream, cfg=cfg)
 
     for _ in range(2):
         step()

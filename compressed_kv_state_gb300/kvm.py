@@ -248,9 +248,37 @@ def kvm_backward_scratch_bytes(cfg: kvm_config, n_tokens: int) -> int:
     return n
 
 
+def check_backward_tensors(cfg: kvm_config, q, k, v, gate, out, dout, n_tokens: int, dq, dk, dv, dgate,
+                           scratch) -> None:
+    """Raise ValueError unless the inputs are what check_prefill_tensors wants, dout is
+    shaped like out, dq / dk / dv are contiguous fp32 [B, H, n_tokens, d], dgate contiguous
+    fp32 [B, H, n_tokens] and scratch a contiguous tensor, all on the current CUDA device
+    (the library reads and writes n_tokens rows through these pointers; it checks the
+    scratch size itself)."""
+    import torch
+    check_prefill_tensors(cfg, q, k, v, gate, n_tokens, out)
+    n_tokens = int(n_tokens)
+    io = torch.bfloat16 if cfg.dtype == KVM_BF16 else torch.float32
+    shp = (cfg.batch, cfg.heads, n_tokens, cfg.head_dim)
+    cur = torch.cuda.current_device() if torch.cuda.is_available() else None
+    for name, t, want, dt in (("dout", dout, shp, io), ("dq", dq, shp, torch.float32),
+                              ("dk", dk, shp, torch.float32), ("dv", dv, shp, torch.float32),
+                              ("dgate", dgate, shp[:3], torch.float32), ("scratch", scratch, None, None)):
+        if t is None or not hasattr(t, "data_ptr"):
+            raise ValueError(f"{name} must be a tensor")
+        if not t.is_contiguous() or (want is not None and (tuple(t.shape) != want or t.dtype != dt)):
+            raise ValueError(f"{name}: expected contiguous {dt} {want}, got {t.dtype} {tuple(t.shape)}")
+        if not t.is_cuda or t.device.index != cur:
+            raise ValueError(f"{name} must be on the current CUDA device (cuda:{cur})")
+
+
 def kvm_prefill_backward(layer, q, k, v, gate, out, dout, record: kvm_debug | None, n_tokens: int,
-                         dq, dk, dv, dgate, scratch, stream=None):
-    """Backward of the layer's last prefill at its fold decisions (fp32 gradients)."""
+                         dq, dk, dv, dgate, scratch, stream=None, cfg: kvm_config | None = None):
+    """Backward of the layer's last prefill at its fold decisions (fp32 gradients).  With
+    cfg (the layer's config) every tensor is checked first (check_backward_tensors).  The
+    record's assign / kind arrays must hold [B, H, max_events, chunk] int32 each."""
+    if cfg is not None:
+        check_backward_tensors(cfg, q, k, v, gate, out, dout, n_tokens, dq, dk, dv, dgate, scratch)
     st = lib.kvm_prefill_backward(layer, _ptr(q), _ptr(k), _ptr(v), _ptr(gate), _ptr(out), _ptr(dout),
                                   ctypes.byref(record) if record is not None else None, int(n_tokens),
                                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgate), _ptr(scratch),
@@ -346,7 +374,8 @@ class KvmLayer:
         dq, dk, dv = (torch.empty(shp, dtype=torch.float32, device=dev) for _ in range(3))
         dg = torch.empty(shp[:3], dtype=torch.float32, device=dev)
         scratch = torch.empty(kvm_backward_scratch_bytes(c, N), dtype=torch.uint8, device=dev)
-        kvm_prefill_backward(self.handle, q, k, v, gate, out, dout, record, N, dq, dk, dv, dg, scratch, stream)
+        kvm_prefill_backward(self.handle, q, k, v, gate, out, dout, record, N, dq, dk, dv, dg, scratch, stream,
+                             cfg=c)
         return dq, dk, dv, dg
 
     def decode_step(self, q, k, v, gate, out=None, stream=None):

@@ -205,6 +205,38 @@ def test_noalloc_tensors_are_checked_before_the_library_is_called(kvm, monkeypat
     assert not calls
 
 
+def test_backward_tensors_are_checked_before_the_library_is_called(kvm, monkeypatch):
+    """kvm_prefill_backward's binding (given the layer's config) rejects inputs, output
+    gradients or scratch of the wrong shape, type, layout or device with ValueError
+    before calling the library."""
+    import torch
+    calls = []
+    monkeypatch.setattr(kvm, "lib", type("L", (), {"kvm_prefill_backward": lambda *a: calls.append(a) or 0})())
+    cfg = kvm.make_config(batch=1, heads=2, chunk=64, window=128, max_slots=24, max_tokens=300)
+    shp = (1, 2, 300, 64)
+    q, k, v, out, dout = (torch.zeros(shp, dtype=torch.bfloat16) for _ in range(5))
+    g = torch.zeros(shp[:3])
+    dq, dk, dv = (torch.zeros(shp) for _ in range(3))
+    dg = torch.zeros(shp[:3])
+    scratch = torch.zeros(1024, dtype=torch.uint8)
+    cases = [
+        dict(dout=torch.zeros(1, 2, 299, 64, dtype=torch.bfloat16)),     # dout shape
+        dict(dq=torch.zeros(shp, dtype=torch.bfloat16)),                 # gradient not fp32
+        dict(dk=torch.zeros(1, 2, 64, 300).transpose(2, 3)),             # strided
+        dict(dgate=torch.zeros(1, 2, 301)),                              # dgate shape
+        dict(q=torch.zeros(1, 2, 300, 32, dtype=torch.bfloat16)),        # input shape
+        dict(n_tokens=301),                                              # beyond the tensors
+        dict(),                                                          # CPU tensors
+    ]
+    for bad in cases:
+        a = dict(q=q, k=k, v=v, gate=g, out=out, dout=dout, n_tokens=300, dq=dq, dk=dk, dv=dv, dgate=dg)
+        a.update(bad)
+        with pytest.raises(ValueError):
+            kvm.kvm_prefill_backward(None, a["q"], a["k"], a["v"], a["gate"], a["out"], a["dout"], None,
+                                     a["n_tokens"], a["dq"], a["dk"], a["dv"], a["dgate"], scratch, cfg=cfg)
+    assert not calls
+
+
 def test_binding_fails_loudly_without_the_library(tmp_path):
     """No fallback: importing the binding without libkvm.so raises (run in a fresh
     interpreter against a copy of the package whose library is absent)."""
