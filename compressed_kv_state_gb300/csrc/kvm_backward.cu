@@ -667,11 +667,12 @@ __global__ void __launch_bounds__(256, 1) bwd_tile(BackwardArgs a) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (i0 + i >= kv) continue;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                atomicAdd(gk + (int64_t)(i0 + i) * D + j0 + j, dk[i][j] * a.inv_sqrt_d);
-                atomicAdd(gv + (int64_t)(i0 + i) * D + j0 + j, dv[i][j]);
-            }
+            // four consecutive dims per vector atomic (16-byte aligned: j0 is a multiple of 4)
+            const float s = a.inv_sqrt_d;
+            atomicAdd(reinterpret_cast<float4*>(gk + (int64_t)(i0 + i) * D + j0),
+                      make_float4(dk[i][0] * s, dk[i][1] * s, dk[i][2] * s, dk[i][3] * s));
+            atomicAdd(reinterpret_cast<float4*>(gv + (int64_t)(i0 + i) * D + j0),
+                      make_float4(dv[i][0], dv[i][1], dv[i][2], dv[i][3]));
         }
     }
     // dq: scaled, then rotated back (pairs across threads: through shared memory)
@@ -1004,10 +1005,11 @@ __global__ void __launch_bounds__(128) bwd_tile_tc(BackwardArgs a) {
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const int dd0 = nt * 8 + 2 * t4;
-                atomicAdd(gk + (int64_t)kj * D + dd0, dk[nt][2 * h] * a.inv_sqrt_d);
-                atomicAdd(gk + (int64_t)kj * D + dd0 + 1, dk[nt][2 * h + 1] * a.inv_sqrt_d);
-                atomicAdd(gv + (int64_t)kj * D + dd0, dv[nt][2 * h]);
-                atomicAdd(gv + (int64_t)kj * D + dd0 + 1, dv[nt][2 * h + 1]);
+                // two consecutive dims per vector atomic (8-byte aligned: dd0 is even)
+                atomicAdd(reinterpret_cast<float2*>(gk + (int64_t)kj * D + dd0),
+                          make_float2(dk[nt][2 * h] * a.inv_sqrt_d, dk[nt][2 * h + 1] * a.inv_sqrt_d));
+                atomicAdd(reinterpret_cast<float2*>(gv + (int64_t)kj * D + dd0),
+                          make_float2(dv[nt][2 * h], dv[nt][2 * h + 1]));
             }
         }
     }
