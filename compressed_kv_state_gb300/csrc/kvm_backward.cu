@@ -1079,10 +1079,14 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
             attr = true;
         }
         const int tiles = (int)((a.N + TQ - 1) / TQ);
-        if (sizeof(T) == 2)
+        if (sizeof(T) == 2 && bwd_tc5_supported(a, true)) {
+            e = launch_bwd_tc5(a, s);
+            if (e != cudaSuccess) return e;
+        } else if (sizeof(T) == 2) {
             bwd_tile_tc<<<(unsigned)(a.BH * tiles), 128, MTILE_SMEM, s>>>(a);
-        else
+        } else {
             bwd_tile<T><<<(unsigned)(a.BH * tiles), 256, TILE_SMEM, s>>>(a);
+        }
         if (a.r > 0) bwd_unrotate_dk<<<2048, 256, 0, s>>>(a);
     } else {
         bwd_stats<T><<<gq, BW_THREADS, 0, s>>>(a);

@@ -249,6 +249,10 @@ struct BackwardArgs {
     int* status;          // a record entry outside [0, M) or of no known kind latches STATUS_DEVICE
 };
 cudaError_t launch_backward(const BackwardArgs& a, bool bf16, cudaStream_t s);
+// The five products on tcgen05 (bf16, chunks a multiple of 128, the forward's
+// log2-sum-exp kept); the caller zeroes the gradient accumulators first.
+bool bwd_tc5_supported(const BackwardArgs& a, bool bf16);
+cudaError_t launch_bwd_tc5(const BackwardArgs& a, cudaStream_t s);
 
 struct DecodeArgs {
     const void* q;
