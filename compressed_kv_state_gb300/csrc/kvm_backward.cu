@@ -1069,8 +1069,10 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
         if (e == cudaSuccess) e = cudaMemsetAsync(a.dv, 0, (size_t)rows * D * sizeof(float), s);
         if (e == cudaSuccess) e = cudaMemsetAsync(a.dg, 0, (size_t)rows * sizeof(float), s);
         const size_t rs = (size_t)a.BH * a.E * a.M * D * sizeof(float);
-        if (e == cudaSuccess && a.E > 0) e = cudaMemsetAsync(a.dks, 0, rs, s);
-        if (e == cudaSuccess && a.E > 0) e = cudaMemsetAsync(a.dvs, 0, rs, s);
+        const bool tc5 = sizeof(T) == 2 && bwd_tc5_supported(a, true);
+        const bool zero_rows = !(tc5 && bwd_tc5_owns_read_rows(a));
+        if (e == cudaSuccess && a.E > 0 && zero_rows) e = cudaMemsetAsync(a.dks, 0, rs, s);
+        if (e == cudaSuccess && a.E > 0 && zero_rows) e = cudaMemsetAsync(a.dvs, 0, rs, s);
         if (e != cudaSuccess) return e;
         static bool attr = false;
         if (!attr) {
@@ -1079,7 +1081,7 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
             attr = true;
         }
         const int tiles = (int)((a.N + TQ - 1) / TQ);
-        if (sizeof(T) == 2 && bwd_tc5_supported(a, true)) {
+        if (tc5) {
             e = launch_bwd_tc5(a, s);
             if (e != cudaSuccess) return e;
         } else if (sizeof(T) == 2) {

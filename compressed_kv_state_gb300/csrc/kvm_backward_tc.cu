@@ -258,14 +258,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             tmem_wait_ld();
             if (rr < kv) {
                 const float sc = a.inv_sqrt_d;
+                // a read row of the state is this tile's alone when the chunk is one tile
+                // (plain stores; the rows were not zeroed); window keys take the sums of
+                // every tile that sees them
+                const bool own = !win && a.C == TQ;
 #pragma unroll
                 for (int q4 = 0; q4 < 8; ++q4) {
-                    atomicAdd(reinterpret_cast<float4*>(gk + 4 * q4),
-                              make_float4(__uint_as_float(x[4 * q4]) * sc, __uint_as_float(x[4 * q4 + 1]) * sc,
-                                          __uint_as_float(x[4 * q4 + 2]) * sc, __uint_as_float(x[4 * q4 + 3]) * sc));
-                    atomicAdd(reinterpret_cast<float4*>(gv + 4 * q4),
-                              make_float4(__uint_as_float(y[4 * q4]), __uint_as_float(y[4 * q4 + 1]),
-                                          __uint_as_float(y[4 * q4 + 2]), __uint_as_float(y[4 * q4 + 3])));
+                    const float4 kx = make_float4(__uint_as_float(x[4 * q4]) * sc, __uint_as_float(x[4 * q4 + 1]) * sc,
+                                                  __uint_as_float(x[4 * q4 + 2]) * sc, __uint_as_float(x[4 * q4 + 3]) * sc);
+                    const float4 vy = make_float4(__uint_as_float(y[4 * q4]), __uint_as_float(y[4 * q4 + 1]),
+                                                  __uint_as_float(y[4 * q4 + 2]), __uint_as_float(y[4 * q4 + 3]));
+                    if (own) {
+                        reinterpret_cast<float4*>(gk)[q4] = kx;
+                        reinterpret_cast<float4*>(gv)[q4] = vy;
+                    } else {
+                        atomicAdd(reinterpret_cast<float4*>(gk + 4 * q4), kx);
+                        atomicAdd(reinterpret_cast<float4*>(gv + 4 * q4), vy);
+                    }
                 }
             }
         };
@@ -377,6 +386,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 }  // namespace bwt
+
+// The read rows' gradients need no zeroing when the chunk is exactly one 128-query tile:
+// the tile of chunk e + W/C + 1 stores every row of event e below its slot count, the rows
+// the slot sweep reads.
+bool bwd_tc5_owns_read_rows(const BackwardArgs& a) { return a.C == bwt::TQ; }
 
 bool bwd_tc5_supported(const BackwardArgs& a, bool bf16) {
     return bf16 && a.C % 128 == 0 && a.lse_fwd != nullptr && a.N > 0 && (a.r % 2) == 0;

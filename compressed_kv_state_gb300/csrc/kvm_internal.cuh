@@ -252,6 +252,7 @@ cudaError_t launch_backward(const BackwardArgs& a, bool bf16, cudaStream_t s);
 // The five products on tcgen05 (bf16, chunks a multiple of 128, the forward's
 // log2-sum-exp kept); the caller zeroes the gradient accumulators first.
 bool bwd_tc5_supported(const BackwardArgs& a, bool bf16);
+bool bwd_tc5_owns_read_rows(const BackwardArgs& a);  // it stores (not adds) the read rows' gradients
 cudaError_t launch_bwd_tc5(const BackwardArgs& a, cudaStream_t s);
 
 struct DecodeArgs {
