@@ -11,11 +11,12 @@
 // gate-weighted member sums (Core mechanism 2) and the founders' read radius
 // rho = |v| (Core mechanism 3).
 //
-// Chunks a multiple of 64 take the tiled path (bwd_tile below: 64-query tiles, 64-key
-// blocks in shared memory, the five products as small fp32 multiplies); the kernels
-// listed here serve the other chunk sizes, and bwd_rotate and bwd_sweep serve both
-// (fp32 arithmetic, inputs in the layer's dtype; one warp per query, key or state row,
-// lanes over the 64 dims, two each):
+// Chunks a multiple of 64 take a tiled path for the five attention products: on tcgen05
+// (kvm_backward_tc.cu) for bf16 layers with chunks a multiple of 128 whose forward kept
+// its log2-sum-exp; otherwise bwd_tile_tc (mma.sync, bf16) or bwd_tile (fp32 FMA), with
+// 64-query tiles and 64-key blocks in shared memory.  The row kernels below serve the
+// other chunk sizes (one warp per query, key or state row, lanes over the 64 dims, two
+// each).  bwd_rotate, bwd_members and bwd_sweep16 serve every path:
 //   bwd_rotate   q and k rotated at their own positions (scratch)
 //   bwd_stats    per query: log2-sum-exp of its scores and D = dout . out
 //   bwd_dq       per query: dq (state part in plain coordinates, window part
@@ -24,12 +25,12 @@
 //                window holds it; dgate = 0
 //   bwd_dstate   per fold event and slot: the gradient of the event's read
 //                rows (key and value) from the chunk that reads them
-//   bwd_sweep    per (batch, head) row, one CTA: replays the fold with the
-//                recorded decisions (the forward's fp32 sums, in its order),
-//                turns each event's read-row gradients into sum and radius
-//                gradients (LayerNorm and normalisation backward), and sums
-//                them from the last event back to each token's own event,
-//                adding the tokens' k, v and gate gradients.
+//   bwd_members  per (batch, head) row: every slot's member tokens in replay order
+//   bwd_sweep16  per slot, half a warp: replays the slot with the recorded decisions
+//                (the forward's fp32 sums, in its order), turns each event's read-row
+//                gradients into sum and radius gradients (LayerNorm and normalisation
+//                backward), and sums them from the last event back to each member's
+//                own event, adding the tokens' k, v and gate gradients.
 #include "kvm_internal.cuh"
 
 namespace kvm {
@@ -324,20 +325,42 @@ __global__ void __launch_bounds__(MB_THREADS) bwd_members(BackwardArgs a) {
     }
 }
 
-// Per slot, one warp (lanes over the dims, two each): every slot's history is its own,
-// so the rows' slots run in parallel.  Pass 1 replays the slot through the events with
-// the recorded decisions (its member list: the founder first, then its merged tokens in
-// position order: the forward's fp32 sums) and turns each event's read-row gradients of
-// the slot into sum and radius gradients (LayerNorm and normalisation backward), in
-// place.  Pass 2 runs the events backwards, summing those gradients, and each of the
-// slot's tokens reads the sum at its own event (the gradients of every state that holds it).
+// Per slot (every slot's history is its own, so the rows' slots run in parallel): pass 1
+// replays the slot through the events with the recorded decisions (its member list: the
+// founder first, then its merged tokens in position order: the forward's fp32 sums) and
+// turns each event's read-row gradients of the slot into sum and radius gradients
+// (LayerNorm and normalisation backward), in place.  Pass 2 runs the events backwards,
+// summing those gradients, and each of the slot's tokens reads the sum at its own event
+// (the gradients of every state that holds it).
+// Half a warp per slot (two slots a warp; lanes over the dims, four each): the reductions
+// take four shuffle levels and each instruction serves two slots.  Every shuffle names only its own half's lanes, which follow their
+// slot's control flow together.
+template <typename T> __device__ __forceinline__ float4 ld4(const T* p);
+template <> __device__ __forceinline__ float4 ld4<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <> __device__ __forceinline__ float4 ld4<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+__device__ __forceinline__ float dot4(float4 a, float4 b) { return (a.x * b.x + a.y * b.y) + (a.z * b.z + a.w * b.w); }
+__device__ __forceinline__ float sum4(float4 a) { return (a.x + a.y) + (a.z + a.w); }
+__device__ __forceinline__ float half_sum(float v, unsigned hm) {
+#pragma unroll
+    for (int k = 8; k >= 1; k >>= 1) v += __shfl_xor_sync(hm, v, k);
+    return v;
+}
+
 template <typename T>
-__global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (w >= (int64_t)a.BH * a.M) return;
-    const int bh = (int)(w / a.M);
-    const int j = (int)(w % a.M);
+__global__ void __launch_bounds__(BW_THREADS) bwd_sweep16(BackwardArgs a) {
+    const int lane = threadIdx.x & 31, hl = lane & 15, hf = lane >> 4;
+    const unsigned hm = 0xFFFFu << (16 * hf);
+    const int64_t sid = 2 * (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) + hf;
+    if (sid >= (int64_t)a.BH * a.M) return;
+    const int bh = (int)(sid / a.M);
+    const int j = (int)(sid % a.M);
     const int C = a.C, M = a.M, r = a.r;
     const int64_t row = (int64_t)bh * a.N;
     const T* kk = reinterpret_cast<const T*>(a.k) + row * D;
@@ -346,17 +369,17 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
     if (a.E == 0 || j >= a.sched[a.E - 1].n_after) return;  // slot never founded
     const int* lst = a.mem + (int64_t)bh * a.E * C;
     const int m0 = a.moff[(int64_t)bh * (M + 1) + j], m1 = a.moff[(int64_t)bh * (M + 1) + j + 1];
-    // the member list through a window of 32 entries in the lanes' registers (p is the
-    // same in every lane): a window starts at p going forwards, ends at p going backwards
+    const int d0 = 4 * hl;  // this lane's dims d0 .. d0 + 3
+    // the member list through a window of 16 entries in the half's registers
     int wbase = -64, wbuf = 0;
     auto member = [&](int p, bool fwd) -> int {
-        if (p < wbase || p >= wbase + 32) {
-            wbase = fwd ? p : max(m0, p - 31);
-            wbuf = wbase + lane < m1 ? lst[wbase + lane] : 0;
+        if (p < wbase || p >= wbase + 16) {
+            wbase = fwd ? p : max(m0, p - 15);
+            wbuf = wbase + hl < m1 ? lst[wbase + hl] : 0;
         }
-        return __shfl_sync(0xffffffffu, wbuf, p - wbase);
+        return __shfl_sync(hm, wbuf, p - wbase, 16);
     };
-    float2 sk = make_float2(0.f, 0.f), sv = sk;
+    float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
     int cnt = 0;
     float rho = 0.0f;
     // pass 1
@@ -371,62 +394,68 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
             if (t >= tend) break;  // a member of a later event
             ++ptr;
             const float gt = gg[t];
-            const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
+            const float4 kx = ld4<T>(kk + t * D + d0), vx = ld4<T>(vv + t * D + d0);
             if ((ent & 3) != 0) {  // the founder sets the slot
-                sk = make_float2(gt * kx.x, gt * kx.y);
-                sv = make_float2(gt * vx.x, gt * vx.y);
+                sk = make_float4(gt * kx.x, gt * kx.y, gt * kx.z, gt * kx.w);
+                sv = make_float4(gt * vx.x, gt * vx.y, gt * vx.z, gt * vx.w);
                 cnt = 1;
-                rho = sqrtf(warp_sum(dot2(vx, vx)));
+                rho = sqrtf(half_sum(dot4(vx, vx), hm));
             } else {
-                sk = make_float2(fmaf(gt, kx.x, sk.x), fmaf(gt, kx.y, sk.y));
-                sv = make_float2(fmaf(gt, vx.x, sv.x), fmaf(gt, vx.y, sv.y));
+                sk = make_float4(fmaf(gt, kx.x, sk.x), fmaf(gt, kx.y, sk.y), fmaf(gt, kx.z, sk.z), fmaf(gt, kx.w, sk.w));
+                sv = make_float4(fmaf(gt, vx.x, sv.x), fmaf(gt, vx.y, sv.y), fmaf(gt, vx.z, sv.z), fmaf(gt, vx.w, sv.w));
                 ++cnt;
             }
         }
         // read-row gradients -> sum and radius gradients of the state after event e
-        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D;
+        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D + d0;
         const float cn = (float)(cnt > 0 ? cnt : 1);
-        const float2 x = make_float2(sk.x / cn, sk.y / cn);
-        const float mu = warp_sum(x.x + x.y) * (1.0f / D);
-        const float2 xc = make_float2(x.x - mu, x.y - mu);
-        const float var = warp_sum(dot2(xc, xc)) * (1.0f / D);
+        const float4 x = make_float4(sk.x / cn, sk.y / cn, sk.z / cn, sk.w / cn);
+        const float mu = half_sum(sum4(x), hm) * (1.0f / D);
+        const float4 xc = make_float4(x.x - mu, x.y - mu, x.z - mu, x.w - mu);
+        const float var = half_sum(dot4(xc, xc), hm) * (1.0f / D);
         const float isd = 1.0f / sqrtf(var + a.ln_eps);
-        const float2 xh = make_float2(xc.x * isd, xc.y * isd);
-        float2 gkh = reinterpret_cast<const float2*>(a.dks + o)[lane];
-        if (2 * lane < r) gkh.x = 0.0f;  // the rotary dims of the read key are constant zeros
-        if (2 * lane + 1 < r) gkh.y = 0.0f;
-        const float mg = warp_sum(gkh.x + gkh.y) * (1.0f / D);
-        const float mgx = warp_sum(dot2(gkh, xh)) * (1.0f / D);
-        const float2 dsk = make_float2((gkh.x - mg - xh.x * mgx) * isd / cn, (gkh.y - mg - xh.y * mgx) * isd / cn);
-        const float2 gvh = reinterpret_cast<const float2*>(a.dvs + o)[lane];
-        float2 dsv;
+        const float4 xh = make_float4(xc.x * isd, xc.y * isd, xc.z * isd, xc.w * isd);
+        float4 gkh = *reinterpret_cast<const float4*>(a.dks + o);
+        // the rotary dims of the read key are constant zeros
+        if (d0 < r) gkh.x = 0.0f;
+        if (d0 + 1 < r) gkh.y = 0.0f;
+        if (d0 + 2 < r) gkh.z = 0.0f;
+        if (d0 + 3 < r) gkh.w = 0.0f;
+        const float mg = half_sum(sum4(gkh), hm) * (1.0f / D);
+        const float mgx = half_sum(dot4(gkh, xh), hm) * (1.0f / D);
+        const float f = isd / cn;
+        const float4 dsk = make_float4((gkh.x - mg - xh.x * mgx) * f, (gkh.y - mg - xh.y * mgx) * f,
+                                       (gkh.z - mg - xh.z * mgx) * f, (gkh.w - mg - xh.w * mgx) * f);
+        const float4 gvh = *reinterpret_cast<const float4*>(a.dvs + o);
+        float4 dsv;
         float dr = 0.0f;
         if (a.no_vnorm) {
-            dsv = make_float2(gvh.x / cn, gvh.y / cn);
+            dsv = make_float4(gvh.x / cn, gvh.y / cn, gvh.z / cn, gvh.w / cn);
         } else {
-            const float nv = sqrtf(warp_sum(dot2(sv, sv)));
+            const float nv = sqrtf(half_sum(dot4(sv, sv), hm));
             const float inv = nv > 0.0f ? 1.0f / nv : 0.0f;
-            const float2 u = make_float2(sv.x * inv, sv.y * inv);
-            dr = warp_sum(dot2(u, gvh));
-            const float f = rho * inv;
-            dsv = make_float2(f * (gvh.x - u.x * dr), f * (gvh.y - u.y * dr));
+            const float4 u = make_float4(sv.x * inv, sv.y * inv, sv.z * inv, sv.w * inv);
+            dr = half_sum(dot4(u, gvh), hm);
+            const float fr = rho * inv;
+            dsv = make_float4(fr * (gvh.x - u.x * dr), fr * (gvh.y - u.y * dr), fr * (gvh.z - u.z * dr),
+                              fr * (gvh.w - u.w * dr));
         }
-        reinterpret_cast<float2*>(a.dks + o)[lane] = dsk;
-        reinterpret_cast<float2*>(a.dvs + o)[lane] = dsv;
-        if (lane == 0) a.drho[((int64_t)bh * a.E + e) * M + j] = dr;
+        *reinterpret_cast<float4*>(a.dks + o) = dsk;
+        *reinterpret_cast<float4*>(a.dvs + o) = dsv;
+        if (hl == 0) a.drho[((int64_t)bh * a.E + e) * M + j] = dr;
     }
     // pass 2: the members from the last backwards
-    float2 Gk = make_float2(0.f, 0.f), Gv = Gk;
+    float4 Gk = make_float4(0.f, 0.f, 0.f, 0.f), Gv = Gk;
     float Gr = 0.0f;
     ptr = m1 - 1;
     for (int e = a.E - 1; e >= 0; --e) {
         const int n = a.sched[e].n_after;
         if (j >= n) continue;
-        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D;
-        const float2 dk = reinterpret_cast<const float2*>(a.dks + o)[lane];
-        const float2 dv = reinterpret_cast<const float2*>(a.dvs + o)[lane];
-        Gk = make_float2(Gk.x + dk.x, Gk.y + dk.y);
-        Gv = make_float2(Gv.x + dv.x, Gv.y + dv.y);
+        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D + d0;
+        const float4 dk = *reinterpret_cast<const float4*>(a.dks + o);
+        const float4 dv = *reinterpret_cast<const float4*>(a.dvs + o);
+        Gk = make_float4(Gk.x + dk.x, Gk.y + dk.y, Gk.z + dk.z, Gk.w + dk.w);
+        Gv = make_float4(Gv.x + dv.x, Gv.y + dv.y, Gv.z + dv.z, Gv.w + dv.w);
         Gr += a.drho[((int64_t)bh * a.E + e) * M + j];
         const int64_t tbeg = (int64_t)e * C;
         while (ptr >= m0) {
@@ -435,24 +464,21 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep(BackwardArgs a) {
             if (t < tbeg) break;  // a member of an earlier event
             --ptr;
             const float gt = gg[t];
-            const float2 kx = ld2<T>(kk + t * D + 2 * lane), vx = ld2<T>(vv + t * D + 2 * lane);
-            float2* dkp = reinterpret_cast<float2*>(a.dk + (row + t) * D) + lane;
-            float2* dvp = reinterpret_cast<float2*>(a.dv + (row + t) * D) + lane;
-            float2 dkt = *dkp, dvt = *dvp;
-            dkt.x = fmaf(gt, Gk.x, dkt.x);
-            dkt.y = fmaf(gt, Gk.y, dkt.y);
-            dvt.x = fmaf(gt, Gv.x, dvt.x);
-            dvt.y = fmaf(gt, Gv.y, dvt.y);
+            const float4 kx = ld4<T>(kk + t * D + d0), vx = ld4<T>(vv + t * D + d0);
+            float4* dkp = reinterpret_cast<float4*>(a.dk + (row + t) * D + d0);
+            float4* dvp = reinterpret_cast<float4*>(a.dv + (row + t) * D + d0);
+            float4 dkt = *dkp, dvt = *dvp;
+            dkt = make_float4(fmaf(gt, Gk.x, dkt.x), fmaf(gt, Gk.y, dkt.y), fmaf(gt, Gk.z, dkt.z), fmaf(gt, Gk.w, dkt.w));
+            dvt = make_float4(fmaf(gt, Gv.x, dvt.x), fmaf(gt, Gv.y, dvt.y), fmaf(gt, Gv.z, dvt.z), fmaf(gt, Gv.w, dvt.w));
             if ((ent & 3) != 0) {  // founder: rho = |v|
-                const float nv = sqrtf(warp_sum(dot2(vx, vx)));
-                const float f = nv > 0.0f ? Gr / nv : 0.0f;
-                dvt.x = fmaf(f, vx.x, dvt.x);
-                dvt.y = fmaf(f, vx.y, dvt.y);
+                const float nv = sqrtf(half_sum(dot4(vx, vx), hm));
+                const float fr = nv > 0.0f ? Gr / nv : 0.0f;
+                dvt = make_float4(fmaf(fr, vx.x, dvt.x), fmaf(fr, vx.y, dvt.y), fmaf(fr, vx.z, dvt.z), fmaf(fr, vx.w, dvt.w));
             }
             *dkp = dkt;
             *dvp = dvt;
-            const float dgt = warp_sum(dot2(kx, Gk) + dot2(vx, Gv));
-            if (lane == 0) a.dg[row + t] += dgt;
+            const float dgt = half_sum(dot4(kx, Gk) + dot4(vx, Gv), hm);
+            if (hl == 0) a.dg[row + t] += dgt;
         }
     }
 }
@@ -1102,7 +1128,8 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
     if (a.E > 0) {
         const int64_t slots = (int64_t)a.BH * a.M;
         bwd_members<<<(unsigned)a.BH, MB_THREADS, (size_t)(a.M + 1) * sizeof(int), s>>>(a);
-        bwd_sweep<T><<<(unsigned)((slots + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
+        // two slots a warp
+        bwd_sweep16<T><<<(unsigned)(((slots + 1) / 2 + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
     }
     return cudaGetLastError();
 }
