@@ -652,8 +652,9 @@ def run_backward(dev, stream, steps):
     flops = 2.5 * aw["flops_4d"]  # five products of 2d per (query, key) pair against two forward
     tf = flops / (ms / 1e3) / 1e12
     layer.close()
-    # bf16 layers run the five products on the tensor cores (mma.sync bf16, fp32 accumulate):
-    # the roofline is the measured bf16 burst rate (the backward is timed alone)
+    # bf16 layers run the five products on the tensor cores (tcgen05 for chunks a multiple
+    # of 128, fp32 accumulators in tensor memory): the roofline is the measured bf16 burst
+    # rate (the backward is timed alone)
     pk = _peaks()
     peak = pk["bf16"]
     return {"ms_per_call": ms, "steps": steps, "value": W.B * W.N / (ms / 1e3), "unit": "tokens/s",
@@ -664,9 +665,10 @@ def run_backward(dev, stream, steps):
             "finite": bool(torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
                            and torch.isfinite(dg).all()),
             "note": "fold decisions from the forward's record are constants (no gradient through the "
-                    "winner-take-all assignment); 64-query x 64-key tiles in shared memory, the five "
-                    "products on the tensor cores (mma.sync m16n8k16 bf16, fp32 accumulate), "
-                    "fp32 softmax and read-row gradients, one warp per slot for the state sweep"}
+                    "winner-take-all assignment); 128-query tiles, 128-key blocks by TMA, the five "
+                    "products on tcgen05 (fp32 accumulators in tensor memory; P and dS as bf16), "
+                    "fp32 softmax-gradient and read-row gradients, half a warp per slot for the "
+                    "state sweep"}
 
 
 def fp32_simt_peak_tflops():
