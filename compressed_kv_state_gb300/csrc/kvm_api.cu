@@ -512,10 +512,19 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
             int64_t t = (e_done + Wc + 1) * tpc;
             return (int)((t < tph ? t : tph) * BH);
         };
+        // segment boundaries (events): equal parts, except that with two segments the first
+        // ends at 40% of the events — the attention partition's own work before the first
+        // segment's chunks (the rotation, the chunks that need no fold) ends well before the
+        // chain's middle, and a shorter first segment hands it those chunks sooner
+        // (measured on the fixed 8k workload: 0.573 -> 0.561 ms a step)
+        auto bnd = [&](int sg) -> int64_t {
+            if (segs == 2 && sg == 1) return E * 2 / 5 > 0 ? E * 2 / 5 : 1;
+            return E * sg / segs;
+        };
         // range 0: chunks that need no fold; range k + 1: the chunks segment k makes ready
         aa.n_ranges = segs + 1;
         aa.range_end[0] = ready(0);
-        for (int sg = 0; sg < segs; ++sg) aa.range_end[sg + 1] = ready(E * (sg + 1) / segs);
+        for (int sg = 0; sg < segs; ++sg) aa.range_end[sg + 1] = ready(bnd(sg + 1));
         e = cudaMemsetAsync(ctr, 0, sizeof(int) * aa.n_ranges, s);
         if (e == cudaSuccess) e = cudaEventRecord(P.ev_fork, s);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(P.s_fold, P.ev_fork, 0);
@@ -541,8 +550,8 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         ly->kernels += 1;
         e = timed(ly, PH_FOLD, P.s_fold, [&] {
             for (int sg = 0; sg < segs; ++sg) {
-                fa.e_begin = (int)(E * sg / segs);
-                fa.e_end = (int)(E * (sg + 1) / segs);
+                fa.e_begin = (int)bnd(sg);
+                fa.e_end = (int)bnd(sg + 1);
                 cudaError_t r = kvm::launch_fold(fa, bf16, P.s_fold);
                 if (r == cudaSuccess) r = cudaEventRecord(P.ev_seg[sg], P.s_fold);
                 if (r != cudaSuccess) return r;
@@ -573,7 +582,7 @@ kvm_status kvm_prefill(kvm_layer* ly, const void* q, const void* k, const void* 
         // the row log, once the last snapshots are rebuilt)
         e = cudaStreamWaitEvent(s, P.ev_seg[segs - 1], 0);
         if (e == cudaSuccess && L.logs) {
-            rb.e_begin = (int)(E * (segs - 1) / segs);
+            rb.e_begin = (int)bnd(segs - 1);
             rb.e_end = (int)E;
             // it reads the previous segment's last snapshot, rebuilt on the attention's SMs
             if (segs > 1) e = cudaStreamWaitEvent(s, P.ev_rebuilt, 0);
