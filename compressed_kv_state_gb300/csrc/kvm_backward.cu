@@ -72,6 +72,45 @@ template <typename T>
 __global__ void bwd_rotate(BackwardArgs a) {
     const int64_t rows = (int64_t)a.BH * a.N;
     const int half = a.r / 2;
+    if constexpr (sizeof(T) == 2) {
+        if ((half & 7) == 0) {
+            // one thread per 16-byte piece (8 dims) of a row, with its rotate-half partner
+            const int hc = half >> 3;
+            const uint4* qs = reinterpret_cast<const uint4*>(a.q);
+            const uint4* ks = reinterpret_cast<const uint4*>(a.k);
+            uint4* qd = reinterpret_cast<uint4*>(a.qr);
+            uint4* kd = reinterpret_cast<uint4*>(a.kr);
+            for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows * 8;
+                 i += (int64_t)gridDim.x * blockDim.x) {
+                const int64_t rw = i >> 3;
+                const int c = (int)(i & 7);
+                uint4 wq = qs[i], wk = ks[i];
+                if (8 * c < a.r) {
+                    const bool low = c < hc;
+                    const int64_t pi = rw * 8 + (low ? c + hc : c - hc);
+                    const uint4 oq = qs[pi], ok = ks[pi];
+                    const float2* tab = a.rope + (rw % a.N) * half + (low ? c : c - hc) * 8;
+                    __nv_bfloat162* mq = reinterpret_cast<__nv_bfloat162*>(&wq);
+                    __nv_bfloat162* mk = reinterpret_cast<__nv_bfloat162*>(&wk);
+                    const __nv_bfloat162* pq = reinterpret_cast<const __nv_bfloat162*>(&oq);
+                    const __nv_bfloat162* pk = reinterpret_cast<const __nv_bfloat162*>(&ok);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 c0 = tab[2 * u], c1 = tab[2 * u + 1];
+                        const float2 a2 = __bfloat1622float2(mq[u]), b2 = __bfloat1622float2(pq[u]);
+                        const float2 e2 = __bfloat1622float2(mk[u]), f2 = __bfloat1622float2(pk[u]);
+                        mq[u] = low ? __floats2bfloat162_rn(a2.x * c0.x - b2.x * c0.y, a2.y * c1.x - b2.y * c1.y)
+                                    : __floats2bfloat162_rn(a2.x * c0.x + b2.x * c0.y, a2.y * c1.x + b2.y * c1.y);
+                        mk[u] = low ? __floats2bfloat162_rn(e2.x * c0.x - f2.x * c0.y, e2.y * c1.x - f2.y * c1.y)
+                                    : __floats2bfloat162_rn(e2.x * c0.x + f2.x * c0.y, e2.y * c1.x + f2.y * c1.y);
+                    }
+                }
+                qd[i] = wq;
+                kd[i] = wk;
+            }
+            return;
+        }
+    }
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows * D;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t row = i / D;
