@@ -29,8 +29,9 @@
 //   bwd_sweep16  per slot, half a warp: replays the slot with the recorded decisions
 //                (the forward's fp32 sums, in its order), turns each event's read-row
 //                gradients into sum and radius gradients (LayerNorm and normalisation
-//                backward), and sums them from the last event back to each member's
-//                own event, adding the tokens' k, v and gate gradients.
+//                backward), and gives each member their sum from its own event to the
+//                last (total minus running sum), adding the tokens' k, v and gate
+//                gradients.
 #include "kvm_internal.cuh"
 
 namespace kvm {
@@ -281,10 +282,14 @@ __global__ void bwd_dstate(BackwardArgs a) {
 // as one list in the replay's order: by event, the founder first, then the merged tokens
 // in position order.  Entry (t << 2) | kind; slot j's part is mem[moff[j] .. moff[j + 1]).
 // A record entry that names no slot of its event or no known kind latches the status
-// word and is left out.
+// word and is left out.  The ordered append is serial (one warp), so the whole CTA first
+// stages a run of events' entries in shared memory, packed (slot << 2) | kind or -1, and
+// the warp reads them there instead of waiting on global loads at every step.
 constexpr int MB_THREADS = 256;
+constexpr int MB_STAGE = 4096;  // entries staged at a time (>= 16 events of the largest chunk)
 __global__ void __launch_bounds__(MB_THREADS) bwd_members(BackwardArgs a) {
-    extern __shared__ int cur[];  // [M + 1]: counts, then list cursors
+    extern __shared__ int cur[];  // [M + 1]: counts, then list cursors; then stage[MB_STAGE]
+    int* stage = cur + a.M + 1;
     __shared__ int part[MB_THREADS / 32];
     const int bh = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int C = a.C, M = a.M, E = a.E;
@@ -342,25 +347,36 @@ __global__ void __launch_bounds__(MB_THREADS) bwd_members(BackwardArgs a) {
     __syncthreads();
     // one warp appends in order: per event the founders, then the merged tokens; lanes of a
     // batch that go to the same slot take consecutive places in lane (= position) order
-    if (warp == 0) {
-        const unsigned below = (1u << lane) - 1u;
-        for (int e = 0; e < E; ++e)
-            for (int pass = 0; pass < 2; ++pass)
-                for (int base = 0; base < C; base += 32) {
-                    const int i = base + lane;
-                    int sj = -1, kn = -1;
-                    if (i < C) kn = entry(e, i, sj);
-                    const bool in = kn >= 0 && (pass == 0 ? kn >= 1 : kn == 0);
-                    const unsigned peers = __match_any_sync(0xffffffffu, in ? sj : -1 - lane);
-                    int at = 0;
-                    if (in) at = cur[sj] + __popc(peers & below);
-                    __syncwarp();
-                    if (in) {
-                        list[at] = (int)((((int64_t)e * C + i) << 2) | kn);
-                        if ((peers & below) == 0u) cur[sj] += __popc(peers);
+    const unsigned below = (1u << lane) - 1u;
+    const int per_stage = MB_STAGE / C;
+    for (int e0 = 0; e0 < E; e0 += per_stage) {
+        const int ne = min(per_stage, E - e0);
+        for (int q = tid; q < ne * C; q += MB_THREADS) {
+            int sj;
+            const int kn = entry(e0 + q / C, q % C, sj);
+            stage[q] = kn >= 0 ? (sj << 2) | kn : -1;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            for (int el = 0; el < ne; ++el)
+                for (int pass = 0; pass < 2; ++pass)
+                    for (int base = 0; base < C; base += 32) {
+                        const int i = base + lane;
+                        const int x = i < C ? stage[el * C + i] : -1;
+                        const int kn = x >= 0 ? (x & 3) : -1, sj = x >> 2;
+                        const bool in = kn >= 0 && (pass == 0 ? kn >= 1 : kn == 0);
+                        const unsigned peers = __match_any_sync(0xffffffffu, in ? sj : -1 - lane);
+                        int at = 0;
+                        if (in) at = cur[sj] + __popc(peers & below);
+                        __syncwarp();
+                        if (in) {
+                            list[at] = (int)((((int64_t)(e0 + el) * C + i) << 2) | kn);
+                            if ((peers & below) == 0u) cur[sj] += __popc(peers);
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
-                }
+        }
+        __syncthreads();
     }
 }
 
@@ -368,9 +384,11 @@ __global__ void __launch_bounds__(MB_THREADS) bwd_members(BackwardArgs a) {
 // replays the slot through the events with the recorded decisions (its member list: the
 // founder first, then its merged tokens in position order: the forward's fp32 sums) and
 // turns each event's read-row gradients of the slot into sum and radius gradients
-// (LayerNorm and normalisation backward), in place.  Pass 2 runs the events backwards,
-// summing those gradients, and each of the slot's tokens reads the sum at its own event
-// (the gradients of every state that holds it).
+// (LayerNorm and normalisation backward), keeping their running sum over the events.  A
+// token that joined at event e is in every state from e on, so its gradient is the sum
+// over events >= e: the total at the end of pass 1 minus the running sum before e, which
+// pass 1 stores (in the read-row gradient buffers, already consumed there) only at the
+// events where some member joined.  Pass 2 then visits each member once.
 // Half a warp per slot (two slots a warp; lanes over the dims, four each): the reductions
 // take four shuffle levels and each instruction serves two slots.  Every shuffle names only its own half's lanes, which follow their
 // slot's control flow together.
@@ -421,17 +439,26 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep16(BackwardArgs a) {
     float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
     int cnt = 0;
     float rho = 0.0f;
+    // running sums over the events so far of the slot's sum and radius gradients
+    float4 Pk = make_float4(0.f, 0.f, 0.f, 0.f), Pv = Pk;
+    float Pr = 0.0f;
     // pass 1
     int ptr = m0;
     for (int e = 0; e < a.E; ++e) {
         const int n = a.sched[e].n_after;
         if (j >= n) continue;  // not founded yet (founding appends at the end)
+        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D + d0;
+        // the event's read-row gradients, loaded while the members are replayed
+        float4 gkh = *reinterpret_cast<const float4*>(a.dks + o);
+        const float4 gvh = *reinterpret_cast<const float4*>(a.dvs + o);
         const int64_t tend = (int64_t)(e + 1) * C;
+        bool joined = false;
         while (ptr < m1) {
             const int ent = member(ptr, true);
             const int64_t t = ent >> 2;
             if (t >= tend) break;  // a member of a later event
             ++ptr;
+            joined = true;
             const float gt = gg[t];
             const float4 kx = ld4<T>(kk + t * D + d0), vx = ld4<T>(vv + t * D + d0);
             if ((ent & 3) != 0) {  // the founder sets the slot
@@ -445,8 +472,15 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep16(BackwardArgs a) {
                 ++cnt;
             }
         }
+        // tokens that joined at this event are in every state from it on: pass 2 takes their
+        // gradient as the total minus the sums before this event, kept here (the read-row
+        // gradients of this event are already in registers)
+        if (joined) {
+            *reinterpret_cast<float4*>(a.dks + o) = Pk;
+            *reinterpret_cast<float4*>(a.dvs + o) = Pv;
+            if (hl == 0) a.drho[((int64_t)bh * a.E + e) * M + j] = Pr;
+        }
         // read-row gradients -> sum and radius gradients of the state after event e
-        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D + d0;
         const float cn = (float)(cnt > 0 ? cnt : 1);
         const float4 x = make_float4(sk.x / cn, sk.y / cn, sk.z / cn, sk.w / cn);
         const float mu = half_sum(sum4(x), hm) * (1.0f / D);
@@ -454,7 +488,6 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep16(BackwardArgs a) {
         const float var = half_sum(dot4(xc, xc), hm) * (1.0f / D);
         const float isd = 1.0f / sqrtf(var + a.ln_eps);
         const float4 xh = make_float4(xc.x * isd, xc.y * isd, xc.z * isd, xc.w * isd);
-        float4 gkh = *reinterpret_cast<const float4*>(a.dks + o);
         // the rotary dims of the read key are constant zeros
         if (d0 < r) gkh.x = 0.0f;
         if (d0 + 1 < r) gkh.y = 0.0f;
@@ -463,62 +496,48 @@ __global__ void __launch_bounds__(BW_THREADS) bwd_sweep16(BackwardArgs a) {
         const float mg = half_sum(sum4(gkh), hm) * (1.0f / D);
         const float mgx = half_sum(dot4(gkh, xh), hm) * (1.0f / D);
         const float f = isd / cn;
-        const float4 dsk = make_float4((gkh.x - mg - xh.x * mgx) * f, (gkh.y - mg - xh.y * mgx) * f,
-                                       (gkh.z - mg - xh.z * mgx) * f, (gkh.w - mg - xh.w * mgx) * f);
-        const float4 gvh = *reinterpret_cast<const float4*>(a.dvs + o);
-        float4 dsv;
-        float dr = 0.0f;
+        Pk = make_float4(Pk.x + (gkh.x - mg - xh.x * mgx) * f, Pk.y + (gkh.y - mg - xh.y * mgx) * f,
+                         Pk.z + (gkh.z - mg - xh.z * mgx) * f, Pk.w + (gkh.w - mg - xh.w * mgx) * f);
         if (a.no_vnorm) {
-            dsv = make_float4(gvh.x / cn, gvh.y / cn, gvh.z / cn, gvh.w / cn);
+            Pv = make_float4(Pv.x + gvh.x / cn, Pv.y + gvh.y / cn, Pv.z + gvh.z / cn, Pv.w + gvh.w / cn);
         } else {
             const float nv = sqrtf(half_sum(dot4(sv, sv), hm));
             const float inv = nv > 0.0f ? 1.0f / nv : 0.0f;
             const float4 u = make_float4(sv.x * inv, sv.y * inv, sv.z * inv, sv.w * inv);
-            dr = half_sum(dot4(u, gvh), hm);
+            const float dr = half_sum(dot4(u, gvh), hm);
             const float fr = rho * inv;
-            dsv = make_float4(fr * (gvh.x - u.x * dr), fr * (gvh.y - u.y * dr), fr * (gvh.z - u.z * dr),
-                              fr * (gvh.w - u.w * dr));
+            Pv = make_float4(Pv.x + fr * (gvh.x - u.x * dr), Pv.y + fr * (gvh.y - u.y * dr),
+                             Pv.z + fr * (gvh.z - u.z * dr), Pv.w + fr * (gvh.w - u.w * dr));
+            Pr += dr;
         }
-        *reinterpret_cast<float4*>(a.dks + o) = dsk;
-        *reinterpret_cast<float4*>(a.dvs + o) = dsv;
-        if (hl == 0) a.drho[((int64_t)bh * a.E + e) * M + j] = dr;
     }
-    // pass 2: the members from the last backwards
-    float4 Gk = make_float4(0.f, 0.f, 0.f, 0.f), Gv = Gk;
-    float Gr = 0.0f;
-    ptr = m1 - 1;
-    for (int e = a.E - 1; e >= 0; --e) {
-        const int n = a.sched[e].n_after;
-        if (j >= n) continue;
-        const int64_t o = (((int64_t)bh * a.E + e) * M + j) * D + d0;
-        const float4 dk = *reinterpret_cast<const float4*>(a.dks + o);
-        const float4 dv = *reinterpret_cast<const float4*>(a.dvs + o);
-        Gk = make_float4(Gk.x + dk.x, Gk.y + dk.y, Gk.z + dk.z, Gk.w + dk.w);
-        Gv = make_float4(Gv.x + dv.x, Gv.y + dv.y, Gv.z + dv.z, Gv.w + dv.w);
-        Gr += a.drho[((int64_t)bh * a.E + e) * M + j];
-        const int64_t tbeg = (int64_t)e * C;
-        while (ptr >= m0) {
-            const int ent = member(ptr, false);
-            const int64_t t = ent >> 2;
-            if (t < tbeg) break;  // a member of an earlier event
-            --ptr;
-            const float gt = gg[t];
-            const float4 kx = ld4<T>(kk + t * D + d0), vx = ld4<T>(vv + t * D + d0);
-            float4* dkp = reinterpret_cast<float4*>(a.dk + (row + t) * D + d0);
-            float4* dvp = reinterpret_cast<float4*>(a.dv + (row + t) * D + d0);
-            float4 dkt = *dkp, dvt = *dvp;
-            dkt = make_float4(fmaf(gt, Gk.x, dkt.x), fmaf(gt, Gk.y, dkt.y), fmaf(gt, Gk.z, dkt.z), fmaf(gt, Gk.w, dkt.w));
-            dvt = make_float4(fmaf(gt, Gv.x, dvt.x), fmaf(gt, Gv.y, dvt.y), fmaf(gt, Gv.z, dvt.z), fmaf(gt, Gv.w, dvt.w));
-            if ((ent & 3) != 0) {  // founder: rho = |v|
-                const float nv = sqrtf(half_sum(dot4(vx, vx), hm));
-                const float fr = nv > 0.0f ? Gr / nv : 0.0f;
-                dvt = make_float4(fmaf(fr, vx.x, dvt.x), fmaf(fr, vx.y, dvt.y), fmaf(fr, vx.z, dvt.z), fmaf(fr, vx.w, dvt.w));
-            }
-            *dkp = dkt;
-            *dvp = dvt;
-            const float dgt = half_sum(dot4(kx, Gk) + dot4(vx, Gv), hm);
-            if (hl == 0) a.dg[row + t] += dgt;
+    // pass 2: member t joined at event t / C; its sum gradient is the slot's total over all
+    // events minus the running sums kept at that event in pass 1
+    for (int p = m0; p < m1; ++p) {
+        const int ent = member(p, true);
+        const int64_t t = ent >> 2;
+        const int64_t eo = ((int64_t)bh * a.E + t / C) * M + j;
+        const float4 bk = *reinterpret_cast<const float4*>(a.dks + eo * D + d0);
+        const float4 bv = *reinterpret_cast<const float4*>(a.dvs + eo * D + d0);
+        const float4 Gk = make_float4(Pk.x - bk.x, Pk.y - bk.y, Pk.z - bk.z, Pk.w - bk.w);
+        const float4 Gv = make_float4(Pv.x - bv.x, Pv.y - bv.y, Pv.z - bv.z, Pv.w - bv.w);
+        const float gt = gg[t];
+        const float4 kx = ld4<T>(kk + t * D + d0), vx = ld4<T>(vv + t * D + d0);
+        float4* dkp = reinterpret_cast<float4*>(a.dk + (row + t) * D + d0);
+        float4* dvp = reinterpret_cast<float4*>(a.dv + (row + t) * D + d0);
+        float4 dkt = *dkp, dvt = *dvp;
+        dkt = make_float4(fmaf(gt, Gk.x, dkt.x), fmaf(gt, Gk.y, dkt.y), fmaf(gt, Gk.z, dkt.z), fmaf(gt, Gk.w, dkt.w));
+        dvt = make_float4(fmaf(gt, Gv.x, dvt.x), fmaf(gt, Gv.y, dvt.y), fmaf(gt, Gv.z, dvt.z), fmaf(gt, Gv.w, dvt.w));
+        if ((ent & 3) != 0) {  // founder: rho = |v|
+            const float Gr = Pr - a.drho[eo];
+            const float nv = sqrtf(half_sum(dot4(vx, vx), hm));
+            const float fr = nv > 0.0f ? Gr / nv : 0.0f;
+            dvt = make_float4(fmaf(fr, vx.x, dvt.x), fmaf(fr, vx.y, dvt.y), fmaf(fr, vx.z, dvt.z), fmaf(fr, vx.w, dvt.w));
         }
+        *dkp = dkt;
+        *dvp = dvt;
+        const float dgt = half_sum(dot4(kx, Gk) + dot4(vx, Gv), hm);
+        if (hl == 0) a.dg[row + t] += dgt;
     }
 }
 
@@ -1166,7 +1185,7 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
     }
     if (a.E > 0) {
         const int64_t slots = (int64_t)a.BH * a.M;
-        bwd_members<<<(unsigned)a.BH, MB_THREADS, (size_t)(a.M + 1) * sizeof(int), s>>>(a);
+        bwd_members<<<(unsigned)a.BH, MB_THREADS, (size_t)(a.M + 1 + MB_STAGE) * sizeof(int), s>>>(a);
         // two slots a warp
         bwd_sweep16<T><<<(unsigned)(((slots + 1) / 2 + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
     }
