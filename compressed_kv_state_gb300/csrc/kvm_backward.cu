@@ -410,8 +410,11 @@ __device__ __forceinline__ float half_sum(float v, unsigned hm) {
     return v;
 }
 
+// CTAs of two warps: at its 88 registers a thread the sweep fits 23 warps an SM, which
+// 256-thread CTAs round down to 16 and 64-thread CTAs to 22
+constexpr int SW_WARPS = 2;
 template <typename T>
-__global__ void __launch_bounds__(BW_THREADS) bwd_sweep16(BackwardArgs a) {
+__global__ void __launch_bounds__(SW_WARPS * 32) bwd_sweep16(BackwardArgs a) {
     const int lane = threadIdx.x & 31, hl = lane & 15, hf = lane >> 4;
     const unsigned hm = 0xFFFFu << (16 * hf);
     const int64_t sid = 2 * (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) + hf;
@@ -1187,7 +1190,7 @@ cudaError_t launch_all(const BackwardArgs& a, cudaStream_t s) {
         const int64_t slots = (int64_t)a.BH * a.M;
         bwd_members<<<(unsigned)a.BH, MB_THREADS, (size_t)(a.M + 1 + MB_STAGE) * sizeof(int), s>>>(a);
         // two slots a warp
-        bwd_sweep16<T><<<(unsigned)(((slots + 1) / 2 + wpb - 1) / wpb), BW_THREADS, 0, s>>>(a);
+        bwd_sweep16<T><<<(unsigned)(((slots + 1) / 2 + SW_WARPS - 1) / SW_WARPS), SW_WARPS * 32, 0, s>>>(a);
     }
     return cudaGetLastError();
 }
