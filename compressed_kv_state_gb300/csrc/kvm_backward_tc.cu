@@ -46,7 +46,9 @@ constexpr int OFF_K = OFF_DO + TILE;        // [NS]
 constexpr int OFF_V = OFF_K + NS * TILE;    // [NS]
 constexpr int OFF_P = OFF_V + NS * TILE;    // two halves: keys [0, 64) and [64, 128), [128 queries][128 B]
 constexpr int OFF_DS = OFF_P + 2 * TILE;    // the same for dS
-constexpr int OFF_BAR = OFF_DS + 2 * TILE;  // 160 KB
+constexpr int OFF_STG = OFF_DS + 2 * TILE;  // per softmax-gradient warp: [32 rows][32 floats]
+constexpr int STG_FLOATS = 32 * 32;
+constexpr int OFF_BAR = OFF_STG + 8 * STG_FLOATS * 4;  // 192 KB
 constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
 constexpr int NTHREADS = 320;
 constexpr int NSM = 256;  // softmax-gradient threads (two warpgroups)
@@ -243,40 +245,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             t0 = win ? ws + (int64_t)KB * (jb - nbs) : (int64_t)KB * jb;
             kv = win ? (int)(q0 + nq - t0 < KB ? q0 + nq - t0 : KB) : (n - KB * jb < KB ? n - KB * jb : KB);
         };
-        // dims [32 wg, 32 wg + 32) of the dK and dV rows of block jb (this thread: key row
-        // rr of the block) to the gradient arrays
+        // dims [32 wg, 32 wg + 32) of the dK and dV rows of block jb to the gradient arrays.
+        // The warp's 32 key rows (lane = row in tensor memory) pass through its staging area
+        // (16-byte columns XOR-swizzled by row: conflict-free both ways), so that each store
+        // or atomic of the warp covers four rows' 128 contiguous bytes instead of one piece
+        // of 32 different rows.
+        float* stg = reinterpret_cast<float*>(sm + OFF_STG) + (warp - 2) * STG_FLOATS;
+        auto spill_rows = [&](const uint32_t (&x)[32], float sc, float* g0, int kv, bool own) {
+            __syncwarp();
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                *reinterpret_cast<float4*>(stg + lane * 32 + ((q4 ^ (lane & 7)) << 2)) =
+                    make_float4(__uint_as_float(x[4 * q4]) * sc, __uint_as_float(x[4 * q4 + 1]) * sc,
+                                __uint_as_float(x[4 * q4 + 2]) * sc, __uint_as_float(x[4 * q4 + 3]) * sc);
+            __syncwarp();
+            // step i: rows 4i + r of the warp's 32 (r = lane / 8), 16-byte column c4 = lane % 8;
+            // row 4i + r sits at swizzle (4i + r) % 8 = r + 4 (i odd) or r (i even)
+            const int c4 = lane & 7, r = lane >> 3, kr0 = wq * 32 + r;
+            const float* src0 = stg + r * 32;
+            const int col_even = (c4 ^ r) << 2, col_odd = (c4 ^ (r + 4)) << 2;
+            float4* dst0 = reinterpret_cast<float4*>(g0 + (int64_t)kr0 * D + 32 * wg) + c4;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = *reinterpret_cast<const float4*>(src0 + 128 * i + ((i & 1) ? col_odd : col_even));
+                if (kr0 + 4 * i < kv) {
+                    float4* dst = dst0 + i * D;  // four rows of D floats = D float4s further
+                    if (own)
+                        *dst = v;
+                    else
+                        atomicAdd(dst, v);
+                }
+            }
+        };
         auto readout = [&](int jb) {
             int64_t t0;
             int kv;
             block_keys(jb, t0, kv);
             const bool win = jb >= nbs;
-            float* gk = (win ? a.dk + (row + t0 + rr) * D : a.dks + (((int64_t)bh * a.E + e) * a.M + t0 + rr) * D) + 32 * wg;
-            float* gv = (win ? a.dv + (row + t0 + rr) * D : a.dvs + (((int64_t)bh * a.E + e) * a.M + t0 + rr) * D) + 32 * wg;
-            uint32_t x[32], y[32];
+            float* gk = win ? a.dk + (row + t0) * D : a.dks + (((int64_t)bh * a.E + e) * a.M + t0) * D;
+            float* gv = win ? a.dv + (row + t0) * D : a.dvs + (((int64_t)bh * a.E + e) * a.M + t0) * D;
+            // a read row of the state is this tile's alone when the chunk is one tile
+            // (plain stores; the rows were not zeroed); window keys take the sums of
+            // every tile that sees them
+            const bool own = !win && a.C == TQ;
+            uint32_t x[32];
             tmem_ld32(tmem + lb + T_DK + 32 * wg, x);
-            tmem_ld32(tmem + lb + T_DV + 32 * wg, y);
             tmem_wait_ld();
-            if (rr < kv) {
-                const float sc = a.inv_sqrt_d;
-                // a read row of the state is this tile's alone when the chunk is one tile
-                // (plain stores; the rows were not zeroed); window keys take the sums of
-                // every tile that sees them
-                const bool own = !win && a.C == TQ;
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                    const float4 kx = make_float4(__uint_as_float(x[4 * q4]) * sc, __uint_as_float(x[4 * q4 + 1]) * sc,
-                                                  __uint_as_float(x[4 * q4 + 2]) * sc, __uint_as_float(x[4 * q4 + 3]) * sc);
-                    const float4 vy = make_float4(__uint_as_float(y[4 * q4]), __uint_as_float(y[4 * q4 + 1]),
-                                                  __uint_as_float(y[4 * q4 + 2]), __uint_as_float(y[4 * q4 + 3]));
-                    if (own) {
-                        reinterpret_cast<float4*>(gk)[q4] = kx;
-                        reinterpret_cast<float4*>(gv)[q4] = vy;
-                    } else {
-                        atomicAdd(reinterpret_cast<float4*>(gk + 4 * q4), kx);
-                        atomicAdd(reinterpret_cast<float4*>(gv + 4 * q4), vy);
-                    }
-                }
-            }
+            spill_rows(x, a.inv_sqrt_d, gk, kv, own);
+            tmem_ld32(tmem + lb + T_DV + 32 * wg, x);
+            tmem_wait_ld();
+            spill_rows(x, 1.0f, gv, kv, own);
         };
         const float2 sl2 = make_float2(sl, sl), nl2 = make_float2(-L, -L);
         bool ok = true;
