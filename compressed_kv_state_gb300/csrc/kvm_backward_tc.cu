@@ -15,14 +15,17 @@
 //   warp 0        producer: the tile's Q and dO, then its key blocks (128 keys: the
 //                 read rows of its chunk's state, then its window) by TMA, 2 stages
 //   warp 1        one thread issues the MMAs: S and dP (A and B K-major) into tensor
-//                 memory; once P and dS are in shared memory, dV = P^T dO and dK = dS^T Q
-//                 (A MN-major: keys run along the rows of P and dS) and dQ += dS K
+//                 memory; once P and dS are in shared memory, the next block's S and dP,
+//                 then dV = P^T dO and dK = dS^T Q (A MN-major: keys run along the rows
+//                 of P and dS) and dQ += dS K
 //   warps 2-9     two warpgroups; thread i of warpgroup g owns query row i (= tensor-
 //                 memory lane i) and keys [64g, 64g + 64) of each block: P and dS of that
-//                 part of its row as bf16 into 64-key 128-byte-swizzled half tile g; then,
-//                 as key row i, dims [32g, 32g + 32) of the block's dK and dV rows to the
-//                 gradient arrays (vector atomics); at the end dims [32g, 32g + 32) of its
-//                 dQ row, scaled and rotated back, to dq.
+//                 part of its row in registers (while the previous block's products run);
+//                 then, as key row i, dims [32g, 32g + 32) of the previous block's dK and
+//                 dV rows to the gradient arrays (vector reductions through a per-warp
+//                 staging area); then P and dS as bf16 into 64-key 128-byte-swizzled half
+//                 tile g; at the end dims [32g, 32g + 32) of its dQ row, scaled and
+//                 rotated back, to dq.
 // Tensor memory (512 columns): S 128, dP 128, dQ 64, dK 64, dV 64.  All mbarrier waits are
 // bounded; on expiry the CTA raises the status word, lets its copies and MMAs land, exits.
 #include <cuda.h>
@@ -60,8 +63,7 @@ enum {
     B_VFULL = B_KFULL + NS,   // [NS]
     B_KVEMPTY = B_VFULL + NS, // [NS] the stage's last MMA done
     B_SPD = B_KVEMPTY + NS,   // S and dP of the block in tensor memory
-    B_SFREE,                  // S and dP read by the softmax threads (256 arrivals)
-    B_PDS,                    // P and dS in shared memory (256 arrivals)
+    B_PDS,                    // S and dP read, P and dS in shared memory (256 arrivals)
     B_MMA2,                   // dV, dK, dQ MMAs of the block done
     B_DKVFREE,                // dK and dV of the block read out (256 arrivals)
     B_FINAL,                  // MMA drain
@@ -115,7 +117,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(bar(B_KVEMPTY + i), 1);
         }
         mbar_init(bar(B_SPD), 1);
-        mbar_init(bar(B_SFREE), NSM);
         mbar_init(bar(B_PDS), NSM);
         mbar_init(bar(B_MMA2), 1);
         mbar_init(bar(B_DKVFREE), NSM);
@@ -175,29 +176,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // dS K-major (K = keys): K-steps 0-3 in the first half, 4-7 in the second
             const uint64_t dds_k = sdesc_sw128(sbase + OFF_DS, 16, 1024);
             bool ok = mbar_wait(bar(B_QFULL), 0, abort_flag, a.status);
-            for (int j = 0; ok && j < nblk; ++j) {
+            // S = Q K^T and dP = dO V^T of block j (both operands K-major)
+            auto issue_sdp = [&](int j) -> bool {
                 const int st = j % NS;
                 if (!mbar_wait(bar(B_KFULL + st), (j / NS) & 1, abort_flag, a.status) ||
-                    !mbar_wait(bar(B_VFULL + st), (j / NS) & 1, abort_flag, a.status) ||
-                    (j > 0 && !mbar_wait(bar(B_SFREE), (j - 1) & 1, abort_flag, a.status))) {
-                    ok = false;
-                    break;
-                }
+                    !mbar_wait(bar(B_VFULL + st), (j / NS) & 1, abort_flag, a.status))
+                    return false;
                 tc_fence_after();
                 const uint64_t dk_k = sdesc_sw128(sbase + OFF_K + st * TILE, 16, 1024);
                 const uint64_t dv_k = sdesc_sw128(sbase + OFF_V + st * TILE, 16, 1024);
-                const uint64_t dk_m = sdesc_sw128(sbase + OFF_K + st * TILE, TILE, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) mma_bf16_ss(tmem + T_S, dq_k + 2 * ks, dk_k + 2 * ks, idesc_s, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) mma_bf16_ss(tmem + T_DP, ddo_k + 2 * ks, dv_k + 2 * ks, idesc_s, ks > 0);
                 mma_commit(bar(B_SPD));
+                return true;
+            };
+            if (ok && nblk > 0) ok = issue_sdp(0);
+            for (int j = 0; ok && j < nblk; ++j) {
+                const int st = j % NS;
+                // P and dS of block j are in shared memory (S and dP were read before them)
+                // and block j - 1's dK, dV are read out
                 if (!mbar_wait(bar(B_PDS), j & 1, abort_flag, a.status) ||
                     (j > 0 && !mbar_wait(bar(B_DKVFREE), (j - 1) & 1, abort_flag, a.status))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // the next block's S and dP first: its P and dS are computed while the
+                // tensor core runs this block's three products
+                if (j + 1 < nblk && !issue_sdp(j + 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t dk_m = sdesc_sw128(sbase + OFF_K + st * TILE, TILE, 1024);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) mma_bf16_ss(tmem + T_DV, dp_m + 128 * ks, ddo_m + 128 * ks, idesc_kv, ks > 0);
 #pragma unroll
@@ -314,22 +326,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             if (!mbar_wait(bar(B_SPD), j & 1, abort_flag, a.status)) { ok = false; break; }
             tc_fence_after();
-            if (j > 0) {
-                // block j - 1's MMAs are done: P and dS are free, its dK and dV final
-                if (!mbar_wait(bar(B_MMA2), (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
-                tc_fence_after();
-                readout(j - 1);
-                tc_fence_before();
-                mbar_arrive(bar(B_DKVFREE));
-            }
-            // P and dS of keys [64 wg, 64 wg + 64), 32 at a time, into half tile wg (row rr)
+            // P and dS of keys [64 wg, 64 wg + 64) into registers, 32 keys at a time (the
+            // tensor core runs block j - 1's dV, dK, dQ meanwhile)
+            uint32_t pw[2][16], dw[2][16];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tmem + lb + T_S + 64 * wg + 32 * h, sv);
                 tmem_ld32(tmem + lb + T_DP + 64 * wg + 32 * h, dp);
                 tmem_wait_ld();
-                uint32_t pw[16], dw[16];
                 const int kb = 64 * wg + 32 * h;
 #pragma unroll
                 for (int x = 0; x < 32; x += 2) {
@@ -337,19 +342,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const float p0 = kb + x < lim ? ex2(t2.x) : 0.0f;
                     const float p1 = kb + x + 1 < lim ? ex2(t2.y) : 0.0f;
                     const float d0 = p0 * (__uint_as_float(dp[x]) - Dv), d1 = p1 * (__uint_as_float(dp[x + 1]) - Dv);
-                    pw[x >> 1] = packbf2(p0, p1);
-                    dw[x >> 1] = packbf2(d0, d1);
+                    pw[h][x >> 1] = packbf2(p0, p1);
+                    dw[h][x >> 1] = packbf2(d0, d1);
                 }
+            }
+            if (j > 0) {
+                // block j - 1's products are done: P and dS are free, its dK and dV final
+                if (!mbar_wait(bar(B_MMA2), (j - 1) & 1, abort_flag, a.status)) { ok = false; break; }
+                tc_fence_after();
+                readout(j - 1);
+                tc_fence_before();
+                mbar_arrive(bar(B_DKVFREE));
+            }
+            // P and dS of this block into half tile wg (row rr)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const int chunk = h * 4 + cc;  // 16-byte chunk of the 128-byte half row
                     const uint32_t off = (uint32_t)(wg * TILE + rr * 128 + ((chunk ^ (rr & 7)) << 4));
-                    *reinterpret_cast<uint4*>(sm + OFF_P + off) = make_uint4(pw[4 * cc], pw[4 * cc + 1], pw[4 * cc + 2], pw[4 * cc + 3]);
-                    *reinterpret_cast<uint4*>(sm + OFF_DS + off) = make_uint4(dw[4 * cc], dw[4 * cc + 1], dw[4 * cc + 2], dw[4 * cc + 3]);
+                    *reinterpret_cast<uint4*>(sm + OFF_P + off) =
+                        make_uint4(pw[h][4 * cc], pw[h][4 * cc + 1], pw[h][4 * cc + 2], pw[h][4 * cc + 3]);
+                    *reinterpret_cast<uint4*>(sm + OFF_DS + off) =
+                        make_uint4(dw[h][4 * cc], dw[h][4 * cc + 1], dw[h][4 * cc + 2], dw[h][4 * cc + 3]);
                 }
-            }
+            // the S and dP loads above complete before the MMA thread may overwrite them
             tc_fence_before();
-            mbar_arrive(bar(B_SFREE));
             fence_proxy_async();  // P and dS (generic-proxy writes) before the MMAs read them
             mbar_arrive(bar(B_PDS));
         }
