@@ -365,6 +365,7 @@ __global__ void __launch_bounds__(MB_THREADS) bwd_members(BackwardArgs a) {
                         const int x = i < C ? stage[el * C + i] : -1;
                         const int kn = x >= 0 ? (x & 3) : -1, sj = x >> 2;
                         const bool in = kn >= 0 && (pass == 0 ? kn >= 1 : kn == 0);
+                        if (__ballot_sync(0xffffffffu, in) == 0u) continue;  // nothing to place (no founder, say)
                         const unsigned peers = __match_any_sync(0xffffffffu, in ? sj : -1 - lane);
                         int at = 0;
                         if (in) at = cur[sj] + __popc(peers & below);
