@@ -141,6 +141,31 @@ def test_read_radius_preserved(sched, M):
     assert (kv[:, :cfg.rope_dims] == 0).all()
 
 
+@pytest.mark.parametrize("sched,M", [(0, 24), (1, 64), (1, 200)])
+def test_slots_founded_once_in_order_before_their_merges(sched, M):
+    """Every slot is founded exactly once (a sink or an appended token), the
+    founders of an event take the next slot numbers (new slots are appended
+    after the existing ones: KVM summary, Core mechanism 3), and no token
+    merges into a slot in an event before the one that founds it (a merge
+    joins an existing slot: Core mechanism 2).  The replay of a slot's history
+    (founder first, then its merged tokens in order) relies on this."""
+    cfg, _, (_, st, dbg) = _random_run(sched=sched, M=M)
+    A, K = dbg["assign"], dbg["kind"]
+    founded_at = {}
+    n = 0
+    for e in range(A.shape[0]):
+        new = sorted(int(A[e, i]) for i in range(cfg.chunk) if K[e, i] in (oracle.APPENDED, oracle.SINK))
+        assert new == list(range(n, n + len(new))), f"event {e}: founders {new} after {n} slots"
+        for j in new:
+            founded_at[j] = e
+        n += len(new)
+        for i in range(cfg.chunk):
+            if K[e, i] == oracle.MERGED:
+                j = int(A[e, i])
+                assert j in founded_at and founded_at[j] <= e, f"event {e}: token {i} merges into slot {j} before it exists"
+    assert n == st.n
+
+
 @pytest.mark.parametrize("sched,M,coef,expo", [(0, 24, 2.0, 0.5), (1, 64, 2.0, 0.5),
                                                 (1, 128, 1.0, 0.75), (1, 80, 8.0, 0.25),
                                                 (1, 200, 0.3, 1.0)])
